@@ -282,6 +282,8 @@ static int32_t inverse_cdf(const double *r, int V, double S, double u, int *near
  * target alone would sample (§9.1; glossary "Garantie de qualité").
  *
  * Readings: accept_i <=> u_accept[i] * q_i(x_i) < p_i(x_i) with u in [0,1);
+ * a sequence with a draft token outside [0, V) or a logits row whose max or
+ * normaliser is not finite (NaN, +inf, or every logit -inf) is invalid input;
  * one extra uniform u_sample per sequence drives the single resample / bonus
  * draw through an inverse CDF in index order; if the residual sums to zero
  * the draw falls back to p_a.  Logits arrive already temperature-scaled.
@@ -308,6 +310,16 @@ int orc_verify_chain(const void *target, const void *draft, int dtype,
         for (int i = 0; i < N; ++i)
             if (draft_tokens[(size_t)b * N + i] < 0 || draft_tokens[(size_t)b * N + i] >= V)
                 st = ORC_ERR_BAD_INPUT;
+        /* a row whose max or normaliser is not finite defines no distribution */
+        for (int i = 0; i < 2 * N + 1 && st == ORC_OK; ++i) {
+            const char *row = i <= N
+                ? (const char *)target + ((size_t)b * (N + 1) + i) * V * esz
+                : (const char *)draft + ((size_t)b * N + (i - N - 1)) * V * esz;
+            double m, s;
+            orc_row_stats(row, dtype, V, &m, &s, NULL);
+            if (!isfinite(m) || !isfinite(s) || !(s > 0.0))
+                st = ORC_ERR_BAD_INPUT;
+        }
         if (st != ORC_OK) {
             accepted_len[b] = -1;
             if (flags)
@@ -466,7 +478,8 @@ int orc_verify_tree_greedy(const void *target, int dtype, const int32_t *node_to
  * the committed continuation and the rest is discarded (§9.1).  Reading: node
  * j's row sits in slot L_b + j; path row d moves to slot L_b + d for
  * d = 0..a, and the cache length becomes L_b + a + 1.  path_nodes == NULL
- * means a chain (path[d] = d: nothing moves).
+ * means a chain (path[d] = d: nothing moves).  A path must start at the root
+ * (path[0] = 0) and increase strictly, with L_b + path[d] < S_max.
  *
  * Written out of place: k_out/v_out start as copies of k_in/v_in and only the
  * destination rows are overwritten from the untouched inputs.  A sequence
@@ -494,9 +507,11 @@ int orc_compact_kv(const uint16_t *k_in, const uint16_t *v_in, uint16_t *k_out, 
         }
         if (L < 0 || L + a + 1 > S_max || (path_nodes && a >= path_stride))
             st = ORC_ERR_BAD_INPUT;
+        /* a valid path starts at the root (node 0) and increases strictly */
         for (int d = 0; d <= a && st == ORC_OK && path_nodes; ++d) {
             int src = path_nodes[(size_t)b * path_stride + d];
-            if (src < d || L + src >= S_max || (d > 0 && src <= path_nodes[(size_t)b * path_stride + d - 1]))
+            if ((d == 0 && src != 0) || L + src >= S_max ||
+                (d > 0 && src <= path_nodes[(size_t)b * path_stride + d - 1]))
                 st = ORC_ERR_BAD_INPUT;
         }
         if (st != ORC_OK) {

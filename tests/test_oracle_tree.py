@@ -145,11 +145,12 @@ def test_compaction_chain_moves_nothing(orc):
 
 def test_compaction_rejects_bad_paths(orc):
     inp = W.attention_inputs(3, 4, 2, 1, 8, [2, 2, 2], S_max=8, seed=6, unused_fill="zero")
-    paths = np.array([[0, 2, 1, -1], [0, 6, -1, -1], [0, 1, -1, -1]], np.int32)
-    acc = np.array([2, 1, -1], np.int32)
+    paths = np.array([[0, 2, 1, -1], [0, 6, -1, -1], [0, 1, -1, -1], [1, 2, -1, -1]], np.int32)
+    acc = np.array([2, 1, -1, 1], np.int32)
+    inp = W.attention_inputs(4, 4, 2, 1, 8, [2, 2, 2, 2], S_max=8, seed=6, unused_fill="zero")
     r = orc.compact_kv(inp["k"], inp["v"], inp["prefix_lens"], paths, acc)
-    assert r["status"].tolist() == [orc.ERR_BAD_INPUT, orc.ERR_BAD_INPUT, orc.OK]
-    assert r["new_kv_lens"].tolist() == [2, 2, 2]
+    assert r["status"].tolist() == [orc.ERR_BAD_INPUT, orc.ERR_BAD_INPUT, orc.OK, orc.ERR_BAD_INPUT]
+    assert r["new_kv_lens"].tolist() == [2, 2, 2, 2]
     assert np.array_equal(r["k"], inp["k"])
 
 

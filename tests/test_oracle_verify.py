@@ -270,3 +270,16 @@ def test_probabilities_definition(orc):
             x = inp["draft_tokens"][b, i]
             assert r["probs"][b, i, 0] == pytest.approx(p[b, i, x], rel=1e-12)
             assert r["probs"][b, i, 1] == pytest.approx(q[b, i, x], rel=1e-12)
+
+
+def test_non_finite_rows_are_bad_input(orc):
+    """A row with NaN, +inf or only -inf logits defines no distribution."""
+    target = np.zeros((4, 3, 5), np.float32)
+    draft = np.zeros((4, 2, 5), np.float32)
+    target[0, 1, 2] = np.nan
+    draft[1, 0, 4] = np.inf
+    target[2, 2, :] = -np.inf
+    r = orc.verify_chain(target, draft, np.zeros((4, 2), np.int32),
+                         np.full((4, 2), 0.5, np.float32), np.full(4, 0.5, np.float32))
+    assert r["status"].tolist() == [orc.ERR_BAD_INPUT] * 3 + [orc.OK]
+    assert (r["accepted_len"][:3] == -1).all() and (r["out_tokens"][:3] == -1).all()
