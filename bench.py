@@ -1,0 +1,437 @@
+"""Benchmark of the fused chain verification step (one JSON line on stdout).
+
+Workload (default): the fused chain verify step -- B=32 sequences, N=8 draft
+tokens (T=9 query positions), prefix KV length 4096, 32 query / 8 KV heads,
+head_dim 128, bf16 K/V ~ N(0,1); bf16 target and draft logits over
+V=128256 (target ~ N(0,3) plus one boosted token per row, draft = target +
+N(0,1)); seeded uniforms.  One step = tree attention with the causal chain
+mask + stochastic acceptance with residual resample / bonus token + KV
+compaction, all through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, one core) on a bounded
+sample of the same workload.  With torchrun (N > 1) every rank runs an
+independent replica (weak scaling, no collective on the data path); rank 0
+prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify steps/s & verified positions/s at 1 GB300; % of HBM roofline"
+UNIT = "verify steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-sample-seqs", type=int, default=32)
+    ap.add_argument("--profile", action="store_true",
+                    help="device-resident steps only (for ncu): no graph, e2e, clocks or CPU leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(cfg):
+    return {
+        "workload": "fused chain verify step: attention (causal chain mask, GQA) + stochastic "
+                    "acceptance + KV compaction",
+        "B": cfg["B"], "N": cfg["N"], "T": cfg["N"] + 1, "prefix_len": cfg["L"],
+        "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "head_dim": cfg["D"], "V": cfg["V"],
+        "logits": "bf16", "kv": "bf16",
+        "l2": "inputs larger than L2 (about 682 MB touched per step vs 126 MB L2)",
+        "parallelism": "replicas (one independent batch per GPU)",
+    }
+
+
+def algorithmic_bytes(cfg):
+    """Unique bytes one step must touch (each counted once)."""
+    B, N, L, Hq, Hkv, D, V = (cfg[k] for k in ("B", "N", "L", "Hq", "Hkv", "D", "V"))
+    T = N + 1
+    kv = B * Hkv * (L + T) * D * 2 * 2        # K and V: prefix + the T new rows
+    q = B * T * Hq * D * 2
+    o = B * T * Hq * D * 2
+    logits = B * (N + 1) * V * 2 + B * N * V * 2
+    small = B * (N * 4 * 2 + 4) + B * (4 + (N + 1) * 4 + 4 * 2)
+    return {"attention": kv + q + o, "step": kv + q + o + logits + small}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("sv_attention.cu", "sv_device.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_verification_81_gb300", "csrc", name),
+                  "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "tree_attention_chain_B32_L4096_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha256_16") == kernel_source_hash():
+            return float(d["dram_bytes_per_launch_full_size"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    def __init__(self, index):
+        self.proc = None
+        self.index = index
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(cfg, inp, nseq):
+    """Run the oracle on the first nseq sequences of the step; returns seconds."""
+    import oracle
+    oracle.build()
+    a, c = inp["attn"], inp["chain"]
+    sel = np.array([[b, t, h] for b in range(nseq) for t in range(cfg["N"] + 1)
+                    for h in range(cfg["Hq"])], np.int32)
+    t0 = time.perf_counter()
+    oracle.tree_attention(a["q"], a["k"], a["v"], a["prefix_lens"], None, cfg["Hkv"], a["S_max"],
+                          sel=sel)
+    r = oracle.verify_chain(c["target"][:nseq], c["draft"][:nseq], c["draft_tokens"][:nseq],
+                            c["u_accept"][:nseq], c["u_sample"][:nseq])
+    oracle.compact_kv(a["k"][:nseq], a["v"][:nseq], a["prefix_lens"][:nseq], None,
+                      r["accepted_len"])
+    return time.perf_counter() - t0
+
+
+def run_reference(args, cfg, inp, rank, budget_s=60.0):
+    """The oracle as it stands, one core.  A step of the reference is one
+    sequence of the workload (its attention rows, its chain acceptance, its
+    compaction) scaled by B to a full step; as many steps as fit in about a
+    minute are timed (at most --steps), so that any --steps/--warmup finishes
+    in a few minutes."""
+    if rank != 0:
+        return None
+    nseq = 1
+    t_first = oracle_sample(cfg, inp, nseq) if args.warmup > 0 else None
+    if t_first is None:
+        t_first = oracle_sample(cfg, inp, nseq)
+    n = max(1, min(args.steps, int(budget_s / max(t_first, 1e-3))))
+    times = [oracle_sample(cfg, inp, nseq) for _ in range(n)]
+    per_step = sum(times) / len(times) * cfg["B"] / nseq      # seconds per full step
+    value = 1.0 / per_step
+    sample = (f"{nseq} of {cfg['B']} sequences per timed step (attention for all its heads and "
+              f"positions, chain acceptance, compaction), {n} steps timed, scaled to full steps")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": n, "requested_steps": args.steps, "warmup": 1,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_desc(cfg),
+        "positions_per_s": value * cfg["B"] * (cfg["N"] + 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ GPU path
+
+def run_ours(args, cfg, inp, rank, world, local_rank):
+    import torch
+    import speculative_decoding_verification_81_gb300 as sv
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    a, c = inp["attn"], inp["chain"]
+    B, N, V = cfg["B"], cfg["N"], cfg["V"]
+
+    def to_host(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(x)
+
+    host = {
+        "q": to_host(a["q"]), "k": to_host(a["k"]), "v": to_host(a["v"]),
+        "prefix_lens": to_host(a["prefix_lens"]),
+        "target": to_host(c["target"]), "draft": to_host(c["draft"]),
+        "tokens": to_host(c["draft_tokens"]), "ua": to_host(c["u_accept"]),
+        "us": to_host(c["u_sample"]),
+    }
+    d = {k: v.to(dev) for k, v in host.items()}
+    out = torch.empty_like(d["q"])
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    newl = torch.empty(B, dtype=torch.int32, device=dev)
+    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, N + 1, 0, cfg["Hq"], cfg["Hkv"], cfg["D"], dev)
+    ws_c = sv.workspace(sv.SV_OP_VERIFY_CHAIN, B, N, V, sv.SV_BF16, 0, 0, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(dd, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sv.sv_tree_attention(dd["q"], dd["k"], dd["v"], dd["prefix_lens"], None, out=out, ws=ws_a)
+        if ev is not None:
+            ev[1].record(stream)
+        sv.sv_verify_chain(dd["target"], dd["draft"], dd["tokens"], dd["ua"], dd["us"],
+                           accepted_len=acc, out_tokens=toks, ws=ws_c)
+        sv.sv_compact_kv(dd["k"], dd["v"], dd["prefix_lens"], acc, None, new_kv_lens=newl)
+
+    launches_per_step = 4  # attention, chain statistics, residual draw, compaction
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x):
+        if world > 1:
+            t = torch.tensor([x], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    # ---- device-resident timed region
+    for _ in range(args.warmup):
+        step(d)
+    if args.profile:
+        for _ in range(args.steps):
+            step(d)
+        torch.cuda.synchronize(dev)
+        return {"profile": True, "steps": args.steps, "warmup": args.warmup,
+                "launches": launches_per_step * (args.steps + args.warmup)}
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local_rank) as clocks:
+        for i in range(K):
+            step(d, evs[i])
+        t_end.record(stream)
+        barrier()
+    total_ms = evs[0][0].elapsed_time(t_end)
+    attn_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = max_over_ranks(total_ms)
+    clk = clocks.summary()
+
+    # ---- whole step as a CUDA graph (same work, launch overhead removed), for reference
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(dev)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            step(d)
+        stream.wait_stream(s2)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g):
+            step(d)
+        for _ in range(10):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = min(K, 2000)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        graph_ms = e0.elapsed_time(e1) / reps
+    except Exception as exc:  # graph capture is optional information
+        graph_ms = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+
+    # ---- end to end: inputs from pinned host memory, result read back, every step
+    e2e = None
+    if not args.no_e2e:
+        pinned = {k: v.pin_memory() for k, v in host.items()}
+        dd = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+        toks_h = torch.empty(B, N + 1, dtype=torch.int32).pin_memory()
+        newl_h = torch.empty(B, dtype=torch.int32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        d2h = sum(x.numel() * x.element_size() for x in (out_h, acc_h, toks_h, newl_h))
+
+        def e2e_step():
+            for k in pinned:
+                dd[k].copy_(pinned[k], non_blocking=True)
+            step(dd)
+            out_h.copy_(out, non_blocking=True)
+            acc_h.copy_(acc, non_blocking=True)
+            toks_h.copy_(toks, non_blocking=True)
+            newl_h.copy_(newl, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        KE = args.e2e_steps
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(KE):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+        e2e = {"value": world * KE / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": KE}
+        del pinned, dd
+
+    ab = algorithmic_bytes(cfg)
+    peak, peak_kind = load_peaks()
+    attn_s = statistics.mean(attn_ms) / 1e3
+    achieved = ab["attention"] / attn_s / 1e9
+    step_s = total_ms / 1e3 / K
+    value = world * K / (total_ms / 1e3)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V and Q, N(0,3) logits; no dataset or weights)",
+        "config": workload_desc(cfg),
+        "positions_per_s": value * B * (N + 1),
+        "drafted_positions_per_s": value * B * N,
+        "step_hbm": {"algorithmic_bytes": ab["step"], "achieved_gbs": ab["step"] / step_s / 1e9,
+                     "peak_gbs": peak, "frac": ab["step"] / step_s / 1e9 / peak,
+                     "peak_kind": peak_kind},
+        "roofline": {"kernel": "tree_attention_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": committed_traffic(), "algorithmic_bytes": ab["attention"],
+                     "avg_launch_ms": statistics.mean(attn_ms),
+                     "peak_kind": f"{peak_kind} (copy bandwidth)"},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * K,
+        "graph_ms_per_step": graph_ms,
+        "accepted_mean": float(acc.float().mean().item()),
+    }
+    if e2e is not None:
+        res["e2e"] = e2e
+    return res
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        world = max(world, 1)
+
+    from speculative_decoding_verification_81_gb300 import workloads as W
+    cfg = dict(W.WORKLOADS[4])
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = W.workload(4)
+        res = run_reference(args, cfg, inp, rank)
+        print(json.dumps(res), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+        __graft_entry__.build()
+    # every rank verifies its own independent batch (different seed)
+    inp = W.workload(4, seed=1004 + 7919 * rank)
+    res = run_ours(args, cfg, inp, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline and not args.profile:
+        nseq = args.cpu_sample_seqs
+        secs = oracle_sample(cfg, inp, nseq)
+        v = (nseq / cfg["B"]) / secs
+        res["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{nseq} of {cfg['B']} sequences of one step (attention over all heads "
+                      f"and positions, chain acceptance, compaction) in {secs:.1f} s, "
+                      f"scaled to full steps"}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

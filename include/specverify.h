@@ -1,0 +1,207 @@
+/*
+ * specverify.h -- C ABI of libspecverify: the target model's verification
+ * step of speculative decoding, on one GPU (sm_103a).
+ *
+ * The step, as the source pages state it ("Chapitre 9 -- Décodage
+ * spéculatif", LLM Primer VI, §9.1-§9.2; "Parallel Decoding" glossary,
+ * Medusa "Tree attention", "L'attention en arbre : la brique commune" and
+ * "Limites du parallel decoding"):
+ *   1. one attention pass in which N+1 chain positions, or T draft-tree
+ *      nodes, attend to the prefix KV cache plus their own tree ancestors
+ *      (sv_tree_attention);
+ *   2. acceptance over the full vocabulary: stochastic min(1, p(x)/q(x))
+ *      with a residual (p-q)+ resample and a bonus token on chains
+ *      (sv_verify_chain), greedy longest agreeing path on trees
+ *      (sv_verify_tree_greedy);
+ *   3. compaction of the accepted path's K/V rows (sv_compact_kv).
+ *
+ * Conventions shared by every call:
+ *   - Every array argument is DEVICE memory owned by the caller.  The
+ *     library allocates nothing and keeps no state between calls.  Calls
+ *     that need scratch take a caller-provided workspace; its size comes
+ *     from sv_workspace_size() and it must be zero-filled once before its
+ *     first use (every call leaves its counters at zero again).
+ *   - Every call is asynchronous on `stream` (NULL = legacy default
+ *     stream); none synchronises.  Two calls that share a workspace must
+ *     not overlap on the GPU.
+ *   - Host-detectable errors (bad sizes, NULL pointers, misalignment,
+ *     workspace too small, unsupported shape) return a non-OK status before
+ *     anything is launched.  Problems only visible on the device (a parent
+ *     array that is not a topologically ordered tree, a token outside
+ *     [0, V), prefix_len + T > S_max, a logits row whose max or normaliser is
+ *     not finite) are reported per sequence in seq_status[b] (nullable);
+ *     such a sequence's outputs are -1 (token/length outputs) or left
+ *     unspecified (attention rows).  No call ever traps the GPU.
+ *   - Layouts are dense row-major with the innermost dimension last.  bf16
+ *     is IEEE binary32's upper 16 bits.  Pointers to bf16/f32 tensors must
+ *     be 16-byte aligned.
+ *   - Tree convention: node 0 is the root (the last committed token, whose
+ *     K/V this pass produces); parents[b][0] = -1 and 0 <= parents[b][i] < i.
+ *     A chain of N drafts is the tree parent[i] = i-1 with T = N+1 nodes.
+ *     Node j's K/V row sits in cache slot prefix_lens[b] + j.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared opaquely so that this header needs no CUDA headers. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum sv_status {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,  /* host: NULL pointer, size <= 0, misaligned pointer, Hq % Hkv */
+    SV_ERR_WORKSPACE = 2,    /* host: workspace NULL or smaller than sv_workspace_size()  */
+    SV_ERR_UNSUPPORTED = 3,  /* host: shape outside the kernels' range (see each call)    */
+    SV_ERR_CUDA = 4,         /* host: a CUDA runtime call or launch failed                 */
+    SV_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel gave up             */
+    SV_ERR_BAD_INPUT = 6     /* device: invalid per-sequence data (see conventions)       */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum sv_op {
+    SV_OP_TREE_ATTENTION = 0,
+    SV_OP_VERIFY_CHAIN = 1,
+    SV_OP_VERIFY_TREE_GREEDY = 2
+} sv_op;
+
+/*
+ * Bytes of workspace a call needs, for the CURRENT device (the kernels size
+ * their persistent grids by its SM count).  Arguments are those of the call:
+ *   SV_OP_TREE_ATTENTION:     B, T, Hq, Hkv, D       (V ignored)
+ *   SV_OP_VERIFY_CHAIN:       B, N (as T_or_N), V, dtype as Hq (0 f32 / 1 bf16)
+ *   SV_OP_VERIFY_TREE_GREEDY: B, T, V, dtype as Hq
+ * Returns 0 for invalid arguments.
+ */
+size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, int D);
+
+/*
+ * Verification attention over a prefix KV cache plus each node's ancestors.
+ * Source: "Chapitre 9 -- Décodage spéculatif" §9.1 (one forward over the
+ * prefix concatenated with the N candidates yields N+1 distributions, and
+ * stays memory-bound) and §9.2 (EAGLE-2's draft tree verified in one
+ * attention pass with a custom mask); "Parallel Decoding" glossary, Medusa
+ * "Tree attention" and "L'attention en arbre" (all branches scored in one
+ * pass under a mask encoding the tree).
+ *
+ * For sequence b, node t, query head h (KV head h / (Hq/Hkv)):
+ *   out[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . k_j) v_j
+ * over cache slots j in [0, L_b) and L_b + i for every node i on the
+ * root->t path (t included), L_b = prefix_lens[b].
+ *
+ *   q           bf16 [B, T, Hq, D]
+ *   k_cache     bf16 [B, Hkv, S_max, D]; v_cache likewise.  Slots at and
+ *               beyond L_b + T are never read (they may hold anything).
+ *   prefix_lens int32 [B]; each 0 <= L_b and L_b + T <= S_max (else
+ *               seq_status[b] = SV_ERR_BAD_INPUT and the sequence is skipped)
+ *   parents     int32 [B, T] parent array, or NULL for a chain (causal mask)
+ *   scale       > 0 and finite, normally 1/sqrt(D)
+ *   out         bf16 [B, T, Hq, D]
+ *   seq_status  int32 [B] or NULL
+ *   workspace   >= sv_workspace_size(SV_OP_TREE_ATTENTION, ...) bytes
+ * Supported: D = 128, 1 <= T <= 64, Hq % Hkv == 0, Hq/Hkv * T <= 512,
+ * B <= 4096, B * Hkv * S_max < 2^31.
+ */
+sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *prefix_lens, const int32_t *parents,
+                            int B, int T, int Hq, int Hkv, int D, int S_max, float scale,
+                            void *out, int32_t *seq_status,
+                            void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/*
+ * Stochastic chain acceptance over the full vocabulary.
+ * Source: "Chapitre 9 -- Décodage spéculatif" §9.1: the target yields a
+ * distribution at each of the N+1 positions; draft token x drawn from q is
+ * accepted with probability min(1, p(x)/q(x)), else a token is drawn from the
+ * normalised residual (p-q)+; the output is then distributed exactly as the
+ * target's own sampling.  The bonus token after N acceptances is drawn from
+ * the (N+1)-th distribution.
+ *
+ * Per sequence b, with p_i = softmax(target[b,i,:]), q_i = softmax(draft[b,i,:]):
+ *   accept_i  <=>  u_accept[b,i] * q_i(x_i) < p_i(x_i)
+ *   a = first i with !accept_i, or N
+ *   r = max(0, p_a - q_a) if a < N (p_a itself if that sums to 0), r = p_N if a = N
+ *   y = min{k : r_0 + ... + r_k > u_sample[b] * sum(r)}   (index order)
+ *   accepted_len[b] = a; out_tokens[b,:] = x_0..x_{a-1}, y, then -1 padding
+ *
+ *   target_logits  [B, N+1, V] of `dtype`, already temperature-scaled
+ *   draft_logits   [B, N, V] of `dtype`
+ *   draft_tokens   int32 [B, N]
+ *   u_accept       f32 [B, N] uniforms in [0, 1); u_sample f32 [B]
+ *   accepted_len   int32 [B];  out_tokens int32 [B, N+1]
+ *   probs_out      f32 [B, N, 2] = (p_i(x_i), q_i(x_i)) for every i, or NULL
+ * Supported: 1 <= N <= 63, 1 <= V < 2^30, dtype SV_F32 or SV_BF16.
+ * Launches two kernels (statistics + decisions, then the residual draw).
+ */
+sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, sv_dtype dtype,
+                          const int32_t *draft_tokens, const float *u_accept,
+                          const float *u_sample, int B, int N, int V,
+                          int32_t *accepted_len, int32_t *out_tokens, float *probs_out,
+                          int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                          sv_stream_t stream);
+
+/*
+ * Greedy longest-agreeing-path acceptance on a draft tree.
+ * Source: "Parallel Decoding" glossary, "L'attention en arbre": the longest
+ * accepted path becomes the generated sequence; "Chapitre 9" §9.1: the
+ * longest prefix on which the candidates agree with the target is kept and
+ * at the divergence the engine takes the target's own choice.
+ *
+ *   am_i = argmax_v target[b,i,v] (smallest v among equal maxima)
+ *   ok_0 = 1; ok_i = ok_{parent_i} and node_tokens[b,i] == am_{parent_i}
+ *   d* = deepest ok node (smallest index among equal depths)
+ *   accepted_len[b] = depth(d*); path_nodes[b,:] = root..d* then -1;
+ *   out_tokens[b,:] = node_tokens of path nodes 1..depth, am_{d*}, then -1
+ *
+ *   target_logits [B, T, V] of `dtype`; node_tokens, parents int32 [B, T]
+ *   accepted_len int32 [B]; path_nodes, out_tokens int32 [B, T]
+ * Supported: 1 <= T <= 1024, 1 <= V < 2^30.
+ */
+sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
+                                const int32_t *node_tokens, const int32_t *parents,
+                                int B, int T, int V, int32_t *accepted_len,
+                                int32_t *path_nodes, int32_t *out_tokens, int32_t *seq_status,
+                                void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/*
+ * Compaction of the accepted path's rows in the enlarged KV cache.
+ * Source: "Parallel Decoding" glossary, "Limites du parallel decoding" (tree
+ * attention needs a KV cache enlarged for the branches); "Chapitre 9" §9.1
+ * (the accepted prefix is kept and the rest discarded).
+ *
+ * In place, per sequence b with a = accepted_len[b] >= 0, L = prefix_lens[b]:
+ *   for d = 0..a, every KV head: row L + d <- row L + path[d]
+ *   new_kv_lens[b] = L + a + 1
+ * path[d] = path_nodes[b * path_stride + d], or d when path_nodes is NULL
+ * (a chain: nothing moves).  A path must start at 0 and increase strictly
+ * (so path[d] >= d) with L + path[a] < S_max, a < path_stride and
+ * L + a + 1 <= S_max; otherwise nothing moves, new_kv_lens[b] = L and
+ * seq_status[b] = SV_ERR_BAD_INPUT.  A negative accepted_len (an upstream
+ * error) leaves the sequence untouched with new_kv_lens[b] = L.
+ * new_kv_lens may alias prefix_lens.
+ *
+ *   k_cache, v_cache bf16 [B, Hkv, S_max, D]
+ * Supported: D % 8 == 0, D <= 256.
+ */
+sv_status sv_compact_kv(void *k_cache, void *v_cache, const int32_t *prefix_lens,
+                        int32_t *new_kv_lens, const int32_t *path_nodes, int path_stride,
+                        const int32_t *accepted_len, int B, int Hkv, int D, int S_max,
+                        int32_t *seq_status, sv_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *sv_status_string(sv_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,230 @@
+"""Thin Python binding of libspecverify (ctypes).
+
+Each function has the name of the C entry point it calls and only marshals
+arguments: torch tensors on the GPU become device pointers, the current torch
+stream becomes the launch stream, and a non-OK status becomes an exception.
+Every step of the computation runs in the library's CUDA kernels; there is no
+fallback.  If the library is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+SV_OK = 0
+SV_ERR_INVALID_ARG = 1
+SV_ERR_WORKSPACE = 2
+SV_ERR_UNSUPPORTED = 3
+SV_ERR_CUDA = 4
+SV_ERR_TIMEOUT = 5
+SV_ERR_BAD_INPUT = 6
+
+SV_F32 = 0
+SV_BF16 = 1
+
+SV_OP_TREE_ATTENTION = 0
+SV_OP_VERIFY_CHAIN = 1
+SV_OP_VERIFY_TREE_GREEDY = 2
+
+EXPORTS = ("sv_workspace_size", "sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy",
+           "sv_compact_kv", "sv_status_string", "sv_version")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB_PATH):
+            raise ImportError(f"libspecverify.so is not built ({_build.LIB_PATH}); "
+                              "run __graft_entry__.build() or python -m "
+                              "speculative_decoding_verification_81_gb300.build")
+        L = ctypes.CDLL(_build.LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.sv_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        L.sv_workspace_size.restype = Z
+        L.sv_tree_attention.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P, Z, P]
+        L.sv_verify_chain.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+        L.sv_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, Z, P]
+        L.sv_compact_kv.argtypes = [P, P, P, P, P, I, P, I, I, I, I, P, P]
+        for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv"):
+            getattr(L, fn).restype = I
+        L.sv_status_string.argtypes = [I]
+        L.sv_status_string.restype = ctypes.c_char_p
+        L.sv_version.argtypes = []
+        L.sv_version.restype = I
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().sv_status_string(int(status)).decode()
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != SV_OK:
+        raise SpecVerifyError(fn, rc)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _req(t, name, dtype=None, ndim=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def sv_workspace_size(op: int, B: int, T_or_N: int, V: int = 0, Hq: int = 0, Hkv: int = 0,
+                      D: int = 0) -> int:
+    return int(lib().sv_workspace_size(op, B, T_or_N, V, Hq, Hkv, D))
+
+
+_ws_cache: dict = {}
+
+
+def workspace(op: int, B: int, T_or_N: int, V: int = 0, Hq: int = 0, Hkv: int = 0, D: int = 0,
+              device=None) -> torch.Tensor:
+    """A zero-filled workspace for one call shape, cached per (shape, device).
+    Calls sharing it must not overlap on the GPU."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    key = (op, B, T_or_N, V, Hq, Hkv, D, str(device))
+    ws = _ws_cache.get(key)
+    if ws is None:
+        n = sv_workspace_size(op, B, T_or_N, V, Hq, Hkv, D)
+        if n == 0:
+            raise SpecVerifyError("sv_workspace_size", SV_ERR_UNSUPPORTED)
+        ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def sv_tree_attention(q, k_cache, v_cache, prefix_lens, parents=None, scale=None, out=None,
+                      seq_status=None, ws=None, stream=None):
+    """q [B,T,Hq,D] bf16; k_cache/v_cache [B,Hkv,S_max,D] bf16; prefix_lens [B] int32;
+    parents [B,T] int32 or None (chain).  Returns out [B,T,Hq,D] bf16."""
+    _req(q, "q", torch.bfloat16, 4)
+    _req(k_cache, "k_cache", torch.bfloat16, 4)
+    _req(v_cache, "v_cache", torch.bfloat16, 4)
+    _req(prefix_lens, "prefix_lens", torch.int32, 1)
+    B, T, Hq, D = q.shape
+    _, Hkv, S_max, _ = k_cache.shape
+    if parents is not None:
+        _req(parents, "parents", torch.int32, 2)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
+    rc = lib().sv_tree_attention(_p(q), _p(k_cache), _p(v_cache), _p(prefix_lens), _p(parents),
+                                 B, T, Hq, Hkv, D, S_max, float(scale), _p(out), _p(seq_status),
+                                 _p(ws), ws.numel(), _stream(stream))
+    _check("sv_tree_attention", rc)
+    return out
+
+
+def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sample,
+                    accepted_len=None, out_tokens=None, probs_out=None, seq_status=None, ws=None,
+                    stream=None):
+    """target [B,N+1,V], draft [B,N,V] (bf16 or f32); draft_tokens [B,N] int32;
+    u_accept [B,N] f32; u_sample [B] f32.  Returns (accepted_len [B], out_tokens [B,N+1])."""
+    _req(target_logits, "target_logits", None, 3)
+    _req(draft_logits, "draft_logits", target_logits.dtype, 3)
+    _req(draft_tokens, "draft_tokens", torch.int32, 2)
+    _req(u_accept, "u_accept", torch.float32, 2)
+    _req(u_sample, "u_sample", torch.float32, 1)
+    dt = _dtype_code(target_logits)
+    B, N1, V = target_logits.shape
+    N = N1 - 1
+    dev = target_logits.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(SV_OP_VERIFY_CHAIN, B, N, V, dt, 0, 0, dev)
+    rc = lib().sv_verify_chain(_p(target_logits), _p(draft_logits), dt, _p(draft_tokens),
+                               _p(u_accept), _p(u_sample), B, N, V, _p(accepted_len),
+                               _p(out_tokens), _p(probs_out), _p(seq_status), _p(ws), ws.numel(),
+                               _stream(stream))
+    _check("sv_verify_chain", rc)
+    return accepted_len, out_tokens
+
+
+def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None, path_nodes=None,
+                          out_tokens=None, seq_status=None, ws=None, stream=None):
+    """target [B,T,V] (bf16 or f32); node_tokens, parents [B,T] int32.
+    Returns (accepted_len [B], path_nodes [B,T], out_tokens [B,T])."""
+    _req(target_logits, "target_logits", None, 3)
+    _req(node_tokens, "node_tokens", torch.int32, 2)
+    _req(parents, "parents", torch.int32, 2)
+    dt = _dtype_code(target_logits)
+    B, T, V = target_logits.shape
+    dev = target_logits.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if path_nodes is None:
+        path_nodes = torch.empty(B, T, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, T, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(SV_OP_VERIFY_TREE_GREEDY, B, T, V, dt, 0, 0, dev)
+    rc = lib().sv_verify_tree_greedy(_p(target_logits), dt, _p(node_tokens), _p(parents), B, T, V,
+                                     _p(accepted_len), _p(path_nodes), _p(out_tokens),
+                                     _p(seq_status), _p(ws), ws.numel(), _stream(stream))
+    _check("sv_verify_tree_greedy", rc)
+    return accepted_len, path_nodes, out_tokens
+
+
+def sv_compact_kv(k_cache, v_cache, prefix_lens, accepted_len, path_nodes=None, new_kv_lens=None,
+                  seq_status=None, stream=None):
+    """In place on k_cache/v_cache [B,Hkv,S_max,D] bf16.  path_nodes [B,P] int32 or
+    None (chain).  Returns new_kv_lens [B] int32 (may be prefix_lens itself)."""
+    _req(k_cache, "k_cache", torch.bfloat16, 4)
+    _req(v_cache, "v_cache", torch.bfloat16, 4)
+    _req(prefix_lens, "prefix_lens", torch.int32, 1)
+    _req(accepted_len, "accepted_len", torch.int32, 1)
+    B, Hkv, S_max, D = k_cache.shape
+    stride = 0
+    if path_nodes is not None:
+        _req(path_nodes, "path_nodes", torch.int32, 2)
+        stride = path_nodes.shape[1]
+    if new_kv_lens is None:
+        new_kv_lens = torch.empty_like(prefix_lens)
+    rc = lib().sv_compact_kv(_p(k_cache), _p(v_cache), _p(prefix_lens), _p(new_kv_lens),
+                             _p(path_nodes), stride, _p(accepted_len), B, Hkv, D, S_max,
+                             _p(seq_status), _stream(stream))
+    _check("sv_compact_kv", rc)
+    return new_kv_lens

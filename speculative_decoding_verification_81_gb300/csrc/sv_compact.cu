@@ -1,0 +1,98 @@
+// sv_compact.cu -- compaction of the accepted path's K/V rows.
+//
+// The enlarged KV cache of tree verification holds one row per candidate
+// node ("Parallel Decoding" glossary, "Limites du parallel decoding"); after
+// acceptance the accepted path becomes the committed continuation and the
+// rest is discarded ("Chapitre 9 -- Décodage spéculatif" §9.1).  Row
+// L + path[d] moves to row L + d for d = 0..a, in place.
+//
+// One CTA per sequence.  The path increases strictly, so path[d] >= d: a
+// destination row can only be the source of an EARLIER path position.  Rows
+// are therefore moved in batches of increasing d, each batch read completely
+// into shared memory before any of it is written back.
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+
+constexpr int kCT = 256;
+constexpr int kCompactBatch = 32;  // path rows per staged batch
+constexpr int kMaxRowVecs = 32;    // 16-byte words per row: D <= 256 bf16
+
+__global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
+    __shared__ uint4 stage[2][kCompactBatch * kMaxRowVecs];
+    __shared__ int s_src[kCompactBatch];
+    const int b = blockIdx.x;
+    const int L = a.prefix_lens[b];
+    const int acc = a.accepted_len[b];
+    const int vpr = a.D / 8;  // 16-byte words per row
+    __syncthreads();          // every thread has read L before new_kv_lens (may alias) is written
+
+    if (acc < 0) {
+        if (threadIdx.x == 0) {
+            a.new_kv_lens[b] = L;
+            if (a.seq_status) a.seq_status[b] = SV_OK;
+        }
+        return;
+    }
+    int bad = (L < 0) || ((long long)L + acc + 1 > a.S_max) ||
+              (a.path_nodes != nullptr && acc >= a.path_stride);
+    if (!bad && a.path_nodes) {
+        const int32_t *path = a.path_nodes + (size_t)b * a.path_stride;
+        for (int d = threadIdx.x; d <= acc; d += kCT) {
+            const int src = path[d];
+            if (d == 0 ? src != 0 : src <= path[d - 1]) bad = 1;
+            if ((long long)L + src >= a.S_max) bad = 1;
+        }
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (threadIdx.x == 0) {
+            a.new_kv_lens[b] = L;
+            if (a.seq_status) a.seq_status[b] = SV_ERR_BAD_INPUT;
+        }
+        return;
+    }
+    if (a.path_nodes) {
+        const int32_t *path = a.path_nodes + (size_t)b * a.path_stride;
+        for (int h = 0; h < a.Hkv; ++h) {
+            const size_t head = ((size_t)b * a.Hkv + h) * (size_t)a.S_max;
+            uint4 *kc = static_cast<uint4 *>(a.k) + head * vpr;
+            uint4 *vc = static_cast<uint4 *>(a.v) + head * vpr;
+            for (int d0 = 1; d0 <= acc; d0 += kCompactBatch) {  // d = 0 is the root: never moves
+                const int nb = min(kCompactBatch, acc + 1 - d0);
+                if (threadIdx.x < nb) s_src[threadIdx.x] = path[d0 + threadIdx.x];
+                __syncthreads();
+                for (int i = threadIdx.x; i < nb * vpr; i += kCT) {
+                    const int r = i / vpr, w = i - r * vpr;
+                    const int src = s_src[r];
+                    if (src != d0 + r) {
+                        stage[0][i] = kc[(size_t)(L + src) * vpr + w];
+                        stage[1][i] = vc[(size_t)(L + src) * vpr + w];
+                    }
+                }
+                __syncthreads();
+                for (int i = threadIdx.x; i < nb * vpr; i += kCT) {
+                    const int r = i / vpr, w = i - r * vpr;
+                    if (s_src[r] != d0 + r) {
+                        kc[(size_t)(L + d0 + r) * vpr + w] = stage[0][i];
+                        vc[(size_t)(L + d0 + r) * vpr + w] = stage[1][i];
+                    }
+                }
+                __syncthreads();
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        a.new_kv_lens[b] = L + acc + 1;
+        if (a.seq_status) a.seq_status[b] = SV_OK;
+    }
+}
+
+sv_status launch_compact_kv(const CompactArgs &a, cudaStream_t st) {
+    if (a.D % 8 != 0 || a.D / 8 > kMaxRowVecs) return SV_ERR_UNSUPPORTED;
+    compact_kv_kernel<<<a.B, kCT, 0, st>>>(a);
+    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv

@@ -1,0 +1,131 @@
+// sv_internal.h -- host-side plans and launchers shared between the C ABI
+// (sv_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/specverify.h"
+
+namespace sv {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- vocabulary pass
+
+// Per (row, chunk) statistics written by the streaming pass.
+struct RowPartial {
+    float m;     // max of logit * log2(e) over the chunk
+    float s;     // sum of exp2(logit * log2(e) - m)
+    float best;  // largest logit (argmax mode)
+    int idx;     // its index, smallest among equal maxima; INT_MAX if none
+};
+
+// Per-sequence result of the chain decision stage, consumed by the residual draw.
+struct ChainDecision {
+    int a;       // first rejected position, N if all accepted, -1 if the sequence is invalid
+    int pad;
+    float ms_t;  // target row a: max * log2(e) and normaliser
+    float s_t;
+    float ms_d;  // draft row a (unused when a == N)
+    float s_d;
+    float pad2[2];
+};
+
+struct VocabPlan {
+    int rows_per_seq;     // 2N+1 (chain) or T (tree)
+    int nchunks;          // streaming chunks per row
+    int chunk_elems;
+    int res_chunks;       // residual-draw chunks per sequence (chain only)
+    int res_chunk_elems;
+    bool vec;             // rows are 16-byte aligned: vector loads
+    size_t off_counters;  // 2*B ints
+    size_t off_partials;  // B * rows_per_seq * nchunks RowPartial
+    size_t off_dec;       // B ChainDecision
+    size_t off_chunktot;  // B * res_chunks float2
+    size_t bytes;
+};
+
+VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype);
+
+struct ChainArgs {
+    const void *target;
+    const void *draft;
+    const int32_t *tokens;
+    const float *u_accept;
+    const float *u_sample;
+    int B, N, V;
+    int32_t *accepted_len;
+    int32_t *out_tokens;
+    float *probs;
+    int32_t *seq_status;
+};
+
+struct TreeArgs {
+    const void *target;
+    const int32_t *tokens;
+    const int32_t *parents;
+    int B, T, V;
+    int32_t *accepted_len;
+    int32_t *path_nodes;
+    int32_t *out_tokens;
+    int32_t *seq_status;
+};
+
+sv_status launch_verify_chain(const ChainArgs &args, int dtype, const VocabPlan &plan, void *ws,
+                              cudaStream_t stream);
+sv_status launch_verify_tree_greedy(const TreeArgs &args, int dtype, const VocabPlan &plan,
+                                    void *ws, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+
+struct AttnPlan {
+    int nwc;          // consumer (math) warps per CTA, 16 query rows each
+    int stages;       // K/V pipeline depth
+    int rows_per_rg;  // query rows per row group = 16 * nwc
+    int rg;           // row groups per (sequence, KV head)
+    int grid;         // persistent CTAs
+    int smem;         // dynamic shared memory bytes
+    size_t off_counters;
+    size_t off_part_o;
+    size_t off_part_ml;
+    size_t bytes;
+};
+
+sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan);
+
+struct AttnArgs {
+    const void *q;
+    const void *k;
+    const void *v;
+    const int32_t *prefix_lens;
+    const int32_t *parents;
+    int B, T, Hq, Hkv, D, S_max;
+    float scale;
+    void *out;
+    int32_t *seq_status;
+};
+
+sv_status launch_tree_attention(const AttnArgs &args, const AttnPlan &plan, void *ws,
+                                cudaStream_t stream);
+
+// ---------------------------------------------------------------- compaction
+
+struct CompactArgs {
+    void *k;
+    void *v;
+    const int32_t *prefix_lens;
+    int32_t *new_kv_lens;
+    const int32_t *path_nodes;
+    int path_stride;
+    const int32_t *accepted_len;
+    int B, Hkv, D, S_max;
+    int32_t *seq_status;
+};
+
+sv_status launch_compact_kv(const CompactArgs &args, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace sv

@@ -1,0 +1,743 @@
+// sv_vocab.cu -- full-vocabulary passes of the verification step.
+//
+// Chain (stochastic) acceptance, "Chapitre 9 -- Décodage spéculatif" §9.1:
+//   kernel 1  streams every target/draft logits row once, chunk by chunk
+//             (one CTA per (row, chunk), 16-byte non-temporal loads), and
+//             keeps per chunk the max and the sum of exp2 in the log2 domain.
+//             The last CTA to finish a sequence merges its chunks, evaluates
+//             p_i(x_i), q_i(x_i), the decisions u*q < p and the first
+//             rejection a.
+//   kernel 2  draws the final token: per chunk of the row pair at a it sums
+//             the weights r = max(0, p_a - q_a) (or p_N for the bonus); the
+//             last CTA per sequence locates u*S in the chunk prefix, then in
+//             the thread prefix of that chunk, then element by element.
+// Greedy tree acceptance ("Parallel Decoding" glossary, "L'attention en
+// arbre"; §9.1): the same streaming pass in argmax mode, and the last CTA per
+// sequence walks the tree.
+//
+// No CTA ever waits for another: the "last CTA" is whoever brings a
+// per-sequence arrival counter to its final value; it resets the counter.
+#include <climits>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+
+constexpr int kVT = 256;                   // threads per vocabulary CTA
+constexpr int kVWarps = kVT / 32;
+constexpr int kLoadsPerThread = 8;         // 16-byte loads per thread per streaming item
+constexpr int kResLoadsPerThread = 4;      // 16-byte loads per thread per row in the residual draw
+constexpr int kMaxChainN = 63;
+constexpr int kMaxTreeT = 1024;
+constexpr int kMaxResChunks = 256;
+constexpr double kLog2eD = 1.4426950408889634073599;
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<uint16_t> {  // bf16
+    static constexpr int kPerVec = 8;
+    __device__ static float at(const uint16_t *p, size_t i) { return bf16_to_f32(__ldg(p + i)); }
+    __device__ static void unpack(const uint4 &v, float (&x)[8]) {
+        x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
+        x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+        x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
+        x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+    }
+};
+
+template <>
+struct Elem<float> {
+    static constexpr int kPerVec = 4;
+    __device__ static float at(const float *p, size_t i) { return __ldg(p + i); }
+    __device__ static void unpack(const uint4 &v, float (&x)[4]) {
+        x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+    }
+};
+
+// ---------------------------------------------------------------- streaming chunk
+
+// Statistics of row[begin, end) over the CTA: per thread the max (scaled by
+// log2 e) and the sum of exp2 (STATS), or the first maximum and its index
+// (ARGMAX).  Vector loads are laid out so that consecutive threads read
+// consecutive 16-byte words; `begin` is a multiple of the vector width.
+template <typename T, bool VEC, bool ARGMAX>
+__device__ __forceinline__ void chunk_thread_stats(const T *row, int begin, int end, float &m,
+                                                   float &s, float &best, int &idx) {
+    constexpr int PV = Elem<T>::kPerVec;
+    const int tid = threadIdx.x;
+    m = kNegInf;
+    s = 0.f;
+    best = kNegInf;
+    idx = INT_MAX;
+    if (VEC) {
+        const int nvec = (end - begin) / PV;
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + begin);
+        uint4 buf[kLoadsPerThread];
+#pragma unroll
+        for (int k = 0; k < kLoadsPerThread; ++k) {
+            const int vi = k * kVT + tid;
+            if (vi < nvec) buf[k] = ldg_stream(src + vi);
+        }
+        const int tail = begin + nvec * PV + tid;  // < PV leftover elements
+        const bool has_tail = tid < (end - begin) - nvec * PV;
+        const float xt = has_tail ? Elem<T>::at(row, tail) : kNegInf;
+        if (ARGMAX) {
+#pragma unroll
+            for (int k = 0; k < kLoadsPerThread; ++k) {
+                const int vi = k * kVT + tid;
+                if (vi < nvec) {
+                    float x[PV];
+                    Elem<T>::unpack(buf[k], x);
+#pragma unroll
+                    for (int j = 0; j < PV; ++j)
+                        if (x[j] > best) {
+                            best = x[j];
+                            idx = begin + vi * PV + j;
+                        }
+                }
+            }
+            if (has_tail && xt > best) {
+                best = xt;
+                idx = tail;
+            }
+        } else {
+            float vmax = xt;
+#pragma unroll
+            for (int k = 0; k < kLoadsPerThread; ++k) {
+                const int vi = k * kVT + tid;
+                if (vi < nvec) {
+                    float x[PV];
+                    Elem<T>::unpack(buf[k], x);
+#pragma unroll
+                    for (int j = 0; j < PV; ++j) vmax = fmaxf(vmax, x[j]);
+                }
+            }
+            m = vmax * kLog2e;
+            if (m != kNegInf) {
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < kLoadsPerThread; ++k) {
+                    const int vi = k * kVT + tid;
+                    if (vi < nvec) {
+                        float x[PV];
+                        Elem<T>::unpack(buf[k], x);
+                        float e[PV];
+#pragma unroll
+                        for (int j = 0; j < PV; ++j) e[j] = exp2f(fmaf(x[j], kLog2e, -m));
+                        // pairwise within the vector, then into the running sum
+#pragma unroll
+                        for (int w = 1; w < PV; w *= 2)
+#pragma unroll
+                            for (int j = 0; j < PV; j += 2 * w) e[j] += e[j + w];
+                        acc += e[0];
+                    }
+                }
+                if (has_tail) acc += exp2f(fmaf(xt, kLog2e, -m));
+                s = acc;
+            }
+        }
+    } else {
+        // unaligned rows: scalar loads, element e = begin + k*kVT + tid
+        const int n = end - begin;
+        if (ARGMAX) {
+            for (int e = tid; e < n; e += kVT) {
+                const float x = Elem<T>::at(row, begin + e);
+                if (x > best) {
+                    best = x;
+                    idx = begin + e;
+                }
+            }
+        } else {
+            float vmax = kNegInf;
+            for (int e = tid; e < n; e += kVT) vmax = fmaxf(vmax, Elem<T>::at(row, begin + e));
+            m = vmax * kLog2e;
+            if (m != kNegInf) {
+                float acc = 0.f;
+                for (int e = tid; e < n; e += kVT)
+                    acc += exp2f(fmaf(Elem<T>::at(row, begin + e), kLog2e, -m));
+                s = acc;
+            }
+        }
+    }
+}
+
+// Reduce per-thread statistics over the CTA; the result is valid in thread 0.
+template <bool ARGMAX>
+__device__ __forceinline__ void cta_reduce_stats(float &m, float &s, float &best, int &idx,
+                                                 float4 *scratch /* [kVWarps] */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (ARGMAX) {
+            const float b2 = __shfl_xor_sync(0xffffffffu, best, off);
+            const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+            merge_argmax(best, idx, b2, i2);
+        } else {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+            merge_ms(m, s, m2, s2);
+        }
+    }
+    if (lane == 0) scratch[warp] = make_float4(m, s, best, __int_as_float(idx));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kVWarps; ++w) {
+            const float4 o = scratch[w];
+            if (ARGMAX)
+                merge_argmax(best, idx, o.z, __float_as_int(o.w));
+            else
+                merge_ms(m, s, o.x, o.y);
+        }
+    }
+}
+
+// Merge the chunk partials of one row, one warp; result valid in lane 0.
+template <bool ARGMAX>
+__device__ __forceinline__ RowPartial warp_merge_row(const RowPartial *parts, int nchunks) {
+    const int lane = threadIdx.x & 31;
+    float m = kNegInf, s = 0.f, best = kNegInf;
+    int idx = INT_MAX;
+    for (int c = lane; c < nchunks; c += 32) {
+        const float4 p = __ldcg(reinterpret_cast<const float4 *>(parts + c));
+        if (ARGMAX)
+            merge_argmax(best, idx, p.z, __float_as_int(p.w));
+        else
+            merge_ms(m, s, p.x, p.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (ARGMAX) {
+            const float b2 = __shfl_xor_sync(0xffffffffu, best, off);
+            const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+            merge_argmax(best, idx, b2, i2);
+        } else {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+            merge_ms(m, s, m2, s2);
+        }
+    }
+    RowPartial r;
+    r.m = m;
+    r.s = s;
+    r.best = best;
+    r.idx = idx;
+    return r;
+}
+
+struct WsView {
+    int *counters;  // [B] streaming pass, [B] residual draw
+    RowPartial *partials;
+    ChainDecision *dec;
+    float2 *chunktot;
+};
+
+__host__ __device__ inline WsView ws_view(void *ws, const VocabPlan &p, int B) {
+    char *base = static_cast<char *>(ws);
+    WsView v;
+    v.counters = reinterpret_cast<int *>(base + p.off_counters);
+    v.partials = reinterpret_cast<RowPartial *>(base + p.off_partials);
+    v.dec = reinterpret_cast<ChainDecision *>(base + p.off_dec);
+    v.chunktot = reinterpret_cast<float2 *>(base + p.off_chunktot);
+    (void)B;
+    return v;
+}
+
+// ---------------------------------------------------------------- chain: kernel 1
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kVT) chain_stats_kernel(ChainArgs a, VocabPlan p, WsView w) {
+    __shared__ float4 scratch[kVWarps];
+    __shared__ int s_last;
+    __shared__ float sm_m[2 * kMaxChainN + 1], sm_s[2 * kMaxChainN + 1];
+    __shared__ int sm_rej[kMaxChainN];
+    __shared__ int sm_bad;
+
+    const int R = 2 * a.N + 1;
+    const int per_seq = R * p.nchunks;
+    const int item = blockIdx.x;
+    const int b = item / per_seq;
+    const int rem = item - b * per_seq;
+    const int r = rem / p.nchunks;
+    const int c = rem - r * p.nchunks;
+    const T *row = r <= a.N
+                       ? static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + r) * a.V
+                       : static_cast<const T *>(a.draft) + ((size_t)b * a.N + (r - a.N - 1)) * a.V;
+    const int begin = c * p.chunk_elems;
+    const int end = min(a.V, begin + p.chunk_elems);
+
+    float m, s, best;
+    int idx;
+    chunk_thread_stats<T, VEC, false>(row, begin, end, m, s, best, idx);
+    cta_reduce_stats<false>(m, s, best, idx, scratch);
+    if (threadIdx.x == 0) {
+        RowPartial out;
+        out.m = m;
+        out.s = s;
+        out.best = 0.f;
+        out.idx = 0;
+        w.partials[item] = out;
+        __threadfence();
+        const int old = atomicAdd(&w.counters[b], 1);
+        s_last = (old == per_seq - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- this CTA is the last of sequence b: merge, decide
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int rr = warp; rr < R; rr += kVWarps) {
+        const RowPartial rp =
+            warp_merge_row<false>(w.partials + (size_t)b * per_seq + (size_t)rr * p.nchunks,
+                                  p.nchunks);
+        if (lane == 0) {
+            sm_m[rr] = rp.m;
+            sm_s[rr] = rp.s;
+        }
+    }
+    if (threadIdx.x == 0) sm_bad = 0;
+    __syncthreads();
+    if (threadIdx.x < R) {
+        const float mm = sm_m[threadIdx.x], ss = sm_s[threadIdx.x];
+        if (!(isfinite(mm) && isfinite(ss) && ss > 0.f)) atomicOr(&sm_bad, 1);
+    }
+    if (threadIdx.x < a.N) {
+        const int i = threadIdx.x;
+        const int x = a.tokens[(size_t)b * a.N + i];
+        float pp = 0.f, qq = 0.f;
+        bool rej = true;
+        if (x < 0 || x >= a.V) {
+            atomicOr(&sm_bad, 1);
+        } else {
+            const T *trow = static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
+            const T *drow = static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V;
+            const double lt = Elem<T>::at(trow, x), ld = Elem<T>::at(drow, x);
+            pp = static_cast<float>(exp2(lt * kLog2eD - (double)sm_m[i]) / (double)sm_s[i]);
+            qq = static_cast<float>(exp2(ld * kLog2eD - (double)sm_m[a.N + 1 + i]) /
+                                    (double)sm_s[a.N + 1 + i]);
+            const float u = a.u_accept[(size_t)b * a.N + i];
+            rej = !(u * qq < pp);
+        }
+        sm_rej[i] = rej;
+        if (a.probs) {
+            a.probs[((size_t)b * a.N + i) * 2 + 0] = pp;
+            a.probs[((size_t)b * a.N + i) * 2 + 1] = qq;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = a.N;
+        for (int i = 0; i < a.N; ++i)
+            if (sm_rej[i]) {
+                acc = i;
+                break;
+            }
+        ChainDecision d;
+        d.pad = 0;
+        d.pad2[0] = d.pad2[1] = 0.f;
+        if (sm_bad) {
+            d.a = -1;
+            d.ms_t = d.s_t = d.ms_d = d.s_d = 0.f;
+            a.accepted_len[b] = -1;
+            if (a.seq_status) a.seq_status[b] = SV_ERR_BAD_INPUT;
+        } else {
+            d.a = acc;
+            d.ms_t = sm_m[acc];
+            d.s_t = sm_s[acc];
+            d.ms_d = acc < a.N ? sm_m[a.N + 1 + acc] : 0.f;
+            d.s_d = acc < a.N ? sm_s[a.N + 1 + acc] : 0.f;
+            a.accepted_len[b] = acc;
+            if (a.seq_status) a.seq_status[b] = SV_OK;
+        }
+        w.dec[b] = d;
+        w.counters[b] = 0;  // ready for the next call
+        s_last = sm_bad ? -1 : acc;
+    }
+    __syncthreads();
+    const int acc = s_last;
+    for (int i = threadIdx.x; i <= a.N; i += kVT) {
+        int v = -1;
+        if (acc >= 0 && i < acc) v = a.tokens[(size_t)b * a.N + i];
+        if (acc < 0 || i != acc) a.out_tokens[(size_t)b * (a.N + 1) + i] = v;
+    }
+}
+
+// ---------------------------------------------------------------- chain: kernel 2
+
+// Weights of this thread's contiguous elements [e0, e0 + n) and their
+// sequential sums.  mode 0: r = max(0, p - q); mode 1: r = p.  Written with
+// explicitly rounded operations so that recomputing gives identical bits.
+template <typename T>
+struct ResidualRow {
+    const T *trow;
+    const T *drow;
+    float ms_t, inv_t, ms_d, inv_d;
+
+    __device__ __forceinline__ float p_at(float lt) const {
+        return __fmul_rn(exp2f(__fmaf_rn(lt, kLog2e, -ms_t)), inv_t);
+    }
+    __device__ __forceinline__ float weight(float lt, float ld, int mode) const {
+        const float pt = p_at(lt);
+        if (mode) return pt;
+        const float pq = __fmul_rn(exp2f(__fmaf_rn(ld, kLog2e, -ms_d)), inv_d);
+        return fmaxf(__fsub_rn(pt, pq), 0.f);
+    }
+};
+
+constexpr int kResElemsPerThread(int per_vec) { return kResLoadsPerThread * per_vec; }
+
+template <typename T, bool VEC>
+__device__ __forceinline__ void load_res_elems(const T *row, int e0, int n,
+                                               float (&x)[kResLoadsPerThread * Elem<T>::kPerVec]) {
+    constexpr int PV = Elem<T>::kPerVec;
+    constexpr int EPT = kResLoadsPerThread * PV;
+    if (VEC && n == EPT) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + e0);
+#pragma unroll
+        for (int k = 0; k < kResLoadsPerThread; ++k) {
+            const uint4 v = __ldg(src + k);
+            float t[PV];
+            Elem<T>::unpack(v, t);
+#pragma unroll
+            for (int j = 0; j < PV; ++j) x[k * PV + j] = t[j];
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) x[j] = j < n ? Elem<T>::at(row, e0 + j) : 0.f;
+    }
+}
+
+// Inclusive prefix over the CTA's 256 per-thread values with a fixed order
+// of additions (warp shuffle scan, then warp totals added in warp order);
+// `total` gets the sum of all 256, bitwise equal to thread 255's result.
+__device__ __forceinline__ float cta_incl_scan(float v, float &total, float *wsum /* [8] */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v = __fadd_rn(v, t);
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    float base = 0.f, tot = 0.f;
+    for (int w = 0; w < kVWarps; ++w) {
+        if (w == warp) base = tot;
+        tot = __fadd_rn(tot, wsum[w]);
+    }
+    __syncthreads();
+    total = tot;
+    return warp == 0 ? v : __fadd_rn(base, v);
+}
+
+template <typename T, bool VEC>
+__device__ __forceinline__ void thread_weight_sums(const ResidualRow<T> &rw, int mode, int e0,
+                                                   int n, float &sr, float &sp,
+                                                   float (&wgt)[kResLoadsPerThread *
+                                                                Elem<T>::kPerVec]) {
+    constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
+    float xt[EPT], xd[EPT];
+    load_res_elems<T, VEC>(rw.trow, e0, n, xt);
+    if (mode == 0) load_res_elems<T, VEC>(rw.drow, e0, n, xd);
+    sr = 0.f;
+    sp = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        float wj = 0.f, pj = 0.f;
+        if (j < n) {
+            pj = rw.p_at(xt[j]);
+            wj = mode == 0 ? rw.weight(xt[j], xd[j], 0) : pj;
+        }
+        wgt[j] = wj;
+        sr = __fadd_rn(sr, wj);
+        sp = __fadd_rn(sp, pj);
+    }
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
+    constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
+    __shared__ float wsum[kVWarps];
+    __shared__ float2 s_tot[kMaxResChunks];
+    __shared__ float s_prefix[kVT];
+    __shared__ int s_last, s_cstar, s_mode, s_fallback, s_pick_min, s_pick_max;
+    __shared__ float s_base, s_theta;
+
+    const int b = blockIdx.x / p.res_chunks;
+    const int c = blockIdx.x - b * p.res_chunks;
+    const ChainDecision d = w.dec[b];
+    if (d.a < 0) return;  // invalid sequence: kernel 1 already wrote -1s
+
+    ResidualRow<T> rw;
+    rw.trow = static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + d.a) * a.V;
+    rw.drow = d.a < a.N ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + d.a) * a.V
+                        : rw.trow;
+    rw.ms_t = d.ms_t;
+    rw.inv_t = __frcp_rn(d.s_t);
+    rw.ms_d = d.ms_d;
+    rw.inv_d = d.a < a.N ? __frcp_rn(d.s_d) : 0.f;
+    const int mode0 = d.a < a.N ? 0 : 1;
+
+    const int cbeg = c * p.res_chunk_elems;
+    const int e0 = cbeg + threadIdx.x * EPT;
+    const int n = max(0, min(EPT, a.V - e0));
+    float wgt[EPT];
+    float sr, sp;
+    thread_weight_sums<T, VEC>(rw, mode0, e0, n, sr, sp, wgt);
+    float tot_r, tot_p;
+    cta_incl_scan(sr, tot_r, wsum);
+    cta_incl_scan(sp, tot_p, wsum);
+    if (threadIdx.x == 0) {
+        w.chunktot[(size_t)b * p.res_chunks + c] = make_float2(tot_r, tot_p);
+        __threadfence();
+        const int old = atomicAdd(&w.counters[a.B + b], 1);
+        s_last = (old == p.res_chunks - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA of sequence b: locate u * S in the chunk prefix
+    for (int i = threadIdx.x; i < p.res_chunks; i += kVT)
+        s_tot[i] = __ldcg(w.chunktot + (size_t)b * p.res_chunks + i);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float S = 0.f;
+        for (int i = 0; i < p.res_chunks; ++i) S = __fadd_rn(S, s_tot[i].x);
+        int mode = mode0;
+        if (!(S > 0.f)) {  // residual vanished: draw from p_a instead
+            mode = 1;
+            S = 0.f;
+            for (int i = 0; i < p.res_chunks; ++i) S = __fadd_rn(S, s_tot[i].y);
+        }
+        const float theta = __fmul_rn(a.u_sample[b], S);
+        float base = 0.f;
+        int cstar = -1;
+        for (int i = 0; i < p.res_chunks; ++i) {
+            const float t = mode == 0 ? s_tot[i].x : s_tot[i].y;
+            const float nb = __fadd_rn(base, t);
+            if (nb > theta) {
+                cstar = i;
+                break;
+            }
+            base = nb;
+        }
+        int fallback = 0;
+        if (cstar < 0) {  // rounding left no crossing: last chunk with weight
+            fallback = 1;
+            cstar = 0;
+            for (int i = p.res_chunks - 1; i >= 0; --i)
+                if ((mode == 0 ? s_tot[i].x : s_tot[i].y) > 0.f) {
+                    cstar = i;
+                    break;
+                }
+        }
+        s_cstar = cstar;
+        s_mode = mode;
+        s_fallback = fallback;
+        s_base = base;
+        s_theta = theta;
+        s_pick_min = kVT;
+        s_pick_max = -1;
+    }
+    __syncthreads();
+    const int cstar = s_cstar, mode = s_mode;
+    const float base = s_base, theta = s_theta;
+    const int f0 = cstar * p.res_chunk_elems + threadIdx.x * EPT;
+    const int fn = max(0, min(EPT, a.V - f0));
+    thread_weight_sums<T, VEC>(rw, mode, f0, fn, sr, sp, wgt);
+    const float own = mode == 0 ? sr : sp;
+    float total;
+    const float incl = cta_incl_scan(own, total, wsum);
+    s_prefix[threadIdx.x] = incl;
+    if (!s_fallback) {
+        // first thread whose inclusive prefix passes u * S
+        if (__fadd_rn(base, incl) > theta) atomicMin(&s_pick_min, (int)threadIdx.x);
+    } else {
+        // last thread holding any weight
+        if (own > 0.f) atomicMax(&s_pick_max, (int)threadIdx.x);
+    }
+    __syncthreads();
+    int pick = s_fallback ? s_pick_max : s_pick_min;
+    if (pick < 0 || pick >= kVT) pick = kVT - 1;
+    if ((int)threadIdx.x == pick) {
+        int y = -1;
+        if (!s_fallback) {
+            float acc = __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f);
+            for (int j = 0; j < fn; ++j) {
+                acc = __fadd_rn(acc, wgt[j]);
+                if (acc > theta) {
+                    y = f0 + j;
+                    break;
+                }
+            }
+        }
+        if (y < 0)
+            for (int j = fn - 1; j >= 0; --j)
+                if (wgt[j] > 0.f) {
+                    y = f0 + j;
+                    break;
+                }
+        if (y < 0) y = max(f0, 0);
+        a.out_tokens[(size_t)b * (a.N + 1) + d.a] = y;
+        w.counters[a.B + b] = 0;  // ready for the next call
+    }
+}
+
+// ---------------------------------------------------------------- tree greedy
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p, WsView w) {
+    __shared__ float4 scratch[kVWarps];
+    __shared__ int s_last;
+    __shared__ int sm_am[kMaxTreeT], sm_par[kMaxTreeT], sm_tok[kMaxTreeT], sm_depth[kMaxTreeT],
+        sm_path[kMaxTreeT];
+    __shared__ unsigned char sm_ok[kMaxTreeT];
+    __shared__ int s_best, s_bad;
+
+    const int per_seq = a.T * p.nchunks;
+    const int item = blockIdx.x;
+    const int b = item / per_seq;
+    const int rem = item - b * per_seq;
+    const int r = rem / p.nchunks;
+    const int c = rem - r * p.nchunks;
+    const T *row = static_cast<const T *>(a.target) + ((size_t)b * a.T + r) * a.V;
+    const int begin = c * p.chunk_elems;
+    const int end = min(a.V, begin + p.chunk_elems);
+
+    float m, s, best;
+    int idx;
+    chunk_thread_stats<T, VEC, true>(row, begin, end, m, s, best, idx);
+    cta_reduce_stats<true>(m, s, best, idx, scratch);
+    if (threadIdx.x == 0) {
+        RowPartial out;
+        out.m = 0.f;
+        out.s = 0.f;
+        out.best = best;
+        out.idx = idx;
+        w.partials[item] = out;
+        __threadfence();
+        const int old = atomicAdd(&w.counters[b], 1);
+        s_last = (old == per_seq - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA of sequence b: argmax per node, then the greedy walk
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int rr = warp; rr < a.T; rr += kVWarps) {
+        const RowPartial rp = warp_merge_row<true>(
+            w.partials + (size_t)b * per_seq + (size_t)rr * p.nchunks, p.nchunks);
+        if (lane == 0) sm_am[rr] = rp.idx == INT_MAX ? -1 : rp.idx;
+    }
+    for (int i = threadIdx.x; i < a.T; i += kVT) {
+        sm_par[i] = a.parents[(size_t)b * a.T + i];
+        sm_tok[i] = a.tokens[(size_t)b * a.T + i];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int bad = sm_par[0] != -1;
+        for (int i = 1; i < a.T && !bad; ++i)
+            if (sm_par[i] < 0 || sm_par[i] >= i || sm_tok[i] < 0 || sm_tok[i] >= a.V) bad = 1;
+        int bst = 0;
+        if (!bad) {
+            sm_ok[0] = 1;
+            sm_depth[0] = 0;
+            for (int i = 1; i < a.T; ++i) {
+                const int pa = sm_par[i];
+                sm_ok[i] = sm_ok[pa] && sm_tok[i] == sm_am[pa];
+                sm_depth[i] = sm_depth[pa] + 1;
+                if (sm_ok[i] && sm_depth[i] > sm_depth[bst]) bst = i;
+            }
+            int node = bst;
+            for (int dd = sm_depth[bst]; dd >= 0; --dd) {
+                sm_path[dd] = node;
+                node = sm_par[node];
+            }
+        }
+        s_bad = bad;
+        s_best = bst;
+        a.accepted_len[b] = bad ? -1 : sm_depth[bst];
+        if (a.seq_status) a.seq_status[b] = bad ? SV_ERR_BAD_INPUT : SV_OK;
+        w.counters[b] = 0;  // ready for the next call
+    }
+    __syncthreads();
+    const int depth = s_bad ? -1 : sm_depth[s_best];
+    for (int i = threadIdx.x; i < a.T; i += kVT) {
+        int pn = -1, ot = -1;
+        if (i <= depth) {
+            pn = sm_path[i];
+            ot = i < depth ? sm_tok[sm_path[i + 1]] : sm_am[s_best];
+        }
+        a.path_nodes[(size_t)b * a.T + i] = pn;
+        a.out_tokens[(size_t)b * a.T + i] = ot;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
+    VocabPlan p{};
+    const int esz = dtype == SV_F32 ? 4 : 2;
+    const int per_vec = 16 / esz;
+    p.rows_per_seq = chain ? 2 * rows_or_n + 1 : rows_or_n;
+    p.chunk_elems = kVT * kLoadsPerThread * per_vec;
+    p.nchunks = (V + p.chunk_elems - 1) / p.chunk_elems;
+    p.res_chunk_elems = kVT * kResLoadsPerThread * per_vec;
+    p.res_chunks = chain ? (V + p.res_chunk_elems - 1) / p.res_chunk_elems : 0;
+    p.vec = ((size_t)V * esz) % 16 == 0;
+    size_t off = 0;
+    p.off_counters = off;
+    off = align_up(off + sizeof(int) * 2 * (size_t)B, 256);
+    p.off_partials = off;
+    off = align_up(off + sizeof(RowPartial) * (size_t)B * p.rows_per_seq * p.nchunks, 256);
+    p.off_dec = off;
+    off = align_up(off + (chain ? sizeof(ChainDecision) * (size_t)B : 0), 256);
+    p.off_chunktot = off;
+    off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks : 0), 256);
+    p.bytes = off;
+    return p;
+}
+
+template <typename T, bool VEC>
+static void launch_chain_t(const ChainArgs &a, const VocabPlan &p, const WsView &w, cudaStream_t st) {
+    const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
+    chain_stats_kernel<T, VEC><<<items, kVT, 0, st>>>(a, p, w);
+    const unsigned res = (unsigned)((size_t)a.B * p.res_chunks);
+    chain_residual_kernel<T, VEC><<<res, kVT, 0, st>>>(a, p, w);
+}
+
+sv_status launch_verify_chain(const ChainArgs &a, int dtype, const VocabPlan &p, void *ws,
+                              cudaStream_t st) {
+    if (a.N > kMaxChainN || p.res_chunks > kMaxResChunks) return SV_ERR_UNSUPPORTED;
+    const WsView w = ws_view(ws, p, a.B);
+    if (dtype == SV_BF16) {
+        if (p.vec) launch_chain_t<uint16_t, true>(a, p, w, st);
+        else launch_chain_t<uint16_t, false>(a, p, w, st);
+    } else {
+        if (p.vec) launch_chain_t<float, true>(a, p, w, st);
+        else launch_chain_t<float, false>(a, p, w, st);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status launch_verify_tree_greedy(const TreeArgs &a, int dtype, const VocabPlan &p, void *ws,
+                                    cudaStream_t st) {
+    if (a.T > kMaxTreeT) return SV_ERR_UNSUPPORTED;
+    const WsView w = ws_view(ws, p, a.B);
+    const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
+    if (dtype == SV_BF16) {
+        if (p.vec) tree_stats_kernel<uint16_t, true><<<items, kVT, 0, st>>>(a, p, w);
+        else tree_stats_kernel<uint16_t, false><<<items, kVT, 0, st>>>(a, p, w);
+    } else {
+        if (p.vec) tree_stats_kernel<float, true><<<items, kVT, 0, st>>>(a, p, w);
+        else tree_stats_kernel<float, false><<<items, kVT, 0, st>>>(a, p, w);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv

@@ -1,0 +1,128 @@
+"""The C ABI without a GPU: the library loads, exports every entry point its
+header declares, and rejects invalid host arguments with the documented
+status before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_81_gb300 as sv
+from speculative_decoding_verification_81_gb300 import build as svbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    svbuild.build()
+    return sv.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    assert set(names) == set(sv.api.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+        assert isinstance(getattr(L, name), ctypes._CFuncPtr)
+
+
+def test_version_and_status_strings(L):
+    assert L.sv_version() >= 100
+    for code in range(7):
+        assert sv.status_string(code).startswith("SV_")
+    assert "unknown" in sv.status_string(99)
+
+
+FAKE = ctypes.c_void_p(0x10000)        # never dereferenced: every case fails validation first
+MISALIGNED = ctypes.c_void_p(0x10004)
+
+
+def _chain(L, **kw):
+    a = dict(t=FAKE, d=FAKE, dt=sv.SV_BF16, tok=FAKE, ua=FAKE, us=FAKE, B=2, N=4, V=1000,
+             acc=FAKE, out=FAKE, probs=None, st=None, ws=None, wsb=0)
+    a.update(kw)
+    return L.sv_verify_chain(a["t"], a["d"], a["dt"], a["tok"], a["ua"], a["us"], a["B"], a["N"],
+                             a["V"], a["acc"], a["out"], a["probs"], a["st"], a["ws"], a["wsb"],
+                             None)
+
+
+def test_verify_chain_host_validation(L):
+    assert _chain(L, t=None) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, out=None) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, B=0) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, N=0) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, V=-3) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, dt=7) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, t=MISALIGNED) == sv.SV_ERR_INVALID_ARG
+    assert _chain(L, N=64) == sv.SV_ERR_UNSUPPORTED
+    assert _chain(L) == sv.SV_ERR_WORKSPACE  # no workspace
+    need = L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 2, 4, 1000, sv.SV_BF16, 0, 0)
+    assert need > 0
+    assert _chain(L, ws=FAKE, wsb=need - 1) == sv.SV_ERR_WORKSPACE
+    assert _chain(L, ws=MISALIGNED, wsb=need) == sv.SV_ERR_WORKSPACE
+
+
+def test_verify_tree_host_validation(L):
+    def call(**kw):
+        a = dict(t=FAKE, dt=sv.SV_BF16, tok=FAKE, par=FAKE, B=2, T=26, V=32000, acc=FAKE,
+                 path=FAKE, out=FAKE, ws=None, wsb=0)
+        a.update(kw)
+        return L.sv_verify_tree_greedy(a["t"], a["dt"], a["tok"], a["par"], a["B"], a["T"], a["V"],
+                                       a["acc"], a["path"], a["out"], None, a["ws"], a["wsb"], None)
+    assert call(par=None) == sv.SV_ERR_INVALID_ARG
+    assert call(T=0) == sv.SV_ERR_INVALID_ARG
+    assert call(T=1025) == sv.SV_ERR_UNSUPPORTED
+    assert call() == sv.SV_ERR_WORKSPACE
+    need = L.sv_workspace_size(sv.SV_OP_VERIFY_TREE_GREEDY, 2, 26, 32000, sv.SV_BF16, 0, 0)
+    assert call(ws=FAKE, wsb=need - 16) == sv.SV_ERR_WORKSPACE
+
+
+def test_attention_host_validation(L):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, pl=FAKE, par=None, B=2, T=9, Hq=32, Hkv=8, D=128,
+                 S=4160, scale=0.088, out=FAKE)
+        a.update(kw)
+        return L.sv_tree_attention(a["q"], a["k"], a["v"], a["pl"], a["par"], a["B"], a["T"],
+                                   a["Hq"], a["Hkv"], a["D"], a["S"], a["scale"], a["out"], None,
+                                   None, 0, None)
+    assert call(q=None) == sv.SV_ERR_INVALID_ARG
+    assert call(pl=None) == sv.SV_ERR_INVALID_ARG
+    assert call(Hq=30) == sv.SV_ERR_INVALID_ARG      # Hq % Hkv
+    assert call(S=8) == sv.SV_ERR_INVALID_ARG        # S_max < T
+    assert call(scale=0.0) == sv.SV_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == sv.SV_ERR_INVALID_ARG
+    assert call(k=MISALIGNED) == sv.SV_ERR_INVALID_ARG
+    assert call(B=1 << 20, Hkv=8, Hq=32, S=4160) == sv.SV_ERR_UNSUPPORTED  # rows >= 2^31
+
+
+def test_compact_host_validation(L):
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, pl=FAKE, nl=FAKE, path=None, stride=0, acc=FAKE, B=2, Hkv=8,
+                 D=128, S=4160)
+        a.update(kw)
+        return L.sv_compact_kv(a["k"], a["v"], a["pl"], a["nl"], a["path"], a["stride"], a["acc"],
+                               a["B"], a["Hkv"], a["D"], a["S"], None, None)
+    assert call(acc=None) == sv.SV_ERR_INVALID_ARG
+    assert call(path=FAKE, stride=0) == sv.SV_ERR_INVALID_ARG
+    assert call(D=100) == sv.SV_ERR_UNSUPPORTED
+    assert call(D=512) == sv.SV_ERR_UNSUPPORTED
+    assert call(v=MISALIGNED) == sv.SV_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_scale_with_shape(L):
+    a = L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 32, 8, 128256, sv.SV_BF16, 0, 0)
+    b = L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 64, 8, 128256, sv.SV_BF16, 0, 0)
+    assert 0 < a < b
+    assert L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 0, 8, 1000, sv.SV_BF16, 0, 0) == 0
+    assert L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 1, 8, 1000, 5, 0, 0) == 0
