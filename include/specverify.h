@@ -17,7 +17,8 @@
  *
  * Conventions shared by every call:
  *   - Every array argument is DEVICE memory owned by the caller.  The
- *     library allocates nothing and keeps no state between calls.  Calls
+ *     library allocates nothing and, apart from the fixed scratch array of
+ *     sv_verify_chain_noalloc, keeps no state between calls.  Calls
  *     that need scratch take a caller-provided workspace; its size comes
  *     from sv_workspace_size() and it must be zero-filled once before its
  *     first use (every call leaves its counters at zero again).
@@ -193,6 +194,40 @@ sv_status sv_compact_kv(void *k_cache, void *v_cache, const int32_t *prefix_lens
                         int32_t *new_kv_lens, const int32_t *path_nodes, int path_stride,
                         const int32_t *accepted_len, int B, int Hkv, int D, int S_max,
                         int32_t *seq_status, sv_stream_t stream);
+
+/*
+ * Chain acceptance with no caller workspace.  There is no counterpart of this
+ * call in the source pages: it is a deployment convenience.
+ *
+ * Some callers cannot hand the library a workspace because they cannot
+ * allocate device memory where they call it: a plugin whose host has given
+ * all device memory to its own pool and exposes no allocator, a real-time
+ * loop that must not take the device-wide synchronisation cudaMalloc and
+ * cudaFree imply, or code that runs while a stream capture is open.  This
+ * call computes exactly what sv_verify_chain computes (same arguments, same
+ * outputs, same kernels) but keeps its scratch in a fixed array inside the
+ * library, SV_NOALLOC_SCRATCH_BYTES long.  Every GPU that loads the library
+ * holds that array until the process exits.
+ *
+ * - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture on the device.
+ * - All calls share the one array, which keeps the last call's contents; each
+ *   call clears the part that must start at zero (cudaMemsetAsync on
+ *   `stream`).  Calls that overlap on the GPU (other streams, other host
+ *   threads) race on the array and give wrong results: serialise them.
+ * - Returns SV_ERR_WORKSPACE, launching nothing, when the scratch this shape
+ *   needs (sv_workspace_size(SV_OP_VERIFY_CHAIN, ...)) exceeds
+ *   SV_NOALLOC_SCRATCH_BYTES; the other errors are those of sv_verify_chain.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+sv_status sv_verify_chain_noalloc(const void *target_logits, const void *draft_logits,
+                                  sv_dtype dtype, const int32_t *draft_tokens,
+                                  const float *u_accept, const float *u_sample, int B, int N,
+                                  int V, int32_t *accepted_len, int32_t *out_tokens,
+                                  float *probs_out, int32_t *seq_status, sv_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *sv_status_string(sv_status status);

@@ -32,7 +32,10 @@ SV_OP_VERIFY_CHAIN = 1
 SV_OP_VERIFY_TREE_GREEDY = 2
 
 EXPORTS = ("sv_workspace_size", "sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy",
-           "sv_compact_kv", "sv_status_string", "sv_version")
+           "sv_compact_kv", "sv_status_string", "sv_version", "sv_verify_chain_noalloc")
+
+# Length of the fixed scratch array behind sv_verify_chain_noalloc.
+SV_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class SpecVerifyError(RuntimeError):
@@ -59,8 +62,10 @@ def lib() -> ctypes.CDLL:
         L.sv_tree_attention.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P, Z, P]
         L.sv_verify_chain.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
         L.sv_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, Z, P]
+        L.sv_verify_chain_noalloc.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         L.sv_compact_kv.argtypes = [P, P, P, P, P, I, P, I, I, I, I, P, P]
-        for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv"):
+        for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
+                   "sv_verify_chain_noalloc"):
             getattr(L, fn).restype = I
         L.sv_status_string.argtypes = [I]
         L.sv_status_string.restype = ctypes.c_char_p
@@ -228,3 +233,25 @@ def sv_compact_kv(k_cache, v_cache, prefix_lens, accepted_len, path_nodes=None, 
                              _p(seq_status), _stream(stream))
     _check("sv_compact_kv", rc)
     return new_kv_lens
+
+
+def sv_verify_chain_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_sample,
+                            accepted_len, out_tokens, probs_out=None, seq_status=None, stream=None):
+    """sv_verify_chain without a workspace, for callers that cannot allocate
+    device memory at the call site; the outputs must be passed in.  Uses the
+    library's fixed scratch array: calls must not overlap on the GPU."""
+    _req(target_logits, "target_logits", None, 3)
+    _req(draft_logits, "draft_logits", target_logits.dtype, 3)
+    _req(draft_tokens, "draft_tokens", torch.int32, 2)
+    _req(u_accept, "u_accept", torch.float32, 2)
+    _req(u_sample, "u_sample", torch.float32, 1)
+    _req(accepted_len, "accepted_len", torch.int32, 1)
+    _req(out_tokens, "out_tokens", torch.int32, 2)
+    dt = _dtype_code(target_logits)
+    B, N1, V = target_logits.shape
+    rc = lib().sv_verify_chain_noalloc(_p(target_logits), _p(draft_logits), dt, _p(draft_tokens),
+                                       _p(u_accept), _p(u_sample), B, N1 - 1, V,
+                                       _p(accepted_len), _p(out_tokens), _p(probs_out),
+                                       _p(seq_status), _stream(stream))
+    _check("sv_verify_chain_noalloc", rc)
+    return accepted_len, out_tokens
