@@ -19,7 +19,8 @@
 //   * Per CTA: one producer warp issues 2-D TMA copies (128-byte swizzle) of
 //     K and V tiles into a multi-stage mbarrier ring; NWC consumer warps own
 //     16 query rows each and run QK^T and PV with mma.sync m16n8k16 (bf16 in,
-//     f32 accumulate), online softmax in the log2 domain.
+//     f32 accumulate), online softmax in the log2 domain whose running max
+//     moves only when it grows by more than 2^8.
 //   * The ancestor mask is a 64-bit set per row built by walking the parent
 //     array; it only applies to the tile(s) holding the T new rows.
 //   * Every wait is bounded; on expiry the CTA records SV_ERR_TIMEOUT for the
@@ -105,6 +106,12 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses) {
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
+
+// The running row max only moves when a tile's max exceeds it by more than
+// this many log2 units; until then probabilities stay below 2^8 relative to
+// the stale max, which the f32 sums and the bf16 P carry without loss, and
+// the final division by the row sum is unchanged.
+constexpr float kRescaleThreshold = 8.0f;
 
 template <int NWC, int STAGES>
 __global__ void __launch_bounds__((NWC + 1) * 32)
@@ -239,6 +246,21 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     uint32_t cbar_uses = 0;
     const int rsub = lane >> 2;  // row within the 8-row half
     const int csub = lane & 3;
+    const float sc = p.scale_log2;
+    // Per-thread offsets of this lane's ldmatrix row inside a stage.  With the
+    // 128-byte swizzle the 16-byte chunk index is XORed with (row mod 8), and
+    // row mod 8 is lane mod 8 for every row this lane addresses.
+    uint32_t offK[4], offV[4];
+    {
+        const int l7 = lane & 7;
+        const int kb = (lane >> 4) & 1, cb = (lane >> 3) & 1;  // K: +8 keys, +1 chunk
+        const int vb = (lane >> 3) & 1, vc = (lane >> 4) & 1;  // V: +8 keys, +1 chunk
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+            offK[qd] = (uint32_t)((kb * 8 + l7) * 128 + (((2 * qd + cb) ^ l7) << 4));
+            offV[qd] = (uint32_t)(2 * kBox + (vb * 8 + l7) * 128 + (((2 * qd + vc) ^ l7) << 4));
+        }
+    }
 
     Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
     long long k = 0;
@@ -304,8 +326,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
             if (p.seq_status) p.seq_status[cur.b] = SV_ERR_TIMEOUT;
             break;
         }
-        const uint32_t sK = base_u32 + s * kStageBytes;
-        const uint32_t sV = sK + 2 * kBox;
+        const uint32_t st_base = base_u32 + s * kStageBytes;
         const int kbase = cur.tile * kBK;
 
         // ---- S = Q K^T over 64 keys
@@ -314,36 +335,35 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         for (int j = 0; j < 8; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t rowK = st_base + offK[kk & 3] + (kk >> 2) * kBox;
 #pragma unroll
             for (int jp = 0; jp < 4; ++jp) {
-                const int key = 16 * jp + ((lane >> 4) & 1) * 8 + (lane & 7);
-                const int cg = 2 * kk + ((lane >> 3) & 1);
-                const uint32_t addr =
-                    sK + (cg >> 3) * kBox + key * 128 + ((((cg & 7) ^ (key & 7))) << 4);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(addr, b0, b1, b2, b3);
+                ldsm_x4(rowK + jp * 2048, b0, b1, b2, b3);
                 mma_bf16_16816(sacc[2 * jp], qf[kk], b0, b1);
                 mma_bf16_16816(sacc[2 * jp + 1], qf[kk], b2, b3);
             }
         }
 
-        // ---- scale, mask, online softmax (log2 domain)
-        const bool need_mask = kbase + kBK > L;
-        float mx0 = kNegInf, mx1 = kNegInf;
+        // ---- mask: only tiles reaching the new rows or the sequence end
+        if (kbase + kBK > L) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 8; ++j) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float x = sacc[j][e] * p.scale_log2;
-                if (need_mask) {
+                for (int e = 0; e < 4; ++e) {
                     const int key = kbase + 8 * j + 2 * csub + (e & 1);
                     const uint64_t anc = e < 2 ? anc0 : anc1;
                     const bool allowed =
                         key < L || (key < kv_end && ((anc >> (unsigned)(key - L)) & 1ull));
-                    x = allowed ? x : kNegInf;
+                    if (!allowed) sacc[j][e] = kNegInf;
                 }
-                sacc[j][e] = x;
             }
+        }
+
+        // ---- online softmax in the log2 domain, max moved lazily
+        float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
             mx0 = fmaxf(mx0, fmaxf(sacc[j][0], sacc[j][1]));
             mx1 = fmaxf(mx1, fmaxf(sacc[j][2], sacc[j][3]));
         }
@@ -351,31 +371,34 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float alpha0 = mn0 == kNegInf ? 1.f : exp2f(m0 - mn0);
-        const float alpha1 = mn1 == kNegInf ? 1.f : exp2f(m1 - mn1);
-        const float base0 = mn0 == kNegInf ? 0.f : mn0;
-        const float base1 = mn1 == kNegInf ? 0.f : mn1;
-        float rs0 = 0.f, rs1 = 0.f;
+        const float c0 = mx0 * sc, c1 = mx1 * sc;   // raw max -> log2 units
+        const bool up0 = c0 > m0 + kRescaleThreshold;
+        const bool up1 = c1 > m1 + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+            const float a0 = up0 ? ex2_approx(m0 - c0) : 1.f;
+            const float a1 = up1 ? ex2_approx(m1 - c1) : 1.f;
+            if (up0) m0 = c0;
+            if (up1) m1 = c1;
+            l0 *= a0;
+            l1 *= a1;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                o[j][0] *= a0;
+                o[j][1] *= a0;
+                o[j][2] *= a1;
+                o[j][3] *= a1;
+            }
+        }
+        const float nb0 = m0 == kNegInf ? 0.f : -m0;
+        const float nb1 = m1 == kNegInf ? 0.f : -m1;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            sacc[j][0] = exp2f(sacc[j][0] - base0);
-            sacc[j][1] = exp2f(sacc[j][1] - base0);
-            sacc[j][2] = exp2f(sacc[j][2] - base1);
-            sacc[j][3] = exp2f(sacc[j][3] - base1);
-            rs0 += sacc[j][0] + sacc[j][1];
-            rs1 += sacc[j][2] + sacc[j][3];
-        }
-        l0 = l0 * alpha0 + rs0;
-        l1 = l1 * alpha1 + rs1;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            o[j][0] *= alpha0;
-            o[j][1] *= alpha0;
-            o[j][2] *= alpha1;
-            o[j][3] *= alpha1;
+            sacc[j][0] = ex2_approx(fmaf(sacc[j][0], sc, nb0));
+            sacc[j][1] = ex2_approx(fmaf(sacc[j][1], sc, nb0));
+            sacc[j][2] = ex2_approx(fmaf(sacc[j][2], sc, nb1));
+            sacc[j][3] = ex2_approx(fmaf(sacc[j][3], sc, nb1));
+            l0 += sacc[j][0] + sacc[j][1];
+            l1 += sacc[j][2] + sacc[j][3];
         }
 
         // ---- O += P V over 64 keys
@@ -387,26 +410,29 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
             pa[1] = pack_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
             pa[2] = pack_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
             pa[3] = pack_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-            if (need_vfix) {  // rows past the sequence's last slot may hold anything
-                const int k0 = kbase + 16 * kk + 2 * csub;
-                mlo = (k0 < kv_end ? 0x0000ffffu : 0u) | (k0 + 1 < kv_end ? 0xffff0000u : 0u);
-                mhi = (k0 + 8 < kv_end ? 0x0000ffffu : 0u) | (k0 + 9 < kv_end ? 0xffff0000u : 0u);
-            }
+            if (!need_vfix) {
 #pragma unroll
-            for (int djp = 0; djp < 8; ++djp) {
-                const int key = 16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int cg = 2 * djp + ((lane >> 4) & 1);
-                const uint32_t addr =
-                    sV + (cg >> 3) * kBox + key * 128 + ((((cg & 7) ^ (key & 7))) << 4);
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(addr, v0, v1, v2, v3);
-                v0 &= mlo;
-                v2 &= mlo;
-                v1 &= mhi;
-                v3 &= mhi;
-                mma_bf16_16816(o[2 * djp], pa, v0, v1);
-                mma_bf16_16816(o[2 * djp + 1], pa, v2, v3);
+                for (int djp = 0; djp < 8; ++djp) {
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(st_base + offV[djp & 3] + (djp >> 2) * kBox + kk * 2048, v0, v1,
+                              v2, v3);
+                    mma_bf16_16816(o[2 * djp], pa, v0, v1);
+                    mma_bf16_16816(o[2 * djp + 1], pa, v2, v3);
+                }
+            } else {  // rows past the sequence's last slot may hold anything: zero them
+                const int k0 = kbase + 16 * kk + 2 * csub;
+                const uint32_t mlo =
+                    (k0 < kv_end ? 0x0000ffffu : 0u) | (k0 + 1 < kv_end ? 0xffff0000u : 0u);
+                const uint32_t mhi =
+                    (k0 + 8 < kv_end ? 0x0000ffffu : 0u) | (k0 + 9 < kv_end ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int djp = 0; djp < 8; ++djp) {
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(st_base + offV[djp & 3] + (djp >> 2) * kBox + kk * 2048, v0, v1,
+                              v2, v3);
+                    mma_bf16_16816(o[2 * djp], pa, v0 & mlo, v1 & mhi);
+                    mma_bf16_16816(o[2 * djp + 1], pa, v2 & mlo, v3 & mhi);
+                }
             }
         }
         __syncwarp();
@@ -586,6 +612,40 @@ int device_sm_count() {
     return n;
 }
 
+// Occupancy of one kernel on one device for a given shared-memory size,
+// queried once and cached: these runtime queries cost far more than a launch
+// and would otherwise make short calls host-bound.
+static int cached_occupancy(const KernelEntry &e, int smem, int *sms_out) {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int smem, occ, sms;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int ncache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ncache; ++i)
+        if (cache[i].dev == dev && cache[i].fn == e.fn && cache[i].smem == smem) {
+            *sms_out = cache[i].sms;
+            return cache[i].occ;
+        }
+    const int threads = (e.nwc + 1) * 32;
+    if (cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes(e.stages, e.nwc, kMaxB)) != cudaSuccess)
+        return -1;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e.fn, threads, smem) != cudaSuccess)
+        return -1;
+    const int sms = device_sm_count();
+    if (sms <= 0 || occ < 1) return -1;
+    if (ncache < 64) cache[ncache++] = Entry{dev, e.fn, smem, occ, sms};
+    *sms_out = sms;
+    return occ;
+}
+
 sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
     if (D != kD || T > kMaxT || B > kMaxB) return SV_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
@@ -605,16 +665,9 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
     pl.rows_per_rg = 16 * pl.nwc;
     pl.rg = rg;
     pl.smem = smem_bytes(pl.stages, pl.nwc, B);
-    const int threads = (pl.nwc + 1) * 32;
-    if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes(pl.stages, pl.nwc, kMaxB)) != cudaSuccess)
-        return SV_ERR_CUDA;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e->fn, threads, pl.smem) != cudaSuccess ||
-        occ < 1)
-        return SV_ERR_CUDA;
-    const int sms = device_sm_count();
-    if (sms <= 0) return SV_ERR_CUDA;
+    int sms = 0;
+    const int occ = cached_occupancy(*e, pl.smem, &sms);
+    if (occ < 1) return SV_ERR_CUDA;
     pl.grid = sms * occ;
     size_t off = 0;
     pl.off_counters = off;

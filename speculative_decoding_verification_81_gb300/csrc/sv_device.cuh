@@ -32,6 +32,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// 2^x by the MUFU approximation (PTX ex2.approx.ftz.f32): relative error of
+// a few ulp, results below 2^-126 flushed to zero.  Deterministic, so
+// recomputing a value gives the same bits.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- memory
 
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {

@@ -127,7 +127,7 @@ __device__ __forceinline__ void chunk_thread_stats(const T *row, int begin, int 
                         Elem<T>::unpack(buf[k], x);
                         float e[PV];
 #pragma unroll
-                        for (int j = 0; j < PV; ++j) e[j] = exp2f(fmaf(x[j], kLog2e, -m));
+                        for (int j = 0; j < PV; ++j) e[j] = ex2_approx(fmaf(x[j], kLog2e, -m));
                         // pairwise within the vector, then into the running sum
 #pragma unroll
                         for (int w = 1; w < PV; w *= 2)
@@ -136,7 +136,7 @@ __device__ __forceinline__ void chunk_thread_stats(const T *row, int begin, int 
                         acc += e[0];
                     }
                 }
-                if (has_tail) acc += exp2f(fmaf(xt, kLog2e, -m));
+                if (has_tail) acc += ex2_approx(fmaf(xt, kLog2e, -m));
                 s = acc;
             }
         }
@@ -158,7 +158,7 @@ __device__ __forceinline__ void chunk_thread_stats(const T *row, int begin, int 
             if (m != kNegInf) {
                 float acc = 0.f;
                 for (int e = tid; e < n; e += kVT)
-                    acc += exp2f(fmaf(Elem<T>::at(row, begin + e), kLog2e, -m));
+                    acc += ex2_approx(fmaf(Elem<T>::at(row, begin + e), kLog2e, -m));
                 s = acc;
             }
         }
@@ -378,12 +378,12 @@ struct ResidualRow {
     float ms_t, inv_t, ms_d, inv_d;
 
     __device__ __forceinline__ float p_at(float lt) const {
-        return __fmul_rn(exp2f(__fmaf_rn(lt, kLog2e, -ms_t)), inv_t);
+        return __fmul_rn(ex2_approx(__fmaf_rn(lt, kLog2e, -ms_t)), inv_t);
     }
     __device__ __forceinline__ float weight(float lt, float ld, int mode) const {
         const float pt = p_at(lt);
         if (mode) return pt;
-        const float pq = __fmul_rn(exp2f(__fmaf_rn(ld, kLog2e, -ms_d)), inv_d);
+        const float pq = __fmul_rn(ex2_approx(__fmaf_rn(ld, kLog2e, -ms_d)), inv_d);
         return fmaxf(__fsub_rn(pt, pq), 0.f);
     }
 };
