@@ -1,0 +1,160 @@
+// sv_attn_common.cuh -- pieces shared by the attention kernels: tile
+// geometry, kernel parameters, the balanced split of (sequence, KV head, row
+// group, tile) units over persistent CTAs, and the per-call prologue.
+#pragma once
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+constexpr int kD = 128;
+constexpr int kBK = 64;                   // keys per tile
+constexpr int kBox = kBK * 64 * 2;        // one 64-key x 64-dim bf16 TMA box: 8 KB
+constexpr int kStageBytes = 4 * kBox;     // K lo/hi + V lo/hi: 32 KB
+constexpr int kMaxB = 4096;
+constexpr int kMaxT = 64;
+
+struct AttnKParams {
+    const uint16_t *q;
+    uint16_t *out;
+    const int32_t *prefix_lens;
+    const int32_t *parents;
+    int32_t *seq_status;
+    int B, T, Hq, Hkv, G, S_max, M, RG, rows_per_rg;
+    float scale_log2;
+    float *part_o;   // [grid][2][rows_per_rg][kD]: unnormalised O of split pairs
+    float *part_ml;  // [grid][2][rows_per_rg][2]: (max in log2 units, row sum)
+    int4 *pair_info; // [B][Hkv][RG]: (first CTA, CTAs sharing the pair, first CTA's slot, 0)
+};
+
+// Position in the unit list: sequence, (kv head * RG + row group), tile.
+struct Cursor {
+    int b, pr, tile, n;
+};
+
+__device__ __forceinline__ long long cta_begin(long long U, int grid, int c) {
+    return (U * c) / grid;
+}
+
+// Index of the CTA whose range holds unit u.
+__device__ __forceinline__ int cta_of(long long U, int grid, long long u) {
+    return (int)(((u + 1) * grid + U - 1) / U) - 1;
+}
+
+__device__ __forceinline__ Cursor cursor_at(const int *tile_base, int B, int HR, long long u) {
+    int lo = 0, hi = B - 1;  // last b with tile_base[b] * HR <= u
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)tile_base[mid] * HR <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    Cursor c;
+    c.b = lo;
+    c.n = tile_base[lo + 1] - tile_base[lo];
+    const long long rem = u - (long long)tile_base[lo] * HR;
+    c.pr = c.n > 0 ? (int)(rem / c.n) : 0;
+    c.tile = c.n > 0 ? (int)(rem - (long long)c.pr * c.n) : 0;
+    return c;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &c, const int *tile_base, int B, int HR) {
+    if (++c.tile < c.n) return;
+    c.tile = 0;
+    if (++c.pr < HR) return;
+    c.pr = 0;
+    do {
+        ++c.b;
+    } while (c.b < B && tile_base[c.b + 1] == tile_base[c.b]);
+    c.n = c.b < B ? tile_base[c.b + 1] - tile_base[c.b] : 0;
+}
+
+// Consumer-group barrier on an mbarrier (bounded, unlike bar.sync).
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait_bounded(bar, uses & 1);
+    ++uses;
+    __syncwarp();
+    return ok;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const uint16_t *p) {
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+
+// The running row max only moves when a tile's max exceeds it by more than
+// this many log2 units; until then probabilities stay below 2^8 relative to
+// the stale max, which the f32 sums and the bf16 P carry without loss, and
+// the final division by the row sum is unchanged.
+constexpr float kRescaleThreshold = 8.0f;
+
+// Every CTA: tiles per sequence and their prefix sums into tile_base[0..B]
+// (identically in every CTA); CTA 0 also writes each sequence's status
+// (prefix length in range, parent array a topologically ordered tree).
+// Contains __syncthreads: call from every thread of the CTA.
+__device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int *scan_tmp,
+                                              int nt) {
+    const int tid = threadIdx.x;
+    {
+        const int per = (p.B + nt - 1) / nt;
+        const int b0 = tid * per, b1 = min(p.B, b0 + per);
+        int sum = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int L = p.prefix_lens[b];
+            const bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
+            sum += ok ? (L + p.T + kBK - 1) / kBK : 0;
+        }
+        scan_tmp[tid] = sum;
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int i = 0; i < nt; ++i) {
+                const int v = scan_tmp[i];
+                scan_tmp[i] = acc;
+                acc += v;
+            }
+            tile_base[p.B] = acc;
+        }
+        __syncthreads();
+        int acc = scan_tmp[tid];
+        for (int b = b0; b < b1; ++b) {
+            tile_base[b] = acc;
+            const int L = p.prefix_lens[b];
+            const bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
+            acc += ok ? (L + p.T + kBK - 1) / kBK : 0;
+        }
+    }
+    if (blockIdx.x == 0 && p.seq_status) {
+        for (int b = tid; b < p.B; b += nt) {
+            const int L = p.prefix_lens[b];
+            p.seq_status[b] = (L >= 0 && (long long)L + p.T <= p.S_max) ? SV_OK : SV_ERR_BAD_INPUT;
+        }
+        __syncthreads();
+        if (p.parents) {
+            for (int i = tid; i < p.B * p.T; i += nt) {
+                const int b = i / p.T, t = i - b * p.T;
+                const int pa = p.parents[i];
+                if (t == 0 ? pa != -1 : (pa < 0 || pa >= t)) p.seq_status[b] = SV_ERR_BAD_INPUT;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Ancestor set of node t (bit j = node j on the root->t path), walking the
+// parent array; NULL parents = a chain.  At most 64 steps; a parent that does
+// not precede its child ends the walk (the call reports such a tree as bad).
+__device__ __forceinline__ uint64_t ancestors(const int32_t *parents, int T, int b, int t) {
+    if (parents == nullptr) return t >= 63 ? ~0ull : ((1ull << (t + 1)) - 1ull);
+    uint64_t anc = 0;
+    int nd = t;
+    for (int step = 0; step < kMaxT && nd >= 0; ++step) {
+        anc |= 1ull << nd;
+        const int pn = parents[(size_t)b * T + nd];
+        if (pn >= nd) break;
+        nd = pn;
+    }
+    return anc;
+}
+
+}  // namespace sv

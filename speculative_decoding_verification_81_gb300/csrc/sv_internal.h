@@ -81,19 +81,24 @@ sv_status launch_verify_tree_greedy(const TreeArgs &args, int dtype, const Vocab
 // ---------------------------------------------------------------- attention
 
 struct AttnPlan {
-    int nwc;          // consumer (math) warps per CTA, 16 query rows each
     int stages;       // K/V pipeline depth
-    int rows_per_rg;  // query rows per row group = 16 * nwc
+    int rows_per_rg;  // query rows per row group (128: the TMEM lanes)
     int rg;           // row groups per (sequence, KV head)
     int grid;         // persistent CTAs
     int smem;         // dynamic shared memory bytes
-    size_t off_counters;
+    size_t off_pair_info;
     size_t off_part_o;
     size_t off_part_ml;
     size_t bytes;
 };
 
 sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan);
+
+// tcgen05 attention kernel and its split merge (sv_attention_tc.cu)
+struct AttnKParams;
+int tc_smem_bytes(int stages, int B);
+const void *tc_kernel_fn(int stages);
+sv_status launch_combine(const AttnKParams &p, cudaStream_t stream);
 
 struct AttnArgs {
     const void *q;
