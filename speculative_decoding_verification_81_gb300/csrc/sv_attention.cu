@@ -99,13 +99,13 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
     const int M = G * T;
     if (M > 512) return SV_ERR_UNSUPPORTED;
     AttnPlan pl{};
-    pl.stages = 5;
-    pl.rows_per_rg = 128;
-    pl.rg = (M + 127) / 128;
+    pl.stages = 3;
+    pl.rows_per_rg = M <= 64 ? 64 : 128;  // M=64 products for small row groups
+    pl.rg = (M + pl.rows_per_rg - 1) / pl.rows_per_rg;
     pl.smem = tc_smem_bytes(pl.stages, B);
     int sms = 0;
-    const int occ = cached_occupancy(tc_kernel_fn(pl.stages), 192, tc_smem_bytes(pl.stages, kMaxB),
-                                     pl.smem, &sms);
+    const int occ = cached_occupancy(tc_kernel_fn(pl.stages, pl.rows_per_rg), 192,
+                                     tc_smem_bytes(pl.stages, kMaxB), pl.smem, &sms);
     if (occ < 1) return SV_ERR_CUDA;
     pl.grid = sms * occ;
     plan_workspace(pl, B, Hkv);
@@ -139,7 +139,8 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.part_o = reinterpret_cast<float *>(base + pl.off_part_o);
     p.part_ml = reinterpret_cast<float *>(base + pl.off_part_ml);
     void *args[] = {&tmk, &tmv, &p};
-    if (cudaLaunchKernel(tc_kernel_fn(pl.stages), dim3(pl.grid), dim3(192), args, pl.smem, st) !=
+    if (cudaLaunchKernel(tc_kernel_fn(pl.stages, pl.rows_per_rg), dim3(pl.grid), dim3(192), args,
+                         pl.smem, st) !=
         cudaSuccess)
         return SV_ERR_CUDA;
     return launch_combine(p, st);

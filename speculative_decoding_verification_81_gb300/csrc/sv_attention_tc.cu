@@ -18,50 +18,62 @@
 //
 //   warp 0      TMA producer: K and V tiles (2-D tensor maps, 128-byte
 //               swizzle) into a ring of STAGES shared-memory stages.
-//   warp 1      owns the tensor memory (256 columns); one lane issues the
-//               MMAs: S = Q K^T (M=128 rows, N=64 keys, K=128) into one of
-//               two TMEM S buffers, and O += P V (M=128, N=128, K=64) into
-//               the TMEM O accumulator, V read as an MN-major operand.
+//   warp 1      owns the tensor memory (512 columns); one lane issues the
+//               MMAs: S = Q K^T (M=128 or 64 rows, N=128 keys, K=128) into
+//               one of two TMEM S buffers, and O += P V (N=128, K=128 keys)
+//               into the TMEM O accumulator.  Q and P are read from TMEM, K
+//               (K-major) and V (MN-major) from the shared-memory ring.  The
+//               tiles are 128 keys wide because a product's issue and
+//               completion take about the same time for small and large
+//               shapes: fewer, larger MMAs keep the tensor pipe fed.
 //   warps 2-5   softmax: thread r owns query row r (TMEM lane r).  It reads
 //               its S row from TMEM, applies the ancestor mask (a 64-bit set
 //               of tree ancestors per row, only in the tile(s) holding the T
 //               new rows), keeps the running max (moved only when it grows by
 //               more than 2^8, the O row then rescaled in TMEM) and row sum,
-//               writes its bf16 P row into shared memory for the PV MMA, and
+//               writes its bf16 P row over the S row it came from in TMEM
+//               (the A operand of the PV MMA), and
 //               at the end of a segment reads its O row back and writes the
 //               output row or its partial.
 //
-// The MMA thread runs one tile ahead: S(j+1) is issued before PV(j), so the
-// softmax of one tile overlaps the products of its neighbours.  Every wait is
-// bounded (SV_ERR_TIMEOUT on expiry); the TMEM is always released.
+// The MMA lane polls its barriers and issues S of the next tile and PV of the
+// oldest pending tile whenever either is ready, so the softmax of one tile
+// overlaps the products of its neighbours and no K/V stage is held longer
+// than its own tile needs.  Every wait is bounded (SV_ERR_TIMEOUT on expiry);
+// the TMEM is always released.
 #include "sv_attn_common.cuh"
 #include "sv_internal.h"
 
 namespace sv {
 
-constexpr int kTcRows = 128;                       // query rows per CTA tile (TMEM lanes)
-constexpr int kTcThreads = 192;                    // 6 warps
-constexpr int kTcQBytes = kTcRows * kD * 2;        // 32 KB: two 64-column halves
-constexpr int kTcPBytes = kTcRows * kBK * 2;       // 16 KB: the P tile
-constexpr uint32_t kTcCols = 256;                  // S0 | S1 | O
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr int kTcThreads = 192;  // 6 warps
+// Tensor-memory columns (32-bit each, one row per lane): two S buffers
+// (128 f32 each; the bf16 P row of a tile overwrites the first 64 columns of
+// its S row), the O accumulator (128 f32) and the Q tile (128 bf16 = 64
+// columns).  Q and P are the A operands of the two products, read by the
+// tensor core straight from TMEM, so shared memory holds only the K/V ring.
+constexpr uint32_t kTcCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
 
 // Byte offset of 16-byte chunk c (0..7) of row `row` in a 128-byte-swizzled
 // block whose rows are 128 bytes (the layout TMA writes with SWIZZLE_128B and
-// the tensor core reads with swizzle mode 2).
+// the tensor core reads with swizzle mode 2).  Used to zero V rows.
 __device__ __forceinline__ uint32_t sw128(int row, int c) {
     return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
 }
 
 struct TcSmem {
-    uint64_t full[8], empty[8];  // TMA ring
-    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+    uint64_t full[4], empty[4];  // TMA ring
+    uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t q_full, fin;
     uint32_t tmem;
     int abort_flag;
 };
 
-template <int STAGES>
+// MROWS query rows per group: 128 (M=128 products, row r in TMEM lane r) or
+// 64 (M=64 products, row r in lane 32*(r/16) + r%16: lanes 0-15 of each
+// 32-lane quarter) for groups of at most 64 rows.
+template <int STAGES, int MROWS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const AttnKParams p) {
@@ -69,11 +81,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base_u32 - raw_u32);
-    const uint32_t q_u32 = base_u32 + STAGES * kStageBytes;
-    const uint32_t p_u32 = q_u32 + kTcQBytes;
-    uint8_t *q_sm = smem + STAGES * kStageBytes;
-    uint8_t *p_sm = q_sm + kTcQBytes;
-    TcSmem *sh = reinterpret_cast<TcSmem *>(p_sm + kTcPBytes);
+    TcSmem *sh = reinterpret_cast<TcSmem *>(smem + STAGES * kStageBytes);
     int *tile_base = reinterpret_cast<int *>(sh + 1);  // [B + 1]
     int *scan_tmp = tile_base + (p.B + 1);             // [kTcThreads]
 
@@ -88,7 +96,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh->s_full[i], 1);
-            mbar_init(&sh->s_free[i], 4);
             mbar_init(&sh->p_full[i], 4);
             mbar_init(&sh->pv_done[i], 1);
         }
@@ -155,61 +162,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) {
         // ================= MMA issue (one lane)
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_bf16(kTcRows, kBK, false);
-            constexpr uint32_t idPV = tc::idesc_bf16(kTcRows, kD, true);
+            constexpr uint32_t idS = tc::idesc_bf16(MROWS, kBK, false);
+            constexpr uint32_t idPV = tc::idesc_bf16(MROWS, kD, true);
+            // Event loop: S of the next tile as soon as its K tile has landed
+            // and its TMEM buffer is free (PV of tile j-2, whose P lived
+            // there, is done), PV of the oldest pending tile as soon as its P
+            // rows are written; never one product waiting on an unrelated one.
             bool ok = true;
             Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
-            int pend = -1, pend_first = 0;
-            uint32_t seg = 0;
-            auto issue_pv = [&](int jt, int first) -> bool {
-                if (!mbar_wait_bounded(&sh->p_full[jt & 1], (uint32_t)((jt >> 1) & 1))) return false;
-                tc::fence_after();
-                const int s = jt % STAGES;
-                const uint32_t vbase = base_u32 + s * kStageBytes + 2 * kBox;
-                const uint32_t pbase = p_u32;
+            const long long nt = u_end - u_begin;
+            long long s_next = 0, pv_next = 0;
+            uint32_t seg = 0, first_bits = 0;  // bit (j & 31): tile j opens a segment
+            bool q_seen = false;
+            long long t_progress = clock64();
+            while (pv_next < nt) {
+                bool progressed = false;
+                if (s_next < nt && s_next - pv_next < 2) {
+                    const bool new_seg = (s_next == 0) || cur.tile == 0;
+                    bool can = !(new_seg && pv_next < s_next);  // finish the old segment first
+                    if (can && new_seg && !q_seen) {
+                        q_seen = mbar_test_wait(&sh->q_full, seg & 1);
+                        can = q_seen;
+                    }
+                    const int s = (int)(s_next % STAGES);
+                    if (can) can = mbar_test_wait(&sh->full[s], (uint32_t)((s_next / STAGES) & 1));
+                    if (can && s_next >= 2)
+                        can = mbar_test_wait(&sh->pv_done[s_next & 1], (uint32_t)(((s_next - 2) >> 1) & 1));
+                    if (can) {
+                        tc::fence_after();
+                        const uint32_t kbase_sm = base_u32 + s * kStageBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t ad = tc::smem_desc(pbase + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kBox, 1024);
-                    tc::mma_bf16(tbase + kColO, ad, bd, idPV, (kk > 0 || !first) ? 1u : 0u);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint64_t bd =
+                                tc::smem_desc(kbase_sm + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+                            tc::mma_bf16_ts(tbase + kColS + (uint32_t)(s_next & 1) * kBK,
+                                            tbase + kColQ + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
+                        }
+                        tc::commit(&sh->s_full[s_next & 1]);
+                        if (new_seg) {
+                            first_bits |= 1u << (s_next & 31);
+                            ++seg;
+                            q_seen = false;
+                        } else {
+                            first_bits &= ~(1u << (s_next & 31));
+                        }
+                        cursor_next(cur, tile_base, p.B, HR);
+                        ++s_next;
+                        progressed = true;
+                    }
                 }
-                tc::commit(&sh->pv_done[jt & 1]);
-                tc::commit(&sh->empty[s]);
-                return true;
-            };
-            long long jt = 0;
-            for (long long u = u_begin; u < u_end && ok; ++u, ++jt) {
-                const bool new_seg = (u == u_begin) || cur.tile == 0;
-                if (new_seg) {
-                    // finish the previous segment before waiting for the new Q tile
-                    if (pend >= 0 && !issue_pv(pend, pend_first)) { ok = false; break; }
-                    pend = -1;
-                    if (!mbar_wait_bounded(&sh->q_full, seg & 1)) { ok = false; break; }
-                    ++seg;
+                if (pv_next < s_next &&
+                    mbar_test_wait(&sh->p_full[pv_next & 1], (uint32_t)((pv_next >> 1) & 1))) {
                     tc::fence_after();
+                    const int s = (int)(pv_next % STAGES);
+                    const bool first = (first_bits >> (pv_next & 31)) & 1u;
+                    const uint32_t vbase = base_u32 + s * kStageBytes + 2 * kBox;
+                    const uint32_t pcol = tbase + kColS + (uint32_t)(pv_next & 1) * kBK;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kBox, 1024);
+                        tc::mma_bf16_ts(tbase + kColO, pcol + kk * 8, bd, idPV,
+                                        (kk > 0 || !first) ? 1u : 0u);
+                    }
+                    tc::commit(&sh->pv_done[pv_next & 1]);
+                    tc::commit(&sh->empty[s]);
+                    ++pv_next;
+                    progressed = true;
                 }
-                const int s = (int)(jt % STAGES);
-                if (!mbar_wait_bounded(&sh->full[s], (uint32_t)((jt / STAGES) & 1))) { ok = false; break; }
-                if (jt >= 2 && !mbar_wait_bounded(&sh->s_free[jt & 1], (uint32_t)(((jt - 2) >> 1) & 1))) {
+                if (progressed) {
+                    t_progress = clock64();
+                } else if (clock64() - t_progress > kWaitCycles || *abort_flag) {
                     ok = false;
                     break;
                 }
-                tc::fence_after();
-                const uint32_t kbase_sm = base_u32 + s * kStageBytes;
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t ad =
-                        tc::smem_desc(q_u32 + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(kbase_sm + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-                    tc::mma_bf16(tbase + kColS + (uint32_t)(jt & 1) * kBK, ad, bd, idS, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&sh->s_full[jt & 1]);
-                if (pend >= 0 && !issue_pv(pend, pend_first)) { ok = false; break; }
-                pend = (int)jt;
-                pend_first = new_seg;
-                cursor_next(cur, tile_base, p.B, HR);
             }
-            if (ok && pend >= 0) ok = issue_pv(pend, pend_first);
             if (!ok) fail(cur.b < p.B ? cur.b : 0);
             // all MMAs this thread issued complete before the TMEM is released
             tc::commit(&sh->fin);
@@ -223,12 +249,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
 
-    // ===================== softmax warps 2..5: thread owns query row r
+    // ===================== softmax warps 2..5: one thread per query row
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;              // row in the 128-row tile = TMEM lane
-    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);
+    constexpr int kRowsPerQuarter = MROWS / 4;  // 32, or 16 with M=64
+    const bool lane_has_row = lane < kRowsPerQuarter;
+    const int r = quarter * kRowsPerQuarter + (lane_has_row ? lane : 0);  // row in the group
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);         // this warp's lanes
     const float sc = p.scale_log2;
-    uint32_t seg = 0;
     float m = kNegInf, l = 0.f;
     uint64_t anc = 0;
     int L = 0, kv_end = 0, seg_first_tile = 0, kvh = 0, rg = 0, rglob = 0;
@@ -244,9 +271,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             kv_end = L + p.T;
             seg_first_tile = cur.tile;
             seg_is_first = (u == u_begin);
-            rglob = rg * kTcRows + r;
-            row_valid = rglob < p.M;
-            warp_active = rg * kTcRows + quarter * 32 < p.M;
+            rglob = rg * MROWS + r;
+            row_valid = lane_has_row && rglob < p.M;
+            warp_active = rg * MROWS + quarter * kRowsPerQuarter < p.M;
             m = kNegInf;
             l = 0.f;
             int t = 0, g = 0;
@@ -255,18 +282,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 g = rglob - t * p.G;
                 anc = ancestors(p.parents, p.T, cur.b, t);
             }
-            // this thread's Q row into the swizzled A tile (zeros past M)
-            const uint4 *qsrc = reinterpret_cast<const uint4 *>(
-                p.q + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD);
+            // this thread's Q row into the TMEM A tile (zeros past M); the
+            // previous segment's products have all completed (its epilogue
+            // waited for its last PV)
+            if (warp_active) {
+                const uint4 *qsrc = reinterpret_cast<const uint4 *>(
+                    p.q + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = row_valid ? qsrc[c] : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(q_sm + (c >> 3) * (kTcQBytes / 2) + sw128(r, c & 7)) = v;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = row_valid ? qsrc[8 * h + c] : make_uint4(0u, 0u, 0u, 0u);
+                        w[4 * c] = v.x;
+                        w[4 * c + 1] = v.y;
+                        w[4 * c + 2] = v.z;
+                        w[4 * c + 3] = v.w;
+                    }
+                    tc::tmem_st32(tl + kColQ + 32 * h, w);
+                }
+                tc::wait_st();
             }
-            tc::fence_proxy_async_smem();
+            tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->q_full);
-            ++seg;
             if (cur.tile == 0 && warp == 2 && lane == 0) {
                 // this CTA holds the pair's first tile: record who shares the pair
                 const long long ub = (long long)tile_base[cur.b] * HR + (long long)cur.pr * cur.n;
@@ -279,31 +318,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool first_tile = new_seg;  // O is overwritten by this tile's PV
         const int kbase = cur.tile * kBK;
         const bool last_of_pair = cur.tile == cur.n - 1;
+        const uint32_t sbuf = tl + kColS + (uint32_t)(jt & 1) * kBK;
 
-        // ---- S row from TMEM
+        // ---- S row from TMEM; P written back over it
         if (!mbar_wait_bounded(&sh->s_full[jt & 1], (uint32_t)((jt >> 1) & 1))) {
             fail(cur.b);
             break;
         }
         tc::fence_after();
-        float sv[kBK];
         if (warp_active) {
-            uint32_t ra[32], rb2[32];
-            tc::tmem_ld32(tl + kColS + (uint32_t)(jt & 1) * kBK, ra);
-            tc::tmem_ld32(tl + kColS + (uint32_t)(jt & 1) * kBK + 32, rb2);
-            tc::wait_ld();
+            float sv[kBK];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                sv[j] = __uint_as_float(ra[j]);
-                sv[32 + j] = __uint_as_float(rb2[j]);
+            for (int h = 0; h < kBK / 32; ++h) {
+                uint32_t ra[32];
+                tc::tmem_ld32(sbuf + 32 * h, ra);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sv[32 * h + j] = __uint_as_float(ra[j]);
             }
-        }
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->s_free[jt & 1]);
-
-        uint32_t pk[kBK / 2];
-        if (warp_active) {
             if (kbase + kBK > L) {
 #pragma unroll
                 for (int j = 0; j < kBK; ++j) {
@@ -318,14 +350,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int j = 0; j < kBK; ++j) mx = fmaxf(mx, sv[j]);
             const float c = mx * sc;
             const bool up = c > m + kRescaleThreshold;
+            bool ok = true;
             if (__any_sync(0xffffffffu, up)) {
                 const float a = up ? ex2_approx(m - c) : 1.f;
                 if (!first_tile) {
                     // O holds earlier tiles of this segment: wait for the last PV, rescale in TMEM
-                    if (!mbar_wait_bounded(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1))) {
-                        fail(cur.b);
-                        break;
-                    }
+                    ok = mbar_wait_bounded(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1));
                     tc::fence_after();
 #pragma unroll
                     for (int h = 0; h < kD / 32; ++h) {
@@ -336,7 +366,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * a);
                         tc::tmem_st32(tl + kColO + 32 * h, ov);
                     }
-                    tc::wait_st();
                 }
                 if (up) {
                     m = c;
@@ -346,25 +375,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float nb = m == kNegInf ? 0.f : -m;
             float ls = 0.f;
 #pragma unroll
-            for (int j = 0; j < kBK / 2; ++j) {
-                const float e0 = ex2_approx(fmaf(sv[2 * j], sc, nb));
-                const float e1 = ex2_approx(fmaf(sv[2 * j + 1], sc, nb));
-                ls += e0 + e1;
-                pk[j] = pack_bf16x2(e0, e1);
-            }
-            l += ls;
-        }
-        // ---- P row into shared memory (the tile is free once PV of tile jt-1 is done)
-        if (jt >= 1 && !mbar_wait_bounded(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1))) {
-            fail(cur.b);
-            break;
-        }
-        if (warp_active) {
-            uint8_t *prow = p_sm;
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(prow + sw128(r, c)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                for (int j = 0; j < 32; ++j) {
+                    const float e0 = ex2_approx(fmaf(sv[64 * h + 2 * j], sc, nb));
+                    const float e1 = ex2_approx(fmaf(sv[64 * h + 2 * j + 1], sc, nb));
+                    ls += e0 + e1;
+                    pk[j] = pack_bf16x2(e0, e1);
+                }
+                tc::tmem_st32(sbuf + 32 * h, pk);  // P columns 0..63 of this S buffer
+            }
+            tc::wait_st();
+            l += ls;
+            if (!ok) {
+                fail(cur.b);
+                break;
+            }
         }
         if (last_of_pair && kbase + kBK > kv_end) {
             // V rows past the sequence's last slot may hold anything (even NaN,
@@ -376,8 +403,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 *reinterpret_cast<uint4 *>(vst + (c >> 3) * kBox + sw128(row, c & 7)) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
+            tc::fence_proxy_async_smem();
         }
-        tc::fence_proxy_async_smem();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->p_full[jt & 1]);
@@ -394,8 +421,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int g = row_valid ? rglob - t * p.G : 0;
             uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD;
             const int slot = seg_is_first ? 0 : 1;
-            float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * kTcRows + r) * kD;
-            float *pml = p.part_ml + (((size_t)blockIdx.x * 2 + slot) * kTcRows + r) * 2;
+            float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD;
+            float *pml = p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 2;
             const float inv = 1.f / l;
             if (warp_active) {
 #pragma unroll
@@ -442,7 +469,7 @@ constexpr int kCombineRows = 8;  // rows (warps) per CTA
 
 __global__ void __launch_bounds__(kCombineRows * 32)
     attention_combine_kernel(const AttnKParams p) {
-    const int chunks = kTcRows / kCombineRows;
+    const int chunks = p.rows_per_rg / kCombineRows;
     const int pair = blockIdx.x / chunks;
     const int r = (blockIdx.x - pair * chunks) * kCombineRows + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -451,14 +478,14 @@ __global__ void __launch_bounds__(kCombineRows * 32)
     const int kvh = rem / p.RG, rg = rem - kvh * p.RG;
     const int L = p.prefix_lens[b];
     if (L < 0 || (long long)L + p.T > p.S_max) return;
-    const int rglob = rg * kTcRows + r;
+    const int rglob = rg * p.rows_per_rg + r;
     if (rglob >= p.M) return;
     const int4 info = __ldcg(p.pair_info + pair);
     const int nc = info.y;
     if (nc <= 1) return;
     auto row_index = [&](int i) -> size_t {  // contributor i's partial row
         const int slot = i == 0 ? info.z : 0;
-        return ((size_t)(info.x + i) * 2 + slot) * kTcRows + r;
+        return ((size_t)(info.x + i) * 2 + slot) * p.rows_per_rg + r;
     };
     float mstar = kNegInf;
     for (int i = lane; i < nc; i += 32) mstar = fmaxf(mstar, __ldcg(p.part_ml + row_index(i) * 2));
@@ -498,18 +525,17 @@ __global__ void __launch_bounds__(kCombineRows * 32)
 // ---------------------------------------------------------------- host side
 
 int tc_smem_bytes(int stages, int B) {
-    return 1024 + stages * kStageBytes + kTcQBytes + kTcPBytes + (int)sizeof(TcSmem) +
-           (B + 1) * 4 + kTcThreads * 4;
+    return 1024 + stages * kStageBytes + (int)sizeof(TcSmem) + (B + 1) * 4 + kTcThreads * 4;
 }
 
-const void *tc_kernel_fn(int stages) {
-    if (stages == 5) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<5>);
-    if (stages == 4) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<4>);
+const void *tc_kernel_fn(int stages, int mrows) {
+    if (stages == 3 && mrows == 128) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 128>);
+    if (stages == 3 && mrows == 64) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 64>);
     return nullptr;
 }
 
 sv_status launch_combine(const AttnKParams &p, cudaStream_t st) {
-    const unsigned grid = (unsigned)(p.B * p.Hkv * p.RG * (kTcRows / kCombineRows));
+    const unsigned grid = (unsigned)(p.B * p.Hkv * p.RG * (p.rows_per_rg / kCombineRows));
     attention_combine_kernel<<<grid, kCombineRows * 32, 0, st>>>(p);
     return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -8,9 +8,9 @@
 namespace sv {
 
 constexpr int kD = 128;
-constexpr int kBK = 64;                   // keys per tile
-constexpr int kBox = kBK * 64 * 2;        // one 64-key x 64-dim bf16 TMA box: 8 KB
-constexpr int kStageBytes = 4 * kBox;     // K lo/hi + V lo/hi: 32 KB
+constexpr int kBK = 128;                  // keys per tile
+constexpr int kBox = kBK * 64 * 2;        // one 128-key x 64-dim bf16 TMA box: 16 KB
+constexpr int kStageBytes = 4 * kBox;     // K lo/hi + V lo/hi: 64 KB
 constexpr int kMaxB = 4096;
 constexpr int kMaxT = 64;
 

@@ -82,7 +82,7 @@ sv_status launch_verify_tree_greedy(const TreeArgs &args, int dtype, const Vocab
 
 struct AttnPlan {
     int stages;       // K/V pipeline depth
-    int rows_per_rg;  // query rows per row group (128: the TMEM lanes)
+    int rows_per_rg;  // query rows per row group: 64 or 128 (the MMA's M)
     int rg;           // row groups per (sequence, KV head)
     int grid;         // persistent CTAs
     int smem;         // dynamic shared memory bytes
@@ -97,7 +97,7 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan);
 // tcgen05 attention kernel and its split merge (sv_attention_tc.cu)
 struct AttnKParams;
 int tc_smem_bytes(int stages, int B);
-const void *tc_kernel_fn(int stages);
+const void *tc_kernel_fn(int stages, int mrows);
 sv_status launch_combine(const AttnKParams &p, cudaStream_t stream);
 
 struct AttnArgs {
