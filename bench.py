@@ -86,7 +86,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("sv_attention.cu", "sv_device.cuh"):
+    for name in ("sv_attention.cu", "sv_attention_tc.cu", "sv_attn_common.cuh", "sv_device.cuh"):
         with open(os.path.join(ROOT, "speculative_decoding_verification_81_gb300", "csrc", name),
                   "rb") as f:
             h.update(f.read())
