@@ -250,7 +250,8 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
                            accepted_len=acc, out_tokens=toks, ws=ws_c)
         sv.sv_compact_kv(dd["k"], dd["v"], dd["prefix_lens"], acc, None, new_kv_lens=newl)
 
-    launches_per_step = 4  # attention, chain statistics, residual draw, compaction
+    # attention, split merge, chain statistics, residual draw, compaction
+    launches_per_step = 5
 
     def barrier():
         if world > 1:

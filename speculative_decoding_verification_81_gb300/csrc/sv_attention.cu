@@ -84,8 +84,8 @@ static int cached_occupancy(const void *fn, int threads, int max_smem, int smem,
 
 static void plan_workspace(AttnPlan &pl, int B, int Hkv) {
     size_t off = 0;
-    pl.off_pair_info = off;
-    off = align_up(off + sizeof(int4) * (size_t)B * Hkv * pl.rg, 256);
+    pl.off_pair_ctr = off;
+    off = align_up(off + sizeof(int) * (size_t)B * Hkv * pl.rg, 256);
     pl.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.rows_per_rg * kD, 256);
     pl.off_part_ml = off;
@@ -104,7 +104,7 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
     pl.rg = (M + pl.rows_per_rg - 1) / pl.rows_per_rg;
     pl.smem = tc_smem_bytes(pl.stages, B);
     int sms = 0;
-    const int occ = cached_occupancy(tc_kernel_fn(pl.stages, pl.rows_per_rg), 192,
+    const int occ = cached_occupancy(tc_kernel_fn(pl.stages, pl.rows_per_rg), kTcThreads,
                                      tc_smem_bytes(pl.stages, kMaxB), pl.smem, &sms);
     if (occ < 1) return SV_ERR_CUDA;
     pl.grid = sms * occ;
@@ -135,15 +135,14 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.rows_per_rg = pl.rows_per_rg;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     char *base = static_cast<char *>(ws);
-    p.pair_info = reinterpret_cast<int4 *>(base + pl.off_pair_info);
+    p.pair_ctr = reinterpret_cast<int *>(base + pl.off_pair_ctr);
     p.part_o = reinterpret_cast<float *>(base + pl.off_part_o);
     p.part_ml = reinterpret_cast<float *>(base + pl.off_part_ml);
     void *args[] = {&tmk, &tmv, &p};
-    if (cudaLaunchKernel(tc_kernel_fn(pl.stages, pl.rows_per_rg), dim3(pl.grid), dim3(192), args,
-                         pl.smem, st) !=
-        cudaSuccess)
-        return SV_ERR_CUDA;
-    return launch_combine(p, st);
+    return launch_pdl(tc_kernel_fn(pl.stages, pl.rows_per_rg), dim3(pl.grid), dim3(kTcThreads),
+                      pl.smem, st, args) == cudaSuccess
+               ? SV_OK
+               : SV_ERR_CUDA;
 }
 
 }  // namespace sv

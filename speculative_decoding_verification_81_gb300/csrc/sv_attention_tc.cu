@@ -13,32 +13,40 @@
 // the flat list of (sequence, KV head, 128-row group, 64-key tile) units; a
 // persistent grid (one CTA per SM) takes equal contiguous ranges of it, so the
 // load is balanced whatever the prefix lengths.  A (sequence, KV head) whose
-// tiles fall to several CTAs leaves one partial (O, max, sum) per CTA, merged
-// afterwards by the combine kernel below.  Inside a CTA (6 warps):
+// tiles fall to several CTAs leaves one partial (O, max, sum) per CTA; the
+// CTA whose partial completes the set (a per-pair arrival counter) merges
+// them into the output rows.  Inside a CTA (12 warps):
 //
-//   warp 0      TMA producer: K and V tiles (2-D tensor maps, 128-byte
-//               swizzle) into a ring of STAGES shared-memory stages.
+//   warps 0, 11 TMA producers: K and V tiles (2-D tensor maps, 128-byte
+//               swizzle) into a ring of STAGES shared-memory stages, K and
+//               V halves refilled independently (K as soon as its S product
+//               is done, V after its PV).
 //   warp 1      owns the tensor memory (512 columns); one lane issues the
-//               MMAs: S = Q K^T (M=128 or 64 rows, N=128 keys, K=128) into
-//               one of two TMEM S buffers, and O += P V (N=128, K=128 keys)
-//               into the TMEM O accumulator.  Q and P are read from TMEM, K
+//               S = Q K^T products (M=128 or 64 rows, N=128 keys, K=128)
+//               into one of two TMEM S buffers.
+//   warp 10     one lane issues O += P V (N=128, K=128 keys) into the TMEM
+//               O accumulator.  Q and P are read from TMEM, K
 //               (K-major) and V (MN-major) from the shared-memory ring.  The
 //               tiles are 128 keys wide because a product's issue and
 //               completion take about the same time for small and large
 //               shapes: fewer, larger MMAs keep the tensor pipe fed.
-//   warps 2-5   softmax: thread r owns query row r (TMEM lane r).  It reads
-//               its S row from TMEM, applies the ancestor mask (a 64-bit set
-//               of tree ancestors per row, only in the tile(s) holding the T
-//               new rows), keeps the running max (moved only when it grows by
-//               more than 2^8, the O row then rescaled in TMEM) and row sum,
-//               writes its bf16 P row over the S row it came from in TMEM
-//               (the A operand of the PV MMA), and
-//               at the end of a segment reads its O row back and writes the
-//               output row or its partial.
+//   warps 2-9   softmax, two threads per query row: a warp may only touch
+//               the TMEM lane quarter of its SM sub-partition (warp % 4), so
+//               warps w and w+4 share the rows of one quarter, the first
+//               taking keys (and output columns) 0-63 of every tile, the
+//               second 64-127.  Each reads its half S row from TMEM, applies
+//               the ancestor mask (a 64-bit set of tree ancestors per row,
+//               only in the tile(s) holding the T new rows), agrees the tile
+//               max with its partner through shared memory, keeps the running
+//               max (moved only when it grows by more than 2^8, its half of
+//               the O row then rescaled in TMEM) and its part of the row sum,
+//               writes its bf16 P half row over the S columns it came from
+//               (the A operand of the PV MMA), and at the end of a segment
+//               reads its half of the O row and writes it out (or a partial).
 //
-// The MMA lane polls its barriers and issues S of the next tile and PV of the
-// oldest pending tile whenever either is ready, so the softmax of one tile
-// overlaps the products of its neighbours and no K/V stage is held longer
+// The two issuing lanes wait (blocking, bounded) on their own barriers, so S
+// of the next tile is issued while the softmax of the current one runs, PV
+// of a tile the moment its P is written, and no K/V stage is held longer
 // than its own tile needs.  Every wait is bounded (SV_ERR_TIMEOUT on expiry);
 // the TMEM is always released.
 #include "sv_attn_common.cuh"
@@ -46,11 +54,10 @@
 
 namespace sv {
 
-constexpr int kTcThreads = 192;  // 6 warps
 // Tensor-memory columns (32-bit each, one row per lane): two S buffers
-// (128 f32 each; the bf16 P row of a tile overwrites the first 64 columns of
-// its S row), the O accumulator (128 f32) and the Q tile (128 bf16 = 64
-// columns).  Q and P are the A operands of the two products, read by the
+// (128 f32 each; the bf16 P of keys 0-63 overwrites S columns 0-31, that of
+// keys 64-127 S columns 64-95), the O accumulator (128 f32) and the Q tile
+// (128 bf16 = 64 columns).  Q and P are the A operands of the two products, read by the
 // tensor core straight from TMEM, so shared memory holds only the K/V ring.
 constexpr uint32_t kTcCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
@@ -63,9 +70,15 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
 }
 
 struct TcSmem {
-    uint64_t full[4], empty[4];  // TMA ring
+    uint64_t full_k[4], empty_k[4];  // TMA ring, K halves of the stages
+    uint64_t full_v[4], empty_v[4];  // V halves
     uint64_t s_full[2], p_full[2], pv_done[2];
-    uint64_t q_full, fin;
+    uint64_t q_full, fin, fin_pv;
+    uint64_t pair[4];            // the two softmax warps of each lane quarter
+    uint64_t seg_bar;            // all softmax warps, at the end of a split segment
+    int merge;                   // this CTA merges the split pair it just finished
+    float xmax[2][4][2][32];     // [tile parity][quarter][half][lane]: half-row tile maxima
+    float xl[4][2][32];          // [quarter][half][lane]: half-row sums at a segment end
     uint32_t tmem;
     int abort_flag;
 };
@@ -83,7 +96,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *smem = smem_raw + (base_u32 - raw_u32);
     TcSmem *sh = reinterpret_cast<TcSmem *>(smem + STAGES * kStageBytes);
     int *tile_base = reinterpret_cast<int *>(sh + 1);  // [B + 1]
-    int *scan_tmp = tile_base + (p.B + 1);             // [kTcThreads]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -91,16 +103,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sh->full[s], 1);
-            mbar_init(&sh->empty[s], 1);
+            mbar_init(&sh->full_k[s], 1);
+            mbar_init(&sh->empty_k[s], 1);
+            mbar_init(&sh->full_v[s], 1);
+            mbar_init(&sh->empty_v[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh->s_full[i], 1);
-            mbar_init(&sh->p_full[i], 4);
+            mbar_init(&sh->p_full[i], kSoftmaxWarps);
             mbar_init(&sh->pv_done[i], 1);
         }
-        mbar_init(&sh->q_full, 4);
+        mbar_init(&sh->q_full, kSoftmaxWarps);
         mbar_init(&sh->fin, 1);
+        mbar_init(&sh->fin_pv, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&sh->pair[q], 2);
+        mbar_init(&sh->seg_bar, kSoftmaxWarps);
         sh->abort_flag = 0;
         fence_mbar_init();
     }
@@ -108,7 +125,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
-    attn_prologue(p, tile_base, scan_tmp, kTcThreads);
+    griddep_wait();
+    griddep_launch_dependents();
+    attn_prologue(p, tile_base, kTcThreads);
 
     const long long U = (long long)tile_base[p.B] * HR;
     const int nctas = (int)(U < (long long)gridDim.x ? U : (long long)gridDim.x);
@@ -128,138 +147,173 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (p.seq_status) p.seq_status[b] = SV_ERR_TIMEOUT;
     };
 
-    if (warp == 0) {
-        // ================= producer
+    if (warp == 0 || warp == kVLoadWarp) {
+        // ================= producers: warp 0 fills the K halves of the ring,
+        // the last warp the V halves.  A K half is refilled as soon as the S
+        // product that read it is done, a V half once its PV product is, so
+        // the next K tiles stream in while a tile's softmax and PV run.
         if (lane == 0) {
+            const bool is_k = warp == 0;
+            uint64_t *full = is_k ? sh->full_k : sh->full_v;
+            uint64_t *empty = is_k ? sh->empty_k : sh->empty_v;
+            const CUtensorMap *map = is_k ? &tmk : &tmv;
+            const int half_off = is_k ? 0 : 2 * kBox;
             Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
             long long k = 0;
             for (long long u = u_begin; u < u_end; ++u, ++k) {
                 const int s = (int)(k % STAGES);
                 const uint32_t ph = (uint32_t)((k / STAGES) & 1);
-                if (!mbar_wait_bounded(&sh->empty[s], ph ^ 1u)) {
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
                     fail(cur.b);
                     break;
                 }
                 if (*abort_flag) break;
                 const int kvh = cur.pr / p.RG;
                 const int y = (cur.b * p.Hkv + kvh) * p.S_max + cur.tile * kBK;
-                uint8_t *st = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
-                tma_load_2d(st, &tmk, 0, y, &sh->full[s]);
-                tma_load_2d(st + kBox, &tmk, 64, y, &sh->full[s]);
-                tma_load_2d(st + 2 * kBox, &tmv, 0, y, &sh->full[s]);
-                tma_load_2d(st + 3 * kBox, &tmv, 64, y, &sh->full[s]);
+                uint8_t *st = smem + s * kStageBytes + half_off;
+                mbar_arrive_expect_tx(&full[s], 2 * kBox);
+                tma_load_2d(st, map, 0, y, &full[s]);
+                tma_load_2d(st + kBox, map, 64, y, &full[s]);
                 cursor_next(cur, tile_base, p.B, HR);
             }
             // every copy issued must land before the CTA may exit
             const long long first = k > STAGES ? k - STAGES : 0;
             for (long long j = first; j < k; ++j)
-                mbar_wait_bounded(&sh->full[j % STAGES], (uint32_t)((j / STAGES) & 1));
+                mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
         }
         return;
     }
 
-    if (warp == 1) {
-        // ================= MMA issue (one lane)
+    if (warp == 1 || warp == kPvWarp) {
+        // ================= MMA issue: lane 0 of warp 1 the S = Q K^T
+        // products, lane 0 of the last warp the O += P V products, each in
+        // tile order behind (bounded) blocking waits, so neither polls nor
+        // holds back the other (tcgen05.commit tracks its own thread's MMAs).
         if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_bf16(MROWS, kBK, false);
-            constexpr uint32_t idPV = tc::idesc_bf16(MROWS, kD, true);
-            // Event loop: S of the next tile as soon as its K tile has landed
-            // and its TMEM buffer is free (PV of tile j-2, whose P lived
-            // there, is done), PV of the oldest pending tile as soon as its P
-            // rows are written; never one product waiting on an unrelated one.
             bool ok = true;
             Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
             const long long nt = u_end - u_begin;
-            long long s_next = 0, pv_next = 0;
-            uint32_t seg = 0, first_bits = 0;  // bit (j & 31): tile j opens a segment
-            bool q_seen = false;
-            long long t_progress = clock64();
-            while (pv_next < nt) {
-                bool progressed = false;
-                if (s_next < nt && s_next - pv_next < 2) {
-                    const bool new_seg = (s_next == 0) || cur.tile == 0;
-                    bool can = !(new_seg && pv_next < s_next);  // finish the old segment first
-                    if (can && new_seg && !q_seen) {
-                        q_seen = mbar_test_wait(&sh->q_full, seg & 1);
-                        can = q_seen;
+            if (warp == 1) {
+                constexpr uint32_t idS = tc::idesc_bf16(MROWS, kBK, false);
+                uint32_t seg = 0;
+                for (long long j = 0; j < nt; ++j) {
+                    const int s = (int)(j % STAGES);
+                    // this segment's Q is in TMEM, the K tile has landed, the
+                    // S buffer is free (PV of tile j-2, whose P lived there, is done)
+                    if (j == 0 || cur.tile == 0) ok = mbar_wait_bounded(&sh->q_full, (seg++) & 1);
+                    if (ok) ok = mbar_wait_bounded(&sh->full_k[s], (uint32_t)((j / STAGES) & 1));
+                    if (ok && j >= 2)
+                        ok = mbar_wait_bounded(&sh->pv_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
+                    if (!ok || *abort_flag) {
+                        ok = false;
+                        break;
                     }
-                    const int s = (int)(s_next % STAGES);
-                    if (can) can = mbar_test_wait(&sh->full[s], (uint32_t)((s_next / STAGES) & 1));
-                    if (can && s_next >= 2)
-                        can = mbar_test_wait(&sh->pv_done[s_next & 1], (uint32_t)(((s_next - 2) >> 1) & 1));
-                    if (can) {
-                        tc::fence_after();
-                        const uint32_t kbase_sm = base_u32 + s * kStageBytes;
-#pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk) {
-                            const uint64_t bd =
-                                tc::smem_desc(kbase_sm + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-                            tc::mma_bf16_ts(tbase + kColS + (uint32_t)(s_next & 1) * kBK,
-                                            tbase + kColQ + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
-                        }
-                        tc::commit(&sh->s_full[s_next & 1]);
-                        if (new_seg) {
-                            first_bits |= 1u << (s_next & 31);
-                            ++seg;
-                            q_seen = false;
-                        } else {
-                            first_bits &= ~(1u << (s_next & 31));
-                        }
-                        cursor_next(cur, tile_base, p.B, HR);
-                        ++s_next;
-                        progressed = true;
-                    }
-                }
-                if (pv_next < s_next &&
-                    mbar_test_wait(&sh->p_full[pv_next & 1], (uint32_t)((pv_next >> 1) & 1))) {
                     tc::fence_after();
-                    const int s = (int)(pv_next % STAGES);
-                    const bool first = (first_bits >> (pv_next & 31)) & 1u;
-                    const uint32_t vbase = base_u32 + s * kStageBytes + 2 * kBox;
-                    const uint32_t pcol = tbase + kColS + (uint32_t)(pv_next & 1) * kBK;
+                    // dims 16kk..: 32 bytes on within a 64-dim box, the next box 16 KB on
+                    const uint64_t dk = tc::smem_desc(base_u32 + s * kStageBytes, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t bd = dk + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2);
+                        tc::mma_bf16_ts(tbase + kColS + (uint32_t)(j & 1) * kBK, tbase + kColQ + kk * 8,
+                                        bd, idS, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&sh->s_full[j & 1]);
+                    tc::commit(&sh->empty_k[s]);  // the K half may be refilled once S(j) is done
+                    cursor_next(cur, tile_base, p.B, HR);
+                }
+            } else {
+                constexpr uint32_t idPV = tc::idesc_bf16(MROWS, kD, true);
+                for (long long j = 0; j < nt; ++j) {
+                    const int s = (int)(j % STAGES);
+                    const bool first = (j == 0) || cur.tile == 0;  // O starts over
+                    ok = mbar_wait_bounded(&sh->p_full[j & 1], (uint32_t)((j >> 1) & 1));
+                    if (ok) ok = mbar_wait_bounded(&sh->full_v[s], (uint32_t)((j / STAGES) & 1));
+                    if (!ok || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    // V rows 16kk.. start 2048 bytes apart (descriptor address units of 16 bytes)
+                    const uint64_t dv = tc::smem_desc(base_u32 + s * kStageBytes + 2 * kBox, kBox, 1024);
+                    const uint32_t pcol = tbase + kColS + (uint32_t)(j & 1) * kBK;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t bd = tc::smem_desc(vbase + kk * 2048, kBox, 1024);
-                        tc::mma_bf16_ts(tbase + kColO, pcol + kk * 8, bd, idPV,
+                        const uint64_t bd = dv + (uint64_t)(kk * (2048 >> 4));
+                        // P of keys 16kk.. : columns 8kk.. of the first half, 64+.. of the second
+                        tc::mma_bf16_ts(tbase + kColO, pcol + kk * 8 + (kk >= 4 ? 32 : 0), bd, idPV,
                                         (kk > 0 || !first) ? 1u : 0u);
                     }
-                    tc::commit(&sh->pv_done[pv_next & 1]);
-                    tc::commit(&sh->empty[s]);
-                    ++pv_next;
-                    progressed = true;
-                }
-                if (progressed) {
-                    t_progress = clock64();
-                } else if (clock64() - t_progress > kWaitCycles || *abort_flag) {
-                    ok = false;
-                    break;
+                    tc::commit(&sh->pv_done[j & 1]);
+                    tc::commit(&sh->empty_v[s]);  // the V half may be refilled once PV(j) is done
+                    cursor_next(cur, tile_base, p.B, HR);
                 }
             }
             if (!ok) fail(cur.b < p.B ? cur.b : 0);
             // all MMAs this thread issued complete before the TMEM is released
-            tc::commit(&sh->fin);
-            mbar_wait_bounded(&sh->fin, 0);
+            uint64_t *fin = warp == 1 ? &sh->fin : &sh->fin_pv;
+            tc::commit(fin);
+            mbar_wait_bounded(fin, 0);
         }
         __syncwarp();
         tc::fence_before();
-        named_bar_sync(1, 5 * 32);
-        tc::fence_after();
-        tc::tmem_dealloc(tbase, kTcCols);
+        named_bar_sync(1, (2 + kSoftmaxWarps) * 32);
+        if (warp == 1) {
+            tc::fence_after();
+            tc::tmem_dealloc(tbase, kTcCols);
+        }
         return;
     }
 
-    // ===================== softmax warps 2..5: one thread per query row
-    const int quarter = warp & 3;
+    // ===================== softmax warps 2..9: two threads per query row
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;      // 0: keys / output columns 0-63, 1: 64-127
+    const int hc = 64 * half;
     constexpr int kRowsPerQuarter = MROWS / 4;  // 32, or 16 with M=64
     const bool lane_has_row = lane < kRowsPerQuarter;
     const int r = quarter * kRowsPerQuarter + (lane_has_row ? lane : 0);  // row in the group
     const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16);         // this warp's lanes
     const float sc = p.scale_log2;
+    const float2 sc2 = make_float2(sc, sc);
     float m = kNegInf, l = 0.f;
     uint64_t anc = 0;
+    uint32_t pair_uses = 0, seg_uses = 0;
     int L = 0, kv_end = 0, seg_first_tile = 0, kvh = 0, rg = 0, rglob = 0;
     bool seg_is_first = true, warp_active = false, row_valid = false;
+    // This thread's half Q row of the segment starting at `c`: its address,
+    // or null for rows past M (zeros).
+    auto q_half_row = [&](const Cursor &c, bool &active) -> const uint4 * {
+        const int kh = c.pr / p.RG, rgc = c.pr - kh * p.RG;
+        const int rgl = rgc * MROWS + r;
+        active = rgc * MROWS + quarter * kRowsPerQuarter < p.M;
+        if (!(lane_has_row && rgl < p.M)) return nullptr;
+        const int tq = rgl / p.G, gq = rgl - tq * p.G;
+        return reinterpret_cast<const uint4 *>(
+            p.q + (((size_t)c.b * p.T + tq) * p.Hq + kh * p.G + gq) * kD + hc);
+    };
+    // Store the Q tile of the segment starting at `c` into TMEM and signal
+    // it.  Only when no S product of an earlier segment is pending (the
+    // caller has seen the S of that segment's last tile).
+    auto store_q = [&](const Cursor &c) {
+        bool active;
+        const uint4 *qsrc = q_half_row(c, active);
+        if (active) {
+            uint32_t w[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 v = qsrc ? qsrc[k] : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * k] = v.x;
+                w[4 * k + 1] = v.y;
+                w[4 * k + 2] = v.z;
+                w[4 * k + 3] = v.w;
+            }
+            tc::tmem_st32(tl + kColQ + 32 * half, w);
+            tc::wait_st();
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->q_full);
+    };
+    bool q_stored = false;  // the current segment's Q was stored ahead of it
     Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
     long long jt = 0;
     for (long long u = u_begin; u < u_end; ++u, ++jt) {
@@ -276,118 +330,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             warp_active = rg * MROWS + quarter * kRowsPerQuarter < p.M;
             m = kNegInf;
             l = 0.f;
-            int t = 0, g = 0;
-            if (row_valid) {
-                t = rglob / p.G;
-                g = rglob - t * p.G;
-                anc = ancestors(p.parents, p.T, cur.b, t);
-            }
-            // this thread's Q row into the TMEM A tile (zeros past M); the
-            // previous segment's products have all completed (its epilogue
-            // waited for its last PV)
-            if (warp_active) {
-                const uint4 *qsrc = reinterpret_cast<const uint4 *>(
-                    p.q + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = row_valid ? qsrc[8 * h + c] : make_uint4(0u, 0u, 0u, 0u);
-                        w[4 * c] = v.x;
-                        w[4 * c + 1] = v.y;
-                        w[4 * c + 2] = v.z;
-                        w[4 * c + 3] = v.w;
-                    }
-                    tc::tmem_st32(tl + kColQ + 32 * h, w);
-                }
-                tc::wait_st();
-            }
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->q_full);
-            if (cur.tile == 0 && warp == 2 && lane == 0) {
-                // this CTA holds the pair's first tile: record who shares the pair
-                const long long ub = (long long)tile_base[cur.b] * HR + (long long)cur.pr * cur.n;
-                const int c_last = cta_of(U, nctas, ub + cur.n - 1);
-                p.pair_info[(cur.b * p.Hkv + kvh) * p.RG + rg] =
-                    make_int4((int)blockIdx.x, c_last - (int)blockIdx.x + 1,
-                              cta_begin(U, nctas, blockIdx.x) >= ub ? 0 : 1, 0);
+            if (row_valid) anc = ancestors(p.parents, p.T, cur.b, rglob / p.G);
+            if (!q_stored) store_q(cur);
+            q_stored = false;
+            const long long u_next = u + (cur.n - cur.tile);  // first unit of the next segment
+            if (u_next < u_end) {
+                // pull the next segment's Q rows into L2 while this one streams
+                Cursor nx = cur;
+                nx.tile = nx.n - 1;
+                cursor_next(nx, tile_base, p.B, HR);
+                bool act;
+                const uint4 *qn = q_half_row(nx, act);
+                if (qn) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn));
             }
         }
         const bool first_tile = new_seg;  // O is overwritten by this tile's PV
         const int kbase = cur.tile * kBK;
         const bool last_of_pair = cur.tile == cur.n - 1;
-        const uint32_t sbuf = tl + kColS + (uint32_t)(jt & 1) * kBK;
+        const uint32_t sbuf = tl + kColS + (uint32_t)(jt & 1) * kBK + hc;  // this half's S columns
 
-        // ---- S row from TMEM; P written back over it
-        if (!mbar_wait_bounded(&sh->s_full[jt & 1], (uint32_t)((jt >> 1) & 1))) {
+        // ---- half S row from TMEM; P written back over its first 32 columns
+        if (!warp_wait_bounded(&sh->s_full[jt & 1], (uint32_t)((jt >> 1) & 1))) {
             fail(cur.b);
             break;
         }
         tc::fence_after();
         if (warp_active) {
-            float sv[kBK];
-#pragma unroll
-            for (int h = 0; h < kBK / 32; ++h) {
-                uint32_t ra[32];
-                tc::tmem_ld32(sbuf + 32 * h, ra);
+            float sv[64];
+            {
+                uint32_t ra[32], rb[32];
+                tc::tmem_ld32(sbuf, ra);
+                tc::tmem_ld32(sbuf + 32, rb);
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sv[32 * h + j] = __uint_as_float(ra[j]);
-            }
-            if (kbase + kBK > L) {
-#pragma unroll
-                for (int j = 0; j < kBK; ++j) {
-                    const int key = kbase + j;
-                    const bool allowed =
-                        key < L || (key < kv_end && ((anc >> (unsigned)(key - L)) & 1ull));
-                    if (!allowed) sv[j] = kNegInf;
+                for (int j = 0; j < 32; ++j) {
+                    sv[j] = __uint_as_float(ra[j]);
+                    sv[32 + j] = __uint_as_float(rb[j]);
                 }
             }
-            float mx = kNegInf;
+            const int k0 = kbase + hc;  // key of sv[0]
+            if (k0 + 64 > L) {
+                // bit j: key k0 + j visible to this row (a prefix key, or a
+                // new node on the row's root path; anc has no bit past T)
+                const int dl = L - k0;  // keys before L in this half tile (may be <= 0)
+                const uint64_t pre = dl <= 0 ? 0ull : ((1ull << dl) - 1ull);
+                const uint64_t nodes = dl >= 0 ? (dl >= 64 ? 0ull : anc << dl)
+                                               : (-dl >= 64 ? 0ull : anc >> -dl);
+                const uint64_t vis = pre | nodes;
+                const uint32_t vlo = (uint32_t)vis, vhi = (uint32_t)(vis >> 32);
 #pragma unroll
-            for (int j = 0; j < kBK; ++j) mx = fmaxf(mx, sv[j]);
+                for (int j = 0; j < 64; ++j) {
+                    const uint32_t w = j < 32 ? vlo : vhi;
+                    if (!((w >> (j & 31)) & 1u)) sv[j] = kNegInf;
+                }
+            }
+            float mq[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+            for (int j = 0; j < 64; ++j) mq[j & 3] = fmaxf(mq[j & 3], sv[j]);
+            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            // the partner holds the other 64 keys of the same rows
+            sh->xmax[jt & 1][quarter][half][lane] = mx;
+            bool ok = group_sync(&sh->pair[quarter], pair_uses);
+            mx = fmaxf(mx, sh->xmax[jt & 1][quarter][half ^ 1][lane]);
             const float c = mx * sc;
             const bool up = c > m + kRescaleThreshold;
-            bool ok = true;
-            if (__any_sync(0xffffffffu, up)) {
-                const float a = up ? ex2_approx(m - c) : 1.f;
-                if (!first_tile) {
-                    // O holds earlier tiles of this segment: wait for the last PV, rescale in TMEM
-                    ok = mbar_wait_bounded(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1));
-                    tc::fence_after();
-#pragma unroll
-                    for (int h = 0; h < kD / 32; ++h) {
-                        uint32_t ov[32];
-                        tc::tmem_ld32(tl + kColO + 32 * h, ov);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * a);
-                        tc::tmem_st32(tl + kColO + 32 * h, ov);
-                    }
-                }
-                if (up) {
-                    m = c;
-                    l *= a;
-                }
+            const bool any_up = __any_sync(0xffffffffu, up);
+            const float a = up ? ex2_approx(m - c) : 1.f;
+            if (up) {
+                m = c;
+                l *= a;
             }
             const float nb = m == kNegInf ? 0.f : -m;
-            float ls = 0.f;
+            const float2 nb2 = make_float2(nb, nb);
+            float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+            uint32_t pk[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+            for (int j = 0; j < 32; ++j) {
+                const float2 tt = __ffma2_rn(make_float2(sv[2 * j], sv[2 * j + 1]), sc2, nb2);
+                const float2 e = make_float2(ex2_approx(tt.x), ex2_approx(tt.y));
+                if (j & 1) ls1 = __fadd2_rn(ls1, e);
+                else ls0 = __fadd2_rn(ls0, e);
+                pk[j] = pack_bf16x2(e.x, e.y);
+            }
+            tc::tmem_st32(sbuf, pk);
+            l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
+            if (ok && any_up && !first_tile) {
+                // O holds earlier tiles of this segment at the old max: once
+                // the last PV is done, rescale this half of the row in TMEM
+                // (before P is released, so this tile's PV sees it)
+                ok = warp_wait_bounded(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1));
+                tc::fence_after();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float e0 = ex2_approx(fmaf(sv[64 * h + 2 * j], sc, nb));
-                    const float e1 = ex2_approx(fmaf(sv[64 * h + 2 * j + 1], sc, nb));
-                    ls += e0 + e1;
-                    pk[j] = pack_bf16x2(e0, e1);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t ov[32];
+                    tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * a);
+                    tc::tmem_st32(tl + kColO + hc + 32 * h, ov);
                 }
-                tc::tmem_st32(sbuf + 32 * h, pk);  // P columns 0..63 of this S buffer
             }
             tc::wait_st();
-            l += ls;
             if (!ok) {
                 fail(cur.b);
                 break;
@@ -395,10 +438,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (last_of_pair && kbase + kBK > kv_end) {
             // V rows past the sequence's last slot may hold anything (even NaN,
-            // and 0 * NaN is NaN in the product): zero them in this stage
+            // and 0 * NaN is NaN in the product): zero them in this stage,
+            // once its V half has landed
+            if (!warp_wait_bounded(&sh->full_v[jt % STAGES], (uint32_t)((jt / STAGES) & 1))) {
+                fail(cur.b);
+                break;
+            }
             const int z0 = kv_end - kbase;
             uint8_t *vst = smem + (int)(jt % STAGES) * kStageBytes + 2 * kBox;
-            for (int i = (quarter * 32 + lane); i < (kBK - z0) * 16; i += 128) {
+            for (int i = (warp - 2) * 32 + lane; i < (kBK - z0) * 16; i += 32 * kSoftmaxWarps) {
                 const int row = z0 + (i >> 4), c = i & 15;
                 *reinterpret_cast<uint4 *>(vst + (c >> 3) * kBox + sw128(row, c & 7)) =
                     make_uint4(0u, 0u, 0u, 0u);
@@ -409,26 +457,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->p_full[jt & 1]);
 
-        // ---- end of a segment: O row out of TMEM
+        if (last_of_pair && u + 1 < u_end) {
+            // the next segment's Q goes in now (this segment's last S is done),
+            // so its first S product overlaps this segment's epilogue
+            Cursor nx = cur;
+            cursor_next(nx, tile_base, p.B, HR);
+            store_q(nx);
+            q_stored = true;
+        }
+
+        // ---- end of a segment: this half of the O row out of TMEM
         if (last_of_pair || u == u_end - 1) {
-            if (!mbar_wait_bounded(&sh->pv_done[jt & 1], (uint32_t)((jt >> 1) & 1))) {
+            if (!warp_wait_bounded(&sh->pv_done[jt & 1], (uint32_t)((jt >> 1) & 1))) {
                 fail(cur.b);
                 break;
             }
             tc::fence_after();
+            // row sum = first half's part + second half's part (same order in both)
+            sh->xl[quarter][half][lane] = l;
+            if (!group_sync(&sh->pair[quarter], pair_uses)) {
+                fail(cur.b);
+                break;
+            }
+            const float lrow = sh->xl[quarter][0][lane] + sh->xl[quarter][1][lane];
             const bool whole = seg_first_tile == 0 && last_of_pair;
             const int t = row_valid ? rglob / p.G : 0;
             const int g = row_valid ? rglob - t * p.G : 0;
-            uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD;
+            uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD + hc;
             const int slot = seg_is_first ? 0 : 1;
-            float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD;
+            float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
             float *pml = p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 2;
-            const float inv = 1.f / l;
+            const float inv = 1.f / lrow;
             if (warp_active) {
 #pragma unroll
-                for (int h = 0; h < kD / 32; ++h) {
+                for (int h = 0; h < 2; ++h) {
                     uint32_t ov[32];
-                    tc::tmem_ld32(tl + kColO + 32 * h, ov);
+                    tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
                     tc::wait_ld();
                     if (!row_valid) continue;
                     if (whole) {
@@ -451,93 +515,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             tc::fence_before();
-            if (!whole && row_valid) *reinterpret_cast<float2 *>(pml) = make_float2(m, l);
+            if (!whole) {
+                if (row_valid && half == 0) *reinterpret_cast<float2 *>(pml) = make_float2(m, lrow);
+                // A split pair: the CTA whose partial completes the set merges
+                // them all (no CTA waits for another).
+                __threadfence();
+                if (!group_sync(&sh->seg_bar, seg_uses)) {
+                    fail(cur.b);
+                    break;
+                }
+                const int pair_idx = (cur.b * p.Hkv + kvh) * p.RG + rg;
+                const long long ub = (long long)tile_base[cur.b] * HR + (long long)cur.pr * cur.n;
+                const int c0 = cta_of(U, nctas, ub);                            // first contributor
+                const int nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;       // contributors
+                const int slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;        // c0's slot for it
+                if (warp == 2 && lane == 0) {
+                    const int done = atomicAdd(&p.pair_ctr[pair_idx], 1) + 1;
+                    sh->merge = done == nc;
+                    if (done == nc) p.pair_ctr[pair_idx] = 0;  // ready for the next call
+                }
+                if (!group_sync(&sh->seg_bar, seg_uses)) {
+                    fail(cur.b);
+                    break;
+                }
+                if (sh->merge) {
+                    __threadfence();
+                    // out = sum_c 2^(m_c - m*) O_c / sum_c 2^(m_c - m*) l_c; a warp
+                    // per row, four columns per lane
+                    for (int row = warp - 2; row < MROWS; row += kSoftmaxWarps) {
+                        const int rgl = rg * MROWS + row;
+                        if (rgl >= p.M) break;
+                        auto part = [&](int i) -> size_t {
+                            return ((size_t)(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * MROWS + row;
+                        };
+                        float mstar = kNegInf;
+                        for (int i = 0; i < nc; ++i) mstar = fmaxf(mstar, __ldcg(p.part_ml + part(i) * 2));
+                        float lsum = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int i = 0; i < nc; ++i) {
+                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part(i) * 2));
+                            const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
+                            lsum += ml.y * w;
+                            const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + part(i) * kD) + lane);
+                            acc.x += o.x * w;
+                            acc.y += o.y * w;
+                            acc.z += o.z * w;
+                            acc.w += o.w * w;
+                        }
+                        const float inv_l = 1.f / lsum;
+                        const int tq = rgl / p.G, gq = rgl - tq * p.G;
+                        uint16_t *orow2 = p.out + (((size_t)cur.b * p.T + tq) * p.Hq + kvh * p.G + gq) * kD;
+                        uint2 pk2;
+                        pk2.x = pack_bf16x2(acc.x * inv_l, acc.y * inv_l);
+                        pk2.y = pack_bf16x2(acc.z * inv_l, acc.w * inv_l);
+                        *reinterpret_cast<uint2 *>(orow2 + lane * 4) = pk2;
+                    }
+                }
+            }
         }
         cursor_next(cur, tile_base, p.B, HR);
     }
     tc::fence_before();
-    named_bar_sync(1, 5 * 32);
-}
-
-// ---------------------------------------------------------------- split merge
-
-// Merge the partials of every (sequence, KV head, row group) whose tiles fell
-// to several CTAs: out = sum_c 2^(m_c - m*) O_c / sum_c 2^(m_c - m*) l_c.
-// One warp per query row, lanes across the 128 columns; pairs held by one
-// CTA (written directly by the attention kernel) and invalid sequences exit.
-constexpr int kCombineRows = 8;  // rows (warps) per CTA
-
-__global__ void __launch_bounds__(kCombineRows * 32)
-    attention_combine_kernel(const AttnKParams p) {
-    const int chunks = p.rows_per_rg / kCombineRows;
-    const int pair = blockIdx.x / chunks;
-    const int r = (blockIdx.x - pair * chunks) * kCombineRows + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int b = pair / (p.Hkv * p.RG);
-    const int rem = pair - b * p.Hkv * p.RG;
-    const int kvh = rem / p.RG, rg = rem - kvh * p.RG;
-    const int L = p.prefix_lens[b];
-    if (L < 0 || (long long)L + p.T > p.S_max) return;
-    const int rglob = rg * p.rows_per_rg + r;
-    if (rglob >= p.M) return;
-    const int4 info = __ldcg(p.pair_info + pair);
-    const int nc = info.y;
-    if (nc <= 1) return;
-    auto row_index = [&](int i) -> size_t {  // contributor i's partial row
-        const int slot = i == 0 ? info.z : 0;
-        return ((size_t)(info.x + i) * 2 + slot) * p.rows_per_rg + r;
-    };
-    float mstar = kNegInf;
-    for (int i = lane; i < nc; i += 32) mstar = fmaxf(mstar, __ldcg(p.part_ml + row_index(i) * 2));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-    float lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = 0; base < nc; base += 32) {
-        float w = 0.f;
-        const int i = base + lane;
-        if (i < nc) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + row_index(i) * 2));
-            w = ml.x == kNegInf ? 0.f : exp2f(ml.x - mstar);
-            lsum += ml.y * w;
-        }
-        const int cnt = min(32, nc - base);
-        for (int j = 0; j < cnt; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row_index(base + j) * kD) + lane);
-            acc.x += v.x * wj;
-            acc.y += v.y * wj;
-            acc.z += v.z * wj;
-            acc.w += v.w * wj;
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    const float inv = 1.f / lsum;
-    const int t = rglob / p.G, g = rglob - t * p.G;
-    uint16_t *orow = p.out + (((size_t)b * p.T + t) * p.Hq + kvh * p.G + g) * kD;
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(orow + lane * 4) = pk;
+    named_bar_sync(1, (2 + kSoftmaxWarps) * 32);
 }
 
 // ---------------------------------------------------------------- host side
 
 int tc_smem_bytes(int stages, int B) {
-    return 1024 + stages * kStageBytes + (int)sizeof(TcSmem) + (B + 1) * 4 + kTcThreads * 4;
+    return 1024 + stages * kStageBytes + (int)sizeof(TcSmem) + (B + 1) * 4;
 }
 
 const void *tc_kernel_fn(int stages, int mrows) {
     if (stages == 3 && mrows == 128) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 128>);
     if (stages == 3 && mrows == 64) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 64>);
     return nullptr;
-}
-
-sv_status launch_combine(const AttnKParams &p, cudaStream_t st) {
-    const unsigned grid = (unsigned)(p.B * p.Hkv * p.RG * (p.rows_per_rg / kCombineRows));
-    attention_combine_kernel<<<grid, kCombineRows * 32, 0, st>>>(p);
-    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace sv

@@ -13,6 +13,10 @@ constexpr int kBox = kBK * 64 * 2;        // one 128-key x 64-dim bf16 TMA box: 
 constexpr int kStageBytes = 4 * kBox;     // K lo/hi + V lo/hi: 64 KB
 constexpr int kMaxB = 4096;
 constexpr int kMaxT = 64;
+constexpr int kSoftmaxWarps = 8;                      // warps 2-9: two per TMEM lane quarter
+constexpr int kPvWarp = 2 + kSoftmaxWarps;              // issues the PV products
+constexpr int kVLoadWarp = 3 + kSoftmaxWarps;           // loads the V tiles
+constexpr int kTcThreads = 32 * (4 + kSoftmaxWarps);    // + K-load and S-issue warps
 
 struct AttnKParams {
     const uint16_t *q;
@@ -24,7 +28,7 @@ struct AttnKParams {
     float scale_log2;
     float *part_o;   // [grid][2][rows_per_rg][kD]: unnormalised O of split pairs
     float *part_ml;  // [grid][2][rows_per_rg][2]: (max in log2 units, row sum)
-    int4 *pair_info; // [B][Hkv][RG]: (first CTA, CTAs sharing the pair, first CTA's slot, 0)
+    int *pair_ctr;   // [B][Hkv][RG]: partials of a split pair written so far (back to 0 after the merge)
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.
@@ -68,13 +72,19 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const int *tile_base, int
     c.n = c.b < B ? tile_base[c.b + 1] - tile_base[c.b] : 0;
 }
 
-// Consumer-group barrier on an mbarrier (bounded, unlike bar.sync).
+// mbar_wait_bounded by a whole warp with one verdict for all its lanes, so
+// that the warp stays converged for the warp-collective operations after it.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+}
+
+// Barrier of several warps on an mbarrier counting one arrival per warp
+// (bounded, unlike bar.sync); the verdict is the same in every lane.
 __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait_bounded(bar, uses & 1);
+    const bool ok = warp_wait_bounded(bar, uses & 1);
     ++uses;
-    __syncwarp();
     return ok;
 }
 
@@ -92,37 +102,29 @@ constexpr float kRescaleThreshold = 8.0f;
 // (identically in every CTA); CTA 0 also writes each sequence's status
 // (prefix length in range, parent array a topologically ordered tree).
 // Contains __syncthreads: call from every thread of the CTA.
-__device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int *scan_tmp,
-                                              int nt) {
+__device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int nt) {
     const int tid = threadIdx.x;
-    {
-        const int per = (p.B + nt - 1) / nt;
-        const int b0 = tid * per, b1 = min(p.B, b0 + per);
-        int sum = 0;
-        for (int b = b0; b < b1; ++b) {
-            const int L = p.prefix_lens[b];
-            const bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
-            sum += ok ? (L + p.T + kBK - 1) / kBK : 0;
-        }
-        scan_tmp[tid] = sum;
-        __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            for (int i = 0; i < nt; ++i) {
-                const int v = scan_tmp[i];
-                scan_tmp[i] = acc;
-                acc += v;
+    for (int b = tid; b < p.B; b += nt) {
+        const int L = p.prefix_lens[b];
+        const bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
+        tile_base[b] = ok ? (L + p.T + kBK - 1) / kBK : 0;
+    }
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan, 32 sequences at a time
+        int carry = 0;
+        for (int c0 = 0; c0 < p.B; c0 += 32) {
+            const int b = c0 + tid;
+            const int v = b < p.B ? tile_base[b] : 0;
+            int x = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (tid >= off) x += y;
             }
-            tile_base[p.B] = acc;
+            if (b < p.B) tile_base[b] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
         }
-        __syncthreads();
-        int acc = scan_tmp[tid];
-        for (int b = b0; b < b1; ++b) {
-            tile_base[b] = acc;
-            const int L = p.prefix_lens[b];
-            const bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
-            acc += ok ? (L + p.T + kBK - 1) / kBK : 0;
-        }
+        if (tid == 0) tile_base[p.B] = carry;
     }
     if (blockIdx.x == 0 && p.seq_status) {
         for (int b = tid; b < p.B; b += nt) {

@@ -22,6 +22,8 @@ constexpr int kMaxRowVecs = 32;    // 16-byte words per row: D <= 256 bf16
 __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
     __shared__ uint4 stage[2][kCompactBatch * kMaxRowVecs];
     __shared__ int s_src[kCompactBatch];
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.x;
     const int L = a.prefix_lens[b];
     const int acc = a.accepted_len[b];
@@ -91,8 +93,12 @@ __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
 
 sv_status launch_compact_kv(const CompactArgs &a, cudaStream_t st) {
     if (a.D % 8 != 0 || a.D / 8 > kMaxRowVecs) return SV_ERR_UNSUPPORTED;
-    compact_kv_kernel<<<a.B, kCT, 0, st>>>(a);
-    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    CompactArgs ka = a;
+    void *args[] = {&ka};
+    return launch_pdl((const void *)compact_kv_kernel, dim3(a.B), dim3(kCT), 0, st, args) ==
+                   cudaSuccess
+               ? SV_OK
+               : SV_ERR_CUDA;
 }
 
 }  // namespace sv

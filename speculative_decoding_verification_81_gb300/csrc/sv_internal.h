@@ -12,6 +12,25 @@ namespace sv {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launch `fn` with programmatic stream serialisation: the grid may begin
+// launching once the stream's previous kernel lets it (or ends), overlapping
+// that kernel's tail.  Every kernel of this library starts with
+// griddep_wait(), so it reads nothing before its predecessor has finished.
+inline cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, void **args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // ---------------------------------------------------------------- vocabulary pass
 
 // Per (row, chunk) statistics written by the streaming pass.
@@ -44,6 +63,7 @@ struct VocabPlan {
     size_t off_partials;  // B * rows_per_seq * nchunks RowPartial
     size_t off_dec;       // B ChainDecision
     size_t off_chunktot;  // B * res_chunks float2
+    size_t off_tprefix;   // B * res_chunks * 256 float4: per-thread prefixes of the residual draw
     size_t bytes;
 };
 
@@ -86,7 +106,7 @@ struct AttnPlan {
     int rg;           // row groups per (sequence, KV head)
     int grid;         // persistent CTAs
     int smem;         // dynamic shared memory bytes
-    size_t off_pair_info;
+    size_t off_pair_ctr;
     size_t off_part_o;
     size_t off_part_ml;
     size_t bytes;
@@ -94,11 +114,10 @@ struct AttnPlan {
 
 sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan);
 
-// tcgen05 attention kernel and its split merge (sv_attention_tc.cu)
+// tcgen05 attention kernel (sv_attention_tc.cu)
 struct AttnKParams;
 int tc_smem_bytes(int stages, int B);
 const void *tc_kernel_fn(int stages, int mrows);
-sv_status launch_combine(const AttnKParams &p, cudaStream_t stream);
 
 struct AttnArgs {
     const void *q;

@@ -3,14 +3,18 @@
 // Chain (stochastic) acceptance, "Chapitre 9 -- Décodage spéculatif" §9.1:
 //   kernel 1  streams every target/draft logits row once, chunk by chunk
 //             (one CTA per (row, chunk), 16-byte non-temporal loads), and
-//             keeps per chunk the max and the sum of exp2 in the log2 domain.
+//             keeps per chunk the max and the sum of exp2 in the log2 domain
+//             (the chunk's max first, by packed bf16 maxima, then one pass of
+//             exp2 against it with paired f32 arithmetic).
 //             The last CTA to finish a sequence merges its chunks, evaluates
 //             p_i(x_i), q_i(x_i), the decisions u*q < p and the first
 //             rejection a.
 //   kernel 2  draws the final token: per chunk of the row pair at a it sums
-//             the weights r = max(0, p_a - q_a) (or p_N for the bonus); the
-//             last CTA per sequence locates u*S in the chunk prefix, then in
-//             the thread prefix of that chunk, then element by element.
+//             the weights r = max(0, p_a - q_a) (or p_N for the bonus) and
+//             keeps the per-thread prefix sums; the last CTA per sequence
+//             locates u*S in the chunk prefix, then in the stored thread
+//             prefix of that chunk, then the one thread it falls in walks its
+//             elements.
 // Greedy tree acceptance ("Parallel Decoding" glossary, "L'attention en
 // arbre"; §9.1): the same streaming pass in argmax mode, and the last CTA per
 // sequence walks the tree.
@@ -60,17 +64,14 @@ struct Elem<float> {
 
 // ---------------------------------------------------------------- streaming chunk
 
-// Statistics of row[begin, end) over the CTA: per thread the max (scaled by
-// log2 e) and the sum of exp2 (STATS), or the first maximum and its index
-// (ARGMAX).  Vector loads are laid out so that consecutive threads read
-// consecutive 16-byte words; `begin` is a multiple of the vector width.
-template <typename T, bool VEC, bool ARGMAX>
-__device__ __forceinline__ void chunk_thread_stats(const T *row, int begin, int end, float &m,
-                                                   float &s, float &best, int &idx) {
+// First maximum of row[begin, end) over the thread's elements and its index.
+// Vector loads are laid out so that consecutive threads read consecutive
+// 16-byte words; `begin` is a multiple of the vector width.
+template <typename T, bool VEC>
+__device__ __forceinline__ void chunk_thread_argmax(const T *row, int begin, int end,
+                                                    float &best, int &idx) {
     constexpr int PV = Elem<T>::kPerVec;
     const int tid = threadIdx.x;
-    m = kNegInf;
-    s = 0.f;
     best = kNegInf;
     idx = INT_MAX;
     if (VEC) {
@@ -82,86 +83,157 @@ __device__ __forceinline__ void chunk_thread_stats(const T *row, int begin, int 
             const int vi = k * kVT + tid;
             if (vi < nvec) buf[k] = ldg_stream(src + vi);
         }
-        const int tail = begin + nvec * PV + tid;  // < PV leftover elements
-        const bool has_tail = tid < (end - begin) - nvec * PV;
-        const float xt = has_tail ? Elem<T>::at(row, tail) : kNegInf;
-        if (ARGMAX) {
 #pragma unroll
-            for (int k = 0; k < kLoadsPerThread; ++k) {
-                const int vi = k * kVT + tid;
-                if (vi < nvec) {
-                    float x[PV];
-                    Elem<T>::unpack(buf[k], x);
+        for (int k = 0; k < kLoadsPerThread; ++k) {
+            const int vi = k * kVT + tid;
+            if (vi < nvec) {
+                float x[PV];
+                Elem<T>::unpack(buf[k], x);
 #pragma unroll
-                    for (int j = 0; j < PV; ++j)
-                        if (x[j] > best) {
-                            best = x[j];
-                            idx = begin + vi * PV + j;
-                        }
-                }
+                for (int j = 0; j < PV; ++j)
+                    if (x[j] > best) {
+                        best = x[j];
+                        idx = begin + vi * PV + j;
+                    }
             }
-            if (has_tail && xt > best) {
+        }
+        const int tail = begin + nvec * PV + tid;  // < PV leftover elements
+        if (tid < (end - begin) - nvec * PV) {
+            const float xt = Elem<T>::at(row, tail);
+            if (xt > best) {
                 best = xt;
                 idx = tail;
             }
-        } else {
-            float vmax = xt;
-#pragma unroll
-            for (int k = 0; k < kLoadsPerThread; ++k) {
-                const int vi = k * kVT + tid;
-                if (vi < nvec) {
-                    float x[PV];
-                    Elem<T>::unpack(buf[k], x);
-#pragma unroll
-                    for (int j = 0; j < PV; ++j) vmax = fmaxf(vmax, x[j]);
-                }
-            }
-            m = vmax * kLog2e;
-            if (m != kNegInf) {
-                float acc = 0.f;
-#pragma unroll
-                for (int k = 0; k < kLoadsPerThread; ++k) {
-                    const int vi = k * kVT + tid;
-                    if (vi < nvec) {
-                        float x[PV];
-                        Elem<T>::unpack(buf[k], x);
-                        float e[PV];
-#pragma unroll
-                        for (int j = 0; j < PV; ++j) e[j] = ex2_approx(fmaf(x[j], kLog2e, -m));
-                        // pairwise within the vector, then into the running sum
-#pragma unroll
-                        for (int w = 1; w < PV; w *= 2)
-#pragma unroll
-                            for (int j = 0; j < PV; j += 2 * w) e[j] += e[j + w];
-                        acc += e[0];
-                    }
-                }
-                if (has_tail) acc += ex2_approx(fmaf(xt, kLog2e, -m));
-                s = acc;
-            }
         }
     } else {
-        // unaligned rows: scalar loads, element e = begin + k*kVT + tid
-        const int n = end - begin;
-        if (ARGMAX) {
-            for (int e = tid; e < n; e += kVT) {
-                const float x = Elem<T>::at(row, begin + e);
-                if (x > best) {
-                    best = x;
-                    idx = begin + e;
-                }
-            }
-        } else {
-            float vmax = kNegInf;
-            for (int e = tid; e < n; e += kVT) vmax = fmaxf(vmax, Elem<T>::at(row, begin + e));
-            m = vmax * kLog2e;
-            if (m != kNegInf) {
-                float acc = 0.f;
-                for (int e = tid; e < n; e += kVT)
-                    acc += ex2_approx(fmaf(Elem<T>::at(row, begin + e), kLog2e, -m));
-                s = acc;
+        for (int e = begin + tid; e < end; e += kVT) {
+            const float x = Elem<T>::at(row, e);
+            if (x > best) {
+                best = x;
+                idx = e;
             }
         }
+    }
+}
+
+// A 16-byte word of -inf logits: padding that contributes nothing.
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+    return sizeof(T) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                          : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+}
+
+// Largest element of the thread's loaded words (bf16: packed maxima, exact).
+template <typename T>
+__device__ __forceinline__ float words_max(const uint4 (&buf)[kLoadsPerThread]) {
+    if (sizeof(T) == 2) {
+        uint32_t a = bmax2(buf[0].x, buf[0].y), c = bmax2(buf[0].z, buf[0].w);
+#pragma unroll
+        for (int k = 1; k < kLoadsPerThread; ++k) {
+            a = bmax2(a, bmax2(buf[k].x, buf[k].y));
+            c = bmax2(c, bmax2(buf[k].z, buf[k].w));
+        }
+        a = bmax2(a, c);
+        return fmaxf(bf16_lo(a), bf16_hi(a));
+    } else {
+        float a = kNegInf, c = kNegInf;
+#pragma unroll
+        for (int k = 0; k < kLoadsPerThread; ++k) {
+            a = fmaxf(a, fmaxf(__uint_as_float(buf[k].x), __uint_as_float(buf[k].y)));
+            c = fmaxf(c, fmaxf(__uint_as_float(buf[k].z), __uint_as_float(buf[k].w)));
+        }
+        return fmaxf(a, c);
+    }
+}
+
+__device__ __forceinline__ float2 ex2_pair(float2 t) {
+    return make_float2(ex2_approx(t.x), ex2_approx(t.y));
+}
+
+// Sum of exp2(x * log2 e - m) over the thread's loaded words, two elements
+// per f32x2 instruction.
+template <typename T>
+__device__ __forceinline__ float words_sumexp(const uint4 (&buf)[kLoadsPerThread], float m) {
+    const float2 l2 = make_float2(kLog2e, kLog2e), nm = make_float2(-m, -m);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kLoadsPerThread; ++k) {
+        const uint4 v = buf[k];
+        float2 x0, x1, x2, x3;
+        if (sizeof(T) == 2) {
+            x0 = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+            x1 = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+            x2 = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+            x3 = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+            acc0 = __fadd2_rn(acc0, ex2_pair(__ffma2_rn(x0, l2, nm)));
+            acc1 = __fadd2_rn(acc1, ex2_pair(__ffma2_rn(x1, l2, nm)));
+            acc0 = __fadd2_rn(acc0, ex2_pair(__ffma2_rn(x2, l2, nm)));
+            acc1 = __fadd2_rn(acc1, ex2_pair(__ffma2_rn(x3, l2, nm)));
+        } else {
+            x0 = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+            x1 = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+            acc0 = __fadd2_rn(acc0, ex2_pair(__ffma2_rn(x0, l2, nm)));
+            acc1 = __fadd2_rn(acc1, ex2_pair(__ffma2_rn(x1, l2, nm)));
+        }
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+// Statistics of row[begin, end) over the whole CTA: the chunk's maximum
+// first (scaled by log2 e into m), then every thread sums exp2 against that
+// one maximum, so the sums add without rescaling.  (m, s) valid in thread 0.
+template <typename T, bool VEC>
+__device__ __forceinline__ void chunk_cta_stats(const T *row, int begin, int end,
+                                                float *red /* [2 * kVWarps] */, float &m_out,
+                                                float &s_out) {
+    constexpr int PV = Elem<T>::kPerVec;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint4 buf[kLoadsPerThread];
+    float xt = kNegInf;
+    float vmax = kNegInf;
+    if (VEC) {
+        const int nvec = (end - begin) / PV;
+        const uint4 *src = reinterpret_cast<const uint4 *>(row + begin);
+#pragma unroll
+        for (int k = 0; k < kLoadsPerThread; ++k) {
+            const int vi = k * kVT + tid;
+            buf[k] = vi < nvec ? ldg_stream(src + vi) : neg_inf_vec<T>();
+        }
+        const int tail = begin + nvec * PV + tid;  // < PV leftover elements
+        if (tid < (end - begin) - nvec * PV) xt = Elem<T>::at(row, tail);
+        vmax = fmaxf(words_max<T>(buf), xt);
+    } else {
+        for (int e = begin + tid; e < end; e += kVT) vmax = fmaxf(vmax, Elem<T>::at(row, e));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+    if (lane == 0) red[warp] = vmax;
+    __syncthreads();
+    float cmax = red[0];
+#pragma unroll
+    for (int w = 1; w < kVWarps; ++w) cmax = fmaxf(cmax, red[w]);
+    const float m = cmax * kLog2e;
+    float s = 0.f;
+    if (m != kNegInf) {  // the same decision in every thread
+        if (VEC) {
+            s = words_sumexp<T>(buf, m);
+            if (xt != kNegInf) s += ex2_approx(fmaf(xt, kLog2e, -m));
+        } else {
+            for (int e = begin + tid; e < end; e += kVT)
+                s += ex2_approx(fmaf(Elem<T>::at(row, e), kLog2e, -m));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) red[kVWarps + warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kVWarps; ++w) t += red[kVWarps + w];
+        m_out = m;
+        s_out = t;
     }
 }
 
@@ -249,8 +321,8 @@ __host__ __device__ inline WsView ws_view(void *ws, const VocabPlan &p, int B) {
 // ---------------------------------------------------------------- chain: kernel 1
 
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kVT) chain_stats_kernel(ChainArgs a, VocabPlan p, WsView w) {
-    __shared__ float4 scratch[kVWarps];
+__global__ void __launch_bounds__(kVT, 5) chain_stats_kernel(ChainArgs a, VocabPlan p, WsView w) {
+    __shared__ float red[2 * kVWarps];
     __shared__ int s_last;
     __shared__ float sm_m[2 * kMaxChainN + 1], sm_s[2 * kMaxChainN + 1];
     __shared__ int sm_rej[kMaxChainN];
@@ -269,10 +341,10 @@ __global__ void __launch_bounds__(kVT) chain_stats_kernel(ChainArgs a, VocabPlan
     const int begin = c * p.chunk_elems;
     const int end = min(a.V, begin + p.chunk_elems);
 
-    float m, s, best;
-    int idx;
-    chunk_thread_stats<T, VEC, false>(row, begin, end, m, s, best, idx);
-    cta_reduce_stats<false>(m, s, best, idx, scratch);
+    griddep_wait();
+    griddep_launch_dependents();
+    float m = 0.f, s = 0.f;
+    chunk_cta_stats<T, VEC>(row, begin, end, red, m, s);
     if (threadIdx.x == 0) {
         RowPartial out;
         out.m = m;
@@ -368,9 +440,9 @@ __global__ void __launch_bounds__(kVT) chain_stats_kernel(ChainArgs a, VocabPlan
 
 // ---------------------------------------------------------------- chain: kernel 2
 
-// Weights of this thread's contiguous elements [e0, e0 + n) and their
-// sequential sums.  mode 0: r = max(0, p - q); mode 1: r = p.  Written with
-// explicitly rounded operations so that recomputing gives identical bits.
+// Weights of the residual draw.  mode 0: r = max(0, p - q); mode 1: r = p.
+// Written with explicitly rounded operations so that recomputing a weight
+// gives identical bits.
 template <typename T>
 struct ResidualRow {
     const T *trow;
@@ -380,92 +452,128 @@ struct ResidualRow {
     __device__ __forceinline__ float p_at(float lt) const {
         return __fmul_rn(ex2_approx(__fmaf_rn(lt, kLog2e, -ms_t)), inv_t);
     }
-    __device__ __forceinline__ float weight(float lt, float ld, int mode) const {
-        const float pt = p_at(lt);
-        if (mode) return pt;
-        const float pq = __fmul_rn(ex2_approx(__fmaf_rn(ld, kLog2e, -ms_d)), inv_d);
-        return fmaxf(__fsub_rn(pt, pq), 0.f);
+    __device__ __forceinline__ float q_at(float ld) const {
+        return __fmul_rn(ex2_approx(__fmaf_rn(ld, kLog2e, -ms_d)), inv_d);
     }
 };
 
-constexpr int kResElemsPerThread(int per_vec) { return kResLoadsPerThread * per_vec; }
+// Raw 32-bit word `bits` of element i (bf16: zero-extended half).
+template <typename T>
+__device__ __forceinline__ uint32_t elem_bits(const T *row, int i) {
+    if (sizeof(T) == 2) return __ldg(reinterpret_cast<const unsigned short *>(row) + i);
+    return __float_as_uint(__ldg(reinterpret_cast<const float *>(row) + i));
+}
 
+// The thread's elements [e0, e0 + n) of one row as raw 16-byte words;
+// elements at and past n read as -inf (weight 0).
 template <typename T, bool VEC>
-__device__ __forceinline__ void load_res_elems(const T *row, int e0, int n,
-                                               float (&x)[kResLoadsPerThread * Elem<T>::kPerVec]) {
+__device__ __forceinline__ void load_res_words(const T *row, int e0, int n,
+                                               uint4 (&raw)[kResLoadsPerThread]) {
     constexpr int PV = Elem<T>::kPerVec;
-    constexpr int EPT = kResLoadsPerThread * PV;
-    if (VEC && n == EPT) {
+    if (VEC && n == kResLoadsPerThread * PV) {
         const uint4 *src = reinterpret_cast<const uint4 *>(row + e0);
 #pragma unroll
-        for (int k = 0; k < kResLoadsPerThread; ++k) {
-            const uint4 v = __ldg(src + k);
-            float t[PV];
-            Elem<T>::unpack(v, t);
+        for (int k = 0; k < kResLoadsPerThread; ++k) raw[k] = __ldg(src + k);
+        return;
+    }
 #pragma unroll
-            for (int j = 0; j < PV; ++j) x[k * PV + j] = t[j];
+    for (int k = 0; k < kResLoadsPerThread; ++k) {
+        uint32_t w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (sizeof(T) == 2) {
+                const int j = k * PV + 2 * c;
+                const uint32_t lo = j < n ? elem_bits(row, e0 + j) : 0xff80u;
+                const uint32_t hi = j + 1 < n ? elem_bits(row, e0 + j + 1) : 0xff80u;
+                w[c] = lo | (hi << 16);
+            } else {
+                const int j = k * PV + c;
+                w[c] = j < n ? elem_bits(row, e0 + j) : 0xff800000u;
+            }
         }
-    } else {
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) x[j] = j < n ? Elem<T>::at(row, e0 + j) : 0.f;
+        raw[k] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-// Inclusive prefix over the CTA's 256 per-thread values with a fixed order
-// of additions (warp shuffle scan, then warp totals added in warp order);
-// `total` gets the sum of all 256, bitwise equal to thread 255's result.
-__device__ __forceinline__ float cta_incl_scan(float v, float &total, float *wsum /* [8] */) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v = __fadd_rn(v, t);
-    }
-    if (lane == 31) wsum[warp] = v;
-    __syncthreads();
-    float base = 0.f, tot = 0.f;
-    for (int w = 0; w < kVWarps; ++w) {
-        if (w == warp) base = tot;
-        tot = __fadd_rn(tot, wsum[w]);
-    }
-    __syncthreads();
-    total = tot;
-    return warp == 0 ? v : __fadd_rn(base, v);
+// Element j of the raw words (j a compile-time constant after unrolling).
+template <typename T>
+__device__ __forceinline__ float raw_elem(const uint4 (&raw)[kResLoadsPerThread], int j) {
+    constexpr int PV = Elem<T>::kPerVec;
+    const uint4 &v = raw[j / PV];
+    const int c = sizeof(T) == 2 ? (j % PV) / 2 : j % PV;
+    const uint32_t w = c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+    if (sizeof(T) == 2) return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+    return __uint_as_float(w);
 }
 
-template <typename T, bool VEC>
-__device__ __forceinline__ void thread_weight_sums(const ResidualRow<T> &rw, int mode, int e0,
-                                                   int n, float &sr, float &sp,
-                                                   float (&wgt)[kResLoadsPerThread *
-                                                                Elem<T>::kPerVec]) {
+template <typename T>
+__device__ __forceinline__ float raw_weight(const ResidualRow<T> &rw, int mode,
+                                            const uint4 (&rt)[kResLoadsPerThread],
+                                            const uint4 (&rd)[kResLoadsPerThread], int j) {
+    const float pj = rw.p_at(raw_elem<T>(rt, j));
+    if (mode) return pj;
+    return fmaxf(__fsub_rn(pj, rw.q_at(raw_elem<T>(rd, j))), 0.f);
+}
+
+// Sequential sums over the thread's elements: sr of the weights in `mode`,
+// sp of p (the fallback weights).
+template <typename T>
+__device__ __forceinline__ void raw_weight_sums(const ResidualRow<T> &rw, int mode,
+                                                const uint4 (&rt)[kResLoadsPerThread],
+                                                const uint4 (&rd)[kResLoadsPerThread], float &sr,
+                                                float &sp) {
     constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
-    float xt[EPT], xd[EPT];
-    load_res_elems<T, VEC>(rw.trow, e0, n, xt);
-    if (mode == 0) load_res_elems<T, VEC>(rw.drow, e0, n, xd);
     sr = 0.f;
     sp = 0.f;
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
-        float wj = 0.f, pj = 0.f;
-        if (j < n) {
-            pj = rw.p_at(xt[j]);
-            wj = mode == 0 ? rw.weight(xt[j], xd[j], 0) : pj;
-        }
-        wgt[j] = wj;
+        const float pj = rw.p_at(raw_elem<T>(rt, j));
+        const float wj = mode ? pj : fmaxf(__fsub_rn(pj, rw.q_at(raw_elem<T>(rd, j))), 0.f);
         sr = __fadd_rn(sr, wj);
         sp = __fadd_rn(sp, pj);
     }
 }
 
+// Inclusive prefix over the CTA's 256 per-thread pairs with a fixed order of
+// additions (warp shuffle scan, then warp totals added in warp order), both
+// components independently; `total` gets the sums of all 256, bitwise equal
+// to thread 255's result.
+__device__ __forceinline__ float2 cta_incl_scan2(float2 v, float2 &total, float2 *wsum /* [8] */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float tx = __shfl_up_sync(0xffffffffu, v.x, off);
+        const float ty = __shfl_up_sync(0xffffffffu, v.y, off);
+        if (lane >= off) {
+            v.x = __fadd_rn(v.x, tx);
+            v.y = __fadd_rn(v.y, ty);
+        }
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    float2 base = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kVWarps; ++w) {
+        if (w == warp) base = tot;
+        tot.x = __fadd_rn(tot.x, wsum[w].x);
+        tot.y = __fadd_rn(tot.y, wsum[w].y);
+    }
+    __syncthreads();
+    total = tot;
+    return warp == 0 ? v : make_float2(__fadd_rn(base.x, v.x), __fadd_rn(base.y, v.y));
+}
+
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
     constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
-    __shared__ float wsum[kVWarps];
+    __shared__ float2 wsum[kVWarps];
     __shared__ float2 s_tot[kMaxResChunks];
     __shared__ float s_prefix[kVT];
     __shared__ int s_last, s_cstar, s_mode, s_fallback, s_pick_min, s_pick_max;
     __shared__ float s_base, s_theta;
 
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.x / p.res_chunks;
     const int c = blockIdx.x - b * p.res_chunks;
     const ChainDecision d = w.dec[b];
@@ -481,17 +589,24 @@ __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabP
     rw.inv_d = d.a < a.N ? __frcp_rn(d.s_d) : 0.f;
     const int mode0 = d.a < a.N ? 0 : 1;
 
-    const int cbeg = c * p.res_chunk_elems;
-    const int e0 = cbeg + threadIdx.x * EPT;
+    // ---- every CTA: weight sums of its chunk, per-thread prefixes kept
+    const int e0 = c * p.res_chunk_elems + threadIdx.x * EPT;
     const int n = max(0, min(EPT, a.V - e0));
-    float wgt[EPT];
+    uint4 rt[kResLoadsPerThread], rd[kResLoadsPerThread];
+    load_res_words<T, VEC>(rw.trow, e0, n, rt);
+    if (mode0 == 0) load_res_words<T, VEC>(rw.drow, e0, n, rd);
     float sr, sp;
-    thread_weight_sums<T, VEC>(rw, mode0, e0, n, sr, sp, wgt);
-    float tot_r, tot_p;
-    cta_incl_scan(sr, tot_r, wsum);
-    cta_incl_scan(sp, tot_p, wsum);
+    raw_weight_sums<T>(rw, mode0, rt, rd, sr, sp);
+    float2 tot;
+    const float2 incl = cta_incl_scan2(make_float2(sr, sp), tot, wsum);
+    float2 *tprefix = reinterpret_cast<float2 *>(reinterpret_cast<char *>(w.chunktot) +
+                                                 (p.off_tprefix - p.off_chunktot)) +
+                      (size_t)b * p.res_chunks * kVT;
+    tprefix[(size_t)c * kVT + threadIdx.x] = incl;
+    __threadfence();
+    __syncthreads();
     if (threadIdx.x == 0) {
-        w.chunktot[(size_t)b * p.res_chunks + c] = make_float2(tot_r, tot_p);
+        w.chunktot[(size_t)b * p.res_chunks + c] = tot;
         __threadfence();
         const int old = atomicAdd(&w.counters[a.B + b], 1);
         s_last = (old == p.res_chunks - 1);
@@ -548,39 +663,41 @@ __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabP
     const float base = s_base, theta = s_theta;
     const int f0 = cstar * p.res_chunk_elems + threadIdx.x * EPT;
     const int fn = max(0, min(EPT, a.V - f0));
-    thread_weight_sums<T, VEC>(rw, mode, f0, fn, sr, sp, wgt);
-    const float own = mode == 0 ? sr : sp;
-    float total;
-    const float incl = cta_incl_scan(own, total, wsum);
-    s_prefix[threadIdx.x] = incl;
+    // ---- then in the thread prefix of chunk cstar, as its CTA stored it
+    const float2 tp = __ldcg(tprefix + (size_t)cstar * kVT + threadIdx.x);
+    const float incl_m = mode == 0 ? tp.x : tp.y;
+    s_prefix[threadIdx.x] = incl_m;
     if (!s_fallback) {
         // first thread whose inclusive prefix passes u * S
-        if (__fadd_rn(base, incl) > theta) atomicMin(&s_pick_min, (int)threadIdx.x);
+        if (__fadd_rn(base, incl_m) > theta) atomicMin(&s_pick_min, (int)threadIdx.x);
     } else {
-        // last thread holding any weight
-        if (own > 0.f) atomicMax(&s_pick_max, (int)threadIdx.x);
+        // last thread holding any weight (rare: recompute the thread sums)
+        load_res_words<T, VEC>(rw.trow, f0, fn, rt);
+        if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
+        raw_weight_sums<T>(rw, mode, rt, rd, sr, sp);
+        if ((mode == 0 ? sr : sp) > 0.f) atomicMax(&s_pick_max, (int)threadIdx.x);
     }
     __syncthreads();
     int pick = s_fallback ? s_pick_max : s_pick_min;
     if (pick < 0 || pick >= kVT) pick = kVT - 1;
     if ((int)threadIdx.x == pick) {
+        // ---- and element by element in that thread's range
+        load_res_words<T, VEC>(rw.trow, f0, fn, rt);
+        if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
         int y = -1;
         if (!s_fallback) {
             float acc = __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f);
-            for (int j = 0; j < fn; ++j) {
-                acc = __fadd_rn(acc, wgt[j]);
-                if (acc > theta) {
-                    y = f0 + j;
-                    break;
-                }
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                acc = __fadd_rn(acc, raw_weight<T>(rw, mode, rt, rd, j));
+                if (y < 0 && j < fn && acc > theta) y = f0 + j;
             }
         }
-        if (y < 0)
-            for (int j = fn - 1; j >= 0; --j)
-                if (wgt[j] > 0.f) {
-                    y = f0 + j;
-                    break;
-                }
+        if (y < 0) {
+#pragma unroll
+            for (int j = 0; j < EPT; ++j)
+                if (j < fn && raw_weight<T>(rw, mode, rt, rd, j) > 0.f) y = f0 + j;
+        }
         if (y < 0) y = max(f0, 0);
         a.out_tokens[(size_t)b * (a.N + 1) + d.a] = y;
         w.counters[a.B + b] = 0;  // ready for the next call
@@ -608,9 +725,12 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
     const int begin = c * p.chunk_elems;
     const int end = min(a.V, begin + p.chunk_elems);
 
-    float m, s, best;
+    griddep_wait();
+    griddep_launch_dependents();
+    float best;
     int idx;
-    chunk_thread_stats<T, VEC, true>(row, begin, end, m, s, best, idx);
+    chunk_thread_argmax<T, VEC>(row, begin, end, best, idx);
+    float m = 0.f, s = 0.f;
     cta_reduce_stats<true>(m, s, best, idx, scratch);
     if (threadIdx.x == 0) {
         RowPartial out;
@@ -699,45 +819,58 @@ VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
     off = align_up(off + (chain ? sizeof(ChainDecision) * (size_t)B : 0), 256);
     p.off_chunktot = off;
     off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks : 0), 256);
+    p.off_tprefix = off;
+    off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks * kVT : 0), 256);
     p.bytes = off;
     return p;
 }
 
 template <typename T, bool VEC>
-static void launch_chain_t(const ChainArgs &a, const VocabPlan &p, const WsView &w, cudaStream_t st) {
+static cudaError_t launch_chain_t(ChainArgs a, VocabPlan p, WsView w, cudaStream_t st) {
+    void *args[] = {&a, &p, &w};
     const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
-    chain_stats_kernel<T, VEC><<<items, kVT, 0, st>>>(a, p, w);
+    cudaError_t e = launch_pdl((const void *)chain_stats_kernel<T, VEC>, dim3(items), dim3(kVT),
+                               0, st, args);
+    if (e != cudaSuccess) return e;
     const unsigned res = (unsigned)((size_t)a.B * p.res_chunks);
-    chain_residual_kernel<T, VEC><<<res, kVT, 0, st>>>(a, p, w);
+    return launch_pdl((const void *)chain_residual_kernel<T, VEC>, dim3(res), dim3(kVT), 0, st,
+                      args);
+}
+
+template <typename T, bool VEC>
+static cudaError_t launch_tree_t(TreeArgs a, VocabPlan p, WsView w, cudaStream_t st) {
+    void *args[] = {&a, &p, &w};
+    const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
+    return launch_pdl((const void *)tree_stats_kernel<T, VEC>, dim3(items), dim3(kVT), 0, st,
+                      args);
 }
 
 sv_status launch_verify_chain(const ChainArgs &a, int dtype, const VocabPlan &p, void *ws,
                               cudaStream_t st) {
     if (a.N > kMaxChainN || p.res_chunks > kMaxResChunks) return SV_ERR_UNSUPPORTED;
     const WsView w = ws_view(ws, p, a.B);
-    if (dtype == SV_BF16) {
-        if (p.vec) launch_chain_t<uint16_t, true>(a, p, w, st);
-        else launch_chain_t<uint16_t, false>(a, p, w, st);
-    } else {
-        if (p.vec) launch_chain_t<float, true>(a, p, w, st);
-        else launch_chain_t<float, false>(a, p, w, st);
-    }
-    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    cudaError_t e;
+    if (dtype == SV_BF16)
+        e = p.vec ? launch_chain_t<uint16_t, true>(a, p, w, st)
+                  : launch_chain_t<uint16_t, false>(a, p, w, st);
+    else
+        e = p.vec ? launch_chain_t<float, true>(a, p, w, st)
+                  : launch_chain_t<float, false>(a, p, w, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 sv_status launch_verify_tree_greedy(const TreeArgs &a, int dtype, const VocabPlan &p, void *ws,
                                     cudaStream_t st) {
     if (a.T > kMaxTreeT) return SV_ERR_UNSUPPORTED;
     const WsView w = ws_view(ws, p, a.B);
-    const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
-    if (dtype == SV_BF16) {
-        if (p.vec) tree_stats_kernel<uint16_t, true><<<items, kVT, 0, st>>>(a, p, w);
-        else tree_stats_kernel<uint16_t, false><<<items, kVT, 0, st>>>(a, p, w);
-    } else {
-        if (p.vec) tree_stats_kernel<float, true><<<items, kVT, 0, st>>>(a, p, w);
-        else tree_stats_kernel<float, false><<<items, kVT, 0, st>>>(a, p, w);
-    }
-    return cudaPeekAtLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    cudaError_t e;
+    if (dtype == SV_BF16)
+        e = p.vec ? launch_tree_t<uint16_t, true>(a, p, w, st)
+                  : launch_tree_t<uint16_t, false>(a, p, w, st);
+    else
+        e = p.vec ? launch_tree_t<float, true>(a, p, w, st)
+                  : launch_tree_t<float, false>(a, p, w, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace sv
