@@ -84,12 +84,12 @@ static int cached_occupancy(const void *fn, int threads, int max_smem, int smem,
 
 static void plan_workspace(AttnPlan &pl, int B, int Hkv) {
     size_t off = 0;
-    pl.off_pair_ctr = off;
-    off = align_up(off + sizeof(int) * (size_t)B * Hkv * pl.rg, 256);
+    pl.off_pair_ctr = off;  // [pair][arrived, ready][softmax warp]
+    off = align_up(off + sizeof(int) * (size_t)B * Hkv * pl.rg * 2 * kSoftmaxWarps, 256);
     pl.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.rows_per_rg * kD, 256);
     pl.off_part_ml = off;
-    off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.rows_per_rg * 2, 256);
+    off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.rows_per_rg * 4, 256);
     pl.bytes = off;
 }
 

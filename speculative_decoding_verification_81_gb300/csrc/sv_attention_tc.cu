@@ -13,9 +13,8 @@
 // the flat list of (sequence, KV head, 128-row group, 64-key tile) units; a
 // persistent grid (one CTA per SM) takes equal contiguous ranges of it, so the
 // load is balanced whatever the prefix lengths.  A (sequence, KV head) whose
-// tiles fall to several CTAs leaves one partial (O, max, sum) per CTA; the
-// CTA whose partial completes the set (a per-pair arrival counter) merges
-// them into the output rows.  Inside a CTA (12 warps):
+// tiles fall to several CTAs is merged by the CTA that finishes its part
+// last: it combines the others' partials (O, max, sum) with its own O.  Inside a CTA (12 warps):
 //
 //   warps 0, 11 TMA producers: K and V tiles (2-D tensor maps, 128-byte
 //               swizzle) into a ring of STAGES shared-memory stages, K and
@@ -75,8 +74,6 @@ struct TcSmem {
     uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t q_full, fin, fin_pv;
     uint64_t pair[4];            // the two softmax warps of each lane quarter
-    uint64_t seg_bar;            // all softmax warps, at the end of a split segment
-    int merge;                   // this CTA merges the split pair it just finished
     float xmax[2][4][2][32];     // [tile parity][quarter][half][lane]: half-row tile maxima
     float xl[4][2][32];          // [quarter][half][lane]: half-row sums at a segment end
     uint32_t tmem;
@@ -117,7 +114,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(&sh->fin, 1);
         mbar_init(&sh->fin_pv, 1);
         for (int q = 0; q < 4; ++q) mbar_init(&sh->pair[q], 2);
-        mbar_init(&sh->seg_bar, kSoftmaxWarps);
         sh->abort_flag = 0;
         fence_mbar_init();
     }
@@ -276,7 +272,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float2 sc2 = make_float2(sc, sc);
     float m = kNegInf, l = 0.f;
     uint64_t anc = 0;
-    uint32_t pair_uses = 0, seg_uses = 0;
+    uint32_t pair_uses = 0;
+    int *ready_ctr = nullptr;  // a partial of this warp waiting to be flagged ready
+    // The warp's partial writes are visible before the ready count moves.
+    auto flag_ready = [&](int *c) {
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            atomicAdd(c, 1);
+        }
+        __syncwarp();
+    };
     int L = 0, kv_end = 0, seg_first_tile = 0, kvh = 0, rg = 0, rglob = 0;
     bool seg_is_first = true, warp_active = false, row_valid = false;
     // This thread's half Q row of the segment starting at `c`: its address,
@@ -456,6 +462,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->p_full[jt & 1]);
+        if (ready_ctr) {  // the partial left at the previous tile has drained by now
+            flag_ready(ready_ctr);
+            ready_ctr = nullptr;
+        }
 
         if (last_of_pair && u + 1 < u_end) {
             // the next segment's Q goes in now (this segment's last S is done),
@@ -484,26 +494,100 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int t = row_valid ? rglob / p.G : 0;
             const int g = row_valid ? rglob - t * p.G : 0;
             uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD + hc;
-            const int slot = seg_is_first ? 0 : 1;
-            float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
-            float *pml = p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 2;
-            const float inv = 1.f / lrow;
+            // A split pair: per warp (its rows, its half of the columns) the
+            // contributing CTAs arrive on a counter; the last to arrive merges
+            // the others' partials into its own O, the others leave a partial
+            // and flag it ready once it is visible.  Nobody waits for a CTA
+            // that has not already arrived.
+            int *ctr = nullptr;
+            int nc = 1, c0 = 0, slot0 = 0;
+            bool merger = whole;
+            if (!whole && warp_active) {
+                const long long ub = (long long)tile_base[cur.b] * HR + (long long)cur.pr * cur.n;
+                c0 = cta_of(U, nctas, ub);
+                nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;
+                slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;
+                ctr = p.pair_ctr + ((size_t)((cur.b * p.Hkv + kvh) * p.RG + rg) * 2) * kSoftmaxWarps +
+                      (warp - 2);
+                int pos = 0;
+                if (lane == 0) pos = atomicAdd(ctr, 1);
+                pos = __shfl_sync(0xffffffffu, pos, 0);
+                merger = pos == nc - 1;
+                if (merger) {
+                    bool ready = true;
+                    if (lane == 0) {
+                        const long long t0 = clock64();
+                        while (ld_acquire_gpu(ctr + kSoftmaxWarps) < nc - 1)
+                            if (clock64() - t0 > kWaitCycles) {
+                                ready = false;
+                                break;
+                            }
+                        if (ready) {
+                            ctr[0] = 0;  // ready for the next call
+                            ctr[kSoftmaxWarps] = 0;
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    __syncwarp();  // the others' partials are read after lane 0's acquire
+                }
+            }
             if (warp_active) {
+                // the other contributors' (max, sum) of this row half
+                auto part_row = [&](int i) -> size_t {
+                    return ((size_t)(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
+                };
+                float mstar = m, lsum = lrow, wown = 1.f;
+                if (!whole && merger && row_valid) {
+                    for (int i = 0; i < nc; ++i) {
+                        if (c0 + i == (int)blockIdx.x) continue;
+                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
+                        if (ml.x == kNegInf) continue;
+                        const float mn = fmaxf(mstar, ml.x);
+                        lsum = lsum * ex2_approx(mstar - mn) + ml.y * ex2_approx(ml.x - mn);
+                        wown *= ex2_approx(mstar - mn);
+                        mstar = mn;
+                    }
+                }
+                const float inv = 1.f / lsum;
+                const int slot = seg_is_first ? 0 : 1;
+                float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t ov[32];
                     tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
                     tc::wait_ld();
                     if (!row_valid) continue;
-                    if (whole) {
+                    if (merger) {
+                        float acc[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(ov[j]) * wown;
+                        if (!whole)
+                            for (int i = 0; i < nc; ++i) {
+                                if (c0 + i == (int)blockIdx.x) continue;
+                                const size_t pr_i = part_row(i);
+                                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr_i * 4 + half * 2));
+                                const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
+                                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + pr_i * kD + hc + 32 * h);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    const float4 o = __ldcg(src + c);
+                                    acc[4 * c] += o.x * w;
+                                    acc[4 * c + 1] += o.y * w;
+                                    acc[4 * c + 2] += o.z * w;
+                                    acc[4 * c + 3] += o.w * w;
+                                }
+                            }
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = w;
+                            uint4 wv;
+                            wv.x = pack_bf16x2(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
+                            wv.y = pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+                            wv.z = pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+                            wv.w = pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+                            *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = wv;
                         }
                     } else {
 #pragma unroll
@@ -513,68 +597,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
                     }
                 }
+                if (!merger) {
+                    if (row_valid)
+                        *reinterpret_cast<float2 *>(p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 4 +
+                                                    half * 2) = make_float2(m, lrow);
+                    ready_ctr = ctr + kSoftmaxWarps;  // flagged after the next tile (or at the end)
+                }
             }
             tc::fence_before();
-            if (!whole) {
-                if (row_valid && half == 0) *reinterpret_cast<float2 *>(pml) = make_float2(m, lrow);
-                // A split pair: the CTA whose partial completes the set merges
-                // them all (no CTA waits for another).
-                __threadfence();
-                if (!group_sync(&sh->seg_bar, seg_uses)) {
-                    fail(cur.b);
-                    break;
-                }
-                const int pair_idx = (cur.b * p.Hkv + kvh) * p.RG + rg;
-                const long long ub = (long long)tile_base[cur.b] * HR + (long long)cur.pr * cur.n;
-                const int c0 = cta_of(U, nctas, ub);                            // first contributor
-                const int nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;       // contributors
-                const int slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;        // c0's slot for it
-                if (warp == 2 && lane == 0) {
-                    const int done = atomicAdd(&p.pair_ctr[pair_idx], 1) + 1;
-                    sh->merge = done == nc;
-                    if (done == nc) p.pair_ctr[pair_idx] = 0;  // ready for the next call
-                }
-                if (!group_sync(&sh->seg_bar, seg_uses)) {
-                    fail(cur.b);
-                    break;
-                }
-                if (sh->merge) {
-                    __threadfence();
-                    // out = sum_c 2^(m_c - m*) O_c / sum_c 2^(m_c - m*) l_c; a warp
-                    // per row, four columns per lane
-                    for (int row = warp - 2; row < MROWS; row += kSoftmaxWarps) {
-                        const int rgl = rg * MROWS + row;
-                        if (rgl >= p.M) break;
-                        auto part = [&](int i) -> size_t {
-                            return ((size_t)(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * MROWS + row;
-                        };
-                        float mstar = kNegInf;
-                        for (int i = 0; i < nc; ++i) mstar = fmaxf(mstar, __ldcg(p.part_ml + part(i) * 2));
-                        float lsum = 0.f;
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int i = 0; i < nc; ++i) {
-                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part(i) * 2));
-                            const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
-                            lsum += ml.y * w;
-                            const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + part(i) * kD) + lane);
-                            acc.x += o.x * w;
-                            acc.y += o.y * w;
-                            acc.z += o.z * w;
-                            acc.w += o.w * w;
-                        }
-                        const float inv_l = 1.f / lsum;
-                        const int tq = rgl / p.G, gq = rgl - tq * p.G;
-                        uint16_t *orow2 = p.out + (((size_t)cur.b * p.T + tq) * p.Hq + kvh * p.G + gq) * kD;
-                        uint2 pk2;
-                        pk2.x = pack_bf16x2(acc.x * inv_l, acc.y * inv_l);
-                        pk2.y = pack_bf16x2(acc.z * inv_l, acc.w * inv_l);
-                        *reinterpret_cast<uint2 *>(orow2 + lane * 4) = pk2;
-                    }
-                }
-            }
         }
         cursor_next(cur, tile_base, p.B, HR);
     }
+    if (ready_ctr) flag_ready(ready_ctr);
     tc::fence_before();
     named_bar_sync(1, (2 + kSoftmaxWarps) * 32);
 }

@@ -27,8 +27,8 @@ struct AttnKParams {
     int B, T, Hq, Hkv, G, S_max, M, RG, rows_per_rg;
     float scale_log2;
     float *part_o;   // [grid][2][rows_per_rg][kD]: unnormalised O of split pairs
-    float *part_ml;  // [grid][2][rows_per_rg][2]: (max in log2 units, row sum)
-    int *pair_ctr;   // [B][Hkv][RG]: partials of a split pair written so far (back to 0 after the merge)
+    float *part_ml;  // [grid][2][rows_per_rg][2 halves][2]: (max in log2 units, row sum)
+    int *pair_ctr;   // [B][Hkv][RG][2][8]: per softmax warp, CTAs arrived / partials ready (0 after the merge)
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.
