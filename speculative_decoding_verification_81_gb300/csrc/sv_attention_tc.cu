@@ -539,16 +539,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 auto part_row = [&](int i) -> size_t {
                     return ((size_t)(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
                 };
-                float mstar = m, lsum = lrow, wown = 1.f;
+                // The merge takes the contributors in index order with the same
+                // arithmetic whoever merges, so the result does not depend on
+                // which CTA finished last.
+                const int self = (int)blockIdx.x - c0;
+                auto ml_of = [&](int i) -> float2 {
+                    return i == self ? make_float2(m, lrow)
+                                     : __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
+                };
+                float mstar = m, lsum = lrow;
                 if (!whole && merger && row_valid) {
+                    for (int i = 0; i < nc; ++i) mstar = fmaxf(mstar, ml_of(i).x);
+                    lsum = 0.f;
                     for (int i = 0; i < nc; ++i) {
-                        if (c0 + i == (int)blockIdx.x) continue;
-                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
-                        if (ml.x == kNegInf) continue;
-                        const float mn = fmaxf(mstar, ml.x);
-                        lsum = lsum * ex2_approx(mstar - mn) + ml.y * ex2_approx(ml.x - mn);
-                        wown *= ex2_approx(mstar - mn);
-                        mstar = mn;
+                        const float2 ml = ml_of(i);
+                        const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
+                        lsum = __fmaf_rn(ml.y, w, lsum);
                     }
                 }
                 const float inv = 1.f / lsum;
@@ -563,23 +569,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (merger) {
                         float acc[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(ov[j]) * wown;
-                        if (!whole)
-                            for (int i = 0; i < nc; ++i) {
-                                if (c0 + i == (int)blockIdx.x) continue;
-                                const size_t pr_i = part_row(i);
-                                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr_i * 4 + half * 2));
-                                const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
-                                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + pr_i * kD + hc + 32 * h);
+                        for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(ov[j]);
+                        if (!whole) {
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) {
-                                    const float4 o = __ldcg(src + c);
-                                    acc[4 * c] += o.x * w;
-                                    acc[4 * c + 1] += o.y * w;
-                                    acc[4 * c + 2] += o.z * w;
-                                    acc[4 * c + 3] += o.w * w;
+                            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+                            for (int i = 0; i < nc; ++i) {
+                                const float2 ml = ml_of(i);
+                                const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
+                                if (i == self) {
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(__uint_as_float(ov[j]), w, acc[j]);
+                                } else {
+                                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + part_row(i) * kD + hc + 32 * h);
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) {
+                                        const float4 o = __ldcg(src + c);
+                                        acc[4 * c] = __fmaf_rn(o.x, w, acc[4 * c]);
+                                        acc[4 * c + 1] = __fmaf_rn(o.y, w, acc[4 * c + 1]);
+                                        acc[4 * c + 2] = __fmaf_rn(o.z, w, acc[4 * c + 2]);
+                                        acc[4 * c + 3] = __fmaf_rn(o.w, w, acc[4 * c + 3]);
+                                    }
                                 }
                             }
+                        }
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             uint4 wv;

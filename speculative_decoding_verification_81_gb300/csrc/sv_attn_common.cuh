@@ -72,12 +72,6 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const int *tile_base, int
     c.n = c.b < B ? tile_base[c.b + 1] - tile_base[c.b] : 0;
 }
 
-// mbar_wait_bounded by a whole warp with one verdict for all its lanes, so
-// that the warp stays converged for the warp-collective operations after it.
-__device__ __forceinline__ bool warp_wait_bounded(uint64_t *bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
-}
-
 // Barrier of several warps on an mbarrier counting one arrival per warp
 // (bounded, unlike bar.sync); the verdict is the same in every lane.
 __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses) {

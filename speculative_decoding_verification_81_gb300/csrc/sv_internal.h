@@ -41,7 +41,7 @@ struct RowPartial {
     int idx;     // its index, smallest among equal maxima; INT_MAX if none
 };
 
-// Per-sequence result of the chain decision stage, consumed by the residual draw.
+// Per-sequence result of the chain decisions, taken at the start of the residual draw.
 struct ChainDecision {
     int a;       // first rejected position, N if all accepted, -1 if the sequence is invalid
     int pad;
@@ -59,9 +59,9 @@ struct VocabPlan {
     int res_chunks;       // residual-draw chunks per sequence (chain only)
     int res_chunk_elems;
     bool vec;             // rows are 16-byte aligned: vector loads
+    int recs_per_unit;    // chain: (max, sum) records per (row, chunk)
     size_t off_counters;  // 2*B ints
     size_t off_partials;  // B * rows_per_seq * nchunks RowPartial
-    size_t off_dec;       // B ChainDecision
     size_t off_chunktot;  // B * res_chunks float2
     size_t off_tprefix;   // B * res_chunks * 256 float4: per-thread prefixes of the residual draw
     size_t bytes;

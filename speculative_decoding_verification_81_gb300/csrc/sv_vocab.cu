@@ -124,12 +124,12 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
 }
 
 // Largest element of the thread's loaded words (bf16: packed maxima, exact).
-template <typename T>
-__device__ __forceinline__ float words_max(const uint4 (&buf)[kLoadsPerThread]) {
+template <typename T, int NW = kLoadsPerThread>
+__device__ __forceinline__ float words_max(const uint4 (&buf)[NW]) {
     if (sizeof(T) == 2) {
         uint32_t a = bmax2(buf[0].x, buf[0].y), c = bmax2(buf[0].z, buf[0].w);
 #pragma unroll
-        for (int k = 1; k < kLoadsPerThread; ++k) {
+        for (int k = 1; k < NW; ++k) {
             a = bmax2(a, bmax2(buf[k].x, buf[k].y));
             c = bmax2(c, bmax2(buf[k].z, buf[k].w));
         }
@@ -138,7 +138,7 @@ __device__ __forceinline__ float words_max(const uint4 (&buf)[kLoadsPerThread]) 
     } else {
         float a = kNegInf, c = kNegInf;
 #pragma unroll
-        for (int k = 0; k < kLoadsPerThread; ++k) {
+        for (int k = 0; k < NW; ++k) {
             a = fmaxf(a, fmaxf(__uint_as_float(buf[k].x), __uint_as_float(buf[k].y)));
             c = fmaxf(c, fmaxf(__uint_as_float(buf[k].z), __uint_as_float(buf[k].w)));
         }
@@ -152,12 +152,12 @@ __device__ __forceinline__ float2 ex2_pair(float2 t) {
 
 // Sum of exp2(x * log2 e - m) over the thread's loaded words, two elements
 // per f32x2 instruction.
-template <typename T>
-__device__ __forceinline__ float words_sumexp(const uint4 (&buf)[kLoadsPerThread], float m) {
+template <typename T, int NW = kLoadsPerThread>
+__device__ __forceinline__ float words_sumexp(const uint4 (&buf)[NW], float m) {
     const float2 l2 = make_float2(kLog2e, kLog2e), nm = make_float2(-m, -m);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kLoadsPerThread; ++k) {
+    for (int k = 0; k < NW; ++k) {
         const uint4 v = buf[k];
         float2 x0, x1, x2, x3;
         if (sizeof(T) == 2) {
@@ -303,7 +303,6 @@ __device__ __forceinline__ RowPartial warp_merge_row(const RowPartial *parts, in
 struct WsView {
     int *counters;  // [B] streaming pass, [B] residual draw
     RowPartial *partials;
-    ChainDecision *dec;
     float2 *chunktot;
 };
 
@@ -312,7 +311,6 @@ __host__ __device__ inline WsView ws_view(void *ws, const VocabPlan &p, int B) {
     WsView v;
     v.counters = reinterpret_cast<int *>(base + p.off_counters);
     v.partials = reinterpret_cast<RowPartial *>(base + p.off_partials);
-    v.dec = reinterpret_cast<ChainDecision *>(base + p.off_dec);
     v.chunktot = reinterpret_cast<float2 *>(base + p.off_chunktot);
     (void)B;
     return v;
@@ -323,11 +321,6 @@ __host__ __device__ inline WsView ws_view(void *ws, const VocabPlan &p, int B) {
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT, 5) chain_stats_kernel(ChainArgs a, VocabPlan p, WsView w) {
     __shared__ float red[2 * kVWarps];
-    __shared__ int s_last;
-    __shared__ float sm_m[2 * kMaxChainN + 1], sm_s[2 * kMaxChainN + 1];
-    __shared__ int sm_rej[kMaxChainN];
-    __shared__ int sm_bad;
-
     const int R = 2 * a.N + 1;
     const int per_seq = R * p.nchunks;
     const int item = blockIdx.x;
@@ -345,96 +338,117 @@ __global__ void __launch_bounds__(kVT, 5) chain_stats_kernel(ChainArgs a, VocabP
     griddep_launch_dependents();
     float m = 0.f, s = 0.f;
     chunk_cta_stats<T, VEC>(row, begin, end, red, m, s);
-    if (threadIdx.x == 0) {
-        RowPartial out;
-        out.m = m;
-        out.s = s;
-        out.best = 0.f;
-        out.idx = 0;
-        w.partials[item] = out;
-        __threadfence();
-        const int old = atomicAdd(&w.counters[b], 1);
-        s_last = (old == per_seq - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+    if (threadIdx.x == 0) reinterpret_cast<float2 *>(w.partials)[item] = make_float2(m, s);
+}
 
-    // ---- this CTA is the last of sequence b: merge, decide
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int rr = warp; rr < R; rr += kVWarps) {
-        const RowPartial rp =
-            warp_merge_row<false>(w.partials + (size_t)b * per_seq + (size_t)rr * p.nchunks,
-                                  p.nchunks);
-        if (lane == 0) {
-            sm_m[rr] = rp.m;
-            sm_s[rr] = rp.s;
-        }
-    }
-    if (threadIdx.x == 0) sm_bad = 0;
-    __syncthreads();
-    if (threadIdx.x < R) {
-        const float mm = sm_m[threadIdx.x], ss = sm_s[threadIdx.x];
-        if (!(isfinite(mm) && isfinite(ss) && ss > 0.f)) atomicOr(&sm_bad, 1);
-    }
-    if (threadIdx.x < a.N) {
-        const int i = threadIdx.x;
-        const int x = a.tokens[(size_t)b * a.N + i];
-        float pp = 0.f, qq = 0.f;
-        bool rej = true;
-        if (x < 0 || x >= a.V) {
-            atomicOr(&sm_bad, 1);
-        } else {
-            const T *trow = static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
-            const T *drow = static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V;
-            const double lt = Elem<T>::at(trow, x), ld = Elem<T>::at(drow, x);
-            pp = static_cast<float>(exp2(lt * kLog2eD - (double)sm_m[i]) / (double)sm_s[i]);
-            qq = static_cast<float>(exp2(ld * kLog2eD - (double)sm_m[a.N + 1 + i]) /
-                                    (double)sm_s[a.N + 1 + i]);
-            const float u = a.u_accept[(size_t)b * a.N + i];
-            rej = !(u * qq < pp);
-        }
-        sm_rej[i] = rej;
-        if (a.probs) {
-            a.probs[((size_t)b * a.N + i) * 2 + 0] = pp;
-            a.probs[((size_t)b * a.N + i) * 2 + 1] = qq;
-        }
-    }
-    __syncthreads();
+// ---------------------------------------------------------------- chain: kernel 1, streaming form
+
+// Rows 16-byte aligned (V * element size a multiple of 16): a persistent grid
+// (one CTA per SM) streams the units (sequence, row, 32 KB chunk) of a
+// balanced contiguous range through a ring of shared-memory stages filled by
+// 1-D bulk copies (one producer thread), so the loads never wait for the
+// arithmetic.  Two groups of 8 consumer warps take alternate units; each warp
+// reduces an eighth of its unit on its own -- its maximum first (packed bf16
+// maxima), then the sum of exp2 against it -- and leaves one (max, sum)
+// record; no CTA-wide barrier.  The decisions are taken by the next kernel.
+constexpr int kSWarps = 16;                      // consumer warps
+constexpr int kSThreads = 32 * (kSWarps + 1);    // + the producer warp
+constexpr int kSUnitBytes = 32768;               // one unit = one chunk of a row
+constexpr int kSStages = 6;
+constexpr int kSGroupWarps = kSWarps / 2;        // warps sharing one unit
+constexpr int kSWordsPerLane = kSUnitBytes / 16 / kSGroupWarps / 32;  // 16-byte words: 8
+
+template <typename T>
+__global__ void __launch_bounds__(kSThreads, 1)
+    chain_stats_stream_kernel(ChainArgs a, VocabPlan p, WsView w) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kSStages * kSUnitBytes
+    __shared__ uint64_t full[kSStages], empty[kSStages];
+    constexpr int PV = Elem<T>::kPerVec;
+    constexpr int kUnitElems = kSUnitBytes / (int)sizeof(T);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = 2 * a.N + 1;
+    const int per_seq = R * p.nchunks;
+    const long long U = (long long)a.B * per_seq;
+    const long long u_begin = U * blockIdx.x / gridDim.x, u_end = U * (blockIdx.x + 1) / gridDim.x;
+    float2 *rec = reinterpret_cast<float2 *>(w.partials);  // [B][R][nchunks][kSGroupWarps]
+
     if (threadIdx.x == 0) {
-        int acc = a.N;
-        for (int i = 0; i < a.N; ++i)
-            if (sm_rej[i]) {
-                acc = i;
-                break;
-            }
-        ChainDecision d;
-        d.pad = 0;
-        d.pad2[0] = d.pad2[1] = 0.f;
-        if (sm_bad) {
-            d.a = -1;
-            d.ms_t = d.s_t = d.ms_d = d.s_d = 0.f;
-            a.accepted_len[b] = -1;
-            if (a.seq_status) a.seq_status[b] = SV_ERR_BAD_INPUT;
-        } else {
-            d.a = acc;
-            d.ms_t = sm_m[acc];
-            d.s_t = sm_s[acc];
-            d.ms_d = acc < a.N ? sm_m[a.N + 1 + acc] : 0.f;
-            d.s_d = acc < a.N ? sm_s[a.N + 1 + acc] : 0.f;
-            a.accepted_len[b] = acc;
-            if (a.seq_status) a.seq_status[b] = SV_OK;
+        for (int s = 0; s < kSStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kSGroupWarps);
         }
-        w.dec[b] = d;
-        w.counters[b] = 0;  // ready for the next call
-        s_last = sm_bad ? -1 : acc;
+        fence_mbar_init();
     }
     __syncthreads();
-    const int acc = s_last;
-    for (int i = threadIdx.x; i <= a.N; i += kVT) {
-        int v = -1;
-        if (acc >= 0 && i < acc) v = a.tokens[(size_t)b * a.N + i];
-        if (acc < 0 || i != acc) a.out_tokens[(size_t)b * (a.N + 1) + i] = v;
+    griddep_wait();
+    griddep_launch_dependents();
+
+    if (warp == kSWarps) {
+        // ================= producer: one bulk copy per unit
+        if (lane == 0) {
+            long long k = 0;
+            for (long long u = u_begin; u < u_end; ++u, ++k) {
+                const int s = (int)(k % kSStages);
+                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((k / kSStages) & 1) ^ 1))) break;
+                const int b = (int)(u / per_seq);
+                const int rem = (int)(u - (long long)b * per_seq);
+                const int r = rem / p.nchunks, c = rem - r * p.nchunks;
+                const T *row = r <= a.N
+                    ? static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + r) * a.V
+                    : static_cast<const T *>(a.draft) + ((size_t)b * a.N + (r - a.N - 1)) * a.V;
+                const int begin = c * kUnitElems;
+                const uint32_t bytes = (uint32_t)(min(kUnitElems, a.V - begin) * (int)sizeof(T));
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_load(ring + s * kSUnitBytes, row + begin, bytes, &full[s]);
+            }
+            // every copy issued must land before the CTA may exit
+            const long long first = k > kSStages ? k - kSStages : 0;
+            for (long long j = first; j < k; ++j)
+                mbar_wait_bounded(&full[j % kSStages], (uint32_t)((j / kSStages) & 1));
+        }
+        return;
+    }
+
+    // ================= consumers
+    // Two groups of eight warps (one pair per SM sub-partition) take
+    // alternate units, so the groups drift out of step and one group's
+    // exponentials overlap the other's loads and shuffles.
+    // group of warp w: (w / 4) % 2, so each sub-partition (w % 4) holds two
+    // warps of each group; warp within the group: 0..7
+    const int grp = (warp >> 2) & 1, gw = ((warp >> 3) << 2) | (warp & 3);
+    for (long long k = grp; k < u_end - u_begin; k += 2) {
+        const long long u = u_begin + k;
+        const int s = (int)(k % kSStages);
+        const int b = (int)(u / per_seq);
+        const int rem = (int)(u - (long long)b * per_seq);
+        const int r = rem / p.nchunks, c = rem - r * p.nchunks;
+        const int n = min(kUnitElems, a.V - c * kUnitElems);  // elements in this unit (a multiple of PV)
+        if (!warp_wait_bounded(&full[s], (uint32_t)((k / kSStages) & 1))) {
+            // the record stays unwritten; the sequence is reported
+            if (lane == 0 && a.seq_status) a.seq_status[b] = SV_ERR_TIMEOUT;
+            break;
+        }
+        uint4 buf[kSWordsPerLane];
+#pragma unroll
+        for (int q = 0; q < kSWordsPerLane; ++q) {
+            const int wi = (gw * kSWordsPerLane + q) * 32 + lane;  // 16-byte word of the unit
+            buf[q] = wi * PV < n ? *reinterpret_cast<const uint4 *>(ring + s * kSUnitBytes + wi * 16)
+                                 : neg_inf_vec<T>();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the words are in registers
+        // the warp's maximum first, then every lane sums exp2 against it
+        // (no exponentials spent on merging lanes)
+        float vmax = words_max<T, kSWordsPerLane>(buf);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+        const float m = vmax * kLog2e;
+        float sum = m == kNegInf ? 0.f : words_sumexp<T, kSWordsPerLane>(buf, m);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0)
+            rec[(((size_t)b * R + r) * p.nchunks + c) * kSGroupWarps + gw] = make_float2(m, sum);
     }
 }
 
@@ -563,6 +577,101 @@ __device__ __forceinline__ float2 cta_incl_scan2(float2 v, float2 &total, float2
     return warp == 0 ? v : make_float2(__fadd_rn(base.x, v.x), __fadd_rn(base.y, v.y));
 }
 
+// Decisions of sequence b from its rows' (max, sum) records, by a whole CTA:
+// a warp per row merges the row's records (their maximum first, then the sums
+// rescaled to it); p_i(x_i) and q_i(x_i) in double from the row statistics
+// (p and q on separate threads); accept while u_i * q < p; a = the first
+// rejection (N if none, -1 if the sequence is invalid).  With `outputs` it
+// also writes accepted_len, seq_status, probs and the emitted tokens except
+// the one drawn at position a.
+template <typename T>
+__device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, const VocabPlan &p,
+                                                         const float2 *rec, int b, bool outputs) {
+    __shared__ float s_ms[2 * kMaxChainN + 1][2];
+    __shared__ float s_pq[kMaxChainN][2];
+    __shared__ int s_bad, s_first;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = 2 * a.N + 1;
+    const int per_row = p.nchunks * p.recs_per_unit;
+    if (tid == 0) {
+        s_bad = 0;
+        s_first = a.N;
+    }
+    for (int rr = warp; rr < R; rr += kVWarps) {
+        const float2 *rw = rec + ((size_t)b * R + rr) * per_row;
+        float mx = kNegInf;
+        for (int i = lane; i < per_row; i += 32) mx = fmaxf(mx, __ldcg(rw + i).x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float sum = 0.f;
+        if (mx != kNegInf)
+            for (int i = lane; i < per_row; i += 32) {
+                const float2 v = __ldcg(rw + i);
+                if (v.x != kNegInf) sum += v.y * exp2f(v.x - mx);
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) {
+            s_ms[rr][0] = mx;
+            s_ms[rr][1] = sum;
+        }
+    }
+    __syncthreads();
+    if (tid < R) {
+        const float mm = s_ms[tid][0], ss = s_ms[tid][1];
+        if (!(isfinite(mm) && isfinite(ss) && ss > 0.f)) atomicOr(&s_bad, 1);
+    }
+    // p_i on threads 0..N-1, q_i on threads 64..64+N-1
+    const int i = tid & 63;
+    const int is_q = (tid >> 6) & 1;
+    if (tid < 128 && i < a.N) {
+        const int x = a.tokens[(size_t)b * a.N + i];
+        float v = 0.f;
+        if (x < 0 || x >= a.V) {
+            atomicOr(&s_bad, 1);
+        } else {
+            const int ri = is_q ? a.N + 1 + i : i;
+            const T *row = is_q ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V
+                                : static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
+            const double l = Elem<T>::at(row, x);
+            v = static_cast<float>(exp2(l * kLog2eD - (double)s_ms[ri][0]) / (double)s_ms[ri][1]);
+        }
+        s_pq[i][is_q] = v;
+    }
+    __syncthreads();
+    if (tid < a.N) {
+        const float pp = s_pq[tid][0], qq = s_pq[tid][1];
+        if (!(a.u_accept[(size_t)b * a.N + tid] * qq < pp)) atomicMin(&s_first, tid);
+        if (outputs && a.probs) {
+            a.probs[((size_t)b * a.N + tid) * 2 + 0] = pp;
+            a.probs[((size_t)b * a.N + tid) * 2 + 1] = qq;
+        }
+    }
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    const int acc = bad ? -1 : s_first;
+    ChainDecision d;
+    d.pad = 0;
+    d.pad2[0] = d.pad2[1] = 0.f;
+    d.a = acc;
+    d.ms_t = bad ? 0.f : s_ms[acc][0];
+    d.s_t = bad ? 0.f : s_ms[acc][1];
+    d.ms_d = (!bad && acc < a.N) ? s_ms[a.N + 1 + acc][0] : 0.f;
+    d.s_d = (!bad && acc < a.N) ? s_ms[a.N + 1 + acc][1] : 0.f;
+    if (outputs) {
+        if (tid == 0) {
+            a.accepted_len[b] = acc;
+            if (a.seq_status) a.seq_status[b] = bad ? SV_ERR_BAD_INPUT : SV_OK;
+        }
+        for (int j = tid; j <= a.N; j += kVT) {
+            int v = -1;
+            if (acc >= 0 && j < acc) v = a.tokens[(size_t)b * a.N + j];
+            if (acc < 0 || j != acc) a.out_tokens[(size_t)b * (a.N + 1) + j] = v;
+        }
+    }
+    return d;
+}
+
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
     constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
@@ -576,8 +685,10 @@ __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabP
     griddep_launch_dependents();
     const int b = blockIdx.x / p.res_chunks;
     const int c = blockIdx.x - b * p.res_chunks;
-    const ChainDecision d = w.dec[b];
-    if (d.a < 0) return;  // invalid sequence: kernel 1 already wrote -1s
+    // every CTA of the sequence takes the decisions; the first one writes them
+    const ChainDecision d =
+        decide_sequence<T>(a, p, reinterpret_cast<const float2 *>(w.partials), b, c == 0);
+    if (d.a < 0) return;  // invalid sequence: -1s written above
 
     ResidualRow<T> rw;
     rw.trow = static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + d.a) * a.V;
@@ -810,13 +921,14 @@ VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
     p.res_chunk_elems = kVT * kResLoadsPerThread * per_vec;
     p.res_chunks = chain ? (V + p.res_chunk_elems - 1) / p.res_chunk_elems : 0;
     p.vec = ((size_t)V * esz) % 16 == 0;
+    p.recs_per_unit = p.vec ? kSGroupWarps : 1;
     size_t off = 0;
     p.off_counters = off;
     off = align_up(off + sizeof(int) * 2 * (size_t)B, 256);
-    p.off_partials = off;
-    off = align_up(off + sizeof(RowPartial) * (size_t)B * p.rows_per_seq * p.nchunks, 256);
-    p.off_dec = off;
-    off = align_up(off + (chain ? sizeof(ChainDecision) * (size_t)B : 0), 256);
+    p.off_partials = off;  // tree: a RowPartial per (row, chunk); chain: recs_per_unit (max, sum) records
+    off = align_up(off + (chain ? sizeof(float2) * p.recs_per_unit : sizeof(RowPartial)) * (size_t)B *
+                             p.rows_per_seq * p.nchunks,
+                   256);
     p.off_chunktot = off;
     off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks : 0), 256);
     p.off_tprefix = off;
@@ -829,8 +941,28 @@ template <typename T, bool VEC>
 static cudaError_t launch_chain_t(ChainArgs a, VocabPlan p, WsView w, cudaStream_t st) {
     void *args[] = {&a, &p, &w};
     const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
-    cudaError_t e = launch_pdl((const void *)chain_stats_kernel<T, VEC>, dim3(items), dim3(kVT),
-                               0, st, args);
+    cudaError_t e;
+    if constexpr (VEC) {
+        // streaming form: one CTA per SM (fewer when there are fewer units)
+        const void *fn = (const void *)chain_stats_stream_kernel<T>;
+        const int smem = kSStages * kSUnitBytes;
+        static int attr_set[64] = {0};
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if (dev < 64 && !attr_set[dev]) {
+            if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+                cudaSuccess)
+                return e;
+            attr_set[dev] = 1;
+        }
+        const int sms = device_sm_count();
+        if (sms <= 0) return cudaErrorUnknown;
+        const unsigned grid = (unsigned)(items < (unsigned)sms ? items : (unsigned)sms);
+        e = launch_pdl(fn, dim3(grid), dim3(kSThreads), smem, st, args);
+    } else {
+        e = launch_pdl((const void *)chain_stats_kernel<T, VEC>, dim3(items), dim3(kVT), 0, st,
+                       args);
+    }
     if (e != cudaSuccess) return e;
     const unsigned res = (unsigned)((size_t)a.B * p.res_chunks);
     return launch_pdl((const void *)chain_residual_kernel<T, VEC>, dim3(res), dim3(kVT), 0, st,
