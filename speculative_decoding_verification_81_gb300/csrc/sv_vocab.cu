@@ -579,7 +579,7 @@ __device__ __forceinline__ float2 cta_incl_scan2(float2 v, float2 &total, float2
 
 // Decisions of sequence b from its rows' (max, sum) records, by a whole CTA:
 // a warp per row merges the row's records (their maximum first, then the sums
-// rescaled to it); p_i(x_i) and q_i(x_i) in double from the row statistics
+// rescaled to it, 64 records at a time); p_i(x_i) and q_i(x_i) in double from the row statistics
 // (p and q on separate threads); accept while u_i * q < p; a = the first
 // rejection (N if none, -1 if the sequence is invalid).  With `outputs` it
 // also writes accepted_len, seq_status, probs and the emitted tokens except
@@ -597,23 +597,69 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
         s_bad = 0;
         s_first = a.N;
     }
-    for (int rr = warp; rr < R; rr += kVWarps) {
-        const float2 *rw = rec + ((size_t)b * R + rr) * per_row;
-        float mx = kNegInf;
-        for (int i = lane; i < per_row; i += 32) mx = fmaxf(mx, __ldcg(rw + i).x);
+    // p_i on threads 0..N-1, q_i on threads 64..64+N-1: the drafted token and
+    // its logit are fetched first, overlapping the record merges below
+    const int i = tid & 63;
+    const int is_q = (tid >> 6) & 1;
+    const bool pos_thread = tid < 128 && i < a.N;
+    double l = 0.0;
+    bool tok_ok = false;
+    if (pos_thread) {
+        const int x = a.tokens[(size_t)b * a.N + i];
+        tok_ok = x >= 0 && x < a.V;
+        if (tok_ok) {
+            const T *row = is_q ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V
+                                : static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
+            l = Elem<T>::at(row, x);
+        }
+    }
+    // rows: a warp per row, four rows of a warp in flight at a time; each row
+    // merges its records once (their maximum, then the rescaled sums)
+    for (int r0 = warp; r0 < R; r0 += 4 * kVWarps) {
+        float mx[4], sm[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float sum = 0.f;
-        if (mx != kNegInf)
-            for (int i = lane; i < per_row; i += 32) {
-                const float2 v = __ldcg(rw + i);
-                if (v.x != kNegInf) sum += v.y * exp2f(v.x - mx);
+        for (int q = 0; q < 4; ++q) {
+            mx[q] = kNegInf;
+            sm[q] = 0.f;
+        }
+        for (int i0 = 0; i0 < per_row; i0 += 64) {
+            float2 v[4][2];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rr = r0 + q * kVWarps;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int ii = i0 + lane + 32 * j;
+                    v[q][j] = (rr < R && ii < per_row)
+                                  ? __ldcg(rec + ((size_t)b * R + rr) * per_row + ii)
+                                  : make_float2(kNegInf, 0.f);
+                }
             }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            for (int q = 0; q < 4; ++q) {
+                float cm = fmaxf(v[q][0].x, v[q][1].x);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+                float cs = 0.f;
+                if (cm != kNegInf) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        if (v[q][j].x != kNegInf) cs += v[q][j].y * exp2f(v[q][j].x - cm);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+                merge_ms(mx[q], sm[q], cm, cs);
+            }
+        }
         if (lane == 0) {
-            s_ms[rr][0] = mx;
-            s_ms[rr][1] = sum;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rr = r0 + q * kVWarps;
+                if (rr < R) {
+                    s_ms[rr][0] = mx[q];
+                    s_ms[rr][1] = sm[q];
+                }
+            }
         }
     }
     __syncthreads();
@@ -621,19 +667,12 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
         const float mm = s_ms[tid][0], ss = s_ms[tid][1];
         if (!(isfinite(mm) && isfinite(ss) && ss > 0.f)) atomicOr(&s_bad, 1);
     }
-    // p_i on threads 0..N-1, q_i on threads 64..64+N-1
-    const int i = tid & 63;
-    const int is_q = (tid >> 6) & 1;
-    if (tid < 128 && i < a.N) {
-        const int x = a.tokens[(size_t)b * a.N + i];
+    if (pos_thread) {
         float v = 0.f;
-        if (x < 0 || x >= a.V) {
+        if (!tok_ok) {
             atomicOr(&s_bad, 1);
         } else {
             const int ri = is_q ? a.N + 1 + i : i;
-            const T *row = is_q ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V
-                                : static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
-            const double l = Elem<T>::at(row, x);
             v = static_cast<float>(exp2(l * kLog2eD - (double)s_ms[ri][0]) / (double)s_ms[ri][1]);
         }
         s_pq[i][is_q] = v;
