@@ -35,7 +35,6 @@ constexpr int kResLoadsPerThread = 4;      // 16-byte loads per thread per row i
 constexpr int kMaxChainN = 63;
 constexpr int kMaxTreeT = 1024;
 constexpr int kMaxResChunks = 256;
-constexpr double kLog2eD = 1.4426950408889634073599;
 
 template <typename T>
 struct Elem;
@@ -577,10 +576,38 @@ __device__ __forceinline__ float2 cta_incl_scan2(float2 v, float2 &total, float2
     return warp == 0 ? v : make_float2(__fadd_rn(base.x, v.x), __fadd_rn(base.y, v.y));
 }
 
+// 2^(l * log2 e - m) in single precision to about 2e-7 relative: l * log2 e
+// is carried as an exact float pair (log2 e split into a float and its
+// remainder), the difference with m by an error-free two-sum, the integer
+// part of the exponent applied by ldexp and the fraction f in [-1/2, 1/2]
+// by the degree-7 Taylor polynomial of e^(f ln 2) (remainder below 6e-9).
+__device__ __forceinline__ float exp2_diff_accurate(float l, float m) {
+    constexpr float kL2eHi = 1.4426950216293335f;   // float nearest log2 e
+    constexpr float kL2eLo = 1.925963033500011e-08f;  // log2 e - kL2eHi
+    constexpr float kLn2 = 0.6931471824645996f;
+    const float hi = l * kL2eHi;
+    const float lo = __fmaf_rn(l, kL2eHi, -hi) + l * kL2eLo;  // l * log2 e = hi + lo
+    const float s = __fsub_rn(hi, m);                           // two-sum of hi and -m
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fsub_rn(hi, __fsub_rn(s, bp)) + __fsub_rn(-m, bp);
+    const float n = rintf(s);
+    const float f = __fsub_rn(s, n) + (err + lo);  // exponent = n + f
+    const float x = f * kLn2;
+    float e = 1.f + x * (1.f / 7.f);
+    e = 1.f + x * (1.f / 6.f) * e;
+    e = 1.f + x * (1.f / 5.f) * e;
+    e = 1.f + x * (1.f / 4.f) * e;
+    e = 1.f + x * (1.f / 3.f) * e;
+    e = 1.f + x * (1.f / 2.f) * e;
+    e = 1.f + x * e;  // e^x = 1 + x (1 + x/2 (1 + x/3 (...)))
+    return ldexpf(e, (int)n);
+}
+
 // Decisions of sequence b from its rows' (max, sum) records, by a whole CTA:
 // a warp per row merges the row's records (their maximum first, then the sums
-// rescaled to it, 64 records at a time); p_i(x_i) and q_i(x_i) in double from the row statistics
-// (p and q on separate threads); accept while u_i * q < p; a = the first
+// rescaled to it, 64 records at a time); p_i(x_i) and q_i(x_i) from the row
+// statistics by exp2_diff_accurate (p and q on separate threads); accept while
+// u_i * q < p; a = the first
 // rejection (N if none, -1 if the sequence is invalid).  With `outputs` it
 // also writes accepted_len, seq_status, probs and the emitted tokens except
 // the one drawn at position a.
@@ -602,7 +629,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     const int i = tid & 63;
     const int is_q = (tid >> 6) & 1;
     const bool pos_thread = tid < 128 && i < a.N;
-    double l = 0.0;
+    float l = 0.f;
     bool tok_ok = false;
     if (pos_thread) {
         const int x = a.tokens[(size_t)b * a.N + i];
@@ -673,7 +700,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
             atomicOr(&s_bad, 1);
         } else {
             const int ri = is_q ? a.N + 1 + i : i;
-            v = static_cast<float>(exp2(l * kLog2eD - (double)s_ms[ri][0]) / (double)s_ms[ri][1]);
+            v = __fdiv_rn(exp2_diff_accurate(l, s_ms[ri][0]), s_ms[ri][1]);
         }
         s_pq[i][is_q] = v;
     }
