@@ -353,6 +353,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool first_tile = new_seg;  // O is overwritten by this tile's PV
         const int kbase = cur.tile * kBK;
         const bool last_of_pair = cur.tile == cur.n - 1;
+        const bool seg_end = last_of_pair || u == u_end - 1;
+        const bool whole = seg_first_tile == 0 && last_of_pair;
+        // The last tile of a split segment: arrive on the pair's counter now
+        // (per warp: its rows, its half of the columns), so the atomic's round
+        // trip overlaps this tile; the last CTA to arrive merges.
+        int *ctr = nullptr;
+        int arrived = 0;
+        if (seg_end && !whole && warp_active) {
+            ctr = p.pair_ctr + ((size_t)((cur.b * p.Hkv + kvh) * p.RG + rg) * 2) * kSoftmaxWarps + (warp - 2);
+            if (lane == 0) arrived = atomicAdd(ctr, 1);
+        }
         const uint32_t sbuf = tl + kColS + (uint32_t)(jt & 1) * kBK + hc;  // this half's S columns
 
         // ---- half S row from TMEM; P written back over its first 32 columns
@@ -490,16 +501,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             const float lrow = sh->xl[quarter][0][lane] + sh->xl[quarter][1][lane];
-            const bool whole = seg_first_tile == 0 && last_of_pair;
             const int t = row_valid ? rglob / p.G : 0;
             const int g = row_valid ? rglob - t * p.G : 0;
             uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD + hc;
-            // A split pair: per warp (its rows, its half of the columns) the
-            // contributing CTAs arrive on a counter; the last to arrive merges
-            // the others' partials into its own O, the others leave a partial
-            // and flag it ready once it is visible.  Nobody waits for a CTA
-            // that has not already arrived.
-            int *ctr = nullptr;
+            // A split pair: the last CTA to arrive merges the others'
+            // partials into its own O; the others leave a partial and flag it
+            // ready once it is visible.  Nobody waits for a CTA that has not
+            // already arrived.
             int nc = 1, c0 = 0, slot0 = 0;
             bool merger = whole;
             if (!whole && warp_active) {
@@ -507,11 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 c0 = cta_of(U, nctas, ub);
                 nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;
                 slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;
-                ctr = p.pair_ctr + ((size_t)((cur.b * p.Hkv + kvh) * p.RG + rg) * 2) * kSoftmaxWarps +
-                      (warp - 2);
-                int pos = 0;
-                if (lane == 0) pos = atomicAdd(ctr, 1);
-                pos = __shfl_sync(0xffffffffu, pos, 0);
+                const int pos = __shfl_sync(0xffffffffu, arrived, 0);
                 merger = pos == nc - 1;
                 if (merger) {
                     bool ready = true;
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                      : __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
                 };
                 float mstar = m, lsum = lrow;
-                if (!whole && merger && row_valid) {
+                if (!whole && merger && row_valid && nc != 2) {
                     for (int i = 0; i < nc; ++i) mstar = fmaxf(mstar, ml_of(i).x);
                     lsum = 0.f;
                     for (int i = 0; i < nc; ++i) {
@@ -557,12 +561,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         lsum = __fmaf_rn(ml.y, w, lsum);
                     }
                 }
-                const float inv = 1.f / lsum;
                 const int slot = seg_is_first ? 0 : 1;
                 float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
+                if (!whole && merger && nc == 2) {  // (the same in every lane)
+                    // two contributors (the usual split): the other's partial
+                    // fetched in one go, then the same arithmetic as below
+                    const int oth = 1 - self;
+                    const size_t pro = part_row(oth);
+                    float2 mlo = make_float2(kNegInf, 0.f);
+                    float4 oo[16];
+                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + pro * kD + hc);
+                    if (row_valid) {
+                        mlo = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pro * 4 + half * 2));
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) oo[c] = __ldcg(src + c);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) oo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    const float ms2 = fmaxf(m, mlo.x);
+                    const float ws = m == kNegInf ? 0.f : ex2_approx(m - ms2);
+                    const float wo = mlo.x == kNegInf ? 0.f : ex2_approx(mlo.x - ms2);
+                    const float w0 = self == 0 ? ws : wo, w1 = self == 0 ? wo : ws;
+                    const float l0 = self == 0 ? lrow : mlo.y, l1 = self == 0 ? mlo.y : lrow;
+                    const float inv2 = 1.f / __fmaf_rn(l1, w1, __fmaf_rn(l0, w0, 0.f));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t ov[32];
+                        __syncwarp();  // converged for the warp-collective load
+                        tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
+                        tc::wait_ld();
+                        if (!row_valid) continue;
+                        float acc[32];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 o = oo[8 * h + c];
+                            const float xo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float xs = __uint_as_float(ov[4 * c + e]);
+                                const float x0 = self == 0 ? xs : xo[e], x1 = self == 0 ? xo[e] : xs;
+                                acc[4 * c + e] = __fmaf_rn(x1, w1, __fmaf_rn(x0, w0, 0.f));
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 wv;
+                            wv.x = pack_bf16x2(acc[8 * c + 0] * inv2, acc[8 * c + 1] * inv2);
+                            wv.y = pack_bf16x2(acc[8 * c + 2] * inv2, acc[8 * c + 3] * inv2);
+                            wv.z = pack_bf16x2(acc[8 * c + 4] * inv2, acc[8 * c + 5] * inv2);
+                            wv.w = pack_bf16x2(acc[8 * c + 6] * inv2, acc[8 * c + 7] * inv2);
+                            *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = wv;
+                        }
+                    }
+                } else {
+                const float inv = 1.f / lsum;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t ov[32];
+                    __syncwarp();  // converged for the warp-collective load
                     tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
                     tc::wait_ld();
                     if (!row_valid) continue;
@@ -609,11 +666,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
                     }
                 }
+                }
                 if (!merger) {
                     if (row_valid)
                         *reinterpret_cast<float2 *>(p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 4 +
                                                     half * 2) = make_float2(m, lrow);
-                    ready_ctr = ctr + kSoftmaxWarps;  // flagged after the next tile (or at the end)
+                    if (ctr) ready_ctr = ctr + kSoftmaxWarps;  // flagged after the next tile (or at the end)
                 }
             }
             tc::fence_before();
