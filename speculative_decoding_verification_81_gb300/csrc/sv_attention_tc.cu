@@ -320,6 +320,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive(&sh->q_full);
     };
     bool q_stored = false;  // the current segment's Q was stored ahead of it
+    int next_L = 0;         // the next segment's prefix length, read ahead
+    bool have_next_L = false;
     Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
     long long jt = 0;
     for (long long u = u_begin; u < u_end; ++u, ++jt) {
@@ -327,7 +329,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (new_seg) {
             kvh = cur.pr / p.RG;
             rg = cur.pr - kvh * p.RG;
-            L = p.prefix_lens[cur.b];
+            L = have_next_L ? next_L : p.prefix_lens[cur.b];
+            have_next_L = false;
             kv_end = L + p.T;
             seg_first_tile = cur.tile;
             seg_is_first = (u == u_begin);
@@ -339,16 +342,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (row_valid) anc = ancestors(p.parents, p.T, cur.b, rglob / p.G);
             if (!q_stored) store_q(cur);
             q_stored = false;
-            const long long u_next = u + (cur.n - cur.tile);  // first unit of the next segment
-            if (u_next < u_end) {
-                // pull the next segment's Q rows into L2 while this one streams
-                Cursor nx = cur;
-                nx.tile = nx.n - 1;
-                cursor_next(nx, tile_base, p.B, HR);
-                bool act;
-                const uint4 *qn = q_half_row(nx, act);
-                if (qn) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn));
-            }
+        }
+        // A few tiles before this segment ends: pull the next segment's Q rows
+        // into L2 and read its prefix length, so the switch waits for neither.
+        if (cur.tile == max(seg_first_tile, cur.n - 5) && u + (cur.n - cur.tile) < u_end) {
+            Cursor nx = cur;
+            nx.tile = nx.n - 1;
+            cursor_next(nx, tile_base, p.B, HR);
+            bool act;
+            const uint4 *qn = q_half_row(nx, act);
+            if (qn) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn));
+            next_L = p.prefix_lens[nx.b];
+            have_next_L = true;
         }
         const bool first_tile = new_seg;  // O is overwritten by this tile's PV
         const int kbase = cur.tile * kBK;
