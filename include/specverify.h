@@ -21,7 +21,8 @@
  *     sv_verify_chain_noalloc, keeps no state between calls.  Calls
  *     that need scratch take a caller-provided workspace; its size comes
  *     from sv_workspace_size() and it must be zero-filled once before its
- *     first use (every call leaves its counters at zero again).
+ *     first use (every call leaves its counters at zero again; after a call
+ *     that reported SV_ERR_TIMEOUT, zero-fill it again).
  *   - Every call is asynchronous on `stream` (NULL = legacy default
  *     stream); none synchronises.  Two calls that share a workspace must
  *     not overlap on the GPU.
