@@ -1,6 +1,6 @@
 // sv_attention.cu -- host side of the verification attention: TMA tensor
-// maps over the K/V caches, the launch plan (grid, shared memory, workspace)
-// and the launches of the tcgen05 kernel and of the split merge, both in
+// maps over the K/V caches and Q, the launch plan (grid, pipeline depth,
+// shared memory, workspace) and the launch of the tcgen05 kernel in
 // sv_attention_tc.cu.
 #include <mutex>
 
@@ -40,6 +40,22 @@ static bool make_cache_map(CUtensorMap *map, const void *base, long long rows) {
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D view [B*T nodes][Hq heads][D] of Q; a box is 64 dims of G heads of
+// `nodes` consecutive nodes, i.e. the rows (t, g) of one row group in the
+// order t*G + g, 128-byte swizzle.  Nodes past B*T read as zeros.
+static bool make_q_map(CUtensorMap *map, const void *q, int B, int T, int Hq, int G, int nodes) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hq, (cuuint64_t)B * T};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hq * kD * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)nodes};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 int device_sm_count() {
@@ -87,9 +103,9 @@ static void plan_workspace(AttnPlan &pl, int B, int Hkv) {
     pl.off_pair_ctr = off;  // [pair][arrived, ready][softmax warp]
     off = align_up(off + sizeof(int) * (size_t)B * Hkv * pl.rg * 2 * kSoftmaxWarps, 256);
     pl.off_part_o = off;
-    off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.rows_per_rg * kD, 256);
+    off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.mrows * kD, 256);
     pl.off_part_ml = off;
-    off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.rows_per_rg * 4, 256);
+    off = align_up(off + sizeof(float) * (size_t)pl.grid * 2 * pl.mrows * 4, 256);
     pl.bytes = off;
 }
 
@@ -97,15 +113,24 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
     if (D != kD || T > kMaxT || B > kMaxB) return SV_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
     const int M = G * T;
-    if (M > 512) return SV_ERR_UNSUPPORTED;
+    if (M > 512 || G > 128) return SV_ERR_UNSUPPORTED;
     AttnPlan pl{};
-    pl.stages = 3;
-    pl.rows_per_rg = M <= 64 ? 64 : 128;  // M=64 products for small row groups
+    pl.mrows = M <= 64 ? 64 : 128;  // M=64 products for small row groups
+    // a row group holds whole nodes (G rows each), so that its Q rows are one box
+    pl.rows_per_rg = pl.mrows - pl.mrows % G;
     pl.rg = (M + pl.rows_per_rg - 1) / pl.rows_per_rg;
-    pl.smem = tc_smem_bytes(pl.stages, B);
+    // three K/V stages when shared memory allows, else two
+    int max_optin = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+        return SV_ERR_CUDA;
+    pl.stages = tc_smem_bytes(3, pl.mrows, B) <= max_optin ? 3 : 2;
+    pl.smem = tc_smem_bytes(pl.stages, pl.mrows, B);
+    if (pl.smem > max_optin) return SV_ERR_UNSUPPORTED;
     int sms = 0;
-    const int occ = cached_occupancy(tc_kernel_fn(pl.stages, pl.rows_per_rg), kTcThreads,
-                                     tc_smem_bytes(pl.stages, kMaxB), pl.smem, &sms);
+    const int occ = cached_occupancy(tc_kernel_fn(pl.stages, pl.mrows), kTcThreads, max_optin,
+                                     pl.smem, &sms);
     if (occ < 1) return SV_ERR_CUDA;
     pl.grid = sms * occ;
     plan_workspace(pl, B, Hkv);
@@ -116,8 +141,11 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
 sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
                                 cudaStream_t st) {
     const long long rows = (long long)a.B * a.Hkv * a.S_max;
-    CUtensorMap tmk, tmv;
-    if (!make_cache_map(&tmk, a.k, rows) || !make_cache_map(&tmv, a.v, rows)) return SV_ERR_CUDA;
+    CUtensorMap tmk, tmv, tmq;
+    const int G = a.Hq / a.Hkv;
+    if (!make_cache_map(&tmk, a.k, rows) || !make_cache_map(&tmv, a.v, rows) ||
+        !make_q_map(&tmq, a.q, a.B, a.T, a.Hq, G, pl.rows_per_rg / G))
+        return SV_ERR_CUDA;
     AttnKParams p{};
     p.q = static_cast<const uint16_t *>(a.q);
     p.out = static_cast<uint16_t *>(a.out);
@@ -138,8 +166,8 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.pair_ctr = reinterpret_cast<int *>(base + pl.off_pair_ctr);
     p.part_o = reinterpret_cast<float *>(base + pl.off_part_o);
     p.part_ml = reinterpret_cast<float *>(base + pl.off_part_ml);
-    void *args[] = {&tmk, &tmv, &p};
-    return launch_pdl(tc_kernel_fn(pl.stages, pl.rows_per_rg), dim3(pl.grid), dim3(kTcThreads),
+    void *args[] = {&tmk, &tmv, &tmq, &p};
+    return launch_pdl(tc_kernel_fn(pl.stages, pl.mrows), dim3(pl.grid), dim3(kTcThreads),
                       pl.smem, st, args) == cudaSuccess
                ? SV_OK
                : SV_ERR_CUDA;

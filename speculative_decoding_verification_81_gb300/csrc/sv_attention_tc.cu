@@ -55,11 +55,12 @@ namespace sv {
 
 // Tensor-memory columns (32-bit each, one row per lane): two S buffers
 // (128 f32 each; the bf16 P of keys 0-63 overwrites S columns 0-31, that of
-// keys 64-127 S columns 64-95), the O accumulator (128 f32) and the Q tile
-// (128 bf16 = 64 columns).  Q and P are the A operands of the two products, read by the
-// tensor core straight from TMEM, so shared memory holds only the K/V ring.
+// keys 64-127 S columns 64-95) and the O accumulator (128 f32).  P is the A
+// operand of the PV product, read by the tensor core from TMEM; Q, the A
+// operand of S, sits in shared memory (double-buffered, loaded by TMA ahead
+// of its segment).
 constexpr uint32_t kTcCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
+constexpr uint32_t kColS = 0, kColO = 256;
 
 // Byte offset of 16-byte chunk c (0..7) of row `row` in a 128-byte-swizzled
 // block whose rows are 128 bytes (the layout TMA writes with SWIZZLE_128B and
@@ -72,7 +73,8 @@ struct TcSmem {
     uint64_t full_k[4], empty_k[4];  // TMA ring, K halves of the stages
     uint64_t full_v[4], empty_v[4];  // V halves
     uint64_t s_full[2], p_full[2], pv_done[2];
-    uint64_t q_full, fin, fin_pv;
+    uint64_t q_full[2], q_empty[2];  // Q tiles in shared memory (double buffer)
+    uint64_t fin, fin_pv;
     uint64_t pair[4];            // the two softmax warps of each lane quarter
     float xmax[2][4][2][32];     // [tile parity][quarter][half][lane]: half-row tile maxima
     float xl[4][2][32];          // [quarter][half][lane]: half-row sums at a segment end
@@ -86,12 +88,15 @@ struct TcSmem {
 template <int STAGES, int MROWS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tree_attention_tc_kernel(const __grid_constant__ CUtensorMap tmk,
-                             const __grid_constant__ CUtensorMap tmv, const AttnKParams p) {
+                             const __grid_constant__ CUtensorMap tmv,
+                             const __grid_constant__ CUtensorMap tmq, const AttnKParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base_u32 - raw_u32);
-    TcSmem *sh = reinterpret_cast<TcSmem *>(smem + STAGES * kStageBytes);
+    uint8_t *qbuf = smem + STAGES * kStageBytes;  // 2 x (two 64-dim boxes of MROWS rows)
+    constexpr int kQBox = MROWS * 128;            // one 64-dim box: MROWS rows of 128 bytes
+    TcSmem *sh = reinterpret_cast<TcSmem *>(qbuf + 2 * 2 * kQBox);
     int *tile_base = reinterpret_cast<int *>(sh + 1);  // [B + 1]
 
     const int tid = threadIdx.x;
@@ -110,7 +115,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&sh->p_full[i], kSoftmaxWarps);
             mbar_init(&sh->pv_done[i], 1);
         }
-        mbar_init(&sh->q_full, kSoftmaxWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh->q_full[i], 1);
+            mbar_init(&sh->q_empty[i], 1);
+        }
         mbar_init(&sh->fin, 1);
         mbar_init(&sh->fin_pv, 1);
         for (int q = 0; q < 4; ++q) mbar_init(&sh->pair[q], 2);
@@ -120,7 +128,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
+        prefetch_tensormap(&tmq);
     }
+    // Q rows past rows_per_rg (when G does not divide MROWS) are never loaded:
+    // zero them once so that the padding rows of S stay finite.
+    for (int i = tid; i < 2 * 2 * (MROWS - p.rows_per_rg) * 8; i += kTcThreads) {
+        const int per_box = (MROWS - p.rows_per_rg) * 8;  // 16-byte words past the loaded rows
+        const int box = i / per_box, w = i - box * per_box;
+        *reinterpret_cast<uint4 *>(qbuf + box * kQBox + p.rows_per_rg * 128 + w * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async_smem();
     griddep_wait();
     griddep_launch_dependents();
     attn_prologue(p, tile_base, kTcThreads);
@@ -156,9 +174,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int half_off = is_k ? 0 : 2 * kBox;
             Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
             long long k = 0;
+            uint32_t qseg = 0;  // segments whose Q was issued
             for (long long u = u_begin; u < u_end; ++u, ++k) {
                 const int s = (int)(k % STAGES);
                 const uint32_t ph = (uint32_t)((k / STAGES) & 1);
+                if (is_k && (u == u_begin || cur.tile == 0)) {
+                    // this segment's Q rows (rows_per_rg of them: rows_per_rg / G
+                    // nodes x G heads, a 3-D box) into Q buffer qseg & 1, once
+                    // the S products of the segment two back are done
+                    const int qb = (int)(qseg & 1);
+                    if (!mbar_wait_bounded(&sh->q_empty[qb], ((qseg >> 1) & 1) ^ 1u)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    const int kvh = cur.pr / p.RG, rg = cur.pr - kvh * p.RG;
+                    const int tpr = p.rows_per_rg / p.G;  // nodes per row group
+                    const int z = cur.b * p.T + rg * tpr;
+                    uint8_t *qd = qbuf + qb * 2 * kQBox;
+                    mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
+                    tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
+                    tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
+                    ++qseg;
+                }
                 if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
                     fail(cur.b);
                     break;
@@ -176,6 +213,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const long long first = k > STAGES ? k - STAGES : 0;
             for (long long j = first; j < k; ++j)
                 mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
+            for (uint32_t g2 = qseg > 2 ? qseg - 2 : 0; g2 < qseg; ++g2)
+                mbar_wait_bounded(&sh->q_full[g2 & 1], (g2 >> 1) & 1);
         }
         return;
     }
@@ -191,12 +230,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const long long nt = u_end - u_begin;
             if (warp == 1) {
                 constexpr uint32_t idS = tc::idesc_bf16(MROWS, kBK, false);
-                uint32_t seg = 0;
+                uint32_t seg = 0;  // segments started
                 for (long long j = 0; j < nt; ++j) {
                     const int s = (int)(j % STAGES);
-                    // this segment's Q is in TMEM, the K tile has landed, the
-                    // S buffer is free (PV of tile j-2, whose P lived there, is done)
-                    if (j == 0 || cur.tile == 0) ok = mbar_wait_bounded(&sh->q_full, (seg++) & 1);
+                    // this segment's Q has landed, the K tile has landed, the S
+                    // buffer is free (PV of tile j-2, whose P lived there, is done)
+                    if (j == 0 || cur.tile == 0) {
+                        ok = mbar_wait_bounded(&sh->q_full[seg & 1], (seg >> 1) & 1);
+                        ++seg;
+                    }
                     if (ok) ok = mbar_wait_bounded(&sh->full_k[s], (uint32_t)((j / STAGES) & 1));
                     if (ok && j >= 2)
                         ok = mbar_wait_bounded(&sh->pv_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
@@ -205,15 +247,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    // dims 16kk..: 32 bytes on within a 64-dim box, the next box 16 KB on
+                    // dims 16kk..: 32 bytes on within a 64-dim box, the next box on
                     const uint64_t dk = tc::smem_desc(base_u32 + s * kStageBytes, 16, 1024);
+                    const uint64_t dq = tc::smem_desc(base_u32 + STAGES * kStageBytes +
+                                                          (uint32_t)(((seg - 1) & 1) * 2 * kQBox),
+                                                      16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint64_t bd = dk + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2);
-                        tc::mma_bf16_ts(tbase + kColS + (uint32_t)(j & 1) * kBK, tbase + kColQ + kk * 8,
-                                        bd, idS, kk > 0 ? 1u : 0u);
+                        const uint64_t ad = dq + (uint64_t)((kk >> 2) * (kQBox >> 4) + (kk & 3) * 2);
+                        tc::mma_bf16(tbase + kColS + (uint32_t)(j & 1) * kBK, ad, bd, idS,
+                                     kk > 0 ? 1u : 0u);
                     }
                     tc::commit(&sh->s_full[j & 1]);
+                    if (cur.tile == cur.n - 1 || j == nt - 1)
+                        tc::commit(&sh->q_empty[(seg - 1) & 1]);  // Q buffer free once these S are done
                     tc::commit(&sh->empty_k[s]);  // the K half may be refilled once S(j) is done
                     cursor_next(cur, tile_base, p.B, HR);
                 }
@@ -285,41 +333,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     int L = 0, kv_end = 0, seg_first_tile = 0, kvh = 0, rg = 0, rglob = 0;
     bool seg_is_first = true, warp_active = false, row_valid = false;
-    // This thread's half Q row of the segment starting at `c`: its address,
-    // or null for rows past M (zeros).
-    auto q_half_row = [&](const Cursor &c, bool &active) -> const uint4 * {
-        const int kh = c.pr / p.RG, rgc = c.pr - kh * p.RG;
-        const int rgl = rgc * MROWS + r;
-        active = rgc * MROWS + quarter * kRowsPerQuarter < p.M;
-        if (!(lane_has_row && rgl < p.M)) return nullptr;
-        const int tq = rgl / p.G, gq = rgl - tq * p.G;
-        return reinterpret_cast<const uint4 *>(
-            p.q + (((size_t)c.b * p.T + tq) * p.Hq + kh * p.G + gq) * kD + hc);
-    };
-    // Store the Q tile of the segment starting at `c` into TMEM and signal
-    // it.  Only when no S product of an earlier segment is pending (the
-    // caller has seen the S of that segment's last tile).
-    auto store_q = [&](const Cursor &c) {
-        bool active;
-        const uint4 *qsrc = q_half_row(c, active);
-        if (active) {
-            uint32_t w[32];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint4 v = qsrc ? qsrc[k] : make_uint4(0u, 0u, 0u, 0u);
-                w[4 * k] = v.x;
-                w[4 * k + 1] = v.y;
-                w[4 * k + 2] = v.z;
-                w[4 * k + 3] = v.w;
-            }
-            tc::tmem_st32(tl + kColQ + 32 * half, w);
-            tc::wait_st();
-        }
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->q_full);
-    };
-    bool q_stored = false;  // the current segment's Q was stored ahead of it
     int next_L = 0;         // the next segment's prefix length, read ahead
     bool have_next_L = false;
     Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
@@ -334,24 +347,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             kv_end = L + p.T;
             seg_first_tile = cur.tile;
             seg_is_first = (u == u_begin);
-            rglob = rg * MROWS + r;
-            row_valid = lane_has_row && rglob < p.M;
-            warp_active = rg * MROWS + quarter * kRowsPerQuarter < p.M;
+            // the group's rows are rows_per_rg (a multiple of G) of the MMA's
+            // MROWS; the others are padding
+            rglob = rg * p.rows_per_rg + r;
+            row_valid = lane_has_row && r < p.rows_per_rg && rglob < p.M;
+            warp_active = quarter * kRowsPerQuarter < p.rows_per_rg &&
+                          rg * p.rows_per_rg + quarter * kRowsPerQuarter < p.M;
             m = kNegInf;
             l = 0.f;
             if (row_valid) anc = ancestors(p.parents, p.T, cur.b, rglob / p.G);
-            if (!q_stored) store_q(cur);
-            q_stored = false;
         }
-        // A few tiles before this segment ends: pull the next segment's Q rows
-        // into L2 and read its prefix length, so the switch waits for neither.
+        // A few tiles before this segment ends: read the next segment's prefix
+        // length (its Q is brought in by the producer).
         if (cur.tile == max(seg_first_tile, cur.n - 5) && u + (cur.n - cur.tile) < u_end) {
             Cursor nx = cur;
             nx.tile = nx.n - 1;
             cursor_next(nx, tile_base, p.B, HR);
-            bool act;
-            const uint4 *qn = q_half_row(nx, act);
-            if (qn) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn));
             next_L = p.prefix_lens[nx.b];
             have_next_L = true;
         }
@@ -481,15 +492,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ready_ctr) {  // the partial left at the previous tile has drained by now
             flag_ready(ready_ctr);
             ready_ctr = nullptr;
-        }
-
-        if (last_of_pair && u + 1 < u_end) {
-            // the next segment's Q goes in now (this segment's last S is done),
-            // so its first S product overlaps this segment's epilogue
-            Cursor nx = cur;
-            cursor_next(nx, tile_base, p.B, HR);
-            store_q(nx);
-            q_stored = true;
         }
 
         // ---- end of a segment: this half of the O row out of TMEM
@@ -690,13 +692,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-int tc_smem_bytes(int stages, int B) {
-    return 1024 + stages * kStageBytes + (int)sizeof(TcSmem) + (B + 1) * 4;
+int tc_smem_bytes(int stages, int mrows, int B) {
+    return 1024 + stages * kStageBytes + 2 * 2 * mrows * 128 + (int)sizeof(TcSmem) + (B + 1) * 4;
 }
 
 const void *tc_kernel_fn(int stages, int mrows) {
     if (stages == 3 && mrows == 128) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 128>);
     if (stages == 3 && mrows == 64) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 64>);
+    if (stages == 2 && mrows == 128) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<2, 128>);
+    if (stages == 2 && mrows == 64) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<2, 64>);
     return nullptr;
 }
 

@@ -102,7 +102,8 @@ sv_status launch_verify_tree_greedy(const TreeArgs &args, int dtype, const Vocab
 
 struct AttnPlan {
     int stages;       // K/V pipeline depth
-    int rows_per_rg;  // query rows per row group: 64 or 128 (the MMA's M)
+    int mrows;        // the MMA's M: 64 or 128
+    int rows_per_rg;  // query rows per row group: the largest multiple of G <= mrows
     int rg;           // row groups per (sequence, KV head)
     int grid;         // persistent CTAs
     int smem;         // dynamic shared memory bytes
@@ -116,7 +117,7 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan);
 
 // tcgen05 attention kernel (sv_attention_tc.cu)
 struct AttnKParams;
-int tc_smem_bytes(int stages, int B);
+int tc_smem_bytes(int stages, int mrows, int B);
 const void *tc_kernel_fn(int stages, int mrows);
 
 struct AttnArgs {
