@@ -335,6 +335,24 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     chain_ms = time_graph(call_chain, reps)
     compact_ms = time_graph(call_compact, reps)
 
+    # ---- the verification pass against plain decoding: the same attention
+    # call with T = 1 (one new token per sequence) and T = 5 (N = 4), over the
+    # same caches; the ratio to T = 1 is the verification overhead per pass
+    decode = {}
+    for Tq in (1, 5):
+        qx = torch.randn(B, Tq, cfg["Hq"], cfg["D"], device=dev).to(torch.bfloat16)
+        ox = torch.empty_like(qx)
+        wsx = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, Tq, 0, cfg["Hq"], cfg["Hkv"], cfg["D"], dev)
+
+        def call_t(qx=qx, ox=ox, wsx=wsx):
+            sv.sv_tree_attention(qx, d["k"], d["v"], d["prefix_lens"], None, out=ox, ws=wsx)
+        decode[Tq] = time_graph(call_t, reps)
+    decode_baseline = {
+        "attention_ms": {"T=1 (decode)": decode[1], "T=5 (N=4)": decode[5], f"T={N + 1} (N={N})": attn_ms},
+        "verify_over_decode": {"N=4": decode[5] / decode[1], f"N={N}": attn_ms / decode[1]},
+        "how": "sv_tree_attention alone, one call per CUDA graph, same K/V caches and prefix",
+    }
+
     # ---- end to end: inputs from pinned host memory, result read back, every step
     e2e = None
     if not args.no_e2e:
@@ -396,6 +414,7 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
         "call_ms": {"sv_tree_attention": attn_ms, "sv_verify_chain": chain_ms,
                     "sv_compact_kv": compact_ms,
                     "how": "each call captured alone in a CUDA graph, replayed back to back"},
+        "decode_baseline": decode_baseline,
         "clocks": clk,
         "gpu_launches": launches_per_step * K,
         "timing": "CUDA-graph replays of the whole step, CUDA events on the launching stream",

@@ -162,6 +162,9 @@ sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, s
  *   out_tokens[b,:] = node_tokens of path nodes 1..depth, am_{d*}, then -1
  *
  *   target_logits [B, T, V] of `dtype`; node_tokens, parents int32 [B, T]
+ *   (parents NULL: a chain, parent_i = i - 1, i.e. greedy chain
+ *   verification -- the longest prefix of draft tokens each equal to the
+ *   target's argmax at the position before it, then that argmax)
  *   accepted_len int32 [B]; path_nodes, out_tokens int32 [B, T]
  * Supported: 1 <= T <= 1024, 1 <= V < 2^30.
  */

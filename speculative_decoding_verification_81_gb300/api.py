@@ -190,11 +190,13 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
 
 def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None, path_nodes=None,
                           out_tokens=None, seq_status=None, ws=None, stream=None):
-    """target [B,T,V] (bf16 or f32); node_tokens, parents [B,T] int32.
+    """target [B,T,V] (bf16 or f32); node_tokens, parents [B,T] int32 (parents
+    None: a chain, i.e. greedy chain verification).
     Returns (accepted_len [B], path_nodes [B,T], out_tokens [B,T])."""
     _req(target_logits, "target_logits", None, 3)
     _req(node_tokens, "node_tokens", torch.int32, 2)
-    _req(parents, "parents", torch.int32, 2)
+    if parents is not None:
+        _req(parents, "parents", torch.int32, 2)
     dt = _dtype_code(target_logits)
     B, T, V = target_logits.shape
     dev = target_logits.device

@@ -94,7 +94,7 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
                                 int V, int32_t *accepted_len, int32_t *path_nodes,
                                 int32_t *out_tokens, int32_t *seq_status, void *workspace,
                                 size_t workspace_bytes, sv_stream_t stream) {
-    if (!target_logits || !node_tokens || !parents || !accepted_len || !path_nodes || !out_tokens)
+    if (!target_logits || !node_tokens || !accepted_len || !path_nodes || !out_tokens)
         return SV_ERR_INVALID_ARG;
     if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || V <= 0) return SV_ERR_INVALID_ARG;

@@ -932,7 +932,7 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
         if (lane == 0) sm_am[rr] = rp.idx == INT_MAX ? -1 : rp.idx;
     }
     for (int i = threadIdx.x; i < a.T; i += kVT) {
-        sm_par[i] = a.parents[(size_t)b * a.T + i];
+        sm_par[i] = a.parents ? a.parents[(size_t)b * a.T + i] : i - 1;  // NULL: a chain
         sm_tok[i] = a.tokens[(size_t)b * a.T + i];
     }
     __syncthreads();

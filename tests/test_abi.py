@@ -80,7 +80,8 @@ def test_verify_tree_host_validation(L):
         a.update(kw)
         return L.sv_verify_tree_greedy(a["t"], a["dt"], a["tok"], a["par"], a["B"], a["T"], a["V"],
                                        a["acc"], a["path"], a["out"], None, a["ws"], a["wsb"], None)
-    assert call(par=None) == sv.SV_ERR_INVALID_ARG
+    assert call(tok=None) == sv.SV_ERR_INVALID_ARG
+    assert call(par=None) == sv.SV_ERR_WORKSPACE  # NULL parents: a chain, valid
     assert call(T=0) == sv.SV_ERR_INVALID_ARG
     assert call(T=1025) == sv.SV_ERR_UNSUPPORTED
     assert call() == sv.SV_ERR_WORKSPACE

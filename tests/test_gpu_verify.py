@@ -139,6 +139,25 @@ def _check_tree(orc, tinp):
     return ref
 
 
+@pytest.mark.parametrize("B,N,V,dtype,seed", [
+    (8, 8, 32000, "bf16", 11),     # the chain workload's draft length, Llama vocabulary
+    (32, 8, 128256, "bf16", 12),   # the fused chain step's shapes
+    (5, 63, 1000, "f32", 13),      # longest chain, unaligned f32 rows
+])
+def test_greedy_chain_parents_null(orc, B, N, V, dtype, seed):
+    """Greedy chain verification: parents NULL is the chain parent_i = i - 1
+    (the oracle gets the explicit chain)."""
+    inp = W.tree_logit_inputs(B, N + 1, V, W.chain_parents(N + 1), p_match=0.85, sigma=2.0,
+                              dtype=dtype, seed=seed)
+    ref = orc.verify_tree_greedy(inp["target"], inp["node_tokens"], inp["parents"])
+    acc, path, out = sv.sv_verify_tree_greedy(dev(inp["target"]), dev(inp["node_tokens"]), None)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(acc), ref["accepted_len"])
+    np.testing.assert_array_equal(host(path), ref["path_nodes"])
+    np.testing.assert_array_equal(host(out), ref["out_tokens"])
+    assert 0 < ref["accepted_len"].max()
+
+
 def test_tree_workload3_logits(orc):
     inp = W.workload(3)
     ref = _check_tree(orc, inp["tree"])
