@@ -347,6 +347,36 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
         def call_t(qx=qx, ox=ox, wsx=wsx):
             sv.sv_tree_attention(qx, d["k"], d["v"], d["prefix_lens"], None, out=ox, ws=wsx)
         decode[Tq] = time_graph(call_t, reps)
+    # ---- the same attention over a paged cache (page table in random order):
+    # page_size 128 (a page per key tile) and 16 (eight pages per tile)
+    paged = {}
+    S_max = d["k"].shape[2]
+    for ps in (128, 16):
+        max_pages = -(-S_max // ps)
+        num_pages = B * max_pages
+        g = torch.Generator(device="cpu").manual_seed(ps)
+        table = torch.randperm(num_pages, generator=g).to(torch.int32).view(B, max_pages).to(dev)
+        kp = torch.empty(num_pages, cfg["Hkv"], ps, cfg["D"], dtype=torch.bfloat16, device=dev)
+        vp = torch.empty_like(kp)
+        pad = max_pages * ps - S_max
+        kl = torch.nn.functional.pad(d["k"], (0, 0, 0, pad))
+        vl = torch.nn.functional.pad(d["v"], (0, 0, 0, pad))
+        # logical page j of sequence b -> physical page table[b, j]
+        kp[table.flatten().long()] = kl.view(B, cfg["Hkv"], max_pages, ps, cfg["D"]).permute(
+            0, 2, 1, 3, 4).reshape(num_pages, cfg["Hkv"], ps, cfg["D"])
+        vp[table.flatten().long()] = vl.view(B, cfg["Hkv"], max_pages, ps, cfg["D"]).permute(
+            0, 2, 1, 3, 4).reshape(num_pages, cfg["Hkv"], ps, cfg["D"])
+        outp = torch.empty_like(out)
+        del kl, vl
+
+        def call_p(kp=kp, vp=vp, table=table, outp=outp):
+            sv.sv_tree_attention_paged(d["q"], kp, vp, table, d["prefix_lens"], None, out=outp,
+                                       ws=ws_a)
+        paged[f"page_size={ps}"] = time_graph(call_p, reps)
+        del kp, vp
+    paged_attention = {"attention_ms": paged, "contiguous_ms": attn_ms,
+                       "how": "sv_tree_attention_paged alone, one call per CUDA graph"}
+
     decode_baseline = {
         "attention_ms": {"T=1 (decode)": decode[1], "T=5 (N=4)": decode[5], f"T={N + 1} (N={N})": attn_ms},
         "verify_over_decode": {"N=4": decode[5] / decode[1], f"N={N}": attn_ms / decode[1]},
@@ -415,6 +445,7 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
                     "sv_compact_kv": compact_ms,
                     "how": "each call captured alone in a CUDA graph, replayed back to back"},
         "decode_baseline": decode_baseline,
+        "paged_attention": paged_attention,
         "clocks": clk,
         "gpu_launches": launches_per_step * K,
         "timing": "CUDA-graph replays of the whole step, CUDA events on the launching stream",

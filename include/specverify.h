@@ -117,6 +117,30 @@ sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_ca
                             void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /*
+ * Verification attention over a paged KV cache ("KV paginé": the cache held in
+ * fixed-size pages reached through a per-sequence page table; "Chapitre 9"
+ * §9.4).  The same computation as sv_tree_attention, with logical slot s of
+ * sequence b (prefix slots 0..L_b-1, node j at slot L_b + j) stored in page
+ * block_table[b][s / page_size] at offset s % page_size.
+ *
+ *   k_pages, v_pages  bf16 [num_pages, Hkv, page_size, D]
+ *   block_table       int32 [B, max_pages]: physical page of each logical page
+ *   other arguments   as sv_tree_attention, with S_max = max_pages * page_size
+ *   workspace         >= sv_workspace_size(SV_OP_TREE_ATTENTION, ...) bytes
+ * Supported: page_size a power of two >= 8 or a multiple of 128;
+ * num_pages * Hkv * page_size < 2^31; otherwise as sv_tree_attention.  A
+ * page id outside [0, num_pages) among the pages that hold slots
+ * [0, L_b + T) is reported as SV_ERR_BAD_INPUT for that sequence (its
+ * rows read as zeros); entries past those pages are never used.
+ */
+sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *block_table, int max_pages, int num_pages,
+                                  int page_size, const int32_t *prefix_lens,
+                                  const int32_t *parents, int B, int T, int Hq, int Hkv, int D,
+                                  float scale, void *out, int32_t *seq_status, void *workspace,
+                                  size_t workspace_bytes, sv_stream_t stream);
+
+/*
  * Stochastic chain acceptance over the full vocabulary.
  * Source: "Chapitre 9 -- Décodage spéculatif" §9.1: the target yields a
  * distribution at each of the N+1 positions; draft token x drawn from q is
@@ -198,6 +222,20 @@ sv_status sv_compact_kv(void *k_cache, void *v_cache, const int32_t *prefix_lens
                         int32_t *new_kv_lens, const int32_t *path_nodes, int path_stride,
                         const int32_t *accepted_len, int B, int Hkv, int D, int S_max,
                         int32_t *seq_status, sv_stream_t stream);
+
+/*
+ * Compaction of the accepted path's rows in a paged KV cache: sv_compact_kv
+ * with rows addressed through the page table (layout as in
+ * sv_tree_attention_paged, S_max = max_pages * page_size).  A page id
+ * outside [0, num_pages) for a slot the move reads or writes makes the
+ * sequence SV_ERR_BAD_INPUT with nothing moved.
+ */
+sv_status sv_compact_kv_paged(void *k_pages, void *v_pages, const int32_t *block_table,
+                              int max_pages, int num_pages, int page_size,
+                              const int32_t *prefix_lens, int32_t *new_kv_lens,
+                              const int32_t *path_nodes, int path_stride,
+                              const int32_t *accepted_len, int B, int Hkv, int D,
+                              int32_t *seq_status, sv_stream_t stream);
 
 /*
  * Chain acceptance with no caller workspace.  There is no counterpart of this

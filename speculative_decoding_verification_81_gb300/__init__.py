@@ -7,13 +7,14 @@ compaction -- as hand-written CUDA kernels behind a C ABI
 from .api import (SV_BF16, SV_ERR_BAD_INPUT, SV_ERR_CUDA, SV_ERR_INVALID_ARG, SV_ERR_TIMEOUT,
                   SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE, SV_F32, SV_OK, SV_OP_TREE_ATTENTION,
                   SV_OP_VERIFY_CHAIN, SV_OP_VERIFY_TREE_GREEDY, SpecVerifyError, lib,
-                  status_string, sv_compact_kv, sv_tree_attention, sv_verify_chain,
-                  sv_verify_tree_greedy, sv_workspace_size, workspace)
+                  status_string, sv_compact_kv, sv_compact_kv_paged, sv_tree_attention,
+                  sv_tree_attention_paged, sv_verify_chain, sv_verify_tree_greedy,
+                  sv_workspace_size, workspace)
 
 __all__ = [
     "SV_BF16", "SV_F32", "SV_OK", "SV_ERR_BAD_INPUT", "SV_ERR_CUDA", "SV_ERR_INVALID_ARG",
     "SV_ERR_TIMEOUT", "SV_ERR_UNSUPPORTED", "SV_ERR_WORKSPACE", "SV_OP_TREE_ATTENTION",
     "SV_OP_VERIFY_CHAIN", "SV_OP_VERIFY_TREE_GREEDY", "SpecVerifyError", "lib", "status_string",
-    "sv_compact_kv", "sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy",
-    "sv_workspace_size", "workspace",
+    "sv_compact_kv", "sv_compact_kv_paged", "sv_tree_attention", "sv_tree_attention_paged",
+    "sv_verify_chain", "sv_verify_tree_greedy", "sv_workspace_size", "workspace",
 ]

@@ -32,7 +32,8 @@ SV_OP_VERIFY_CHAIN = 1
 SV_OP_VERIFY_TREE_GREEDY = 2
 
 EXPORTS = ("sv_workspace_size", "sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy",
-           "sv_compact_kv", "sv_status_string", "sv_version", "sv_verify_chain_noalloc")
+           "sv_compact_kv", "sv_status_string", "sv_version", "sv_verify_chain_noalloc",
+           "sv_tree_attention_paged", "sv_compact_kv_paged")
 
 # Length of the fixed scratch array behind sv_verify_chain_noalloc.
 SV_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -64,8 +65,11 @@ def lib() -> ctypes.CDLL:
         L.sv_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, Z, P]
         L.sv_verify_chain_noalloc.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         L.sv_compact_kv.argtypes = [P, P, P, P, P, I, P, I, I, I, I, P, P]
+        L.sv_tree_attention_paged.argtypes = [P, P, P, P, I, I, I, P, P, I, I, I, I, I,
+                                              ctypes.c_float, P, P, P, Z, P]
+        L.sv_compact_kv_paged.argtypes = [P, P, P, I, I, I, P, P, P, I, P, I, I, I, P, P]
         for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
-                   "sv_verify_chain_noalloc"):
+                   "sv_verify_chain_noalloc", "sv_tree_attention_paged", "sv_compact_kv_paged"):
             getattr(L, fn).restype = I
         L.sv_status_string.argtypes = [I]
         L.sv_status_string.restype = ctypes.c_char_p
@@ -160,6 +164,35 @@ def sv_tree_attention(q, k_cache, v_cache, prefix_lens, parents=None, scale=None
     return out
 
 
+def sv_tree_attention_paged(q, k_pages, v_pages, block_table, prefix_lens, parents=None,
+                            scale=None, out=None, seq_status=None, ws=None, stream=None):
+    """q [B,T,Hq,D] bf16; k_pages/v_pages [num_pages,Hkv,page_size,D] bf16;
+    block_table [B,max_pages] int32; prefix_lens [B] int32; parents [B,T] int32
+    or None (chain).  Returns out [B,T,Hq,D] bf16."""
+    _req(q, "q", torch.bfloat16, 4)
+    _req(k_pages, "k_pages", torch.bfloat16, 4)
+    _req(v_pages, "v_pages", torch.bfloat16, 4)
+    _req(block_table, "block_table", torch.int32, 2)
+    _req(prefix_lens, "prefix_lens", torch.int32, 1)
+    B, T, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    if parents is not None:
+        _req(parents, "parents", torch.int32, 2)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
+    rc = lib().sv_tree_attention_paged(_p(q), _p(k_pages), _p(v_pages), _p(block_table), max_pages,
+                                       num_pages, page_size, _p(prefix_lens), _p(parents), B, T,
+                                       Hq, Hkv, D, float(scale), _p(out), _p(seq_status), _p(ws),
+                                       ws.numel(), _stream(stream))
+    _check("sv_tree_attention_paged", rc)
+    return out
+
+
 def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sample,
                     accepted_len=None, out_tokens=None, probs_out=None, seq_status=None, ws=None,
                     stream=None):
@@ -234,6 +267,32 @@ def sv_compact_kv(k_cache, v_cache, prefix_lens, accepted_len, path_nodes=None, 
                              _p(path_nodes), stride, _p(accepted_len), B, Hkv, D, S_max,
                              _p(seq_status), _stream(stream))
     _check("sv_compact_kv", rc)
+    return new_kv_lens
+
+
+def sv_compact_kv_paged(k_pages, v_pages, block_table, prefix_lens, accepted_len,
+                        path_nodes=None, new_kv_lens=None, seq_status=None, stream=None):
+    """In place on k_pages/v_pages [num_pages,Hkv,page_size,D] bf16 through
+    block_table [B,max_pages] int32.  path_nodes [B,P] int32 or None (chain).
+    Returns new_kv_lens [B] int32 (may be prefix_lens itself)."""
+    _req(k_pages, "k_pages", torch.bfloat16, 4)
+    _req(v_pages, "v_pages", torch.bfloat16, 4)
+    _req(block_table, "block_table", torch.int32, 2)
+    _req(prefix_lens, "prefix_lens", torch.int32, 1)
+    _req(accepted_len, "accepted_len", torch.int32, 1)
+    num_pages, Hkv, page_size, D = k_pages.shape
+    B, max_pages = block_table.shape
+    stride = 0
+    if path_nodes is not None:
+        _req(path_nodes, "path_nodes", torch.int32, 2)
+        stride = path_nodes.shape[1]
+    if new_kv_lens is None:
+        new_kv_lens = torch.empty_like(prefix_lens)
+    rc = lib().sv_compact_kv_paged(_p(k_pages), _p(v_pages), _p(block_table), max_pages, num_pages,
+                                   page_size, _p(prefix_lens), _p(new_kv_lens), _p(path_nodes),
+                                   stride, _p(accepted_len), B, Hkv, D, _p(seq_status),
+                                   _stream(stream))
+    _check("sv_compact_kv_paged", rc)
     return new_kv_lens
 
 

@@ -64,8 +64,40 @@ sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_ca
     const sv_status st = sv::plan_attention(B, T, Hq, Hkv, D, &pl);
     if (st != SV_OK) return st;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
-    sv::AttnArgs a{q, k_cache, v_cache, prefix_lens, parents, B, T, Hq, Hkv, D, S_max, scale, out,
-                   seq_status};
+    sv::AttnArgs a{q,   k_cache, v_cache, prefix_lens, parents,    B,       T, Hq, Hkv, D,
+                   S_max, scale, out,  seq_status, nullptr, 0, 0, 0};
+    return sv::launch_tree_attention(a, pl, workspace, as_stream(stream));
+}
+
+static bool valid_page_size(int ps) {
+    // a power of two from 8 (one swizzle atom of rows) up, or a multiple of the 128-key tile
+    return ps >= 8 && ((ps & (ps - 1)) == 0 || ps % 128 == 0);
+}
+
+sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *block_table, int max_pages, int num_pages,
+                                  int page_size, const int32_t *prefix_lens,
+                                  const int32_t *parents, int B, int T, int Hq, int Hkv, int D,
+                                  float scale, void *out, int32_t *seq_status, void *workspace,
+                                  size_t workspace_bytes, sv_stream_t stream) {
+    if (!q || !k_pages || !v_pages || !block_table || !prefix_lens || !out) return SV_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_pages <= 0 || num_pages <= 0)
+        return SV_ERR_INVALID_ARG;
+    if (!valid_page_size(page_size)) return SV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !(scale > 0.f) || !std::isfinite(scale)) return SV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+        return SV_ERR_INVALID_ARG;
+    const long long S_max = (long long)max_pages * page_size;
+    if (S_max < T) return SV_ERR_INVALID_ARG;
+    if ((long long)num_pages * Hkv * page_size >= (1LL << 31) || S_max >= (1LL << 30))
+        return SV_ERR_UNSUPPORTED;
+    sv::AttnPlan pl;
+    const sv_status st = sv::plan_attention(B, T, Hq, Hkv, D, &pl);
+    if (st != SV_OK) return st;
+    if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
+    sv::AttnArgs a{q,  k_pages, v_pages, prefix_lens, parents,     B,         T,        Hq,
+                   Hkv, D,      (int)S_max, scale,     out,         seq_status, block_table,
+                   max_pages, num_pages, page_size};
     return sv::launch_tree_attention(a, pl, workspace, as_stream(stream));
 }
 
@@ -119,7 +151,30 @@ sv_status sv_compact_kv(void *k_cache, void *v_cache, const int32_t *prefix_lens
     if (!aligned16(k_cache) || !aligned16(v_cache)) return SV_ERR_INVALID_ARG;
     if (D % 8 != 0 || D > 256) return SV_ERR_UNSUPPORTED;
     sv::CompactArgs a{k_cache, v_cache, prefix_lens, new_kv_lens, path_nodes, path_stride,
-                      accepted_len, B, Hkv, D, S_max, seq_status};
+                      accepted_len, B, Hkv, D, S_max, seq_status, nullptr, 0, 0};
+    return sv::launch_compact_kv(a, as_stream(stream));
+}
+
+sv_status sv_compact_kv_paged(void *k_pages, void *v_pages, const int32_t *block_table,
+                              int max_pages, int num_pages, int page_size,
+                              const int32_t *prefix_lens, int32_t *new_kv_lens,
+                              const int32_t *path_nodes, int path_stride,
+                              const int32_t *accepted_len, int B, int Hkv, int D,
+                              int32_t *seq_status, sv_stream_t stream) {
+    if (!k_pages || !v_pages || !block_table || !prefix_lens || !new_kv_lens || !accepted_len)
+        return SV_ERR_INVALID_ARG;
+    if (B <= 0 || Hkv <= 0 || D <= 0 || max_pages <= 0 || num_pages <= 0 || page_size <= 0)
+        return SV_ERR_INVALID_ARG;
+    if (path_nodes && path_stride <= 0) return SV_ERR_INVALID_ARG;
+    if (!aligned16(k_pages) || !aligned16(v_pages)) return SV_ERR_INVALID_ARG;
+    if (D % 8 != 0 || D > 256) return SV_ERR_UNSUPPORTED;
+    const long long S_max = (long long)max_pages * page_size;
+    if (S_max >= (1LL << 30) || (long long)num_pages * Hkv * page_size >= (1LL << 31))
+        return SV_ERR_UNSUPPORTED;
+    sv::CompactArgs a{k_pages, v_pages,    prefix_lens, new_kv_lens, path_nodes, path_stride,
+                      accepted_len, B, Hkv, D, (int)S_max, seq_status, block_table, max_pages,
+                      page_size};
+    a.num_pages = num_pages;
     return sv::launch_compact_kv(a, as_stream(stream));
 }
 

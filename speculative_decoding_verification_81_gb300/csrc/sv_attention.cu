@@ -28,13 +28,14 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// 2-D view [rows = B*Hkv*S_max, D] of a bf16 cache, 64x64 boxes, 128-byte swizzle.
-static bool make_cache_map(CUtensorMap *map, const void *base, long long rows) {
+// 2-D view [rows, D] of a bf16 cache (rows = B*Hkv*S_max, or num_pages*Hkv*page_size
+// for a paged one), boxes of 64 dims x box_rows rows, 128-byte swizzle.
+static bool make_cache_map(CUtensorMap *map, const void *base, long long rows, int box_rows) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kBK};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -140,10 +141,13 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
 
 sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
                                 cudaStream_t st) {
-    const long long rows = (long long)a.B * a.Hkv * a.S_max;
+    const bool paged = a.block_table != nullptr;
+    const long long rows = paged ? (long long)a.num_pages * a.Hkv * a.page_size
+                                 : (long long)a.B * a.Hkv * a.S_max;
+    const int box_rows = paged && a.page_size < kBK ? a.page_size : kBK;
     CUtensorMap tmk, tmv, tmq;
     const int G = a.Hq / a.Hkv;
-    if (!make_cache_map(&tmk, a.k, rows) || !make_cache_map(&tmv, a.v, rows) ||
+    if (!make_cache_map(&tmk, a.k, rows, box_rows) || !make_cache_map(&tmv, a.v, rows, box_rows) ||
         !make_q_map(&tmq, a.q, a.B, a.T, a.Hq, G, pl.rows_per_rg / G))
         return SV_ERR_CUDA;
     AttnKParams p{};
@@ -166,6 +170,10 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.pair_ctr = reinterpret_cast<int *>(base + pl.off_pair_ctr);
     p.part_o = reinterpret_cast<float *>(base + pl.off_part_o);
     p.part_ml = reinterpret_cast<float *>(base + pl.off_part_ml);
+    p.block_table = a.block_table;
+    p.max_pages = a.max_pages;
+    p.num_pages = a.num_pages;
+    p.page_size = a.page_size;
     void *args[] = {&tmk, &tmv, &tmq, &p};
     return launch_pdl(tc_kernel_fn(pl.stages, pl.mrows), dim3(pl.grid), dim3(kTcThreads),
                       pl.smem, st, args) == cudaSuccess

@@ -196,17 +196,64 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
                     ++qseg;
                 }
-                if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
-                    fail(cur.b);
-                    break;
-                }
-                if (*abort_flag) break;
                 const int kvh = cur.pr / p.RG;
-                const int y = (cur.b * p.Hkv + kvh) * p.S_max + cur.tile * kBK;
-                uint8_t *st = smem + s * kStageBytes + half_off;
-                mbar_arrive_expect_tx(&full[s], 2 * kBox);
-                tma_load_2d(st, map, 0, y, &full[s]);
-                tma_load_2d(st + kBox, map, 64, y, &full[s]);
+                const int kb = cur.tile * kBK;
+                if (!p.block_table) {
+                    // contiguous caches: the tile is 128 consecutive rows
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    const int y = (cur.b * p.Hkv + kvh) * p.S_max + kb;
+                    uint8_t *st = smem + s * kStageBytes + half_off;
+                    mbar_arrive_expect_tx(&full[s], 2 * kBox);
+                    tma_load_2d(st, map, 0, y, &full[s]);
+                    tma_load_2d(st + kBox, map, 64, y, &full[s]);
+                } else if (p.page_size >= kBK) {
+                    // paged, pages of 128 slots or more: the tile sits in one page
+                    // (its id read before the wait, so the load overlaps it); an
+                    // id out of range (reported by the prologue) reads zeros
+                    const int pg = p.block_table[(size_t)cur.b * p.max_pages + kb / p.page_size];
+                    const int y = (pg >= 0 && pg < p.num_pages)
+                                      ? (pg * p.Hkv + kvh) * p.page_size + kb % p.page_size
+                                      : -kBK;
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    uint8_t *st = smem + s * kStageBytes + half_off;
+                    mbar_arrive_expect_tx(&full[s], 2 * kBox);
+                    tma_load_2d(st, map, 0, y, &full[s]);
+                    tma_load_2d(st + kBox, map, 64, y, &full[s]);
+                } else {
+                    // paged, smaller pages: one block of page_size rows per page
+                    // (pages past the sequence's end may hold any id: an id out
+                    // of range reads zeros; those keys are masked anyway)
+                    const int ps = p.page_size;
+                    const int nsub = min(kBK / ps, p.max_pages - kb / ps);
+                    int y[kMaxSubBlocks];
+#pragma unroll
+                    for (int i = 0; i < kMaxSubBlocks; ++i)
+                        if (i < nsub) {
+                            const int pg = p.block_table[(size_t)cur.b * p.max_pages + kb / ps + i];
+                            y[i] = (pg >= 0 && pg < p.num_pages) ? (pg * p.Hkv + kvh) * ps : -kBK;
+                        }
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    uint8_t *st = smem + s * kStageBytes + half_off;
+                    mbar_arrive_expect_tx(&full[s], 2u * 128u * (uint32_t)(nsub * ps));
+#pragma unroll
+                    for (int i = 0; i < kMaxSubBlocks; ++i)
+                        if (i < nsub) {
+                            tma_load_2d(st + i * ps * 128, map, 0, y[i], &full[s]);
+                            tma_load_2d(st + kBox + i * ps * 128, map, 64, y[i], &full[s]);
+                        }
+                }
                 cursor_next(cur, tile_base, p.B, HR);
             }
             // every copy issued must land before the CTA may exit

@@ -12,6 +12,8 @@ constexpr int kBK = 128;                  // keys per tile
 constexpr int kBox = kBK * 64 * 2;        // one 128-key x 64-dim bf16 TMA box: 16 KB
 constexpr int kStageBytes = 4 * kBox;     // K lo/hi + V lo/hi: 64 KB
 constexpr int kMaxB = 4096;
+constexpr int kMinPage = 8;                      // smallest page (a swizzle atom of rows)
+constexpr int kMaxSubBlocks = kBK / kMinPage;    // pages per key tile at most
 constexpr int kMaxT = 64;
 constexpr int kSoftmaxWarps = 8;                      // warps 2-9: two per TMEM lane quarter
 constexpr int kPvWarp = 2 + kSoftmaxWarps;              // issues the PV products
@@ -29,6 +31,10 @@ struct AttnKParams {
     float *part_o;   // [grid][2][rows_per_rg][kD]: unnormalised O of split pairs
     float *part_ml;  // [grid][2][rows_per_rg][2 halves][2]: (max in log2 units, row sum)
     int *pair_ctr;   // [B][Hkv][RG][2][8]: per softmax warp, CTAs arrived / partials ready (0 after the merge)
+    // paged caches (block_table non-null): K/V [num_pages][Hkv][page_size][D];
+    // logical slot s of sequence b is in page block_table[b][s / page_size]
+    const int32_t *block_table;
+    int max_pages, num_pages, page_size;
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.
@@ -123,7 +129,15 @@ __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_ba
     if (blockIdx.x == 0 && p.seq_status) {
         for (int b = tid; b < p.B; b += nt) {
             const int L = p.prefix_lens[b];
-            p.seq_status[b] = (L >= 0 && (long long)L + p.T <= p.S_max) ? SV_OK : SV_ERR_BAD_INPUT;
+            bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
+            if (ok && p.block_table) {  // the pages holding slots [0, L + T) exist
+                const int np = (L + p.T + p.page_size - 1) / p.page_size;
+                for (int j = 0; j < np; ++j) {
+                    const int pg = p.block_table[(size_t)b * p.max_pages + j];
+                    if (pg < 0 || pg >= p.num_pages) ok = false;
+                }
+            }
+            p.seq_status[b] = ok ? SV_OK : SV_ERR_BAD_INPUT;
         }
         __syncthreads();
         if (p.parents) {

@@ -22,6 +22,7 @@ constexpr int kMaxRowVecs = 32;    // 16-byte words per row: D <= 256 bf16
 __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
     __shared__ uint4 stage[2][kCompactBatch * kMaxRowVecs];
     __shared__ int s_src[kCompactBatch];
+    __shared__ size_t s_src_off[kCompactBatch], s_dst_off[kCompactBatch];
     griddep_wait();
     griddep_launch_dependents();
     const int b = blockIdx.x;
@@ -39,12 +40,18 @@ __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
     }
     int bad = (L < 0) || ((long long)L + acc + 1 > a.S_max) ||
               (a.path_nodes != nullptr && acc >= a.path_stride);
+    // a paged cache: the page of a slot must exist
+    auto page_ok = [&](int slot) {
+        const int pg = a.block_table[(size_t)b * a.max_pages + slot / a.page_size];
+        return pg >= 0 && pg < a.num_pages;
+    };
     if (!bad && a.path_nodes) {
         const int32_t *path = a.path_nodes + (size_t)b * a.path_stride;
         for (int d = threadIdx.x; d <= acc; d += kCT) {
             const int src = path[d];
             if (d == 0 ? src != 0 : src <= path[d - 1]) bad = 1;
             if ((long long)L + src >= a.S_max) bad = 1;
+            if (!bad && a.block_table && (!page_ok(L + src) || !page_ok(L + d))) bad = 1;
         }
     }
     bad = __syncthreads_or(bad);
@@ -57,28 +64,38 @@ __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
     }
     if (a.path_nodes) {
         const int32_t *path = a.path_nodes + (size_t)b * a.path_stride;
+        uint4 *kc = static_cast<uint4 *>(a.k);
+        uint4 *vc = static_cast<uint4 *>(a.v);
+        // offset (16-byte words) of row `slot` of KV head h: contiguous
+        // [B, Hkv, S_max, D], or through the page table
+        auto row_off = [&](int h, int slot) -> size_t {
+            if (!a.block_table) return (((size_t)b * a.Hkv + h) * a.S_max + slot) * vpr;
+            const int pg = a.block_table[(size_t)b * a.max_pages + slot / a.page_size];
+            return (((size_t)pg * a.Hkv + h) * a.page_size + slot % a.page_size) * vpr;
+        };
         for (int h = 0; h < a.Hkv; ++h) {
-            const size_t head = ((size_t)b * a.Hkv + h) * (size_t)a.S_max;
-            uint4 *kc = static_cast<uint4 *>(a.k) + head * vpr;
-            uint4 *vc = static_cast<uint4 *>(a.v) + head * vpr;
             for (int d0 = 1; d0 <= acc; d0 += kCompactBatch) {  // d = 0 is the root: never moves
                 const int nb = min(kCompactBatch, acc + 1 - d0);
-                if (threadIdx.x < nb) s_src[threadIdx.x] = path[d0 + threadIdx.x];
+                if (threadIdx.x < nb) {
+                    const int src = path[d0 + threadIdx.x];
+                    s_src[threadIdx.x] = src;
+                    s_src_off[threadIdx.x] = row_off(h, L + src);
+                    s_dst_off[threadIdx.x] = row_off(h, L + d0 + threadIdx.x);
+                }
                 __syncthreads();
                 for (int i = threadIdx.x; i < nb * vpr; i += kCT) {
                     const int r = i / vpr, w = i - r * vpr;
-                    const int src = s_src[r];
-                    if (src != d0 + r) {
-                        stage[0][i] = kc[(size_t)(L + src) * vpr + w];
-                        stage[1][i] = vc[(size_t)(L + src) * vpr + w];
+                    if (s_src[r] != d0 + r) {
+                        stage[0][i] = kc[s_src_off[r] + w];
+                        stage[1][i] = vc[s_src_off[r] + w];
                     }
                 }
                 __syncthreads();
                 for (int i = threadIdx.x; i < nb * vpr; i += kCT) {
                     const int r = i / vpr, w = i - r * vpr;
                     if (s_src[r] != d0 + r) {
-                        kc[(size_t)(L + d0 + r) * vpr + w] = stage[0][i];
-                        vc[(size_t)(L + d0 + r) * vpr + w] = stage[1][i];
+                        kc[s_dst_off[r] + w] = stage[0][i];
+                        vc[s_dst_off[r] + w] = stage[1][i];
                     }
                 }
                 __syncthreads();

@@ -126,10 +126,12 @@ struct AttnArgs {
     const void *v;
     const int32_t *prefix_lens;
     const int32_t *parents;
-    int B, T, Hq, Hkv, D, S_max;
+    int B, T, Hq, Hkv, D, S_max;  // S_max = max_pages * page_size for a paged cache
     float scale;
     void *out;
     int32_t *seq_status;
+    const int32_t *block_table;  // null: contiguous caches [B, Hkv, S_max, D]
+    int max_pages, num_pages, page_size;
 };
 
 sv_status launch_tree_attention(const AttnArgs &args, const AttnPlan &plan, void *ws,
@@ -145,8 +147,11 @@ struct CompactArgs {
     const int32_t *path_nodes;
     int path_stride;
     const int32_t *accepted_len;
-    int B, Hkv, D, S_max;
+    int B, Hkv, D, S_max;  // S_max = max_pages * page_size for a paged cache
     int32_t *seq_status;
+    const int32_t *block_table;  // null: contiguous caches [B, Hkv, S_max, D]
+    int max_pages, page_size;
+    int num_pages;
 };
 
 sv_status launch_compact_kv(const CompactArgs &args, cudaStream_t stream);

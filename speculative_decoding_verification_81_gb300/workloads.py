@@ -208,6 +208,44 @@ def attention_inputs(B, T, Hq, Hkv, D, prefix_lens, S_max=None, parents=None, se
 # --------------------------------------------------------------------------
 # the five named workloads
 
+_T_PAGES = 18
+
+
+def paged_cache(k, v, page_size, seed=0, spare_pages=3, nan_fill=True):
+    """Scatter contiguous caches k, v [B, Hkv, S_max, D] (bf16 bits) into pages
+    [num_pages, Hkv, page_size, D] under a random page table: logical page j
+    of sequence b is physical page block_table[b, j].  Page slots past S_max
+    and the spare pages that no sequence uses hold NaN (zeros without
+    nan_fill), so that a stray read shows.  Returns (k_pages, v_pages,
+    block_table)."""
+    B, Hkv, S_max, D = k.shape
+    max_pages = -(-S_max // page_size)
+    num_pages = B * max_pages + spare_pages
+    r = _rng(seed, _T_PAGES)
+    perm = r.permutation(num_pages).astype(np.int32)
+    table = perm[:B * max_pages].reshape(B, max_pages)
+    fill = 0x7FC0 if nan_fill else 0
+    kp = np.full((num_pages, Hkv, page_size, D), fill, np.uint16)
+    vp = np.full((num_pages, Hkv, page_size, D), fill, np.uint16)
+    for b in range(B):
+        for j in range(max_pages):
+            s0, s1 = j * page_size, min(S_max, (j + 1) * page_size)
+            kp[table[b, j], :, :s1 - s0] = k[b, :, s0:s1]
+            vp[table[b, j], :, :s1 - s0] = v[b, :, s0:s1]
+    return kp, vp, table
+
+
+def gather_paged(pages, block_table, S_max):
+    """Inverse of paged_cache for one cache: [B, Hkv, S_max, D] from the pages."""
+    num_pages, Hkv, page_size, D = pages.shape
+    B, max_pages = block_table.shape
+    out = np.empty((B, Hkv, max_pages * page_size, D), pages.dtype)
+    for b in range(B):
+        for j in range(max_pages):
+            out[b, :, j * page_size:(j + 1) * page_size] = pages[block_table[b, j]]
+    return out[:, :, :S_max]
+
+
 WORKLOADS = {
     1: dict(name="chain rejection-sampling verify, B=1 N=4 V=1024 fp32",
             kind="chain", B=1, N=4, V=1024, dtype="f32", target_sigma=2.0, draft_sigma=0.5,
