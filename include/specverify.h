@@ -103,6 +103,10 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
  *   prefix_lens int32 [B]; each 0 <= L_b and L_b + T <= S_max (else
  *               seq_status[b] = SV_ERR_BAD_INPUT and the sequence is skipped)
  *   parents     int32 [B, T] parent array, or NULL for a chain (causal mask)
+ *   node_counts int32 [B] or NULL: sequence b has T_b nodes (1 <= T_b <= T;
+ *               a variable-length batch), nodes t >= T_b are padding -- their
+ *               output rows are left unspecified and their slots unread, and
+ *               L_b + T_b replaces L_b + T above; NULL means T_b = T
  *   scale       > 0 and finite, normally 1/sqrt(D)
  *   out         bf16 [B, T, Hq, D]
  *   seq_status  int32 [B] or NULL
@@ -112,14 +116,14 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
  */
 sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *prefix_lens, const int32_t *parents,
-                            int B, int T, int Hq, int Hkv, int D, int S_max, float scale,
-                            void *out, int32_t *seq_status,
+                            const int32_t *node_counts, int B, int T, int Hq, int Hkv, int D,
+                            int S_max, float scale, void *out, int32_t *seq_status,
                             void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /*
- * Verification attention over a paged KV cache ("KV paginé": the cache held in
- * fixed-size pages reached through a per-sequence page table; "Chapitre 9"
- * §9.4).  The same computation as sv_tree_attention, with logical slot s of
+ * Verification attention over a paged KV cache (the paged KV of "Chapitre 9",
+ * section "Ce que prépare le Chapitre 9": the cache held in fixed-size pages
+ * reached through a per-sequence page table).  The same computation as sv_tree_attention, with logical slot s of
  * sequence b (prefix slots 0..L_b-1, node j at slot L_b + j) stored in page
  * block_table[b][s / page_size] at offset s % page_size.
  *
@@ -136,9 +140,10 @@ sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_ca
 sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void *v_pages,
                                   const int32_t *block_table, int max_pages, int num_pages,
                                   int page_size, const int32_t *prefix_lens,
-                                  const int32_t *parents, int B, int T, int Hq, int Hkv, int D,
-                                  float scale, void *out, int32_t *seq_status, void *workspace,
-                                  size_t workspace_bytes, sv_stream_t stream);
+                                  const int32_t *parents, const int32_t *node_counts, int B,
+                                  int T, int Hq, int Hkv, int D, float scale, void *out,
+                                  int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                                  sv_stream_t stream);
 
 /*
  * Stochastic chain acceptance over the full vocabulary.
@@ -159,15 +164,20 @@ sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void
  *   target_logits  [B, N+1, V] of `dtype`, already temperature-scaled
  *   draft_logits   [B, N, V] of `dtype`
  *   draft_tokens   int32 [B, N]
+ *   draft_lens     int32 [B] or NULL: sequence b drafted N_b tokens
+ *                  (0 <= N_b <= N; a variable-length batch): positions and
+ *                  rows past N_b are padding, the bonus after N_b acceptances
+ *                  comes from target row N_b, out_tokens holds N_b + 1 entries
+ *                  then -1, probs_out is 0 past N_b; NULL means N_b = N
  *   u_accept       f32 [B, N] uniforms in [0, 1); u_sample f32 [B]
  *   accepted_len   int32 [B];  out_tokens int32 [B, N+1]
  *   probs_out      f32 [B, N, 2] = (p_i(x_i), q_i(x_i)) for every i, or NULL
  * Supported: 1 <= N <= 63, 1 <= V < 2^30, dtype SV_F32 or SV_BF16.
- * Launches two kernels (statistics + decisions, then the residual draw).
+ * Launches two kernels (row statistics, then the decisions and the residual draw).
  */
 sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, sv_dtype dtype,
-                          const int32_t *draft_tokens, const float *u_accept,
-                          const float *u_sample, int B, int N, int V,
+                          const int32_t *draft_tokens, const int32_t *draft_lens,
+                          const float *u_accept, const float *u_sample, int B, int N, int V,
                           int32_t *accepted_len, int32_t *out_tokens, float *probs_out,
                           int32_t *seq_status, void *workspace, size_t workspace_bytes,
                           sv_stream_t stream);
@@ -186,6 +196,8 @@ sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, s
  *   out_tokens[b,:] = node_tokens of path nodes 1..depth, am_{d*}, then -1
  *
  *   target_logits [B, T, V] of `dtype`; node_tokens, parents int32 [B, T]
+ *   node_counts int32 [B] or NULL: sequence b has T_b nodes (1 <= T_b <= T),
+ *   those past T_b are padding and never accepted; NULL means T_b = T
  *   (parents NULL: a chain, parent_i = i - 1, i.e. greedy chain
  *   verification -- the longest prefix of draft tokens each equal to the
  *   target's argmax at the position before it, then that argmax)
@@ -194,9 +206,10 @@ sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, s
  */
 sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
                                 const int32_t *node_tokens, const int32_t *parents,
-                                int B, int T, int V, int32_t *accepted_len,
-                                int32_t *path_nodes, int32_t *out_tokens, int32_t *seq_status,
-                                void *workspace, size_t workspace_bytes, sv_stream_t stream);
+                                const int32_t *node_counts, int B, int T, int V,
+                                int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
+                                int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                                sv_stream_t stream);
 
 /*
  * Compaction of the accepted path's rows in the enlarged KV cache.

@@ -17,7 +17,7 @@
  *     min(1, p(x)/q(x)) with the normalised residual (p-q)+ and the bonus
  *     token drawn from the (N+1)-th distribution (Chapitre 9 §9.1),
  *   - greedy longest-agreeing-path acceptance on a draft tree (glossary,
- *     "L'attention en arbre"; Chapitre 9 §9.1 "le plus long préfixe"),
+ *     "L'attention en arbre"; Chapitre 9 §9.1, the longest agreeing prefix),
  *   - compaction of the accepted path's K/V rows ("Parallel Decoding",
  *     "Limites du parallel decoding": the enlarged KV cache for branches).
  *
@@ -279,7 +279,7 @@ static int32_t inverse_cdf(const double *r, int V, double S, double u, int *near
  * positions left to right; the first rejected position a is replaced by a
  * draw from the normalised residual (p_a - q_a)+; when all N are accepted a
  * bonus token is drawn from p_N.  Output is then distributed exactly as the
- * target alone would sample (§9.1; glossary "Garantie de qualité").
+ * target alone would sample (§9.1; glossary, "Speculative Decoding (Google, 2022)").
  *
  * Readings: accept_i <=> u_accept[i] * q_i(x_i) < p_i(x_i) with u in [0,1);
  * a sequence with a draft token outside [0, V) or a logits row whose max or

@@ -60,12 +60,13 @@ def lib() -> ctypes.CDLL:
         P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         L.sv_workspace_size.argtypes = [I, I, I, I, I, I, I]
         L.sv_workspace_size.restype = Z
-        L.sv_tree_attention.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P, Z, P]
-        L.sv_verify_chain.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
-        L.sv_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P, P, Z, P]
+        L.sv_tree_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P,
+                                        Z, P]
+        L.sv_verify_chain.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+        L.sv_verify_tree_greedy.argtypes = [P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
         L.sv_verify_chain_noalloc.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         L.sv_compact_kv.argtypes = [P, P, P, P, P, I, P, I, I, I, I, P, P]
-        L.sv_tree_attention_paged.argtypes = [P, P, P, P, I, I, I, P, P, I, I, I, I, I,
+        L.sv_tree_attention_paged.argtypes = [P, P, P, P, I, I, I, P, P, P, I, I, I, I, I,
                                               ctypes.c_float, P, P, P, Z, P]
         L.sv_compact_kv_paged.argtypes = [P, P, P, I, I, I, P, P, P, I, P, I, I, I, P, P]
         for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
@@ -140,9 +141,10 @@ def workspace(op: int, B: int, T_or_N: int, V: int = 0, Hq: int = 0, Hkv: int = 
 
 
 def sv_tree_attention(q, k_cache, v_cache, prefix_lens, parents=None, scale=None, out=None,
-                      seq_status=None, ws=None, stream=None):
+                      seq_status=None, ws=None, stream=None, node_counts=None):
     """q [B,T,Hq,D] bf16; k_cache/v_cache [B,Hkv,S_max,D] bf16; prefix_lens [B] int32;
-    parents [B,T] int32 or None (chain).  Returns out [B,T,Hq,D] bf16."""
+    parents [B,T] int32 or None (chain); node_counts [B] int32 or None (every
+    sequence has T nodes).  Returns out [B,T,Hq,D] bf16."""
     _req(q, "q", torch.bfloat16, 4)
     _req(k_cache, "k_cache", torch.bfloat16, 4)
     _req(v_cache, "v_cache", torch.bfloat16, 4)
@@ -157,15 +159,18 @@ def sv_tree_attention(q, k_cache, v_cache, prefix_lens, parents=None, scale=None
         out = torch.empty_like(q)
     if ws is None:
         ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
+    if node_counts is not None:
+        _req(node_counts, "node_counts", torch.int32, 1)
     rc = lib().sv_tree_attention(_p(q), _p(k_cache), _p(v_cache), _p(prefix_lens), _p(parents),
-                                 B, T, Hq, Hkv, D, S_max, float(scale), _p(out), _p(seq_status),
-                                 _p(ws), ws.numel(), _stream(stream))
+                                 _p(node_counts), B, T, Hq, Hkv, D, S_max, float(scale), _p(out),
+                                 _p(seq_status), _p(ws), ws.numel(), _stream(stream))
     _check("sv_tree_attention", rc)
     return out
 
 
 def sv_tree_attention_paged(q, k_pages, v_pages, block_table, prefix_lens, parents=None,
-                            scale=None, out=None, seq_status=None, ws=None, stream=None):
+                            scale=None, out=None, seq_status=None, ws=None, stream=None,
+                            node_counts=None):
     """q [B,T,Hq,D] bf16; k_pages/v_pages [num_pages,Hkv,page_size,D] bf16;
     block_table [B,max_pages] int32; prefix_lens [B] int32; parents [B,T] int32
     or None (chain).  Returns out [B,T,Hq,D] bf16."""
@@ -185,24 +190,29 @@ def sv_tree_attention_paged(q, k_pages, v_pages, block_table, prefix_lens, paren
         out = torch.empty_like(q)
     if ws is None:
         ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
+    if node_counts is not None:
+        _req(node_counts, "node_counts", torch.int32, 1)
     rc = lib().sv_tree_attention_paged(_p(q), _p(k_pages), _p(v_pages), _p(block_table), max_pages,
-                                       num_pages, page_size, _p(prefix_lens), _p(parents), B, T,
-                                       Hq, Hkv, D, float(scale), _p(out), _p(seq_status), _p(ws),
-                                       ws.numel(), _stream(stream))
+                                       num_pages, page_size, _p(prefix_lens), _p(parents),
+                                       _p(node_counts), B, T, Hq, Hkv, D, float(scale), _p(out),
+                                       _p(seq_status), _p(ws), ws.numel(), _stream(stream))
     _check("sv_tree_attention_paged", rc)
     return out
 
 
 def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sample,
                     accepted_len=None, out_tokens=None, probs_out=None, seq_status=None, ws=None,
-                    stream=None):
+                    stream=None, draft_lens=None):
     """target [B,N+1,V], draft [B,N,V] (bf16 or f32); draft_tokens [B,N] int32;
-    u_accept [B,N] f32; u_sample [B] f32.  Returns (accepted_len [B], out_tokens [B,N+1])."""
+    u_accept [B,N] f32; u_sample [B] f32; draft_lens [B] int32 or None (every
+    sequence drafted N tokens).  Returns (accepted_len [B], out_tokens [B,N+1])."""
     _req(target_logits, "target_logits", None, 3)
     _req(draft_logits, "draft_logits", target_logits.dtype, 3)
     _req(draft_tokens, "draft_tokens", torch.int32, 2)
     _req(u_accept, "u_accept", torch.float32, 2)
     _req(u_sample, "u_sample", torch.float32, 1)
+    if draft_lens is not None:
+        _req(draft_lens, "draft_lens", torch.int32, 1)
     dt = _dtype_code(target_logits)
     B, N1, V = target_logits.shape
     N = N1 - 1
@@ -214,7 +224,7 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
     if ws is None:
         ws = workspace(SV_OP_VERIFY_CHAIN, B, N, V, dt, 0, 0, dev)
     rc = lib().sv_verify_chain(_p(target_logits), _p(draft_logits), dt, _p(draft_tokens),
-                               _p(u_accept), _p(u_sample), B, N, V, _p(accepted_len),
+                               _p(draft_lens), _p(u_accept), _p(u_sample), B, N, V, _p(accepted_len),
                                _p(out_tokens), _p(probs_out), _p(seq_status), _p(ws), ws.numel(),
                                _stream(stream))
     _check("sv_verify_chain", rc)
@@ -222,14 +232,18 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
 
 
 def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None, path_nodes=None,
-                          out_tokens=None, seq_status=None, ws=None, stream=None):
+                          out_tokens=None, seq_status=None, ws=None, stream=None,
+                          node_counts=None):
     """target [B,T,V] (bf16 or f32); node_tokens, parents [B,T] int32 (parents
-    None: a chain, i.e. greedy chain verification).
+    None: a chain, i.e. greedy chain verification); node_counts [B] int32 or
+    None (every sequence has T nodes).
     Returns (accepted_len [B], path_nodes [B,T], out_tokens [B,T])."""
     _req(target_logits, "target_logits", None, 3)
     _req(node_tokens, "node_tokens", torch.int32, 2)
     if parents is not None:
         _req(parents, "parents", torch.int32, 2)
+    if node_counts is not None:
+        _req(node_counts, "node_counts", torch.int32, 1)
     dt = _dtype_code(target_logits)
     B, T, V = target_logits.shape
     dev = target_logits.device
@@ -241,7 +255,8 @@ def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None
         out_tokens = torch.empty(B, T, dtype=torch.int32, device=dev)
     if ws is None:
         ws = workspace(SV_OP_VERIFY_TREE_GREEDY, B, T, V, dt, 0, 0, dev)
-    rc = lib().sv_verify_tree_greedy(_p(target_logits), dt, _p(node_tokens), _p(parents), B, T, V,
+    rc = lib().sv_verify_tree_greedy(_p(target_logits), dt, _p(node_tokens), _p(parents),
+                                     _p(node_counts), B, T, V,
                                      _p(accepted_len), _p(path_nodes), _p(out_tokens),
                                      _p(seq_status), _p(ws), ws.numel(), _stream(stream))
     _check("sv_verify_tree_greedy", rc)

@@ -50,10 +50,10 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
 }
 
 sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_cache,
-                            const int32_t *prefix_lens, const int32_t *parents, int B, int T,
-                            int Hq, int Hkv, int D, int S_max, float scale, void *out,
-                            int32_t *seq_status, void *workspace, size_t workspace_bytes,
-                            sv_stream_t stream) {
+                            const int32_t *prefix_lens, const int32_t *parents,
+                            const int32_t *node_counts, int B, int T, int Hq, int Hkv, int D,
+                            int S_max, float scale, void *out, int32_t *seq_status,
+                            void *workspace, size_t workspace_bytes, sv_stream_t stream) {
     if (!q || !k_cache || !v_cache || !prefix_lens || !out) return SV_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || S_max < T) return SV_ERR_INVALID_ARG;
     if (Hq % Hkv != 0 || !(scale > 0.f) || !std::isfinite(scale)) return SV_ERR_INVALID_ARG;
@@ -65,7 +65,7 @@ sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_ca
     if (st != SV_OK) return st;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
     sv::AttnArgs a{q,   k_cache, v_cache, prefix_lens, parents,    B,       T, Hq, Hkv, D,
-                   S_max, scale, out,  seq_status, nullptr, 0, 0, 0};
+                   S_max, scale, out,  seq_status, nullptr, 0, 0, 0, node_counts};
     return sv::launch_tree_attention(a, pl, workspace, as_stream(stream));
 }
 
@@ -77,9 +77,10 @@ static bool valid_page_size(int ps) {
 sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void *v_pages,
                                   const int32_t *block_table, int max_pages, int num_pages,
                                   int page_size, const int32_t *prefix_lens,
-                                  const int32_t *parents, int B, int T, int Hq, int Hkv, int D,
-                                  float scale, void *out, int32_t *seq_status, void *workspace,
-                                  size_t workspace_bytes, sv_stream_t stream) {
+                                  const int32_t *parents, const int32_t *node_counts, int B,
+                                  int T, int Hq, int Hkv, int D, float scale, void *out,
+                                  int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                                  sv_stream_t stream) {
     if (!q || !k_pages || !v_pages || !block_table || !prefix_lens || !out) return SV_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_pages <= 0 || num_pages <= 0)
         return SV_ERR_INVALID_ARG;
@@ -97,15 +98,16 @@ sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
     sv::AttnArgs a{q,  k_pages, v_pages, prefix_lens, parents,     B,         T,        Hq,
                    Hkv, D,      (int)S_max, scale,     out,         seq_status, block_table,
-                   max_pages, num_pages, page_size};
+                   max_pages, num_pages, page_size, node_counts};
     return sv::launch_tree_attention(a, pl, workspace, as_stream(stream));
 }
 
 sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, sv_dtype dtype,
-                          const int32_t *draft_tokens, const float *u_accept,
-                          const float *u_sample, int B, int N, int V, int32_t *accepted_len,
-                          int32_t *out_tokens, float *probs_out, int32_t *seq_status,
-                          void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+                          const int32_t *draft_tokens, const int32_t *draft_lens,
+                          const float *u_accept, const float *u_sample, int B, int N, int V,
+                          int32_t *accepted_len, int32_t *out_tokens, float *probs_out,
+                          int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                          sv_stream_t stream) {
     if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample ||
         !accepted_len || !out_tokens)
         return SV_ERR_INVALID_ARG;
@@ -116,16 +118,18 @@ sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, s
     const sv::VocabPlan pl = sv::plan_vocab(true, B, N, V, dtype);
     if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return SV_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
-    sv::ChainArgs a{target_logits, draft_logits, draft_tokens, u_accept, u_sample, B, N, V,
-                    accepted_len, out_tokens, probs_out, seq_status};
+    sv::ChainArgs a{target_logits, draft_logits, draft_tokens, draft_lens, u_accept, u_sample,
+                    B,             N,            V,            accepted_len, out_tokens,
+                    probs_out,     seq_status};
     return sv::launch_verify_chain(a, dtype, pl, workspace, as_stream(stream));
 }
 
 sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
-                                const int32_t *node_tokens, const int32_t *parents, int B, int T,
-                                int V, int32_t *accepted_len, int32_t *path_nodes,
-                                int32_t *out_tokens, int32_t *seq_status, void *workspace,
-                                size_t workspace_bytes, sv_stream_t stream) {
+                                const int32_t *node_tokens, const int32_t *parents,
+                                const int32_t *node_counts, int B, int T, int V,
+                                int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
+                                int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                                sv_stream_t stream) {
     if (!target_logits || !node_tokens || !accepted_len || !path_nodes || !out_tokens)
         return SV_ERR_INVALID_ARG;
     if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
@@ -135,8 +139,8 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
     const sv::VocabPlan pl = sv::plan_vocab(false, B, T, V, dtype);
     if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return SV_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
-    sv::TreeArgs a{target_logits, node_tokens, parents, B, T, V, accepted_len, path_nodes,
-                   out_tokens, seq_status};
+    sv::TreeArgs a{target_logits, node_tokens, parents,    node_counts, B, T, V, accepted_len,
+                   path_nodes,    out_tokens,  seq_status};
     return sv::launch_verify_tree_greedy(a, dtype, pl, workspace, as_stream(stream));
 }
 

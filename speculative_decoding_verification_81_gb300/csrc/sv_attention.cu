@@ -174,6 +174,7 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.max_pages = a.max_pages;
     p.num_pages = a.num_pages;
     p.page_size = a.page_size;
+    p.node_counts = a.node_counts;
     void *args[] = {&tmk, &tmv, &tmq, &p};
     return launch_pdl(tc_kernel_fn(pl.stages, pl.mrows), dim3(pl.grid), dim3(kTcThreads),
                       pl.smem, st, args) == cudaSuccess

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     int L = 0, kv_end = 0, seg_first_tile = 0, kvh = 0, rg = 0, rglob = 0;
     bool seg_is_first = true, warp_active = false, row_valid = false;
-    int next_L = 0;         // the next segment's prefix length, read ahead
+    int next_L = 0, next_T = 0;  // the next segment's prefix length and nodes, read ahead
     bool have_next_L = false;
     Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
     long long jt = 0;
@@ -390,14 +390,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             kvh = cur.pr / p.RG;
             rg = cur.pr - kvh * p.RG;
             L = have_next_L ? next_L : p.prefix_lens[cur.b];
+            const int Tb = have_next_L ? next_T : nodes_of(p, cur.b);
             have_next_L = false;
-            kv_end = L + p.T;
+            kv_end = L + Tb;
             seg_first_tile = cur.tile;
             seg_is_first = (u == u_begin);
             // the group's rows are rows_per_rg (a multiple of G) of the MMA's
             // MROWS; the others are padding
             rglob = rg * p.rows_per_rg + r;
-            row_valid = lane_has_row && r < p.rows_per_rg && rglob < p.M;
+            row_valid = lane_has_row && r < p.rows_per_rg && rglob < p.M && rglob / p.G < Tb;
             warp_active = quarter * kRowsPerQuarter < p.rows_per_rg &&
                           rg * p.rows_per_rg + quarter * kRowsPerQuarter < p.M;
             m = kNegInf;
@@ -411,6 +412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             nx.tile = nx.n - 1;
             cursor_next(nx, tile_base, p.B, HR);
             next_L = p.prefix_lens[nx.b];
+            next_T = nodes_of(p, nx.b);
             have_next_L = true;
         }
         const bool first_tile = new_seg;  // O is overwritten by this tile's PV

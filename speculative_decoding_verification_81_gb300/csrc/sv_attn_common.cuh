@@ -35,6 +35,8 @@ struct AttnKParams {
     // logical slot s of sequence b is in page block_table[b][s / page_size]
     const int32_t *block_table;
     int max_pages, num_pages, page_size;
+    // per-sequence node counts T_b (1 <= T_b <= T; nodes past T_b are padding), or null: all T
+    const int32_t *node_counts;
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.
@@ -102,12 +104,19 @@ constexpr float kRescaleThreshold = 8.0f;
 // (identically in every CTA); CTA 0 also writes each sequence's status
 // (prefix length in range, parent array a topologically ordered tree).
 // Contains __syncthreads: call from every thread of the CTA.
+// Nodes of sequence b: T_b, or 0 when out of range (the sequence is then invalid).
+__device__ __forceinline__ int nodes_of(const AttnKParams &p, int b) {
+    if (!p.node_counts) return p.T;
+    const int n = p.node_counts[b];
+    return (n >= 1 && n <= p.T) ? n : 0;
+}
+
 __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int nt) {
     const int tid = threadIdx.x;
     for (int b = tid; b < p.B; b += nt) {
-        const int L = p.prefix_lens[b];
-        const bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
-        tile_base[b] = ok ? (L + p.T + kBK - 1) / kBK : 0;
+        const int L = p.prefix_lens[b], Tb = nodes_of(p, b);
+        const bool ok = L >= 0 && Tb > 0 && (long long)L + Tb <= p.S_max;
+        tile_base[b] = ok ? (L + Tb + kBK - 1) / kBK : 0;
     }
     __syncthreads();
     if (tid < 32) {  // exclusive scan, 32 sequences at a time
@@ -128,10 +137,10 @@ __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_ba
     }
     if (blockIdx.x == 0 && p.seq_status) {
         for (int b = tid; b < p.B; b += nt) {
-            const int L = p.prefix_lens[b];
-            bool ok = L >= 0 && (long long)L + p.T <= p.S_max;
-            if (ok && p.block_table) {  // the pages holding slots [0, L + T) exist
-                const int np = (L + p.T + p.page_size - 1) / p.page_size;
+            const int L = p.prefix_lens[b], Tb = nodes_of(p, b);
+            bool ok = L >= 0 && Tb > 0 && (long long)L + Tb <= p.S_max;
+            if (ok && p.block_table) {  // the pages holding slots [0, L + T_b) exist
+                const int np = (L + Tb + p.page_size - 1) / p.page_size;
                 for (int j = 0; j < np; ++j) {
                     const int pg = p.block_table[(size_t)b * p.max_pages + j];
                     if (pg < 0 || pg >= p.num_pages) ok = false;
@@ -143,6 +152,7 @@ __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_ba
         if (p.parents) {
             for (int i = tid; i < p.B * p.T; i += nt) {
                 const int b = i / p.T, t = i - b * p.T;
+                if (t >= nodes_of(p, b)) continue;  // padding node
                 const int pa = p.parents[i];
                 if (t == 0 ? pa != -1 : (pa < 0 || pa >= t)) p.seq_status[b] = SV_ERR_BAD_INPUT;
             }

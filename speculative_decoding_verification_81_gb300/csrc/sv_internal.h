@@ -43,8 +43,8 @@ struct RowPartial {
 
 // Per-sequence result of the chain decisions, taken at the start of the residual draw.
 struct ChainDecision {
-    int a;       // first rejected position, N if all accepted, -1 if the sequence is invalid
-    int pad;
+    int a;       // first rejected position, N_b if all accepted, -1 if the sequence is invalid
+    int n_draft; // N_b, the sequence's draft length
     float ms_t;  // target row a: max * log2(e) and normaliser
     float s_t;
     float ms_d;  // draft row a (unused when a == N)
@@ -73,6 +73,7 @@ struct ChainArgs {
     const void *target;
     const void *draft;
     const int32_t *tokens;
+    const int32_t *draft_lens;  // per-sequence N_b (0 <= N_b <= N), or null: all N
     const float *u_accept;
     const float *u_sample;
     int B, N, V;
@@ -86,6 +87,7 @@ struct TreeArgs {
     const void *target;
     const int32_t *tokens;
     const int32_t *parents;
+    const int32_t *node_counts;  // per-sequence T_b (1 <= T_b <= T), or null: all T
     int B, T, V;
     int32_t *accepted_len;
     int32_t *path_nodes;
@@ -132,6 +134,7 @@ struct AttnArgs {
     int32_t *seq_status;
     const int32_t *block_table;  // null: contiguous caches [B, Hkv, S_max, D]
     int max_pages, num_pages, page_size;
+    const int32_t *node_counts;  // per-sequence T_b, or null
 };
 
 sv_status launch_tree_attention(const AttnArgs &args, const AttnPlan &plan, void *ws,

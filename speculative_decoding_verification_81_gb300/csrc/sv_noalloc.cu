@@ -64,7 +64,7 @@ extern "C" sv_status sv_verify_chain_noalloc(const void *target_logits, const vo
     if (cudaMemsetAsync(static_cast<char *>(scratch) + pl.off_counters, 0,
                         sizeof(int) * 2 * (size_t)B, s) != cudaSuccess)
         return SV_ERR_CUDA;
-    sv::ChainArgs a{target_logits, draft_logits, draft_tokens, u_accept, u_sample, B, N, V,
+    sv::ChainArgs a{target_logits, draft_logits, draft_tokens, nullptr, u_accept, u_sample, B, N, V,
                     accepted_len, out_tokens, probs_out, seq_status};
     return sv::launch_verify_chain(a, dtype, pl, scratch, s);
 }

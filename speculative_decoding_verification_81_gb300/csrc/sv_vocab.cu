@@ -317,6 +317,21 @@ __host__ __device__ inline WsView ws_view(void *ws, const VocabPlan &p, int B) {
 
 // ---------------------------------------------------------------- chain: kernel 1
 
+// Draft length N_b of chain sequence b (N without a length array; 0 for an
+// invalid length, whose sequence the decisions report).
+__device__ __forceinline__ int chain_draft_len(const ChainArgs &a, int b) {
+    if (!a.draft_lens) return a.N;
+    const int n = a.draft_lens[b];
+    return (n >= 0 && n <= a.N) ? n : 0;
+}
+
+// Row r of the [target rows 0..N, draft rows 0..N-1] order is in use for a
+// sequence with N_b drafts: target rows 0..N_b and draft rows 0..N_b-1.  The
+// others are padding, never read.
+__device__ __forceinline__ bool chain_row_in_use(int N, int nb, int r) {
+    return r <= nb || (r > N && r - N - 1 < nb);
+}
+
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT, 5) chain_stats_kernel(ChainArgs a, VocabPlan p, WsView w) {
     __shared__ float red[2 * kVWarps];
@@ -335,6 +350,10 @@ __global__ void __launch_bounds__(kVT, 5) chain_stats_kernel(ChainArgs a, VocabP
 
     griddep_wait();
     griddep_launch_dependents();
+    if (!chain_row_in_use(a.N, chain_draft_len(a, b), r)) {  // a padding row: an empty record
+        if (threadIdx.x == 0) reinterpret_cast<float2 *>(w.partials)[item] = make_float2(kNegInf, 0.f);
+        return;
+    }
     float m = 0.f, s = 0.f;
     chunk_cta_stats<T, VEC>(row, begin, end, red, m, s);
     if (threadIdx.x == 0) reinterpret_cast<float2 *>(w.partials)[item] = make_float2(m, s);
@@ -386,12 +405,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // ================= producer: one bulk copy per unit
         if (lane == 0) {
             long long k = 0;
+            int cb = -1, nb = 0;  // the sequence of the last unit and its draft length
             for (long long u = u_begin; u < u_end; ++u, ++k) {
                 const int s = (int)(k % kSStages);
                 if (!mbar_wait_bounded(&empty[s], (uint32_t)(((k / kSStages) & 1) ^ 1))) break;
                 const int b = (int)(u / per_seq);
                 const int rem = (int)(u - (long long)b * per_seq);
                 const int r = rem / p.nchunks, c = rem - r * p.nchunks;
+                if (b != cb) {
+                    cb = b;
+                    nb = chain_draft_len(a, b);
+                }
+                if (!chain_row_in_use(a.N, nb, r)) {  // padding: the stage's phase, no copy
+                    mbar_arrive(&full[s]);
+                    continue;
+                }
                 const T *row = r <= a.N
                     ? static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + r) * a.V
                     : static_cast<const T *>(a.draft) + ((size_t)b * a.N + (r - a.N - 1)) * a.V;
@@ -415,6 +443,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // group of warp w: (w / 4) % 2, so each sub-partition (w % 4) holds two
     // warps of each group; warp within the group: 0..7
     const int grp = (warp >> 2) & 1, gw = ((warp >> 3) << 2) | (warp & 3);
+    int cb = -1, nb = 0;
     for (long long k = grp; k < u_end - u_begin; k += 2) {
         const long long u = u_begin + k;
         const int s = (int)(k % kSStages);
@@ -422,10 +451,23 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int rem = (int)(u - (long long)b * per_seq);
         const int r = rem / p.nchunks, c = rem - r * p.nchunks;
         const int n = min(kUnitElems, a.V - c * kUnitElems);  // elements in this unit (a multiple of PV)
+        if (b != cb) {
+            cb = b;
+            nb = chain_draft_len(a, b);
+        }
         if (!warp_wait_bounded(&full[s], (uint32_t)((k / kSStages) & 1))) {
             // the record stays unwritten; the sequence is reported
             if (lane == 0 && a.seq_status) a.seq_status[b] = SV_ERR_TIMEOUT;
             break;
+        }
+        if (!chain_row_in_use(a.N, nb, r)) {  // padding: nothing landed, an empty record
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[s]);
+                rec[(((size_t)b * R + r) * p.nchunks + c) * kSGroupWarps + gw] =
+                    make_float2(kNegInf, 0.f);
+            }
+            continue;
         }
         uint4 buf[kSWordsPerLane];
 #pragma unroll
@@ -620,15 +662,19 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int R = 2 * a.N + 1;
     const int per_row = p.nchunks * p.recs_per_unit;
+    // this sequence's draft length; rows and positions past it are padding
+    const int nb_raw = a.draft_lens ? a.draft_lens[b] : a.N;
+    const bool nb_ok = nb_raw >= 0 && nb_raw <= a.N;
+    const int Nb = nb_ok ? nb_raw : 0;
     if (tid == 0) {
-        s_bad = 0;
-        s_first = a.N;
+        s_bad = nb_ok ? 0 : 1;
+        s_first = Nb;
     }
     // p_i on threads 0..N-1, q_i on threads 64..64+N-1: the drafted token and
     // its logit are fetched first, overlapping the record merges below
     const int i = tid & 63;
     const int is_q = (tid >> 6) & 1;
-    const bool pos_thread = tid < 128 && i < a.N;
+    const bool pos_thread = tid < 128 && i < Nb;
     float l = 0.f;
     bool tok_ok = false;
     if (pos_thread) {
@@ -690,7 +736,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
         }
     }
     __syncthreads();
-    if (tid < R) {
+    if (tid < R && (tid <= Nb || (tid > a.N && tid - a.N - 1 < Nb))) {  // rows in use
         const float mm = s_ms[tid][0], ss = s_ms[tid][1];
         if (!(isfinite(mm) && isfinite(ss) && ss > 0.f)) atomicOr(&s_bad, 1);
     }
@@ -706,8 +752,9 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     }
     __syncthreads();
     if (tid < a.N) {
-        const float pp = s_pq[tid][0], qq = s_pq[tid][1];
-        if (!(a.u_accept[(size_t)b * a.N + tid] * qq < pp)) atomicMin(&s_first, tid);
+        const bool used = tid < Nb;
+        const float pp = used ? s_pq[tid][0] : 0.f, qq = used ? s_pq[tid][1] : 0.f;
+        if (used && !(a.u_accept[(size_t)b * a.N + tid] * qq < pp)) atomicMin(&s_first, tid);
         if (outputs && a.probs) {
             a.probs[((size_t)b * a.N + tid) * 2 + 0] = pp;
             a.probs[((size_t)b * a.N + tid) * 2 + 1] = qq;
@@ -717,13 +764,13 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     const bool bad = s_bad != 0;
     const int acc = bad ? -1 : s_first;
     ChainDecision d;
-    d.pad = 0;
+    d.n_draft = Nb;
     d.pad2[0] = d.pad2[1] = 0.f;
     d.a = acc;
     d.ms_t = bad ? 0.f : s_ms[acc][0];
     d.s_t = bad ? 0.f : s_ms[acc][1];
-    d.ms_d = (!bad && acc < a.N) ? s_ms[a.N + 1 + acc][0] : 0.f;
-    d.s_d = (!bad && acc < a.N) ? s_ms[a.N + 1 + acc][1] : 0.f;
+    d.ms_d = (!bad && acc < Nb) ? s_ms[a.N + 1 + acc][0] : 0.f;
+    d.s_d = (!bad && acc < Nb) ? s_ms[a.N + 1 + acc][1] : 0.f;
     if (outputs) {
         if (tid == 0) {
             a.accepted_len[b] = acc;
@@ -758,13 +805,13 @@ __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabP
 
     ResidualRow<T> rw;
     rw.trow = static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + d.a) * a.V;
-    rw.drow = d.a < a.N ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + d.a) * a.V
+    rw.drow = d.a < d.n_draft ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + d.a) * a.V
                         : rw.trow;
     rw.ms_t = d.ms_t;
     rw.inv_t = __frcp_rn(d.s_t);
     rw.ms_d = d.ms_d;
-    rw.inv_d = d.a < a.N ? __frcp_rn(d.s_d) : 0.f;
-    const int mode0 = d.a < a.N ? 0 : 1;
+    rw.inv_d = d.a < d.n_draft ? __frcp_rn(d.s_d) : 0.f;
+    const int mode0 = d.a < d.n_draft ? 0 : 1;  // residual at a rejection, else the bonus
 
     // ---- every CTA: weight sums of its chunk, per-thread prefixes kept
     const int e0 = c * p.res_chunk_elems + threadIdx.x * EPT;
@@ -904,9 +951,11 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
 
     griddep_wait();
     griddep_launch_dependents();
-    float best;
-    int idx;
-    chunk_thread_argmax<T, VEC>(row, begin, end, best, idx);
+    float best = kNegInf;
+    int idx = INT_MAX;
+    // a padding node's row (past T_b) is never read
+    const bool pad_row = a.node_counts != nullptr && r > 0 && r >= a.node_counts[b];
+    if (!pad_row) chunk_thread_argmax<T, VEC>(row, begin, end, best, idx);
     float m = 0.f, s = 0.f;
     cta_reduce_stats<true>(m, s, best, idx, scratch);
     if (threadIdx.x == 0) {
@@ -937,14 +986,17 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int bad = sm_par[0] != -1;
-        for (int i = 1; i < a.T && !bad; ++i)
+        // this sequence's nodes; those past T_b are padding
+        const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+        int bad = sm_par[0] != -1 || tb_raw < 1 || tb_raw > a.T;
+        const int Tb = bad ? 1 : tb_raw;
+        for (int i = 1; i < Tb && !bad; ++i)
             if (sm_par[i] < 0 || sm_par[i] >= i || sm_tok[i] < 0 || sm_tok[i] >= a.V) bad = 1;
         int bst = 0;
         if (!bad) {
             sm_ok[0] = 1;
             sm_depth[0] = 0;
-            for (int i = 1; i < a.T; ++i) {
+            for (int i = 1; i < Tb; ++i) {
                 const int pa = sm_par[i];
                 sm_ok[i] = sm_ok[pa] && sm_tok[i] == sm_am[pa];
                 sm_depth[i] = sm_depth[pa] + 1;

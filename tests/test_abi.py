@@ -49,10 +49,11 @@ MISALIGNED = ctypes.c_void_p(0x10004)
 
 
 def _chain(L, **kw):
-    a = dict(t=FAKE, d=FAKE, dt=sv.SV_BF16, tok=FAKE, ua=FAKE, us=FAKE, B=2, N=4, V=1000,
-             acc=FAKE, out=FAKE, probs=None, st=None, ws=None, wsb=0)
+    a = dict(t=FAKE, d=FAKE, dt=sv.SV_BF16, tok=FAKE, lens=None, ua=FAKE, us=FAKE, B=2, N=4,
+             V=1000, acc=FAKE, out=FAKE, probs=None, st=None, ws=None, wsb=0)
     a.update(kw)
-    return L.sv_verify_chain(a["t"], a["d"], a["dt"], a["tok"], a["ua"], a["us"], a["B"], a["N"],
+    return L.sv_verify_chain(a["t"], a["d"], a["dt"], a["tok"], a["lens"], a["ua"], a["us"],
+                             a["B"], a["N"],
                              a["V"], a["acc"], a["out"], a["probs"], a["st"], a["ws"], a["wsb"],
                              None)
 
@@ -67,6 +68,7 @@ def test_verify_chain_host_validation(L):
     assert _chain(L, t=MISALIGNED) == sv.SV_ERR_INVALID_ARG
     assert _chain(L, N=64) == sv.SV_ERR_UNSUPPORTED
     assert _chain(L) == sv.SV_ERR_WORKSPACE  # no workspace
+    assert _chain(L, lens=FAKE) == sv.SV_ERR_WORKSPACE  # draft lengths are checked on the device
     need = L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 2, 4, 1000, sv.SV_BF16, 0, 0)
     assert need > 0
     assert _chain(L, ws=FAKE, wsb=need - 1) == sv.SV_ERR_WORKSPACE
@@ -75,26 +77,29 @@ def test_verify_chain_host_validation(L):
 
 def test_verify_tree_host_validation(L):
     def call(**kw):
-        a = dict(t=FAKE, dt=sv.SV_BF16, tok=FAKE, par=FAKE, B=2, T=26, V=32000, acc=FAKE,
-                 path=FAKE, out=FAKE, ws=None, wsb=0)
+        a = dict(t=FAKE, dt=sv.SV_BF16, tok=FAKE, par=FAKE, cnt=None, B=2, T=26, V=32000,
+                 acc=FAKE, path=FAKE, out=FAKE, ws=None, wsb=0)
         a.update(kw)
-        return L.sv_verify_tree_greedy(a["t"], a["dt"], a["tok"], a["par"], a["B"], a["T"], a["V"],
+        return L.sv_verify_tree_greedy(a["t"], a["dt"], a["tok"], a["par"], a["cnt"], a["B"],
+                                       a["T"], a["V"],
                                        a["acc"], a["path"], a["out"], None, a["ws"], a["wsb"], None)
     assert call(tok=None) == sv.SV_ERR_INVALID_ARG
     assert call(par=None) == sv.SV_ERR_WORKSPACE  # NULL parents: a chain, valid
     assert call(T=0) == sv.SV_ERR_INVALID_ARG
     assert call(T=1025) == sv.SV_ERR_UNSUPPORTED
     assert call() == sv.SV_ERR_WORKSPACE
+    assert call(cnt=FAKE) == sv.SV_ERR_WORKSPACE  # node counts are checked on the device
     need = L.sv_workspace_size(sv.SV_OP_VERIFY_TREE_GREEDY, 2, 26, 32000, sv.SV_BF16, 0, 0)
     assert call(ws=FAKE, wsb=need - 16) == sv.SV_ERR_WORKSPACE
 
 
 def test_attention_host_validation(L):
     def call(**kw):
-        a = dict(q=FAKE, k=FAKE, v=FAKE, pl=FAKE, par=None, B=2, T=9, Hq=32, Hkv=8, D=128,
-                 S=4160, scale=0.088, out=FAKE)
+        a = dict(q=FAKE, k=FAKE, v=FAKE, pl=FAKE, par=None, cnt=None, B=2, T=9, Hq=32, Hkv=8,
+                 D=128, S=4160, scale=0.088, out=FAKE)
         a.update(kw)
-        return L.sv_tree_attention(a["q"], a["k"], a["v"], a["pl"], a["par"], a["B"], a["T"],
+        return L.sv_tree_attention(a["q"], a["k"], a["v"], a["pl"], a["par"], a["cnt"], a["B"],
+                                   a["T"],
                                    a["Hq"], a["Hkv"], a["D"], a["S"], a["scale"], a["out"], None,
                                    None, 0, None)
     assert call(q=None) == sv.SV_ERR_INVALID_ARG
