@@ -173,7 +173,9 @@ sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void
  *   accepted_len   int32 [B];  out_tokens int32 [B, N+1]
  *   probs_out      f32 [B, N, 2] = (p_i(x_i), q_i(x_i)) for every i, or NULL
  * Supported: 1 <= N <= 63, 1 <= V < 2^30, dtype SV_F32 or SV_BF16.
- * Launches two kernels (row statistics, then the decisions and the residual draw).
+ * Launches two kernels (row statistics, then the decisions and the residual
+ * draw).  If a bounded wait of the statistics pass gives up, every sequence
+ * of the call reports SV_ERR_TIMEOUT (outputs -1).
  */
 sv_status sv_verify_chain(const void *target_logits, const void *draft_logits, sv_dtype dtype,
                           const int32_t *draft_tokens, const int32_t *draft_lens,

@@ -60,7 +60,7 @@ struct VocabPlan {
     int res_chunk_elems;
     bool vec;             // rows are 16-byte aligned: vector loads
     int recs_per_unit;    // chain: (max, sum) records per (row, chunk)
-    size_t off_counters;  // 2*B ints
+    size_t off_counters;  // 2*B + 4 ints: arrivals per sequence, then [2*B] a timeout flag
     size_t off_partials;  // B * rows_per_seq * nchunks RowPartial
     size_t off_chunktot;  // B * res_chunks float2
     size_t off_tprefix;   // B * res_chunks * 256 float4: per-thread prefixes of the residual draw

@@ -60,9 +60,10 @@ extern "C" sv_status sv_verify_chain_noalloc(const void *target_logits, const vo
     const sv_status st = scratch_on_current_device(&scratch);
     if (st != SV_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the arrival counters must start at zero; everything else is written before it is read
+    // the counters (arrivals, the timeout flag) must start at zero; everything
+    // else is written before it is read
     if (cudaMemsetAsync(static_cast<char *>(scratch) + pl.off_counters, 0,
-                        sizeof(int) * 2 * (size_t)B, s) != cudaSuccess)
+                        sizeof(int) * (2 * (size_t)B + 4), s) != cudaSuccess)
         return SV_ERR_CUDA;
     sv::ChainArgs a{target_logits, draft_logits, draft_tokens, nullptr, u_accept, u_sample, B, N, V,
                     accepted_len, out_tokens, probs_out, seq_status};

@@ -300,7 +300,7 @@ __device__ __forceinline__ RowPartial warp_merge_row(const RowPartial *parts, in
 }
 
 struct WsView {
-    int *counters;  // [B] streaming pass, [B] residual draw
+    int *counters;  // [B] tree pass, [B] residual draw, [1] statistics pass timed out
     RowPartial *partials;
     float2 *chunktot;
 };
@@ -408,7 +408,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
             int cb = -1, nb = 0;  // the sequence of the last unit and its draft length
             for (long long u = u_begin; u < u_end; ++u, ++k) {
                 const int s = (int)(k % kSStages);
-                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((k / kSStages) & 1) ^ 1))) break;
+                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((k / kSStages) & 1) ^ 1))) {
+                    atomicExch(w.counters + 2 * a.B, 1);  // a stage never came free
+                    break;
+                }
                 const int b = (int)(u / per_seq);
                 const int rem = (int)(u - (long long)b * per_seq);
                 const int r = rem / p.nchunks, c = rem - r * p.nchunks;
@@ -456,8 +459,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
             nb = chain_draft_len(a, b);
         }
         if (!warp_wait_bounded(&full[s], (uint32_t)((k / kSStages) & 1))) {
-            // the record stays unwritten; the sequence is reported
-            if (lane == 0 && a.seq_status) a.seq_status[b] = SV_ERR_TIMEOUT;
+            // the record stays unwritten: the decisions report every sequence
+            if (lane == 0) atomicExch(w.counters + 2 * a.B, 1);
             break;
         }
         if (!chain_row_in_use(a.N, nb, r)) {  // padding: nothing landed, an empty record
@@ -570,6 +573,22 @@ __device__ __forceinline__ float raw_weight(const ResidualRow<T> &rw, int mode,
     return fmaxf(__fsub_rn(pj, rw.q_at(raw_elem<T>(rd, j))), 0.f);
 }
 
+// The same weight from one target logit and one draft logit.
+template <typename T>
+__device__ __forceinline__ float elem_weight(const ResidualRow<T> &rw, int mode, float lt, float ld) {
+    const float pj = rw.p_at(lt);
+    if (mode) return pj;
+    return fmaxf(__fsub_rn(pj, rw.q_at(ld)), 0.f);
+}
+
+// Element j of a thread's run kept as raw 16-byte words in shared memory.
+template <typename T>
+__device__ __forceinline__ float smem_elem(const uint4 *words, int j) {
+    if (sizeof(T) == 2)
+        return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short *>(words)[j] << 16);
+    return reinterpret_cast<const float *>(words)[j];
+}
+
 // Sequential sums over the thread's elements: sr of the weights in `mode`,
 // sp of p (the fallback weights).
 template <typename T>
@@ -655,7 +674,8 @@ __device__ __forceinline__ float exp2_diff_accurate(float l, float m) {
 // the one drawn at position a.
 template <typename T>
 __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, const VocabPlan &p,
-                                                         const float2 *rec, int b, bool outputs) {
+                                                         const float2 *rec, const int *timed_out,
+                                                         int b, bool outputs) {
     __shared__ float s_ms[2 * kMaxChainN + 1][2];
     __shared__ float s_pq[kMaxChainN][2];
     __shared__ int s_bad, s_first;
@@ -667,7 +687,9 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     const bool nb_ok = nb_raw >= 0 && nb_raw <= a.N;
     const int Nb = nb_ok ? nb_raw : 0;
     if (tid == 0) {
-        s_bad = nb_ok ? 0 : 1;
+        // bit 0: invalid input; bit 1: the statistics pass gave up (records
+        // left unwritten), so no decision is taken
+        s_bad = (nb_ok ? 0 : 1) | (__ldcg(timed_out) != 0 ? 2 : 0);
         s_first = Nb;
     }
     // p_i on threads 0..N-1, q_i on threads 64..64+N-1: the drafted token and
@@ -761,6 +783,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
         }
     }
     __syncthreads();
+    const bool late = (s_bad & 2) != 0;
     const bool bad = s_bad != 0;
     const int acc = bad ? -1 : s_first;
     ChainDecision d;
@@ -774,7 +797,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     if (outputs) {
         if (tid == 0) {
             a.accepted_len[b] = acc;
-            if (a.seq_status) a.seq_status[b] = bad ? SV_ERR_BAD_INPUT : SV_OK;
+            if (a.seq_status) a.seq_status[b] = late ? SV_ERR_TIMEOUT : bad ? SV_ERR_BAD_INPUT : SV_OK;
         }
         for (int j = tid; j <= a.N; j += kVT) {
             int v = -1;
@@ -786,12 +809,15 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
 }
 
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
+// (Aligned rows: at most 64 registers, so that four CTAs per SM keep a
+// B = 32, V = 128256 grid in one wave.)
+__global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
     constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
     __shared__ float2 wsum[kVWarps];
     __shared__ float2 s_tot[kMaxResChunks];
     __shared__ float s_prefix[kVT];
     __shared__ int s_last, s_cstar, s_mode, s_fallback, s_pick_min, s_pick_max;
+    __shared__ uint4 s_words[2][kResLoadsPerThread];  // the picked thread's run
     __shared__ float s_base, s_theta;
 
     griddep_wait();
@@ -800,7 +826,8 @@ __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabP
     const int c = blockIdx.x - b * p.res_chunks;
     // every CTA of the sequence takes the decisions; the first one writes them
     const ChainDecision d =
-        decide_sequence<T>(a, p, reinterpret_cast<const float2 *>(w.partials), b, c == 0);
+        decide_sequence<T>(a, p, reinterpret_cast<const float2 *>(w.partials),
+                           w.counters + 2 * a.B, b, c == 0);
     if (d.a < 0) return;  // invalid sequence: -1s written above
 
     ResidualRow<T> rw;
@@ -887,44 +914,92 @@ __global__ void __launch_bounds__(kVT) chain_residual_kernel(ChainArgs a, VocabP
     const float base = s_base, theta = s_theta;
     const int f0 = cstar * p.res_chunk_elems + threadIdx.x * EPT;
     const int fn = max(0, min(EPT, a.V - f0));
-    // ---- then in the thread prefix of chunk cstar, as its CTA stored it
+    // ---- then in the thread prefix of chunk cstar, as its CTA stored it:
+    // the thread where it passes u * S (or, after a fallback, the last thread
+    // holding any weight), one vote per warp
     const float2 tp = __ldcg(tprefix + (size_t)cstar * kVT + threadIdx.x);
     const float incl_m = mode == 0 ? tp.x : tp.y;
     s_prefix[threadIdx.x] = incl_m;
-    if (!s_fallback) {
-        // first thread whose inclusive prefix passes u * S
-        if (__fadd_rn(base, incl_m) > theta) atomicMin(&s_pick_min, (int)threadIdx.x);
+    const bool fb = s_fallback != 0;
+    bool hit;
+    if (!fb) {
+        hit = __fadd_rn(base, incl_m) > theta;
     } else {
-        // last thread holding any weight (rare: recompute the thread sums)
         load_res_words<T, VEC>(rw.trow, f0, fn, rt);
         if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
         raw_weight_sums<T>(rw, mode, rt, rd, sr, sp);
-        if ((mode == 0 ? sr : sp) > 0.f) atomicMax(&s_pick_max, (int)threadIdx.x);
+        hit = (mode == 0 ? sr : sp) > 0.f;
+    }
+    const unsigned vote = __ballot_sync(0xffffffffu, hit);
+    if ((threadIdx.x & 31) == 0 && vote != 0u) {
+        const int wbase = threadIdx.x & ~31;
+        if (fb) atomicMax(&s_pick_max, wbase + 31 - __clz((int)vote));
+        else atomicMin(&s_pick_min, wbase + __ffs((int)vote) - 1);
     }
     __syncthreads();
-    int pick = s_fallback ? s_pick_max : s_pick_min;
+    int pick = fb ? s_pick_max : s_pick_min;
     if (pick < 0 || pick >= kVT) pick = kVT - 1;
+    // ---- and the element: the picked thread's words go to shared memory
+    // and the first warp walks them, EPT / 32 elements (at least one) a lane
     if ((int)threadIdx.x == pick) {
-        // ---- and element by element in that thread's range
-        load_res_words<T, VEC>(rw.trow, f0, fn, rt);
-        if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
-        int y = -1;
-        if (!s_fallback) {
-            float acc = __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f);
-#pragma unroll
-            for (int j = 0; j < EPT; ++j) {
-                acc = __fadd_rn(acc, raw_weight<T>(rw, mode, rt, rd, j));
-                if (y < 0 && j < fn && acc > theta) y = f0 + j;
-            }
+        if (!fb) {
+            load_res_words<T, VEC>(rw.trow, f0, fn, rt);
+            if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
         }
-        if (y < 0) {
 #pragma unroll
-            for (int j = 0; j < EPT; ++j)
-                if (j < fn && raw_weight<T>(rw, mode, rt, rd, j) > 0.f) y = f0 + j;
+        for (int k = 0; k < kResLoadsPerThread; ++k) {
+            s_words[0][k] = rt[k];
+            s_words[1][k] = rd[k];
         }
-        if (y < 0) y = max(f0, 0);
-        a.out_tokens[(size_t)b * (a.N + 1) + d.a] = y;
-        w.counters[a.B + b] = 0;  // ready for the next call
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        constexpr int EPL = EPT >= 32 ? EPT / 32 : 1;
+        const int lane = threadIdx.x;
+        const int f0p = cstar * p.res_chunk_elems + pick * EPT;
+        const int fnp = max(0, min(EPT, a.V - f0p));
+        float wv[EPL], lsum = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const int j = lane * EPL + e;
+            wv[e] = j < fnp ? elem_weight<T>(rw, mode, smem_elem<T>(s_words[0], j),
+                                             mode == 0 ? smem_elem<T>(s_words[1], j) : 0.f)
+                            : 0.f;
+            lsum = __fadd_rn(lsum, wv[e]);
+        }
+        // the weight before this lane's elements (lanes in order), after the
+        // prefix of the threads before the picked one
+        float incl_l = lsum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, incl_l, off);
+            if (lane >= off) incl_l = __fadd_rn(incl_l, t);
+        }
+        float acc = __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f);
+        acc = __fadd_rn(acc, __fsub_rn(incl_l, lsum));
+        int hit_e = -1, last_e = -1;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            acc = __fadd_rn(acc, wv[e]);
+            if (hit_e < 0 && lane * EPL + e < fnp && acc > theta) hit_e = e;
+            if (wv[e] > 0.f) last_e = e;
+        }
+        const unsigned hv = __ballot_sync(0xffffffffu, hit_e >= 0);
+        const unsigned pv = __ballot_sync(0xffffffffu, last_e >= 0);
+        int y;
+        if (!fb && hv != 0u) {
+            const int l = __ffs((int)hv) - 1;  // the first crossing
+            y = f0p + l * EPL + __shfl_sync(0xffffffffu, hit_e, l);
+        } else if (pv != 0u) {
+            const int l = 31 - __clz((int)pv);  // no crossing: the last element with weight
+            y = f0p + l * EPL + __shfl_sync(0xffffffffu, last_e, l);
+        } else {
+            y = max(f0p, 0);
+        }
+        if (lane == 0) {
+            a.out_tokens[(size_t)b * (a.N + 1) + d.a] = y;
+            w.counters[a.B + b] = 0;  // ready for the next call
+        }
     }
 }
 
@@ -1042,7 +1117,7 @@ VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
     p.recs_per_unit = p.vec ? kSGroupWarps : 1;
     size_t off = 0;
     p.off_counters = off;
-    off = align_up(off + sizeof(int) * 2 * (size_t)B, 256);
+    off = align_up(off + sizeof(int) * (2 * (size_t)B + 4), 256);
     p.off_partials = off;  // tree: a RowPartial per (row, chunk); chain: recs_per_unit (max, sum) records
     off = align_up(off + (chain ? sizeof(float2) * p.recs_per_unit : sizeof(RowPartial)) * (size_t)B *
                              p.rows_per_seq * p.nchunks,

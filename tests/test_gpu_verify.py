@@ -210,3 +210,26 @@ def test_repeated_calls_reuse_workspace(orc):
     r2 = _run_chain(inp)
     for a, b in zip(r1, r2):
         np.testing.assert_array_equal(a, b)
+
+
+def test_chain_statistics_timeout_reported():
+    """A statistics pass whose bounded wait gave up raises a flag in the
+    workspace (after the per-sequence arrival counters); the decisions then
+    report SV_ERR_TIMEOUT for every sequence instead of deciding on records
+    that were never written.  The flag is raised here by the host, no wait is
+    made to run out; re-zeroing the workspace clears it."""
+    inp = W.chain_inputs(4, 3, 5000, "bf16", 2.0, 1.0, 4.0, seed=41)
+    B, N = inp["draft_tokens"].shape
+    ws = torch.zeros(sv.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, B, N, 5000, sv.SV_BF16, 0, 0),
+                     dtype=torch.uint8, device="cuda")
+    ws.view(torch.int32)[2 * B] = 1
+    st = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    args = [dev(inp[n]) for n in ("target", "draft", "draft_tokens", "u_accept", "u_sample")]
+    acc, out = sv.sv_verify_chain(*args, seq_status=st, ws=ws)
+    torch.cuda.synchronize()
+    assert (host(st) == sv.SV_ERR_TIMEOUT).all()
+    assert (host(acc) == -1).all() and (host(out) == -1).all()
+    ws.zero_()
+    acc, out = sv.sv_verify_chain(*args, seq_status=st, ws=ws)
+    torch.cuda.synchronize()
+    assert (host(st) == 0).all() and (host(acc) >= 0).all()
