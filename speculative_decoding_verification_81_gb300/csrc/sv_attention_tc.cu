@@ -76,6 +76,7 @@ struct TcSmem {
     uint64_t q_full[2], q_empty[2];  // Q tiles in shared memory (double buffer)
     uint64_t fin, fin_pv;
     uint64_t pair[4];            // the two softmax warps of each lane quarter
+    uint64_t k_first;            // the first K tile has been requested
     float xmax[2][4][2][32];     // [tile parity][quarter][half][lane]: half-row tile maxima
     float xl[4][2][32];          // [quarter][half][lane]: half-row sums at a segment end
     uint32_t tmem;
@@ -103,6 +104,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = tid >> 5, lane = tid & 31;
     const int HR = p.Hkv * p.RG;
 
+    griddep_wait();
+    griddep_launch_dependents();
+    // the prologue's first loads go out before the barrier set-up
+    const int pre_L = tid < p.B ? p.prefix_lens[tid] : 0;
+    const int pre_T = tid < p.B ? nodes_of(p, tid) : 0;
+
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sh->full_k[s], 1);
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(&sh->fin, 1);
         mbar_init(&sh->fin_pv, 1);
         for (int q = 0; q < 4; ++q) mbar_init(&sh->pair[q], 2);
+        mbar_init(&sh->k_first, 1);
         sh->abort_flag = 0;
         fence_mbar_init();
     }
@@ -139,9 +147,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             make_uint4(0u, 0u, 0u, 0u);
     }
     tc::fence_proxy_async_smem();
-    griddep_wait();
-    griddep_launch_dependents();
-    attn_prologue(p, tile_base, kTcThreads);
+    attn_prologue(p, tile_base, kTcThreads, pre_L, pre_T);
 
     const long long U = (long long)tile_base[p.B] * HR;
     const int nctas = (int)(U < (long long)gridDim.x ? U : (long long)gridDim.x);
@@ -178,6 +184,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (long long u = u_begin; u < u_end; ++u, ++k) {
                 const int s = (int)(k % STAGES);
                 const uint32_t ph = (uint32_t)((k / STAGES) & 1);
+                // At the start every SM asks for its ring at once: the first V
+                // tile waits until the first K tile (which the first S
+                // product needs) has been requested.
+                if (!is_k && k == 0 && !mbar_wait_bounded(&sh->k_first, 0)) {
+                    fail(cur.b);
+                    break;
+                }
                 if (is_k && (u == u_begin || cur.tile == 0)) {
                     // this segment's Q rows (rows_per_rg of them: rows_per_rg / G
                     // nodes x G heads, a 3-D box) into Q buffer qseg & 1, once
@@ -254,8 +267,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             tma_load_2d(st + kBox + i * ps * 128, map, 64, y[i], &full[s]);
                         }
                 }
+                if (is_k && k == 0) mbar_arrive(&sh->k_first);
                 cursor_next(cur, tile_base, p.B, HR);
             }
+            if (is_k && k == 0) mbar_arrive(&sh->k_first);  // none issued: release the V side
             // every copy issued must land before the CTA may exit
             const long long first = k > STAGES ? k - STAGES : 0;
             for (long long j = first; j < k; ++j)

@@ -111,10 +111,14 @@ __device__ __forceinline__ int nodes_of(const AttnKParams &p, int b) {
     return (n >= 1 && n <= p.T) ? n : 0;
 }
 
-__device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int nt) {
+// pre_L, pre_T: prefix length and node count of sequence threadIdx.x, loaded
+// by the caller ahead of its own set-up.
+__device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int nt, int pre_L,
+                                              int pre_T) {
     const int tid = threadIdx.x;
     for (int b = tid; b < p.B; b += nt) {
-        const int L = p.prefix_lens[b], Tb = nodes_of(p, b);
+        const int L = b == tid ? pre_L : p.prefix_lens[b];
+        const int Tb = b == tid ? pre_T : nodes_of(p, b);
         const bool ok = L >= 0 && Tb > 0 && (long long)L + Tb <= p.S_max;
         tile_base[b] = ok ? (L + Tb + kBK - 1) / kBK : 0;
     }

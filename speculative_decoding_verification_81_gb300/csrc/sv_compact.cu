@@ -6,23 +6,25 @@
 // rest is discarded ("Chapitre 9 -- Décodage spéculatif" §9.1).  Row
 // L + path[d] moves to row L + d for d = 0..a, in place.
 //
-// One CTA per sequence.  The path increases strictly, so path[d] >= d: a
-// destination row can only be the source of an EARLIER path position.  Rows
-// are therefore moved in batches of increasing d, each batch read completely
-// into shared memory before any of it is written back.
+// One CTA per sequence.  The path increases strictly, so path[d] >= d: the
+// destination slot L + d of position d is never the source of a LATER
+// position.  The moves, one per (position, KV head) pair in order of d, go in
+// rounds of consecutive pairs, every head at once: a round reads all its rows
+// (K and V) into registers before any of them is written back, so a source
+// is always read before a move of an earlier round could have overwritten it.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
 namespace sv {
 
 constexpr int kCT = 256;
-constexpr int kCompactBatch = 32;  // path rows per staged batch
-constexpr int kMaxRowVecs = 32;    // 16-byte words per row: D <= 256 bf16
+constexpr int kCompactRegs = 8;        // 16-byte words a thread holds in a round
+constexpr int kMaxRoundPairs = 256;    // (position, head) pairs per round
+constexpr int kMaxRowVecs = 32;        // 16-byte words per row: D <= 256 bf16
 
 __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
-    __shared__ uint4 stage[2][kCompactBatch * kMaxRowVecs];
-    __shared__ int s_src[kCompactBatch];
-    __shared__ size_t s_src_off[kCompactBatch], s_dst_off[kCompactBatch];
+    __shared__ size_t s_src_off[kMaxRoundPairs], s_dst_off[kMaxRoundPairs];
+    __shared__ unsigned char s_move[kMaxRoundPairs];
     griddep_wait();
     griddep_launch_dependents();
     const int b = blockIdx.x;
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
         }
         return;
     }
-    if (a.path_nodes) {
+    if (a.path_nodes && acc > 0) {
         const int32_t *path = a.path_nodes + (size_t)b * a.path_stride;
         uint4 *kc = static_cast<uint4 *>(a.k);
         uint4 *vc = static_cast<uint4 *>(a.v);
@@ -73,33 +75,41 @@ __global__ void __launch_bounds__(kCT) compact_kv_kernel(CompactArgs a) {
             const int pg = a.block_table[(size_t)b * a.max_pages + slot / a.page_size];
             return (((size_t)pg * a.Hkv + h) * a.page_size + slot % a.page_size) * vpr;
         };
-        for (int h = 0; h < a.Hkv; ++h) {
-            for (int d0 = 1; d0 <= acc; d0 += kCompactBatch) {  // d = 0 is the root: never moves
-                const int nb = min(kCompactBatch, acc + 1 - d0);
-                if (threadIdx.x < nb) {
-                    const int src = path[d0 + threadIdx.x];
-                    s_src[threadIdx.x] = src;
-                    s_src_off[threadIdx.x] = row_off(h, L + src);
-                    s_dst_off[threadIdx.x] = row_off(h, L + d0 + threadIdx.x);
-                }
-                __syncthreads();
-                for (int i = threadIdx.x; i < nb * vpr; i += kCT) {
-                    const int r = i / vpr, w = i - r * vpr;
-                    if (s_src[r] != d0 + r) {
-                        stage[0][i] = kc[s_src_off[r] + w];
-                        stage[1][i] = vc[s_src_off[r] + w];
-                    }
-                }
-                __syncthreads();
-                for (int i = threadIdx.x; i < nb * vpr; i += kCT) {
-                    const int r = i / vpr, w = i - r * vpr;
-                    if (s_src[r] != d0 + r) {
-                        kc[s_dst_off[r] + w] = stage[0][i];
-                        vc[s_dst_off[r] + w] = stage[1][i];
-                    }
-                }
-                __syncthreads();
+        const int per_pair = 2 * vpr;  // K and V words of one row
+        const int npairs = acc * a.Hkv;  // positions 1..acc (the root never moves) x heads
+        const int round = min(kMaxRoundPairs, kCT * kCompactRegs / per_pair);
+        for (int q0 = 0; q0 < npairs; q0 += round) {
+            const int np = min(round, npairs - q0);
+            for (int i = threadIdx.x; i < np; i += kCT) {
+                const int q = q0 + i, d = 1 + q / a.Hkv, h = q - (d - 1) * a.Hkv;
+                const int src = path[d];
+                s_move[i] = src != d;
+                s_src_off[i] = row_off(h, L + src);
+                s_dst_off[i] = row_off(h, L + d);
             }
+            __syncthreads();
+            const int items = np * per_pair;
+            uint4 reg[kCompactRegs];
+#pragma unroll
+            for (int k = 0; k < kCompactRegs; ++k) {
+                const int it = threadIdx.x + k * kCT;
+                if (it < items) {
+                    const int pr = it / per_pair, rem = it - pr * per_pair;
+                    const int kv = rem >= vpr, w = rem - kv * vpr;
+                    if (s_move[pr]) reg[k] = (kv ? vc : kc)[s_src_off[pr] + w];
+                }
+            }
+            __syncthreads();  // every source of the round is read
+#pragma unroll
+            for (int k = 0; k < kCompactRegs; ++k) {
+                const int it = threadIdx.x + k * kCT;
+                if (it < items) {
+                    const int pr = it / per_pair, rem = it - pr * per_pair;
+                    const int kv = rem >= vpr, w = rem - kv * vpr;
+                    if (s_move[pr]) (kv ? vc : kc)[s_dst_off[pr] + w] = reg[k];
+                }
+            }
+            __syncthreads();  // before the next round's offsets replace these
         }
     }
     if (threadIdx.x == 0) {
