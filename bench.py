@@ -213,6 +213,96 @@ def run_reference(args, cfg, inp, rank, budget_s=60.0):
 
 # ------------------------------------------------------------------ GPU path
 
+def tree_step_bench(cfg, dev, capture, stream, reps):
+    """Steps/s and HBM fraction of one tree verification step (attention over
+    the tree, greedy acceptance, compaction) on synthetic inputs of `cfg`."""
+    import torch
+    import speculative_decoding_verification_81_gb300 as sv
+    from speculative_decoding_verification_81_gb300 import workloads as W
+    B, T, L, Hq, Hkv, D, V = (cfg[k] for k in ("B", "T", "L", "Hq", "Hkv", "D", "V"))
+    S_max = L + 64
+    rng = np.random.default_rng(77)
+    if cfg["tree"] == "medusa":
+        par_np = np.broadcast_to(W.medusa_tree(T), (B, T)).copy()
+    else:
+        par_np = np.stack([W.random_tree(T, cfg["max_depth"], rng) for _ in range(B)])
+    g = torch.Generator(device=dev).manual_seed(5)
+    one = (B * Hkv * S_max * D * 2 * 2 + 2 * B * T * Hq * D * 2 + B * T * V * 2)
+    copies = max(1, -(-160 * 2**20 // one))  # enough copies to exceed L2
+    sets = []
+    for _ in range(copies):
+        x = dict(q=torch.randn(B, T, Hq, D, device=dev, generator=g).to(torch.bfloat16),
+                 k=torch.randn(B, Hkv, S_max, D, device=dev, generator=g).to(torch.bfloat16),
+                 v=torch.randn(B, Hkv, S_max, D, device=dev, generator=g).to(torch.bfloat16),
+                 logits=(torch.randn(B, T, V, device=dev, generator=g) * 3).to(torch.bfloat16))
+        x["out"] = torch.empty_like(x["q"])
+        sets.append(x)
+    pl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    par = torch.from_numpy(par_np).to(dev)
+    for x in sets:  # node tokens: the target's argmax at the parent with probability p_match
+        am = x["logits"].float().argmax(-1).to(torch.int32)
+        x["tok"] = torch.where(torch.rand(B, T, device=dev, generator=g) < cfg["p_match"],
+                               am.gather(1, par.clamp(min=0).long()),
+                               torch.randint(0, V, (B, T), device=dev, generator=g,
+                                             dtype=torch.int32))
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty(B, T, dtype=torch.int32, device=dev)
+    otok = torch.empty(B, T, dtype=torch.int32, device=dev)
+    newl = torch.empty(B, dtype=torch.int32, device=dev)
+    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, dev)
+    ws_t = sv.workspace(sv.SV_OP_VERIFY_TREE_GREEDY, B, T, V, sv.SV_BF16, 0, 0, dev)
+
+    def attention(x):
+        sv.sv_tree_attention(x["q"], x["k"], x["v"], pl, par, out=x["out"], ws=ws_a)
+
+    def greedy(x):
+        sv.sv_verify_tree_greedy(x["logits"], x["tok"], par, accepted_len=acc, path_nodes=path,
+                                 out_tokens=otok, ws=ws_t)
+
+    def compact(x):
+        sv.sv_compact_kv(x["k"], x["v"], pl, acc, path, new_kv_lens=newl)
+
+    def cycle(fns):
+        def f():
+            for x in sets:
+                for fn in fns:
+                    fn(x)
+        return f
+
+    def per_step(fns):
+        gr = capture(cycle(fns))
+        for _ in range(3):
+            gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        n = max(20, reps // copies)
+        e0.record(stream)
+        for _ in range(n):
+            gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (n * copies)
+
+    peak, _ = load_peaks()
+    step_ms = per_step([attention, greedy, compact])
+    attn_ms = per_step([attention])
+    greedy_ms = per_step([greedy])
+    kv = B * Hkv * (L + T) * D * 2 * 2
+    qo = 2 * B * T * Hq * D * 2
+    attn_bytes = kv + qo
+    step_bytes = attn_bytes + B * T * V * 2
+    res = {"workload": cfg["name"], "steps_per_s": 1e3 / step_ms,
+           "verified_positions_per_s": B * T * 1e3 / step_ms, "step_ms": step_ms,
+           "attention_ms": attn_ms, "greedy_ms": greedy_ms,
+           "step_hbm_frac": step_bytes / (step_ms / 1e3) / 1e9 / peak,
+           "attention_hbm_frac": attn_bytes / (attn_ms / 1e3) / 1e9 / peak,
+           "algorithmic_bytes": {"step": step_bytes, "attention": attn_bytes},
+           "l2": f"{copies} input copies cycled" if copies > 1 else "inputs larger than L2",
+           "accepted_mean": float(acc.float().mean().item())}
+    del sets
+    return res
+
+
 def run_ours(args, cfg, inp, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_81_gb300 as sv
@@ -377,6 +467,16 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     paged_attention = {"attention_ms": paged, "contiguous_ms": attn_ms,
                        "how": "sv_tree_attention_paged alone, one call per CUDA graph"}
 
+    # ---- the tree verification steps (Medusa tree, B=4 L=2048 T=26 V=32000;
+    # EAGLE-style random tree, B=16 L=8192 T=64 V=128256): attention, greedy
+    # acceptance and compaction, device-resident, one step per graph replay.
+    # The Medusa step's inputs (41 MB) fit in L2, so its graph cycles through
+    # four copies (164 MB) and each step reads inputs last touched four steps
+    # before.
+    from speculative_decoding_verification_81_gb300 import workloads as W
+    tree_steps = {wl: tree_step_bench(W.WORKLOADS[wl], dev, capture, stream, reps)
+                  for wl in (3, 5)}
+
     decode_baseline = {
         "attention_ms": {"T=1 (decode)": decode[1], "T=5 (N=4)": decode[5], f"T={N + 1} (N={N})": attn_ms},
         "verify_over_decode": {"N=4": decode[5] / decode[1], f"N={N}": attn_ms / decode[1]},
@@ -446,6 +546,7 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
                     "how": "each call captured alone in a CUDA graph, replayed back to back"},
         "decode_baseline": decode_baseline,
         "paged_attention": paged_attention,
+        "tree_steps": tree_steps,
         "clocks": clk,
         "gpu_launches": launches_per_step * K,
         "timing": "CUDA-graph replays of the whole step, CUDA events on the launching stream",

@@ -149,11 +149,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::fence_proxy_async_smem();
     attn_prologue(p, tile_base, kTcThreads, pre_L, pre_T);
 
-    const long long U = (long long)tile_base[p.B] * HR;
-    const int nctas = (int)(U < (long long)gridDim.x ? U : (long long)gridDim.x);
-    if ((int)blockIdx.x >= nctas) return;
-    const long long u_begin = cta_begin(U, nctas, blockIdx.x);
-    const long long u_end = cta_begin(U, nctas, blockIdx.x + 1);
+    // With several row groups per KV head, the CTAs go in lanes, one per row
+    // group: CTA c works in lane c % RG, and the lanes split the (sequence,
+    // KV head, tile) units identically, so the RG CTAs of a slot stream the
+    // same K/V tiles side by side and all but the first read them from L2.
+    const int nlane = p.RG;
+    const PairLane pl{nlane > 1 ? p.Hkv : HR, nlane, (int)blockIdx.x % nlane};
+    const long long U = (long long)tile_base[p.B] * pl.npr;  // units of one lane
+    // At least kMinTilesPerCta tiles a slot: below that a CTA's fixed costs
+    // (pipeline fill, epilogue) and many-way merges outweigh the parallelism.
+    const int slots_max = (int)gridDim.x / nlane;
+    const long long want = U / kMinTilesPerCta > 0 ? U / kMinTilesPerCta : 1;
+    const int nctas = (int)(want < (long long)slots_max ? want : (long long)slots_max);  // slots in use
+    const int myslot = (int)blockIdx.x / nlane;
+    if (myslot >= nctas) return;
+    const long long u_begin = cta_begin(U, nctas, myslot);
+    const long long u_end = cta_begin(U, nctas, myslot + 1);
     volatile int *abort_flag = &sh->abort_flag;
 
     if (warp == 1) tc::tmem_alloc(&sh->tmem, kTcCols);
@@ -178,7 +189,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint64_t *empty = is_k ? sh->empty_k : sh->empty_v;
             const CUtensorMap *map = is_k ? &tmk : &tmv;
             const int half_off = is_k ? 0 : 2 * kBox;
-            Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
+            // K/V tiles are streamed: evict-first keeps the stream from
+            // pushing code, Q and partials out of L2.  (Among evict-first
+            // lines the oldest go first, so a tile still outlives the few
+            // microseconds between the reads of the lanes of one slot.)
+            const uint64_t pol = l2_policy_evict_first();
+            auto load = [&](void *dst, int x, int y, uint64_t *bar) {
+                tma_load_2d_hint(dst, map, x, y, bar, pol);
+            };
+            Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
             long long k = 0;
             uint32_t qseg = 0;  // segments whose Q was issued
             for (long long u = u_begin; u < u_end; ++u, ++k) {
@@ -221,8 +240,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int y = (cur.b * p.Hkv + kvh) * p.S_max + kb;
                     uint8_t *st = smem + s * kStageBytes + half_off;
                     mbar_arrive_expect_tx(&full[s], 2 * kBox);
-                    tma_load_2d(st, map, 0, y, &full[s]);
-                    tma_load_2d(st + kBox, map, 64, y, &full[s]);
+                    load(st, 0, y, &full[s]);
+                    load(st + kBox, 64, y, &full[s]);
                 } else if (p.page_size >= kBK) {
                     // paged, pages of 128 slots or more: the tile sits in one page
                     // (its id read before the wait, so the load overlaps it); an
@@ -238,8 +257,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (*abort_flag) break;
                     uint8_t *st = smem + s * kStageBytes + half_off;
                     mbar_arrive_expect_tx(&full[s], 2 * kBox);
-                    tma_load_2d(st, map, 0, y, &full[s]);
-                    tma_load_2d(st + kBox, map, 64, y, &full[s]);
+                    load(st, 0, y, &full[s]);
+                    load(st + kBox, 64, y, &full[s]);
                 } else {
                     // paged, smaller pages: one block of page_size rows per page
                     // (pages past the sequence's end may hold any id: an id out
@@ -263,12 +282,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kMaxSubBlocks; ++i)
                         if (i < nsub) {
-                            tma_load_2d(st + i * ps * 128, map, 0, y[i], &full[s]);
-                            tma_load_2d(st + kBox + i * ps * 128, map, 64, y[i], &full[s]);
+                            load(st + i * ps * 128, 0, y[i], &full[s]);
+                            load(st + kBox + i * ps * 128, 64, y[i], &full[s]);
                         }
                 }
                 if (is_k && k == 0) mbar_arrive(&sh->k_first);
-                cursor_next(cur, tile_base, p.B, HR);
+                cursor_next(cur, tile_base, p.B, pl);
             }
             if (is_k && k == 0) mbar_arrive(&sh->k_first);  // none issued: release the V side
             // every copy issued must land before the CTA may exit
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // holds back the other (tcgen05.commit tracks its own thread's MMAs).
         if (lane == 0) {
             bool ok = true;
-            Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
+            Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
             const long long nt = u_end - u_begin;
             if (warp == 1) {
                 constexpr uint32_t idS = tc::idesc_bf16(MROWS, kBK, false);
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (cur.tile == cur.n - 1 || j == nt - 1)
                         tc::commit(&sh->q_empty[(seg - 1) & 1]);  // Q buffer free once these S are done
                     tc::commit(&sh->empty_k[s]);  // the K half may be refilled once S(j) is done
-                    cursor_next(cur, tile_base, p.B, HR);
+                    cursor_next(cur, tile_base, p.B, pl);
                 }
             } else {
                 constexpr uint32_t idPV = tc::idesc_bf16(MROWS, kD, true);
@@ -351,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc::commit(&sh->pv_done[j & 1]);
                     tc::commit(&sh->empty_v[s]);  // the V half may be refilled once PV(j) is done
-                    cursor_next(cur, tile_base, p.B, HR);
+                    cursor_next(cur, tile_base, p.B, pl);
                 }
             }
             if (!ok) fail(cur.b < p.B ? cur.b : 0);
@@ -396,8 +415,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int L = 0, kv_end = 0, seg_first_tile = 0, kvh = 0, rg = 0, rglob = 0;
     bool seg_is_first = true, warp_active = false, row_valid = false;
     int next_L = 0, next_T = 0;  // the next segment's prefix length and nodes, read ahead
+    int2 next_par = make_int2(-1, -1);  // and its parents (two nodes a lane)
     bool have_next_L = false;
-    Cursor cur = cursor_at(tile_base, p.B, HR, u_begin);
+    Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
     long long jt = 0;
     for (long long u = u_begin; u < u_end; ++u, ++jt) {
         const bool new_seg = (u == u_begin) || cur.tile == 0;
@@ -406,6 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             rg = cur.pr - kvh * p.RG;
             L = have_next_L ? next_L : p.prefix_lens[cur.b];
             const int Tb = have_next_L ? next_T : nodes_of(p, cur.b);
+            const int2 par = have_next_L ? next_par : load_parents_warp(p.parents, p.T, cur.b, lane);
             have_next_L = false;
             kv_end = L + Tb;
             seg_first_tile = cur.tile;
@@ -418,16 +439,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           rg * p.rows_per_rg + quarter * kRowsPerQuarter < p.M;
             m = kNegInf;
             l = 0.f;
-            if (row_valid) anc = ancestors(p.parents, p.T, cur.b, rglob / p.G);
+            anc = ancestors_warp(p.parents == nullptr, par.x, par.y, rglob / p.G, row_valid);
         }
         // A few tiles before this segment ends: read the next segment's prefix
         // length (its Q is brought in by the producer).
         if (cur.tile == max(seg_first_tile, cur.n - 5) && u + (cur.n - cur.tile) < u_end) {
             Cursor nx = cur;
             nx.tile = nx.n - 1;
-            cursor_next(nx, tile_base, p.B, HR);
+            cursor_next(nx, tile_base, p.B, pl);
             next_L = p.prefix_lens[nx.b];
             next_T = nodes_of(p, nx.b);
+            next_par = load_parents_warp(p.parents, p.T, nx.b, lane);
             have_next_L = true;
         }
         const bool first_tile = new_seg;  // O is overwritten by this tile's PV
@@ -582,8 +604,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int nc = 1, c0 = 0, slot0 = 0;
             bool merger = whole;
             if (!whole && warp_active) {
-                const long long ub = (long long)tile_base[cur.b] * HR + (long long)cur.pr * cur.n;
-                c0 = cta_of(U, nctas, ub);
+                const long long ub = (long long)tile_base[cur.b] * pl.npr + (long long)cur.pi * cur.n;
+                c0 = cta_of(U, nctas, ub);  // slots; contributor i is CTA (c0 + i) * nlane + lane
                 nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;
                 slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;
                 const int pos = __shfl_sync(0xffffffffu, arrived, 0);
@@ -612,12 +634,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (warp_active) {
                 // the other contributors' (max, sum) of this row half
                 auto part_row = [&](int i) -> size_t {
-                    return ((size_t)(c0 + i) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
+                    return ((size_t)((c0 + i) * nlane + pl.poff) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
                 };
                 // The merge takes the contributors in index order with the same
                 // arithmetic whoever merges, so the result does not depend on
                 // which CTA finished last.
-                const int self = (int)blockIdx.x - c0;
+                const int self = myslot - c0;
                 auto ml_of = [&](int i) -> float2 {
                     return i == self ? make_float2(m, lrow)
                                      : __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
@@ -747,7 +769,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc::fence_before();
         }
-        cursor_next(cur, tile_base, p.B, HR);
+        cursor_next(cur, tile_base, p.B, pl);
     }
     if (ready_ctr) flag_ready(ready_ctr);
     tc::fence_before();

@@ -15,6 +15,7 @@ constexpr int kMaxB = 4096;
 constexpr int kMinPage = 8;                      // smallest page (a swizzle atom of rows)
 constexpr int kMaxSubBlocks = kBK / kMinPage;    // pages per key tile at most
 constexpr int kMaxT = 64;
+constexpr int kMinTilesPerCta = 8;  // key tiles a CTA takes at least (small problems)
 constexpr int kSoftmaxWarps = 8;                      // warps 2-9: two per TMEM lane quarter
 constexpr int kPvWarp = 2 + kSoftmaxWarps;              // issues the PV products
 constexpr int kVLoadWarp = 3 + kSoftmaxWarps;           // loads the V tiles
@@ -40,8 +41,11 @@ struct AttnKParams {
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.
+// Position in a CTA's run of units (sequence, pair, tile): the pairs a run
+// visits are pr = pi * pstride + poff for pi = 0..npr-1 (all pairs, or one row
+// group of every KV head).
 struct Cursor {
-    int b, pr, tile, n;
+    int b, pr, tile, n, pi;
 };
 
 __device__ __forceinline__ long long cta_begin(long long U, int grid, int c) {
@@ -53,27 +57,37 @@ __device__ __forceinline__ int cta_of(long long U, int grid, long long u) {
     return (int)(((u + 1) * grid + U - 1) / U) - 1;
 }
 
-__device__ __forceinline__ Cursor cursor_at(const int *tile_base, int B, int HR, long long u) {
-    int lo = 0, hi = B - 1;  // last b with tile_base[b] * HR <= u
+// Pairs a CTA's run visits: npr per sequence, pair pi is pr = pi * pstride + poff.
+struct PairLane {
+    int npr, pstride, poff;
+};
+
+__device__ __forceinline__ Cursor cursor_at(const int *tile_base, int B, PairLane pl, long long u) {
+    int lo = 0, hi = B - 1;  // last b with tile_base[b] * npr <= u
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((long long)tile_base[mid] * HR <= u) lo = mid;
+        if ((long long)tile_base[mid] * pl.npr <= u) lo = mid;
         else hi = mid - 1;
     }
     Cursor c;
     c.b = lo;
     c.n = tile_base[lo + 1] - tile_base[lo];
-    const long long rem = u - (long long)tile_base[lo] * HR;
-    c.pr = c.n > 0 ? (int)(rem / c.n) : 0;
-    c.tile = c.n > 0 ? (int)(rem - (long long)c.pr * c.n) : 0;
+    const long long rem = u - (long long)tile_base[lo] * pl.npr;
+    c.pi = c.n > 0 ? (int)(rem / c.n) : 0;
+    c.pr = c.pi * pl.pstride + pl.poff;
+    c.tile = c.n > 0 ? (int)(rem - (long long)c.pi * c.n) : 0;
     return c;
 }
 
-__device__ __forceinline__ void cursor_next(Cursor &c, const int *tile_base, int B, int HR) {
+__device__ __forceinline__ void cursor_next(Cursor &c, const int *tile_base, int B, PairLane pl) {
     if (++c.tile < c.n) return;
     c.tile = 0;
-    if (++c.pr < HR) return;
-    c.pr = 0;
+    if (++c.pi < pl.npr) {
+        c.pr = c.pi * pl.pstride + pl.poff;
+        return;
+    }
+    c.pi = 0;
+    c.pr = pl.poff;
     do {
         ++c.b;
     } while (c.b < B && tile_base[c.b + 1] == tile_base[c.b]);
@@ -165,20 +179,33 @@ __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_ba
     __syncthreads();
 }
 
-// Ancestor set of node t (bit j = node j on the root->t path), walking the
-// parent array; NULL parents = a chain.  At most 64 steps; a parent that does
-// not precede its child ends the walk (the call reports such a tree as bad).
-__device__ __forceinline__ uint64_t ancestors(const int32_t *parents, int T, int b, int t) {
-    if (parents == nullptr) return t >= 63 ? ~0ull : ((1ull << (t + 1)) - 1ull);
+// Ancestor set of node t (bit j = node j on the root->t path) from sequence
+// b's parent array held across a warp (lane l has the parents of nodes l and
+// 32 + l, -1 past T): the path is walked with shuffles, not dependent loads.
+// At most 64 steps; a parent that does not precede its child ends the walk
+// (the call reports such a tree as bad).  Every lane of the warp calls it; a
+// lane with valid == false gets 0.  chain (parents NULL): the causal set.
+__device__ __forceinline__ uint64_t ancestors_warp(bool chain, int par_lo, int par_hi, int t,
+                                                   bool valid) {
+    if (chain) return !valid ? 0ull : t >= 63 ? ~0ull : ((1ull << (t + 1)) - 1ull);
     uint64_t anc = 0;
-    int nd = t;
-    for (int step = 0; step < kMaxT && nd >= 0; ++step) {
-        anc |= 1ull << nd;
-        const int pn = parents[(size_t)b * T + nd];
-        if (pn >= nd) break;
-        nd = pn;
+    int nd = valid ? t : -1;
+    for (int step = 0; step < kMaxT; ++step) {
+        if (__all_sync(0xffffffffu, nd < 0)) break;
+        if (nd >= 0) anc |= 1ull << nd;
+        const int lo = __shfl_sync(0xffffffffu, par_lo, nd & 31);
+        const int hi = __shfl_sync(0xffffffffu, par_hi, nd & 31);
+        const int pn = nd >= 32 ? hi : lo;
+        if (nd >= 0) nd = pn < nd ? pn : -1;  // up to the root; a parent not before its node ends it
     }
     return anc;
+}
+
+// Parents of nodes lane and 32 + lane of sequence b (-1 past T or for a chain).
+__device__ __forceinline__ int2 load_parents_warp(const int32_t *parents, int T, int b, int lane) {
+    if (!parents) return make_int2(-1, -1);
+    const int32_t *row = parents + (size_t)b * T;
+    return make_int2(lane < T ? row[lane] : -1, 32 + lane < T ? row[32 + lane] : -1);
 }
 
 }  // namespace sv

@@ -402,8 +402,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     griddep_launch_dependents();
 
     if (warp == kSWarps) {
-        // ================= producer: one bulk copy per unit
+        // ================= producer: one bulk copy per unit (evict-first: the
+        // stream does not push the records and code of what follows out of L2)
         if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
             long long k = 0;
             int cb = -1, nb = 0;  // the sequence of the last unit and its draft length
             for (long long u = u_begin; u < u_end; ++u, ++k) {
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 const int begin = c * kUnitElems;
                 const uint32_t bytes = (uint32_t)(min(kUnitElems, a.V - begin) * (int)sizeof(T));
                 mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_load(ring + s * kSUnitBytes, row + begin, bytes, &full[s]);
+                bulk_load_hint(ring + s * kSUnitBytes, row + begin, bytes, &full[s], pol);
             }
             // every copy issued must land before the CTA may exit
             const long long first = k > kSStages ? k - kSStages : 0;
