@@ -1007,14 +1007,69 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
 
 // ---------------------------------------------------------------- tree greedy
 
+// Shared state of the greedy walk over one sequence's tree.
+struct TreeWalkSmem {
+    int am[kMaxTreeT], par[kMaxTreeT], tok[kMaxTreeT], depth[kMaxTreeT], path[kMaxTreeT];
+    unsigned char ok[kMaxTreeT];
+    int best, bad;
+};
+
+// Greedy longest agreeing path of sequence b from the target's argmax per
+// node (ts.am, -1 for none), by a whole CTA of kVT threads: validation, the
+// walk in node order, then the outputs.  `late`: the statistics pass gave
+// up, so no decision is taken.
+__device__ __forceinline__ void tree_walk(const TreeArgs &a, int b, bool late, TreeWalkSmem &ts) {
+    for (int i = threadIdx.x; i < a.T; i += kVT) {
+        ts.par[i] = a.parents ? a.parents[(size_t)b * a.T + i] : i - 1;  // NULL: a chain
+        ts.tok[i] = a.tokens[(size_t)b * a.T + i];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // this sequence's nodes; those past T_b are padding
+        const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+        int bad = late || ts.par[0] != -1 || tb_raw < 1 || tb_raw > a.T;
+        const int Tb = bad ? 1 : tb_raw;
+        for (int i = 1; i < Tb && !bad; ++i)
+            if (ts.par[i] < 0 || ts.par[i] >= i || ts.tok[i] < 0 || ts.tok[i] >= a.V) bad = 1;
+        int bst = 0;
+        if (!bad) {
+            ts.ok[0] = 1;
+            ts.depth[0] = 0;
+            for (int i = 1; i < Tb; ++i) {
+                const int pa = ts.par[i];
+                ts.ok[i] = ts.ok[pa] && ts.tok[i] == ts.am[pa];
+                ts.depth[i] = ts.depth[pa] + 1;
+                if (ts.ok[i] && ts.depth[i] > ts.depth[bst]) bst = i;
+            }
+            int node = bst;
+            for (int dd = ts.depth[bst]; dd >= 0; --dd) {
+                ts.path[dd] = node;
+                node = ts.par[node];
+            }
+        }
+        ts.bad = bad;
+        ts.best = bst;
+        a.accepted_len[b] = bad ? -1 : ts.depth[bst];
+        if (a.seq_status) a.seq_status[b] = late ? SV_ERR_TIMEOUT : bad ? SV_ERR_BAD_INPUT : SV_OK;
+    }
+    __syncthreads();
+    const int depth = ts.bad ? -1 : ts.depth[ts.best];
+    for (int i = threadIdx.x; i < a.T; i += kVT) {
+        int pn = -1, ot = -1;
+        if (i <= depth) {
+            pn = ts.path[i];
+            ot = i < depth ? ts.tok[ts.path[i + 1]] : ts.am[ts.best];
+        }
+        a.path_nodes[(size_t)b * a.T + i] = pn;
+        a.out_tokens[(size_t)b * a.T + i] = ot;
+    }
+}
+
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p, WsView w) {
     __shared__ float4 scratch[kVWarps];
     __shared__ int s_last;
-    __shared__ int sm_am[kMaxTreeT], sm_par[kMaxTreeT], sm_tok[kMaxTreeT], sm_depth[kMaxTreeT],
-        sm_path[kMaxTreeT];
-    __shared__ unsigned char sm_ok[kMaxTreeT];
-    __shared__ int s_best, s_bad;
+    __shared__ TreeWalkSmem ts;
 
     const int per_seq = a.T * p.nchunks;
     const int item = blockIdx.x;
@@ -1055,53 +1110,164 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
     for (int rr = warp; rr < a.T; rr += kVWarps) {
         const RowPartial rp = warp_merge_row<true>(
             w.partials + (size_t)b * per_seq + (size_t)rr * p.nchunks, p.nchunks);
-        if (lane == 0) sm_am[rr] = rp.idx == INT_MAX ? -1 : rp.idx;
+        if (lane == 0) ts.am[rr] = rp.idx == INT_MAX ? -1 : rp.idx;
     }
-    for (int i = threadIdx.x; i < a.T; i += kVT) {
-        sm_par[i] = a.parents ? a.parents[(size_t)b * a.T + i] : i - 1;  // NULL: a chain
-        sm_tok[i] = a.tokens[(size_t)b * a.T + i];
-    }
-    __syncthreads();
+    tree_walk(a, b, false, ts);
+    if (threadIdx.x == 0) w.counters[b] = 0;  // ready for the next call
+}
+
+// ---------------------------------------------------------------- tree greedy, streaming form
+
+// Rows 16-byte aligned: the argmax pass as a persistent grid streaming the
+// units (sequence, node row, 32 KB chunk) of a balanced contiguous range
+// through the same ring of bulk copies as the chain statistics (evict-first).
+// Each consumer warp reduces an eighth of a unit to (largest value, smallest
+// index holding it) -- the packed maximum first, then the first element
+// equal to it -- and leaves one record.  The walk is the next kernel's.
+// Rows of padding nodes (past T_b) are not read.
+template <typename T>
+__global__ void __launch_bounds__(kSThreads, 1)
+    tree_stats_stream_kernel(TreeArgs a, VocabPlan p, WsView w) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kSStages * kSUnitBytes
+    __shared__ uint64_t full[kSStages], empty[kSStages];
+    constexpr int PV = Elem<T>::kPerVec;
+    constexpr int kUnitElems = kSUnitBytes / (int)sizeof(T);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_seq = a.T * p.nchunks;
+    const long long U = (long long)a.B * per_seq;
+    const long long u_begin = U * blockIdx.x / gridDim.x, u_end = U * (blockIdx.x + 1) / gridDim.x;
+    float2 *rec = reinterpret_cast<float2 *>(w.partials);  // [B][T][nchunks][kSGroupWarps]
+    int *timed_out = w.counters + 2 * a.B;
+    // node r of sequence b is read unless it is padding (node 0 always is read)
+    auto row_in_use = [&](int b, int r) {
+        return r == 0 || a.node_counts == nullptr || r < a.node_counts[b];
+    };
+
     if (threadIdx.x == 0) {
-        // this sequence's nodes; those past T_b are padding
-        const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
-        int bad = sm_par[0] != -1 || tb_raw < 1 || tb_raw > a.T;
-        const int Tb = bad ? 1 : tb_raw;
-        for (int i = 1; i < Tb && !bad; ++i)
-            if (sm_par[i] < 0 || sm_par[i] >= i || sm_tok[i] < 0 || sm_tok[i] >= a.V) bad = 1;
-        int bst = 0;
-        if (!bad) {
-            sm_ok[0] = 1;
-            sm_depth[0] = 0;
-            for (int i = 1; i < Tb; ++i) {
-                const int pa = sm_par[i];
-                sm_ok[i] = sm_ok[pa] && sm_tok[i] == sm_am[pa];
-                sm_depth[i] = sm_depth[pa] + 1;
-                if (sm_ok[i] && sm_depth[i] > sm_depth[bst]) bst = i;
-            }
-            int node = bst;
-            for (int dd = sm_depth[bst]; dd >= 0; --dd) {
-                sm_path[dd] = node;
-                node = sm_par[node];
-            }
+        for (int s = 0; s < kSStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kSGroupWarps);
         }
-        s_bad = bad;
-        s_best = bst;
-        a.accepted_len[b] = bad ? -1 : sm_depth[bst];
-        if (a.seq_status) a.seq_status[b] = bad ? SV_ERR_BAD_INPUT : SV_OK;
-        w.counters[b] = 0;  // ready for the next call
+        fence_mbar_init();
     }
     __syncthreads();
-    const int depth = s_bad ? -1 : sm_depth[s_best];
-    for (int i = threadIdx.x; i < a.T; i += kVT) {
-        int pn = -1, ot = -1;
-        if (i <= depth) {
-            pn = sm_path[i];
-            ot = i < depth ? sm_tok[sm_path[i + 1]] : sm_am[s_best];
+    griddep_wait();
+    griddep_launch_dependents();
+
+    if (warp == kSWarps) {
+        // ================= producer: one bulk copy per unit
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            long long k = 0;
+            for (long long u = u_begin; u < u_end; ++u, ++k) {
+                const int s = (int)(k % kSStages);
+                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((k / kSStages) & 1) ^ 1))) {
+                    atomicExch(timed_out, 1);  // a stage never came free
+                    break;
+                }
+                const int b = (int)(u / per_seq);
+                const int rem = (int)(u - (long long)b * per_seq);
+                const int r = rem / p.nchunks, c = rem - r * p.nchunks;
+                if (!row_in_use(b, r)) {  // padding: the stage's phase, no copy
+                    mbar_arrive(&full[s]);
+                    continue;
+                }
+                const T *row = static_cast<const T *>(a.target) + ((size_t)b * a.T + r) * a.V;
+                const int begin = c * kUnitElems;
+                const uint32_t bytes = (uint32_t)(min(kUnitElems, a.V - begin) * (int)sizeof(T));
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_load_hint(ring + s * kSUnitBytes, row + begin, bytes, &full[s], pol);
+            }
+            // every copy issued must land before the CTA may exit
+            const long long first = k > kSStages ? k - kSStages : 0;
+            for (long long j = first; j < k; ++j)
+                mbar_wait_bounded(&full[j % kSStages], (uint32_t)((j / kSStages) & 1));
         }
-        a.path_nodes[(size_t)b * a.T + i] = pn;
-        a.out_tokens[(size_t)b * a.T + i] = ot;
+        return;
     }
+
+    // ================= consumers: two groups of eight warps, alternate units
+    const int grp = (warp >> 2) & 1, gw = ((warp >> 3) << 2) | (warp & 3);
+    for (long long k = grp; k < u_end - u_begin; k += 2) {
+        const long long u = u_begin + k;
+        const int s = (int)(k % kSStages);
+        const int b = (int)(u / per_seq);
+        const int rem = (int)(u - (long long)b * per_seq);
+        const int r = rem / p.nchunks, c = rem - r * p.nchunks;
+        const int n = min(kUnitElems, a.V - c * kUnitElems);  // elements in this unit (a multiple of PV)
+        if (!warp_wait_bounded(&full[s], (uint32_t)((k / kSStages) & 1))) {
+            if (lane == 0) atomicExch(timed_out, 1);  // records left unwritten
+            break;
+        }
+        float2 *dst = rec + (((size_t)b * a.T + r) * p.nchunks + c) * kSGroupWarps + gw;
+        if (!row_in_use(b, r)) {  // padding: nothing landed, an empty record
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[s]);
+                *dst = make_float2(kNegInf, __int_as_float(INT_MAX));
+            }
+            continue;
+        }
+        uint4 buf[kSWordsPerLane];
+#pragma unroll
+        for (int q = 0; q < kSWordsPerLane; ++q) {
+            const int wi = (gw * kSWordsPerLane + q) * 32 + lane;  // 16-byte word of the unit
+            buf[q] = wi * PV < n ? *reinterpret_cast<const uint4 *>(ring + s * kSUnitBytes + wi * 16)
+                                 : neg_inf_vec<T>();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the words are in registers
+        // the warp's maximum (NaN never wins), then the smallest index holding it
+        float vmax = words_max<T, kSWordsPerLane>(buf);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+        int idx = INT_MAX;
+        if (vmax != kNegInf && vmax == vmax) {  // some element is larger than -inf
+#pragma unroll
+            for (int q = kSWordsPerLane - 1; q >= 0; --q) {
+                float x[PV];
+                Elem<T>::unpack(buf[q], x);
+                const int e0 = c * kUnitElems + ((gw * kSWordsPerLane + q) * 32 + lane) * PV;
+#pragma unroll
+                for (int j = PV - 1; j >= 0; --j)
+                    if (x[j] == vmax) idx = e0 + j;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, off));
+        if (lane == 0) *dst = make_float2(vmax, __int_as_float(idx));
+    }
+}
+
+// The greedy walk after the streaming argmax pass: one CTA per sequence
+// merges each node row's records into the row's argmax, then walks.
+template <typename T>
+__global__ void __launch_bounds__(kVT) tree_decide_kernel(TreeArgs a, VocabPlan p, WsView w) {
+    __shared__ TreeWalkSmem ts;
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_row = p.nchunks * kSGroupWarps;
+    const float2 *rec = reinterpret_cast<const float2 *>(w.partials) + (size_t)b * a.T * per_row;
+    for (int rr = warp; rr < a.T; rr += kVWarps) {
+        float best = kNegInf;
+        int idx = INT_MAX;
+        for (int i = lane; i < per_row; i += 32) {
+            const float2 r2 = __ldcg(rec + (size_t)rr * per_row + i);
+            merge_argmax(best, idx, r2.x, __float_as_int(r2.y));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float b2 = __shfl_xor_sync(0xffffffffu, best, off);
+            const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+            merge_argmax(best, idx, b2, i2);
+        }
+        if (lane == 0) ts.am[rr] = idx == INT_MAX ? -1 : idx;
+    }
+    const bool late = __ldcg(w.counters + 2 * a.B) != 0;
+    tree_walk(a, b, late, ts);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1121,9 +1287,9 @@ VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
     p.off_counters = off;
     off = align_up(off + sizeof(int) * (2 * (size_t)B + 4), 256);
     p.off_partials = off;  // tree: a RowPartial per (row, chunk); chain: recs_per_unit (max, sum) records
-    off = align_up(off + (chain ? sizeof(float2) * p.recs_per_unit : sizeof(RowPartial)) * (size_t)B *
-                             p.rows_per_seq * p.nchunks,
-                   256);
+    const size_t per_unit = chain ? sizeof(float2) * p.recs_per_unit
+                                  : (p.vec ? sizeof(float2) * kSGroupWarps : sizeof(RowPartial));
+    off = align_up(off + per_unit * (size_t)B * p.rows_per_seq * p.nchunks, 256);
     p.off_chunktot = off;
     off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks : 0), 256);
     p.off_tprefix = off;
@@ -1168,8 +1334,30 @@ template <typename T, bool VEC>
 static cudaError_t launch_tree_t(TreeArgs a, VocabPlan p, WsView w, cudaStream_t st) {
     void *args[] = {&a, &p, &w};
     const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
-    return launch_pdl((const void *)tree_stats_kernel<T, VEC>, dim3(items), dim3(kVT), 0, st,
-                      args);
+    if constexpr (VEC) {
+        // streaming argmax pass (one CTA per SM, fewer for fewer units), then the walk
+        const void *fn = (const void *)tree_stats_stream_kernel<T>;
+        const int smem = kSStages * kSUnitBytes;
+        static int attr_set[64] = {0};
+        int dev = 0;
+        cudaError_t e;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if (dev < 64 && !attr_set[dev]) {
+            if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+                cudaSuccess)
+                return e;
+            attr_set[dev] = 1;
+        }
+        const int sms = device_sm_count();
+        if (sms <= 0) return cudaErrorUnknown;
+        const unsigned grid = (unsigned)(items < (unsigned)sms ? items : (unsigned)sms);
+        if ((e = launch_pdl(fn, dim3(grid), dim3(kSThreads), smem, st, args)) != cudaSuccess) return e;
+        return launch_pdl((const void *)tree_decide_kernel<T>, dim3((unsigned)a.B), dim3(kVT), 0, st,
+                          args);
+    } else {
+        return launch_pdl((const void *)tree_stats_kernel<T, VEC>, dim3(items), dim3(kVT), 0, st,
+                          args);
+    }
 }
 
 sv_status launch_verify_chain(const ChainArgs &a, int dtype, const VocabPlan &p, void *ws,
