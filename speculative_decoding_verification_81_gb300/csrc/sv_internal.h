@@ -63,7 +63,6 @@ struct VocabPlan {
     size_t off_counters;  // 2*B + 4 ints: arrivals per sequence, then [2*B] a timeout flag
     size_t off_partials;  // B * rows_per_seq * nchunks RowPartial
     size_t off_chunktot;  // B * res_chunks float2
-    size_t off_tprefix;   // B * res_chunks * 256 float4: per-thread prefixes of the residual draw
     size_t bytes;
 };
 

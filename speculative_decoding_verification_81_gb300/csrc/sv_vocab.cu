@@ -826,6 +826,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     griddep_launch_dependents();
     const int b = blockIdx.x / p.res_chunks;
     const int c = blockIdx.x - b * p.res_chunks;
+    const float u_s = threadIdx.x == 0 ? __ldg(a.u_sample + b) : 0.f;  // for the last CTA's search
     // every CTA of the sequence takes the decisions; the first one writes them
     const ChainDecision d =
         decide_sequence<T>(a, p, reinterpret_cast<const float2 *>(w.partials),
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     rw.inv_d = d.a < d.n_draft ? __frcp_rn(d.s_d) : 0.f;
     const int mode0 = d.a < d.n_draft ? 0 : 1;  // residual at a rejection, else the bonus
 
-    // ---- every CTA: weight sums of its chunk, per-thread prefixes kept
+    // ---- every CTA: weight sums of its chunk (the residual's and p's)
     const int e0 = c * p.res_chunk_elems + threadIdx.x * EPT;
     const int n = max(0, min(EPT, a.V - e0));
     uint4 rt[kResLoadsPerThread], rd[kResLoadsPerThread];
@@ -851,13 +852,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     float sr, sp;
     raw_weight_sums<T>(rw, mode0, rt, rd, sr, sp);
     float2 tot;
-    const float2 incl = cta_incl_scan2(make_float2(sr, sp), tot, wsum);
-    float2 *tprefix = reinterpret_cast<float2 *>(reinterpret_cast<char *>(w.chunktot) +
-                                                 (p.off_tprefix - p.off_chunktot)) +
-                      (size_t)b * p.res_chunks * kVT;
-    tprefix[(size_t)c * kVT + threadIdx.x] = incl;
-    __threadfence();
-    __syncthreads();
+    float2 incl = cta_incl_scan2(make_float2(sr, sp), tot, wsum);
     if (threadIdx.x == 0) {
         w.chunktot[(size_t)b * p.res_chunks + c] = tot;
         __threadfence();
@@ -881,7 +876,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
             S = 0.f;
             for (int i = 0; i < p.res_chunks; ++i) S = __fadd_rn(S, s_tot[i].y);
         }
-        const float theta = __fmul_rn(a.u_sample[b], S);
+        const float theta = __fmul_rn(u_s, S);
         float base = 0.f;
         int cstar = -1;
         for (int i = 0; i < p.res_chunks; ++i) {
@@ -916,22 +911,21 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     const float base = s_base, theta = s_theta;
     const int f0 = cstar * p.res_chunk_elems + threadIdx.x * EPT;
     const int fn = max(0, min(EPT, a.V - f0));
-    // ---- then in the thread prefix of chunk cstar, as its CTA stored it:
-    // the thread where it passes u * S (or, after a fallback, the last thread
-    // holding any weight), one vote per warp
-    const float2 tp = __ldcg(tprefix + (size_t)cstar * kVT + threadIdx.x);
-    const float incl_m = mode == 0 ? tp.x : tp.y;
+    // ---- then chunk cstar again: its words (from L2) and the same thread
+    // sums and scan as its CTA computed, so its thread prefixes need no
+    // round trip through memory (the last CTA's own chunk is at hand) ...
+    if (cstar != c) {
+        load_res_words<T, VEC>(rw.trow, f0, fn, rt);
+        if (mode0 == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
+        raw_weight_sums<T>(rw, mode0, rt, rd, sr, sp);
+        incl = cta_incl_scan2(make_float2(sr, sp), tot, wsum);
+    }
+    // ... the thread where the prefix passes u * S (or, after a fallback, the
+    // last thread holding any weight), one vote per warp
+    const float incl_m = mode == 0 ? incl.x : incl.y;
     s_prefix[threadIdx.x] = incl_m;
     const bool fb = s_fallback != 0;
-    bool hit;
-    if (!fb) {
-        hit = __fadd_rn(base, incl_m) > theta;
-    } else {
-        load_res_words<T, VEC>(rw.trow, f0, fn, rt);
-        if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
-        raw_weight_sums<T>(rw, mode, rt, rd, sr, sp);
-        hit = (mode == 0 ? sr : sp) > 0.f;
-    }
+    const bool hit = fb ? (mode == 0 ? sr : sp) > 0.f : __fadd_rn(base, incl_m) > theta;
     const unsigned vote = __ballot_sync(0xffffffffu, hit);
     if ((threadIdx.x & 31) == 0 && vote != 0u) {
         const int wbase = threadIdx.x & ~31;
@@ -944,10 +938,6 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     // ---- and the element: the picked thread's words go to shared memory
     // and the first warp walks them, EPT / 32 elements (at least one) a lane
     if ((int)threadIdx.x == pick) {
-        if (!fb) {
-            load_res_words<T, VEC>(rw.trow, f0, fn, rt);
-            if (mode == 0) load_res_words<T, VEC>(rw.drow, f0, fn, rd);
-        }
 #pragma unroll
         for (int k = 0; k < kResLoadsPerThread; ++k) {
             s_words[0][k] = rt[k];
@@ -1292,8 +1282,6 @@ VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
     off = align_up(off + per_unit * (size_t)B * p.rows_per_seq * p.nchunks, 256);
     p.off_chunktot = off;
     off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks : 0), 256);
-    p.off_tprefix = off;
-    off = align_up(off + (chain ? sizeof(float2) * (size_t)B * p.res_chunks * kVT : 0), 256);
     p.bytes = off;
     return p;
 }

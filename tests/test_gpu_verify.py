@@ -233,3 +233,23 @@ def test_chain_statistics_timeout_reported():
     acc, out = sv.sv_verify_chain(*args, seq_status=st, ws=ws)
     torch.cuda.synchronize()
     assert (host(st) == 0).all() and (host(acc) >= 0).all()
+
+
+def test_tree_statistics_timeout_reported():
+    """The same flag for greedy tree verification (aligned rows: the streaming
+    argmax pass): every sequence reports SV_ERR_TIMEOUT with -1 outputs."""
+    B, T, V = 3, 9, 4096
+    inp = W.tree_logit_inputs(B, T, V, W.chain_parents(T), 0.9, seed=42)
+    ws = torch.zeros(sv.sv_workspace_size(sv.SV_OP_VERIFY_TREE_GREEDY, B, T, V, sv.SV_BF16, 0, 0),
+                     dtype=torch.uint8, device="cuda")
+    ws.view(torch.int32)[2 * B] = 1
+    st = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    args = [dev(inp[n]) for n in ("target", "node_tokens", "parents")]
+    acc, path, out = sv.sv_verify_tree_greedy(*args, seq_status=st, ws=ws)
+    torch.cuda.synchronize()
+    assert (host(st) == sv.SV_ERR_TIMEOUT).all()
+    assert (host(acc) == -1).all() and (host(path) == -1).all() and (host(out) == -1).all()
+    ws.zero_()
+    acc, path, out = sv.sv_verify_tree_greedy(*args, seq_status=st, ws=ws)
+    torch.cuda.synchronize()
+    assert (host(st) == 0).all() and (host(acc) >= 0).all()
