@@ -340,8 +340,9 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
                            accepted_len=acc, out_tokens=toks, ws=ws_c)
         sv.sv_compact_kv(dd["k"], dd["v"], dd["prefix_lens"], acc, None, new_kv_lens=newl)
 
-    # attention, split merge, chain statistics, residual draw, compaction
-    launches_per_step = 5
+    # attention (split pairs merged in-kernel), chain statistics, decisions and
+    # residual draw, compaction: four kernels a step
+    launches_per_step = 4
 
     def barrier():
         if world > 1:
