@@ -181,6 +181,23 @@ def oracle_sample(cfg, inp, nseq):
     return time.perf_counter() - t0
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (the slowest rank's time): an all-reduce
+    on `device` (the GPU under NCCL, the CPU under gloo); x itself with one rank."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, steps_per_rank, ms):
+    """Steps of the whole job per second: every rank ran steps_per_rank steps
+    of its own batch (replicas), and the job took the slowest rank's ms."""
+    return world * steps_per_rank / (ms / 1e3)
+
+
 def run_reference(args, cfg, inp, rank, budget_s=60.0):
     """The oracle as it stands, one core.  A step of the reference is one
     sequence of the workload (its attention rows, its chain acceptance, its
@@ -349,12 +366,8 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(x):
-        if world > 1:
-            t = torch.tensor([x], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            return float(t.item())
-        return x
+    def slowest(x):
+        return max_over_ranks(x, world, dev)
 
     # ---- device-resident timed region
     for _ in range(args.warmup):
@@ -405,7 +418,7 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
             g_step.replay()
         t1.record(stream)
         barrier()
-    total_ms = max_over_ranks(t0.elapsed_time(t1))
+    total_ms = slowest(t0.elapsed_time(t1))
     clk = clocks.summary()
 
     def time_graph(fn, reps):
@@ -515,8 +528,8 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-        e2e = {"value": world * KE / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e_ms = slowest(e0.elapsed_time(e1))
+        e2e = {"value": whole_job_rate(world, KE, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": KE}
         del pinned, dd
 
@@ -525,7 +538,7 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     attn_s = attn_ms / 1e3
     achieved = ab["attention"] / attn_s / 1e9
     step_s = total_ms / 1e3 / K
-    value = world * K / (total_ms / 1e3)
+    value = whole_job_rate(world, K, total_ms)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
