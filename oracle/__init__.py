@@ -62,9 +62,10 @@ def lib() -> ctypes.CDLL:
         _lib.orc_row_stats.restype = None
         _lib.orc_verify_chain.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         _lib.orc_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P]
+        _lib.orc_verify_tree_stochastic.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, P, P, P]
         _lib.orc_compact_kv.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
         for name in ("orc_ancestor_mask", "orc_tree_attention", "orc_verify_chain",
-                     "orc_verify_tree_greedy", "orc_compact_kv"):
+                     "orc_verify_tree_greedy", "orc_verify_tree_stochastic", "orc_compact_kv"):
             getattr(_lib, name).restype = ctypes.c_int
     return _lib
 
@@ -174,6 +175,32 @@ def verify_tree_greedy(target, node_tokens, parents):
     if rc != OK:
         raise ValueError(f"orc_verify_tree_greedy status {rc}")
     return dict(accepted_len=acc, path_nodes=path, out_tokens=out, status=status)
+
+
+def verify_tree_stochastic(target, draft, node_tokens, parents, u_accept, u_sample):
+    """Multi-draft stochastic acceptance on a tree.  Returns dict of
+    accepted_len [B], path_nodes [B,T], out_tokens [B,T], flags [B], status [B]."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    dt = _logits_dtype(target)
+    assert _logits_dtype(draft) == dt
+    B, T, V = target.shape
+    assert draft.shape == (B, T, V)
+    tok = _c(node_tokens, np.int32).reshape(B, T)
+    par = _c(parents, np.int32).reshape(B, T)
+    ua = _c(u_accept, np.float32).reshape(B, T)
+    us = _c(u_sample, np.float32).reshape(B)
+    acc = np.zeros(B, np.int32)
+    path = np.zeros((B, T), np.int32)
+    out = np.zeros((B, T), np.int32)
+    flags = np.zeros(B, np.int32)
+    status = np.zeros(B, np.int32)
+    rc = lib().orc_verify_tree_stochastic(_ptr(target), _ptr(draft), dt, _ptr(tok), _ptr(par),
+                                          _ptr(ua), _ptr(us), B, T, V, _ptr(acc), _ptr(path),
+                                          _ptr(out), _ptr(flags), _ptr(status))
+    if rc != OK:
+        raise ValueError(f"orc_verify_tree_stochastic status {rc}")
+    return dict(accepted_len=acc, path_nodes=path, out_tokens=out, flags=flags, status=status)
 
 
 def compact_kv(k, v, prefix_lens, path_nodes, accepted_len):

@@ -18,6 +18,9 @@
  *     token drawn from the (N+1)-th distribution (Chapitre 9 §9.1),
  *   - greedy longest-agreeing-path acceptance on a draft tree (glossary,
  *     "L'attention en arbre"; Chapitre 9 §9.1, the longest agreeing prefix),
+ *   - stochastic acceptance on a draft tree (Chapitre 9 §9.2 has the target
+ *     choose among several drafted paths but gives no rule; the rule here is
+ *     the multi-draft speculative sampling of SpecInfer, Miao et al. 2024),
  *   - compaction of the accepted path's K/V rows ("Parallel Decoding",
  *     "Limites du parallel decoding": the enlarged KV cache for branches).
  *
@@ -467,6 +470,172 @@ int orc_verify_tree_greedy(const void *target, int dtype, const int32_t *node_to
     free(ok);
     free(depth);
     free(amax);
+    return ORC_OK;
+}
+
+/* ---- stochastic tree acceptance ------------------------------------------ */
+
+/*
+ * Multi-draft speculative sampling on a tree (the SpecInfer rule; the pages,
+ * Chapitre 9 §9.2, only say that the target picks among several drafted
+ * paths).  Node u's children were drawn independently from the draft's
+ * distribution at u, q_u = softmax(draft row u); the target's is
+ * p_u = softmax(target row u).  From the root:
+ *
+ *   c = 0 (the current residual is r_c = max(0, p_u - c q_u) / N(c) with
+ *   N(c) = sum_v max(0, p_u(v) - c q_u(v)); c = 0 gives p_u itself);
+ *   for the children v of u in index order, with token x = node_tokens[v]:
+ *     accept v  <=>  u_accept[v] * q_u(x) * N(c) < max(0, p_u(x) - c q_u(x));
+ *     accepted: the walk moves to v (c = 0 there);
+ *     rejected: c = c + N(c).
+ *   No child accepted (or u a leaf): the final token is drawn from the weights
+ *   max(0, p_u - c q_u) (from p_u when they sum to zero) by the inverse CDF of
+ *   inverse_cdf with u_sample.
+ *
+ * The update of c is the rejection step of speculative sampling applied to
+ * the current residual: max(0, r_c - q_u) vanishes where p_u <= c q_u and is
+ * (p_u - (c + N(c)) q_u) / N(c) elsewhere, so after normalising it is
+ * r_{c + N(c)}.  It is written here in that closed form; the direct
+ * recursion on vectors gives the same numbers up to rounding.
+ *
+ * Readings: a chain-shaped tree gives the chain rule of orc_verify_chain
+ * exactly (one child per node, c = 0 at each test, c = 1 after a rejection);
+ * u_accept has one uniform per node (entry 0 unused); a decision with
+ * |u q N - r| < 1e-5 max(r, u q N) is a flagged near-tie (the sum N of a
+ * full vocabulary differs between precisions by more than the chain's 1e-6);
+ * parents, tokens and rows are checked as in the greedy walk and the chain.
+ *
+ * Layouts: target, draft [B, T, V] (draft row u: the distribution u's
+ * children came from; leaves' rows unused); node_tokens, parents, u_accept
+ * [B, T]; u_sample [B]; accepted_len [B]; path_nodes, out_tokens [B, T]
+ * (-1 padded); flags, status [B] (nullable).
+ */
+int orc_verify_tree_stochastic(const void *target, const void *draft, int dtype,
+                               const int32_t *node_tokens, const int32_t *parents,
+                               const float *u_accept, const float *u_sample, int B, int T, int V,
+                               int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
+                               int32_t *flags, int32_t *status)
+{
+    if (B <= 0 || T <= 0 || V <= 0 || (dtype != 0 && dtype != 1))
+        return ORC_ERR_INVALID_ARG;
+    const size_t esz = dtype == 0 ? 4 : 2;
+    int32_t *depth = (int32_t *)malloc(sizeof(int32_t) * (size_t)T);
+    uint8_t *mask = (uint8_t *)malloc((size_t)T * T);
+    double *pu = (double *)malloc(sizeof(double) * (size_t)V);
+    double *qu = (double *)malloc(sizeof(double) * (size_t)V);
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parents + (size_t)b * T;
+        const int32_t *tok = node_tokens + (size_t)b * T;
+        int32_t flag = 0;
+        for (int i = 0; i < T; ++i) {
+            path_nodes[(size_t)b * T + i] = -1;
+            out_tokens[(size_t)b * T + i] = -1;
+        }
+        int st = orc_ancestor_mask(par, T, mask, depth);
+        for (int i = 1; i < T && st == ORC_OK; ++i)
+            if (tok[i] < 0 || tok[i] >= V)
+                st = ORC_ERR_BAD_INPUT;
+        /* every target row, and the draft row of every node with children,
+           must define a distribution */
+        for (int i = 0; i < T && st == ORC_OK; ++i) {
+            int has_child = 0;
+            for (int j = i + 1; j < T; ++j)
+                if (par[j] == i)
+                    has_child = 1;
+            for (int which = 0; which < 1 + has_child && st == ORC_OK; ++which) {
+                const char *row = (const char *)(which ? draft : target) + ((size_t)b * T + i) * V * esz;
+                double m, s;
+                orc_row_stats(row, dtype, V, &m, &s, NULL);
+                if (!isfinite(m) || !isfinite(s) || !(s > 0.0))
+                    st = ORC_ERR_BAD_INPUT;
+            }
+        }
+        if (st != ORC_OK) {
+            accepted_len[b] = -1;
+            if (flags)
+                flags[b] = 0;
+            if (status)
+                status[b] = ORC_ERR_BAD_INPUT;
+            continue;
+        }
+        int u = 0, dd = 0;
+        path_nodes[(size_t)b * T] = 0;
+        double c = 0.0;
+        for (;;) {
+            const char *trow = (const char *)target + ((size_t)b * T + u) * V * esz;
+            const char *drow = (const char *)draft + ((size_t)b * T + u) * V * esz;
+            double mt, sT, md, sd;
+            orc_row_stats(trow, dtype, V, &mt, &sT, NULL);
+            orc_row_stats(drow, dtype, V, &md, &sd, NULL);
+            for (int v = 0; v < V; ++v) {
+                pu[v] = row_prob(trow, dtype, v, mt, sT);
+                qu[v] = row_prob(drow, dtype, v, md, sd);
+            }
+            c = 0.0;
+            int next = -1;
+            for (int v = u + 1; v < T && next < 0; ++v) {
+                if (par[v] != u)
+                    continue;
+                double n = 0.0; /* N(c) */
+                if (c == 0.0) {
+                    n = 1.0;
+                } else {
+                    for (int k = 0; k < V; ++k) {
+                        const double d = pu[k] - c * qu[k];
+                        n += d > 0.0 ? d : 0.0;
+                    }
+                }
+                const int x = tok[v];
+                const double r = pu[x] - c * qu[x] > 0.0 ? pu[x] - c * qu[x] : 0.0;
+                const double lhs = (double)u_accept[(size_t)b * T + v] * qu[x] * n;
+                const double big = r > lhs ? r : lhs;
+                if (fabs(lhs - r) < 1e-5 * big)
+                    flag |= ORC_FLAG_ACCEPT_NEAR_TIE;
+                if (lhs < r)
+                    next = v;
+                else
+                    c += n;
+            }
+            if (next >= 0) {
+                u = next;
+                ++dd;
+                path_nodes[(size_t)b * T + dd] = u;
+                out_tokens[(size_t)b * T + dd - 1] = tok[u];
+                continue;
+            }
+            /* no child accepted, or a leaf: the final draw */
+            double S = 0.0;
+            for (int k = 0; k < V; ++k) {
+                const double d = pu[k] - c * qu[k];
+                w[k] = c == 0.0 ? pu[k] : (d > 0.0 ? d : 0.0);
+                S += w[k];
+            }
+            if (!(S > 0.0)) {
+                flag |= ORC_FLAG_DEGENERATE_RESIDUAL;
+                S = 0.0;
+                for (int k = 0; k < V; ++k) {
+                    w[k] = pu[k];
+                    S += w[k];
+                }
+            }
+            int near = 0;
+            out_tokens[(size_t)b * T + dd] = inverse_cdf(w, V, S, (double)u_sample[b], &near);
+            if (near)
+                flag |= ORC_FLAG_SAMPLE_NEAR_TIE;
+            break;
+        }
+        accepted_len[b] = dd;
+        if (flags)
+            flags[b] = flag;
+        if (status)
+            status[b] = ORC_OK;
+    }
+    free(w);
+    free(qu);
+    free(pu);
+    free(mask);
+    free(depth);
     return ORC_OK;
 }
 

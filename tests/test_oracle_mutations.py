@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 import test_oracle_attention as TA
+import test_oracle_stree as TS
 import test_oracle_tree as TT
 import test_oracle_verify as TV
 
@@ -45,6 +46,16 @@ MUTANTS = [
      [TT.test_exhaustive_tiny_trees]),
     ("argmax tie takes the last index", "if (x > m) {", "if (x >= m) {",
      [TV.test_row_stats_argmax_ties_take_smallest_index]),
+    ("siblings tested against p (no residual update)", "                    c += n;",
+     "                    c += 0.0;", [lambda o: TS.test_first_token_follows_target_at_root(3, 1.0)]),
+    ("residual normaliser dropped from the sibling test",
+     "const double lhs = (double)u_accept[(size_t)b * T + v] * qu[x] * n;",
+     "const double lhs = (double)u_accept[(size_t)b * T + v] * qu[x];",
+     [lambda o: TS.test_first_token_follows_target_at_root(3, 3.0)]),
+    ("tree's final draw from p after rejections",
+     "w[k] = c == 0.0 ? pu[k] : (d > 0.0 ? d : 0.0);", "w[k] = pu[k];",
+     [lambda o: TS.test_chain_tree_equals_chain_rule(64, 4, 300, "f32", 1),
+      lambda o: TS.test_first_token_follows_target_at_root(1, 1.0)]),
     ("compaction copies from the wrong slot",
      "k_in + base + (size_t)(L + src) * D", "k_in + base + (size_t)(L + d) * D",
      [TT.test_compaction_invariants]),
@@ -63,7 +74,7 @@ def test_mutant_is_caught(tmp_path, name, old, new, checks):
     real = oracle.lib()
     mutant = ctypes.CDLL(str(so))
     for fn in ("orc_ancestor_mask", "orc_tree_attention", "orc_row_stats", "orc_verify_chain",
-               "orc_verify_tree_greedy", "orc_compact_kv"):
+               "orc_verify_tree_greedy", "orc_verify_tree_stochastic", "orc_compact_kv"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     caught = 0
