@@ -244,7 +244,7 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     else:
         par_np = np.stack([W.random_tree(T, cfg["max_depth"], rng) for _ in range(B)])
     g = torch.Generator(device=dev).manual_seed(5)
-    one = (B * Hkv * S_max * D * 2 * 2 + 2 * B * T * Hq * D * 2 + B * T * V * 2)
+    one = (B * Hkv * S_max * D * 2 * 2 + 2 * B * T * Hq * D * 2 + 2 * B * T * V * 2)
     copies = max(1, -(-160 * 2**20 // one))  # enough copies to exceed L2
     sets = []
     for _ in range(copies):
@@ -253,9 +253,18 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
                  v=torch.randn(B, Hkv, S_max, D, device=dev, generator=g).to(torch.bfloat16),
                  logits=(torch.randn(B, T, V, device=dev, generator=g) * 3).to(torch.bfloat16))
         x["out"] = torch.empty_like(x["q"])
+        # the drafter's logits at each node (for stochastic acceptance)
+        x["draft"] = (x["logits"].float()
+                      + torch.randn(B, T, V, device=dev, generator=g)).to(torch.bfloat16)
         sets.append(x)
     pl = torch.full((B,), L, dtype=torch.int32, device=dev)
     par = torch.from_numpy(par_np).to(dev)
+    for x in sets:
+        # stochastic acceptance: each child drawn from the drafter's distribution at its parent
+        probs = torch.softmax(x["draft"].float(), -1)
+        rows = probs[torch.arange(B, device=dev)[:, None], par.clamp(min=0).long()]
+        x["stok"] = torch.multinomial(rows.view(B * T, V), 1, generator=g).view(B, T).to(torch.int32)
+        del probs, rows
     for x in sets:  # node tokens: the target's argmax at the parent with probability p_match
         am = x["logits"].float().argmax(-1).to(torch.int32)
         x["tok"] = torch.where(torch.rand(B, T, device=dev, generator=g) < cfg["p_match"],
@@ -266,8 +275,11 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     path = torch.empty(B, T, dtype=torch.int32, device=dev)
     otok = torch.empty(B, T, dtype=torch.int32, device=dev)
     newl = torch.empty(B, dtype=torch.int32, device=dev)
+    ua = torch.rand(B, T, device=dev, generator=g)
+    us = torch.rand(B, device=dev, generator=g)
     ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, dev)
     ws_t = sv.workspace(sv.SV_OP_VERIFY_TREE_GREEDY, B, T, V, sv.SV_BF16, 0, 0, dev)
+    ws_s = sv.workspace(sv.SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, sv.SV_BF16, 0, 0, dev)
 
     def attention(x):
         sv.sv_tree_attention(x["q"], x["k"], x["v"], pl, par, out=x["out"], ws=ws_a)
@@ -278,6 +290,10 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
 
     def compact(x):
         sv.sv_compact_kv(x["k"], x["v"], pl, acc, path, new_kv_lens=newl)
+
+    def stochastic(x):
+        sv.sv_verify_tree_stochastic(x["logits"], x["draft"], x["stok"], par, ua, us,
+                                     accepted_len=acc, path_nodes=path, out_tokens=otok, ws=ws_s)
 
     def cycle(fns):
         def f():
@@ -304,6 +320,9 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     step_ms = per_step([attention, greedy, compact])
     attn_ms = per_step([attention])
     greedy_ms = per_step([greedy])
+    greedy_acc = float(acc.float().mean().item())
+    stochastic_ms = per_step([stochastic])
+    stoch_acc = float(acc.float().mean().item())
     kv = B * Hkv * (L + T) * D * 2 * 2
     qo = 2 * B * T * Hq * D * 2
     attn_bytes = kv + qo
@@ -311,11 +330,12 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     res = {"workload": cfg["name"], "steps_per_s": 1e3 / step_ms,
            "verified_positions_per_s": B * T * 1e3 / step_ms, "step_ms": step_ms,
            "attention_ms": attn_ms, "greedy_ms": greedy_ms,
+           "stochastic_ms": stochastic_ms, "stochastic_accepted_mean": stoch_acc,
            "step_hbm_frac": step_bytes / (step_ms / 1e3) / 1e9 / peak,
            "attention_hbm_frac": attn_bytes / (attn_ms / 1e3) / 1e9 / peak,
            "algorithmic_bytes": {"step": step_bytes, "attention": attn_bytes},
            "l2": f"{copies} input copies cycled" if copies > 1 else "inputs larger than L2",
-           "accepted_mean": float(acc.float().mean().item())}
+           "accepted_mean": greedy_acc}
     del sets
     return res
 

@@ -70,7 +70,8 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 typedef enum sv_op {
     SV_OP_TREE_ATTENTION = 0,
     SV_OP_VERIFY_CHAIN = 1,
-    SV_OP_VERIFY_TREE_GREEDY = 2
+    SV_OP_VERIFY_TREE_GREEDY = 2,
+    SV_OP_VERIFY_TREE_STOCHASTIC = 3
 } sv_op;
 
 /*
@@ -79,6 +80,7 @@ typedef enum sv_op {
  *   SV_OP_TREE_ATTENTION:     B, T, Hq, Hkv, D       (V ignored)
  *   SV_OP_VERIFY_CHAIN:       B, N (as T_or_N), V, dtype as Hq (0 f32 / 1 bf16)
  *   SV_OP_VERIFY_TREE_GREEDY: B, T, V, dtype as Hq
+ *   SV_OP_VERIFY_TREE_STOCHASTIC: B, T, V, dtype as Hq
  * Returns 0 for invalid arguments.
  */
 size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, int D);
@@ -212,6 +214,47 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
                                 int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
                                 int32_t *seq_status, void *workspace, size_t workspace_bytes,
                                 sv_stream_t stream);
+
+/*
+ * Stochastic acceptance on a draft tree: multi-draft speculative sampling.
+ * Source: "Chapitre 9 -- Décodage spéculatif" §9.2 has the target choose
+ * among several drafted paths (EAGLE-2's tree) but gives no rule; the rule
+ * here is the one of SpecInfer (Miao et al., ASPLOS 2024).  Node u's children
+ * were drawn independently from the draft's distribution at u,
+ * q_u = softmax(draft[b,u,:]); the target's is p_u = softmax(target[b,u,:]).
+ *
+ * From the root, at node u with c = 0:
+ *   N(c) = sum_v max(0, p_u(v) - c q_u(v))          (1 for c = 0)
+ *   for the children v of u in index order, x = node_tokens[b,v]:
+ *     accept v  <=>  u_accept[b,v] * q_u(x) * N(c) < max(0, p_u(x) - c q_u(x))
+ *     accepted: the walk moves to v (c = 0 there); rejected: c = c + N(c)
+ *   no child accepted, or u a leaf: y drawn from the weights max(0, p_u - c q_u)
+ *   (p_u if they sum to 0) by y = min{k : w_0 + ... + w_k > u_sample[b] * sum(w)}
+ * (the rejection step of speculative sampling applied to the current residual
+ * r_c = max(0, p_u - c q_u) / N(c), in closed form).  A chain-shaped tree is
+ * the chain rule of sv_verify_chain.
+ *   accepted_len[b] = depth of the last accepted node; path_nodes[b,:] = root..it,
+ *   then -1; out_tokens[b,:] = tokens of path nodes 1..depth, y, then -1
+ *
+ *   target_logits, draft_logits [B, T, V] of `dtype`, temperature-scaled
+ *                  (draft row u: the distribution u's children came from;
+ *                  rows of leaves are not read)
+ *   node_tokens, parents int32 [B, T] (parents NULL: a chain); u_accept f32
+ *   [B, T] (entry v tests node v; entry 0 unused); u_sample f32 [B]
+ *   accepted_len int32 [B]; path_nodes, out_tokens int32 [B, T]
+ *   workspace  >= sv_workspace_size(SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, dtype, 0, 0)
+ * Supported: 1 <= T <= 1024, 1 <= V <= 2^22.  A tree that is not
+ * topologically ordered, a token outside [0, V) or a used row without a
+ * finite distribution is reported as SV_ERR_BAD_INPUT for its sequence.
+ * Each rejected sibling costs one pass over its node's row pair.
+ */
+sv_status sv_verify_tree_stochastic(const void *target_logits, const void *draft_logits,
+                                    sv_dtype dtype, const int32_t *node_tokens,
+                                    const int32_t *parents, const float *u_accept,
+                                    const float *u_sample, int B, int T, int V,
+                                    int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
+                                    int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                                    sv_stream_t stream);
 
 /*
  * Compaction of the accepted path's rows in the enlarged KV cache.

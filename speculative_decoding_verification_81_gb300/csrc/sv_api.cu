@@ -45,6 +45,10 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
             if (V <= 0 || (Hq != SV_F32 && Hq != SV_BF16)) return 0;
             return sv::plan_vocab(op == SV_OP_VERIFY_CHAIN, B, T_or_N, V, Hq).bytes;
         }
+        case SV_OP_VERIFY_TREE_STOCHASTIC: {
+            if (V <= 0 || (Hq != SV_F32 && Hq != SV_BF16)) return 0;
+            return sv::plan_vocab_stree(B, T_or_N, V, Hq).bytes;
+        }
     }
     return 0;
 }
@@ -142,6 +146,28 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
     sv::TreeArgs a{target_logits, node_tokens, parents,    node_counts, B, T, V, accepted_len,
                    path_nodes,    out_tokens,  seq_status};
     return sv::launch_verify_tree_greedy(a, dtype, pl, workspace, as_stream(stream));
+}
+
+sv_status sv_verify_tree_stochastic(const void *target_logits, const void *draft_logits,
+                                    sv_dtype dtype, const int32_t *node_tokens,
+                                    const int32_t *parents, const float *u_accept,
+                                    const float *u_sample, int B, int T, int V,
+                                    int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
+                                    int32_t *seq_status, void *workspace, size_t workspace_bytes,
+                                    sv_stream_t stream) {
+    if (!target_logits || !draft_logits || !node_tokens || !u_accept || !u_sample ||
+        !accepted_len || !path_nodes || !out_tokens)
+        return SV_ERR_INVALID_ARG;
+    if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || V <= 0) return SV_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return SV_ERR_INVALID_ARG;
+    if (T > 1024 || V > (1 << 22)) return SV_ERR_UNSUPPORTED;
+    const sv::VocabPlan pl = sv::plan_vocab_stree(B, T, V, dtype);
+    if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return SV_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
+    sv::STreeArgs a{target_logits, draft_logits, node_tokens, parents, u_accept, u_sample, B, T, V,
+                    accepted_len, path_nodes, out_tokens, seq_status};
+    return sv::launch_verify_tree_stochastic(a, dtype, pl, workspace, as_stream(stream));
 }
 
 sv_status sv_compact_kv(void *k_cache, void *v_cache, const int32_t *prefix_lens,

@@ -94,6 +94,26 @@ struct TreeArgs {
     int32_t *seq_status;
 };
 
+// Stochastic (multi-draft) acceptance on a tree.
+struct STreeArgs {
+    const void *target;  // [B, T, V]
+    const void *draft;   // [B, T, V]: row u is the distribution u's children were drawn from
+    const int32_t *tokens;
+    const int32_t *parents;  // or null: a chain
+    const float *u_accept;   // [B, T]
+    const float *u_sample;   // [B]
+    int B, T, V;
+    int32_t *accepted_len;
+    int32_t *path_nodes;
+    int32_t *out_tokens;
+    int32_t *seq_status;
+};
+
+// Workspace of the stochastic tree walk: (max, sum) per (sequence, row, chunk).
+VocabPlan plan_vocab_stree(int B, int T, int V, int dtype);
+sv_status launch_verify_tree_stochastic(const STreeArgs &args, int dtype, const VocabPlan &plan,
+                                        void *ws, cudaStream_t stream);
+
 sv_status launch_verify_chain(const ChainArgs &args, int dtype, const VocabPlan &plan, void *ws,
                               cudaStream_t stream);
 sv_status launch_verify_tree_greedy(const TreeArgs &args, int dtype, const VocabPlan &plan,

@@ -1260,6 +1260,305 @@ __global__ void __launch_bounds__(kVT) tree_decide_kernel(TreeArgs a, VocabPlan 
     tree_walk(a, b, late, ts);
 }
 
+// ---------------------------------------------------------------- stochastic tree
+
+// Multi-draft speculative sampling on a tree (the SpecInfer rule: the pages,
+// "Chapitre 9 -- Décodage spéculatif" §9.2, have the target choose among
+// drafted paths without giving a rule).  Node u's children were drawn from
+// q_u = softmax(draft row u); the target's distribution is p_u.  From the
+// root, the children of u are tried in index order against the residual
+// max(0, p_u - c q_u) / N(c), N(c) = sum_v max(0, p_u(v) - c q_u(v)), c = 0 at
+// the first child: child v (token x) is accepted iff
+// u_accept[v] * q_u(x) * N(c) < max(0, p_u(x) - c q_u(x)); a rejection sets
+// c = c + N(c) (the rejection step applied to the residual, in closed form).
+// With no child accepted, or at a leaf, the final token is drawn from
+// max(0, p_u - c q_u) (p_u when that sums to zero).
+//
+// Kernel 1: the (max, sum) records of every target row and of the draft row of
+// every node with children, one CTA per (row, chunk).  Kernel 2: one CTA of
+// 1024 threads per sequence walks the tree; each N(c) and the final draw are
+// block-wide passes over the row pair in coalesced 8192-element chunks.
+
+constexpr int kWT = 1024;                 // threads of the walking CTA
+constexpr int kWWarps = kWT / 32;
+constexpr int kWChunk = kWT * 8;          // elements of a pass chunk: 8 consecutive a thread
+constexpr int kMaxWChunks = 512;          // V <= 2^22
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kVT) stree_stats_kernel(STreeArgs a, VocabPlan p, float2 *rec) {
+    __shared__ float red[2 * kVWarps];
+    const int per_seq = 2 * a.T * p.nchunks;
+    const int item = blockIdx.x;
+    const int b = item / per_seq;
+    const int rem = item - b * per_seq;
+    const int r = rem / p.nchunks;  // rows 0..T-1 target, T..2T-1 draft
+    const int c = rem - r * p.nchunks;
+    griddep_wait();
+    griddep_launch_dependents();
+    if (r >= a.T) {  // a leaf's draft row is not used: not read
+        const int u = r - a.T;
+        int has_child = 0;
+        for (int v = u + 1 + (int)threadIdx.x; v < a.T; v += kVT)
+            if ((a.parents ? a.parents[(size_t)b * a.T + v] : v - 1) == u) has_child = 1;
+        if (!__syncthreads_or(has_child)) {
+            if (threadIdx.x == 0) rec[item] = make_float2(kNegInf, 0.f);
+            return;
+        }
+    }
+    const T *row = r < a.T ? static_cast<const T *>(a.target) + ((size_t)b * a.T + r) * a.V
+                           : static_cast<const T *>(a.draft) + ((size_t)b * a.T + (r - a.T)) * a.V;
+    const int begin = c * p.chunk_elems;
+    const int end = min(a.V, begin + p.chunk_elems);
+    float m = 0.f, s = 0.f;
+    chunk_cta_stats<T, VEC>(row, begin, end, red, m, s);
+    if (threadIdx.x == 0) rec[item] = make_float2(m, s);
+}
+
+// Sum over the CTA of one value per thread, in a fixed order (warp shuffles,
+// then the warps in order); every thread gets the total.
+__device__ __forceinline__ float walk_block_sum(float v, float *red /* [kWWarps] */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWWarps; ++w) t += red[w];
+    return t;
+}
+
+// p_u and q_u of one element (the same arithmetic everywhere in the walk).
+struct STreeRow {
+    float mt, it, md, id;  // log2-domain maxima and reciprocal sums of the target and draft rows
+    __device__ __forceinline__ float p(float lt) const {
+        return __fmul_rn(ex2_approx(__fmaf_rn(lt, kLog2e, -mt)), it);
+    }
+    __device__ __forceinline__ float q(float ld) const {
+        return __fmul_rn(ex2_approx(__fmaf_rn(ld, kLog2e, -md)), id);
+    }
+};
+
+// The weight of element e in the residual max(0, p - c q) (p itself for c = 0).
+template <typename T>
+__device__ __forceinline__ float stree_weight(const T *trow, const T *drow, const STreeRow &rs,
+                                              float c, int e) {
+    const float pe = rs.p(Elem<T>::at(trow, e));
+    if (c == 0.f) return pe;
+    return fmaxf(__fsub_rn(pe, __fmul_rn(c, rs.q(Elem<T>::at(drow, e)))), 0.f);
+}
+
+// This thread's sum over its 8 consecutive elements of chunk k (index order).
+template <typename T>
+__device__ __forceinline__ float stree_thread_sum(const T *trow, const T *drow, const STreeRow &rs,
+                                                  float c, int V, int k) {
+    const int e0 = k * kWChunk + (int)threadIdx.x * 8;
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (e0 + j < V) s = __fadd_rn(s, stree_weight<T>(trow, drow, rs, c, e0 + j));
+    return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan p, const float2 *rec) {
+    __shared__ int s_par[kMaxTreeT], s_tok[kMaxTreeT], s_kids[kMaxTreeT];
+    __shared__ unsigned char s_child[kMaxTreeT];
+    __shared__ float2 s_ms[2][kMaxTreeT];  // merged (max, sum) of the target / draft row of each node
+    __shared__ float s_red[kWWarps];
+    __shared__ float s_chunk[kMaxWChunks];
+    __shared__ int s_bad, s_nkids, s_next, s_pick;
+    __shared__ float s_prefix[kWT];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nT = a.T, V = a.V;
+    for (int i = tid; i < nT; i += kWT) {
+        s_par[i] = a.parents ? a.parents[(size_t)b * nT + i] : i - 1;  // NULL: a chain
+        s_tok[i] = a.tokens[(size_t)b * nT + i];
+        s_child[i] = 0;
+    }
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    for (int i = 1 + tid; i < nT; i += kWT) {
+        const int pa = s_par[i];
+        if (pa < 0 || pa >= i || s_tok[i] < 0 || s_tok[i] >= V) s_bad = 1;
+        else s_child[pa] = 1;
+    }
+    if (tid == 0 && s_par[0] != -1) s_bad = 1;
+    __syncthreads();
+    // merge the records of each used row; a row without a finite distribution is bad input
+    for (int rr = warp; rr < 2 * nT; rr += kWWarps) {
+        const int u = rr < nT ? rr : rr - nT;
+        if (rr >= nT && !s_child[u]) continue;
+        float m = kNegInf, s = 0.f;
+        for (int c = lane; c < p.nchunks; c += 32) {
+            const float2 r2 = __ldcg(rec + ((size_t)b * 2 * nT + rr) * p.nchunks + c);
+            merge_ms(m, s, r2.x, r2.y);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            merge_ms(m, s, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, s, off));
+        if (lane == 0) {
+            s_ms[rr < nT ? 0 : 1][u] = make_float2(m, s);
+            if (!(isfinite(m) && isfinite(s) && s > 0.f)) s_bad = 1;
+        }
+    }
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    int depth = 0, u = 0;
+    if (!bad) {
+        for (int step = 0; step < nT; ++step) {
+            // children of u in index order
+            if (tid == 0) {
+                int n = 0;
+                for (int v = u + 1; v < nT; ++v)
+                    if (s_par[v] == u) s_kids[n++] = v;
+                s_nkids = n;
+                s_next = -1;
+            }
+            __syncthreads();
+            const int nk = s_nkids;
+            const T *trow = static_cast<const T *>(a.target) + ((size_t)b * nT + u) * V;
+            const T *drow = static_cast<const T *>(a.draft) + ((size_t)b * nT + u) * V;
+            STreeRow rs;
+            rs.mt = s_ms[0][u].x;
+            rs.it = __frcp_rn(s_ms[0][u].y);
+            rs.md = nk > 0 ? s_ms[1][u].x : 0.f;
+            rs.id = nk > 0 ? __frcp_rn(s_ms[1][u].y) : 0.f;
+            const int nchunks = (V + kWChunk - 1) / kWChunk;
+            float c = 0.f;
+            for (int i = 0; i < nk; ++i) {
+                // N(c): 1 for c = 0, else a pass over the row pair
+                float n = 1.f;
+                if (c != 0.f) {
+                    n = 0.f;
+                    for (int k = 0; k < nchunks; ++k)
+                        n = __fadd_rn(n, walk_block_sum(stree_thread_sum<T>(trow, drow, rs, c, V, k), s_red));
+                }
+                const int v = s_kids[i];
+                if (tid == 0) {
+                    const int x = s_tok[v];
+                    const float px = __fdiv_rn(exp2_diff_accurate(Elem<T>::at(trow, x), rs.mt), s_ms[0][u].y);
+                    const float qx = __fdiv_rn(exp2_diff_accurate(Elem<T>::at(drow, x), rs.md), s_ms[1][u].y);
+                    const float r = fmaxf(__fsub_rn(px, __fmul_rn(c, qx)), 0.f);
+                    const float lhs = __fmul_rn(__fmul_rn(a.u_accept[(size_t)b * nT + v], qx), n);
+                    if (lhs < r) s_next = v;
+                }
+                __syncthreads();
+                if (s_next >= 0) break;
+                c = __fadd_rn(c, n);
+            }
+            const int next = s_next;
+            if (next >= 0) {
+                u = next;
+                ++depth;
+                if (tid == 0) {
+                    a.path_nodes[(size_t)b * nT + depth] = u;
+                    a.out_tokens[(size_t)b * nT + depth - 1] = s_tok[u];
+                }
+                __syncthreads();  // s_next and s_kids are rewritten for the next node
+                continue;
+            }
+            // ---- the final draw: chunk totals, then the chunk, the thread, the element
+            float S = 0.f;
+            for (int k = 0; k < nchunks; ++k) {
+                const float t = walk_block_sum(stree_thread_sum<T>(trow, drow, rs, c, V, k), s_red);
+                if (tid == 0) s_chunk[k] = t;
+                S = __fadd_rn(S, t);
+            }
+            if (!(S > 0.f)) {  // the residual vanished: draw from p_u
+                c = 0.f;
+                S = 0.f;
+                for (int k = 0; k < nchunks; ++k) {
+                    const float t = walk_block_sum(stree_thread_sum<T>(trow, drow, rs, c, V, k), s_red);
+                    if (tid == 0) s_chunk[k] = t;
+                    S = __fadd_rn(S, t);
+                }
+            }
+            __syncthreads();
+            const float theta = __fmul_rn(a.u_sample[b], S);
+            int ks = nchunks - 1;
+            float base = 0.f;
+            {
+                float run = 0.f;
+                int found = -1;
+                for (int k = 0; k < nchunks; ++k) {  // every thread, the same order
+                    const float nb = __fadd_rn(run, s_chunk[k]);
+                    if (found < 0 && nb > theta) {
+                        found = k;
+                        base = run;
+                    }
+                    run = nb;
+                }
+                if (found < 0) {  // rounding left no crossing: the last chunk with weight
+                    for (int k = nchunks - 1; k >= 0; --k)
+                        if (s_chunk[k] > 0.f) {
+                            found = k;
+                            break;
+                        }
+                    base = 0.f;
+                    for (int k = 0; k < found; ++k) base = __fadd_rn(base, s_chunk[k]);
+                }
+                ks = found < 0 ? 0 : found;
+            }
+            // inclusive prefix of the thread sums of chunk ks (warp scan, then warps in order)
+            const float ts = stree_thread_sum<T>(trow, drow, rs, c, V, ks);
+            float incl = ts;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl = __fadd_rn(incl, t);
+            }
+            if (lane == 31) s_red[warp] = incl;
+            if (tid == 0) s_pick = kWT;
+            __syncthreads();
+            float wbase = 0.f;
+            for (int w = 0; w < warp; ++w) wbase = __fadd_rn(wbase, s_red[w]);
+            incl = __fadd_rn(wbase, incl);
+            s_prefix[tid] = incl;
+            if (__fadd_rn(base, incl) > theta) atomicMin(&s_pick, tid);
+            __syncthreads();
+            int pick = s_pick;
+            if (pick >= kWT) {  // no crossing: the last thread holding weight
+                pick = 0;
+                for (int t2 = kWT - 1; t2 > 0; --t2)
+                    if (s_prefix[t2] > s_prefix[t2 - 1]) {
+                        pick = t2;
+                        break;
+                    }
+            }
+            if (tid == pick) {
+                const int e0 = ks * kWChunk + pick * 8;
+                float acc = __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f);
+                int y = -1, last = -1;
+                for (int j = 0; j < 8; ++j) {
+                    if (e0 + j >= V) break;
+                    const float wj = stree_weight<T>(trow, drow, rs, c, e0 + j);
+                    acc = __fadd_rn(acc, wj);
+                    if (wj > 0.f) last = e0 + j;
+                    if (y < 0 && acc > theta) y = e0 + j;
+                }
+                if (y < 0) y = last >= 0 ? last : max(e0, 0);
+                a.out_tokens[(size_t)b * nT + depth] = y;
+            }
+            break;
+        }
+    }
+    __syncthreads();
+    // outputs: the path and tokens past the end, the length and the status
+    for (int i = tid; i < nT; i += kWT) {
+        if (bad || i > depth) a.path_nodes[(size_t)b * nT + i] = -1;
+        if (bad || i > depth) a.out_tokens[(size_t)b * nT + i] = -1;
+    }
+    if (tid == 0) {
+        if (!bad) a.path_nodes[(size_t)b * nT] = 0;
+        a.accepted_len[b] = bad ? -1 : depth;
+        if (a.seq_status) a.seq_status[b] = bad ? SV_ERR_BAD_INPUT : SV_OK;
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
@@ -1373,6 +1672,50 @@ sv_status launch_verify_tree_greedy(const TreeArgs &a, int dtype, const VocabPla
     else
         e = p.vec ? launch_tree_t<float, true>(a, p, w, st)
                   : launch_tree_t<float, false>(a, p, w, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv
+
+namespace sv {
+
+VocabPlan plan_vocab_stree(int B, int T, int V, int dtype) {
+    VocabPlan p{};
+    const int esz = dtype == SV_F32 ? 4 : 2;
+    const int per_vec = 16 / esz;
+    p.rows_per_seq = 2 * T;
+    p.chunk_elems = kVT * kLoadsPerThread * per_vec;
+    p.nchunks = (V + p.chunk_elems - 1) / p.chunk_elems;
+    p.vec = ((size_t)V * esz) % 16 == 0;
+    p.recs_per_unit = 1;
+    p.off_counters = 0;
+    p.off_partials = 0;
+    p.bytes = align_up(sizeof(float2) * (size_t)B * p.rows_per_seq * p.nchunks, 256);
+    return p;
+}
+
+template <typename T, bool VEC>
+static cudaError_t launch_stree_t(STreeArgs a, VocabPlan p, float2 *rec, cudaStream_t st) {
+    void *args[] = {&a, &p, &rec};
+    const unsigned items = (unsigned)((size_t)a.B * p.rows_per_seq * p.nchunks);
+    cudaError_t e = launch_pdl((const void *)stree_stats_kernel<T, VEC>, dim3(items), dim3(kVT), 0,
+                               st, args);
+    if (e != cudaSuccess) return e;
+    return launch_pdl((const void *)stree_walk_kernel<T>, dim3((unsigned)a.B), dim3(kWT), 0, st,
+                      args);
+}
+
+sv_status launch_verify_tree_stochastic(const STreeArgs &a, int dtype, const VocabPlan &p, void *ws,
+                                        cudaStream_t st) {
+    if (a.T > kMaxTreeT || (a.V + kWChunk - 1) / kWChunk > kMaxWChunks) return SV_ERR_UNSUPPORTED;
+    float2 *rec = static_cast<float2 *>(ws);
+    cudaError_t e;
+    if (dtype == SV_BF16)
+        e = p.vec ? launch_stree_t<uint16_t, true>(a, p, rec, st)
+                  : launch_stree_t<uint16_t, false>(a, p, rec, st);
+    else
+        e = p.vec ? launch_stree_t<float, true>(a, p, rec, st)
+                  : launch_stree_t<float, false>(a, p, rec, st);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -159,6 +159,45 @@ def chain_inputs(B, N, V, dtype="bf16", target_sigma=3.0, draft_sigma=1.0, boost
                 u_sample=u_sample, B=B, N=N, V=V, dtype=dtype)
 
 
+def stree_inputs(B, T, V, parents, dtype="bf16", target_sigma=3.0, draft_sigma=1.0, boost=8.0,
+                 seed=0):
+    """Inputs of stochastic tree verification.
+
+    target logits [B, T, V] ~ N(0, target_sigma^2) plus `boost` on one random
+    token per row; draft logits [B, T, V] = target + N(0, draft_sigma^2) (row
+    u: the drafter at node u); the children of node u drawn independently
+    from softmax(draft_u) (node 0's token: 0); seeded uniforms u_accept
+    [B, T] and u_sample [B].  parents: [T] (shared) or [B, T].
+    """
+    par = np.broadcast_to(np.asarray(parents, np.int32), (B, T)).copy()
+    t = _normal(_rng(seed, _T_TARGET), (B, T, V), target_sigma)
+    if boost:
+        idx = _rng(seed, _T_BOOST).integers(0, V, size=(B, T))
+        np.add.at(t, (np.arange(B)[:, None], np.arange(T)[None, :], idx), np.float32(boost))
+    if dtype == "bf16":
+        t_store = f32_to_bf16_bits(t)
+        t_val = bf16_bits_to_f32(t_store)
+    else:
+        t_store = t
+        t_val = t
+    d = t_val + _normal(_rng(seed, _T_DRAFT), (B, T, V), draft_sigma)
+    if dtype == "bf16":
+        d_store = f32_to_bf16_bits(d)
+        d_val = bf16_bits_to_f32(d_store)
+    else:
+        d_store = d.astype(np.float32)
+        d_val = d_store
+    ud = _rng(seed, _T_DTOK).random((B, T))
+    tok = np.zeros((B, T), np.int32)
+    for b in range(B):
+        for v in range(1, T):
+            tok[b, v] = _sample_from_logits(d_val[b, par[b, v]], ud[b, v])
+    u_accept = _rng(seed, _T_UACC).random((B, T), dtype=np.float32)
+    u_sample = _rng(seed, _T_USAMP).random(B, dtype=np.float32)
+    return dict(target=t_store, draft=d_store, node_tokens=tok, parents=par, u_accept=u_accept,
+                u_sample=u_sample, B=B, T=T, V=V, dtype=dtype)
+
+
 def tree_logit_inputs(B, T, V, parents, p_match, sigma=3.0, dtype="bf16", seed=0):
     """Inputs of greedy tree verification: target logits [B, T, V] ~ N(0,
     sigma^2); node tokens where each non-root node independently copies the
