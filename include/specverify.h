@@ -241,6 +241,8 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
  *                  rows of leaves are not read)
  *   node_tokens, parents int32 [B, T] (parents NULL: a chain); u_accept f32
  *   [B, T] (entry v tests node v; entry 0 unused); u_sample f32 [B]
+ *   node_counts int32 [B] or NULL: sequence b has T_b nodes (1 <= T_b <= T),
+ *   those past T_b are padding (never read); NULL means T_b = T
  *   accepted_len int32 [B]; path_nodes, out_tokens int32 [B, T]
  *   workspace  >= sv_workspace_size(SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, dtype, 0, 0)
  * Supported: 1 <= T <= 1024, 1 <= V <= 2^22.  A tree that is not
@@ -250,8 +252,9 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
  */
 sv_status sv_verify_tree_stochastic(const void *target_logits, const void *draft_logits,
                                     sv_dtype dtype, const int32_t *node_tokens,
-                                    const int32_t *parents, const float *u_accept,
-                                    const float *u_sample, int B, int T, int V,
+                                    const int32_t *parents, const int32_t *node_counts,
+                                    const float *u_accept, const float *u_sample, int B, int T,
+                                    int V,
                                     int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
                                     int32_t *seq_status, void *workspace, size_t workspace_bytes,
                                     sv_stream_t stream);

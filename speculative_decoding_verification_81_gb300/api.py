@@ -70,7 +70,8 @@ def lib() -> ctypes.CDLL:
         L.sv_tree_attention_paged.argtypes = [P, P, P, P, I, I, I, P, P, P, I, I, I, I, I,
                                               ctypes.c_float, P, P, P, Z, P]
         L.sv_compact_kv_paged.argtypes = [P, P, P, I, I, I, P, P, P, I, P, I, I, I, P, P]
-        L.sv_verify_tree_stochastic.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+        L.sv_verify_tree_stochastic.argtypes = [P, P, I, P, P, P, P, P, I, I, I, P, P, P, P, P, Z,
+                                                P]
         for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
                    "sv_verify_chain_noalloc", "sv_tree_attention_paged", "sv_compact_kv_paged",
                    "sv_verify_tree_stochastic"):
@@ -268,10 +269,11 @@ def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None
 
 def sv_verify_tree_stochastic(target_logits, draft_logits, node_tokens, parents, u_accept,
                               u_sample, accepted_len=None, path_nodes=None, out_tokens=None,
-                              seq_status=None, ws=None, stream=None):
+                              seq_status=None, ws=None, stream=None, node_counts=None):
     """target, draft [B,T,V] (bf16 or f32; draft row u: the distribution u's
     children were drawn from); node_tokens, parents [B,T] int32 (parents None:
-    a chain); u_accept [B,T] f32; u_sample [B] f32.
+    a chain); u_accept [B,T] f32; u_sample [B] f32; node_counts [B] int32 or
+    None (every sequence has T nodes).
     Returns (accepted_len [B], path_nodes [B,T], out_tokens [B,T])."""
     _req(target_logits, "target_logits", None, 3)
     _req(draft_logits, "draft_logits", target_logits.dtype, 3)
@@ -280,6 +282,8 @@ def sv_verify_tree_stochastic(target_logits, draft_logits, node_tokens, parents,
         _req(parents, "parents", torch.int32, 2)
     _req(u_accept, "u_accept", torch.float32, 2)
     _req(u_sample, "u_sample", torch.float32, 1)
+    if node_counts is not None:
+        _req(node_counts, "node_counts", torch.int32, 1)
     dt = _dtype_code(target_logits)
     B, T, V = target_logits.shape
     dev = target_logits.device
@@ -292,7 +296,8 @@ def sv_verify_tree_stochastic(target_logits, draft_logits, node_tokens, parents,
     if ws is None:
         ws = workspace(SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, dt, 0, 0, dev)
     rc = lib().sv_verify_tree_stochastic(_p(target_logits), _p(draft_logits), dt, _p(node_tokens),
-                                         _p(parents), _p(u_accept), _p(u_sample), B, T, V,
+                                         _p(parents), _p(node_counts), _p(u_accept),
+                                         _p(u_sample), B, T, V,
                                          _p(accepted_len), _p(path_nodes), _p(out_tokens),
                                          _p(seq_status), _p(ws), ws.numel(), _stream(stream))
     _check("sv_verify_tree_stochastic", rc)

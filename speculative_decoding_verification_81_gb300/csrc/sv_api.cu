@@ -150,8 +150,9 @@ sv_status sv_verify_tree_greedy(const void *target_logits, sv_dtype dtype,
 
 sv_status sv_verify_tree_stochastic(const void *target_logits, const void *draft_logits,
                                     sv_dtype dtype, const int32_t *node_tokens,
-                                    const int32_t *parents, const float *u_accept,
-                                    const float *u_sample, int B, int T, int V,
+                                    const int32_t *parents, const int32_t *node_counts,
+                                    const float *u_accept, const float *u_sample, int B, int T,
+                                    int V,
                                     int32_t *accepted_len, int32_t *path_nodes, int32_t *out_tokens,
                                     int32_t *seq_status, void *workspace, size_t workspace_bytes,
                                     sv_stream_t stream) {
@@ -165,8 +166,9 @@ sv_status sv_verify_tree_stochastic(const void *target_logits, const void *draft
     const sv::VocabPlan pl = sv::plan_vocab_stree(B, T, V, dtype);
     if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return SV_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
-    sv::STreeArgs a{target_logits, draft_logits, node_tokens, parents, u_accept, u_sample, B, T, V,
-                    accepted_len, path_nodes, out_tokens, seq_status};
+    sv::STreeArgs a{target_logits, draft_logits, node_tokens, parents,    node_counts, u_accept,
+                    u_sample,      B,            T,           V,          accepted_len, path_nodes,
+                    out_tokens,    seq_status};
     return sv::launch_verify_tree_stochastic(a, dtype, pl, workspace, as_stream(stream));
 }
 

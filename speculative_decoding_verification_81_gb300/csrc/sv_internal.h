@@ -99,8 +99,9 @@ struct STreeArgs {
     const void *target;  // [B, T, V]
     const void *draft;   // [B, T, V]: row u is the distribution u's children were drawn from
     const int32_t *tokens;
-    const int32_t *parents;  // or null: a chain
-    const float *u_accept;   // [B, T]
+    const int32_t *parents;      // or null: a chain
+    const int32_t *node_counts;  // per-sequence T_b (1 <= T_b <= T), or null: all T
+    const float *u_accept;       // [B, T]
     const float *u_sample;   // [B]
     int B, T, V;
     int32_t *accepted_len;

@@ -1295,15 +1295,20 @@ __global__ void __launch_bounds__(kVT) stree_stats_kernel(STreeArgs a, VocabPlan
     const int c = rem - r * p.nchunks;
     griddep_wait();
     griddep_launch_dependents();
-    if (r >= a.T) {  // a leaf's draft row is not used: not read
-        const int u = r - a.T;
+    // this sequence's nodes (an invalid count is reported by the walk)
+    const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+    const int tb = (tb_raw >= 1 && tb_raw <= a.T) ? tb_raw : a.T;
+    const int u = r < a.T ? r : r - a.T;
+    bool used = u < tb;
+    if (used && r >= a.T) {  // a draft row is read only for a node with children
         int has_child = 0;
-        for (int v = u + 1 + (int)threadIdx.x; v < a.T; v += kVT)
+        for (int v = u + 1 + (int)threadIdx.x; v < tb; v += kVT)
             if ((a.parents ? a.parents[(size_t)b * a.T + v] : v - 1) == u) has_child = 1;
-        if (!__syncthreads_or(has_child)) {
-            if (threadIdx.x == 0) rec[item] = make_float2(kNegInf, 0.f);
-            return;
-        }
+        used = __syncthreads_or(has_child) != 0;
+    }
+    if (!used) {  // a padding node's row, a leaf's draft row: not read
+        if (threadIdx.x == 0) rec[item] = make_float2(kNegInf, 0.f);
+        return;
     }
     const T *row = r < a.T ? static_cast<const T *>(a.target) + ((size_t)b * a.T + r) * a.V
                            : static_cast<const T *>(a.draft) + ((size_t)b * a.T + (r - a.T)) * a.V;
@@ -1374,14 +1379,18 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     griddep_launch_dependents();
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nT = a.T, V = a.V;
+    // this sequence's nodes; those past T_b are padding
+    const int tb_raw = a.node_counts ? a.node_counts[b] : nT;
+    const bool tb_ok = tb_raw >= 1 && tb_raw <= nT;
+    const int nb = tb_ok ? tb_raw : 1;
     for (int i = tid; i < nT; i += kWT) {
         s_par[i] = a.parents ? a.parents[(size_t)b * nT + i] : i - 1;  // NULL: a chain
         s_tok[i] = a.tokens[(size_t)b * nT + i];
         s_child[i] = 0;
     }
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) s_bad = tb_ok ? 0 : 1;
     __syncthreads();
-    for (int i = 1 + tid; i < nT; i += kWT) {
+    for (int i = 1 + tid; i < nb; i += kWT) {
         const int pa = s_par[i];
         if (pa < 0 || pa >= i || s_tok[i] < 0 || s_tok[i] >= V) s_bad = 1;
         else s_child[pa] = 1;
@@ -1391,7 +1400,7 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     // merge the records of each used row; a row without a finite distribution is bad input
     for (int rr = warp; rr < 2 * nT; rr += kWWarps) {
         const int u = rr < nT ? rr : rr - nT;
-        if (rr >= nT && !s_child[u]) continue;
+        if (u >= nb || (rr >= nT && !s_child[u])) continue;
         float m = kNegInf, s = 0.f;
         for (int c = lane; c < p.nchunks; c += 32) {
             const float2 r2 = __ldcg(rec + ((size_t)b * 2 * nT + rr) * p.nchunks + c);
@@ -1409,11 +1418,11 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     const bool bad = s_bad != 0;
     int depth = 0, u = 0;
     if (!bad) {
-        for (int step = 0; step < nT; ++step) {
+        for (int step = 0; step < nb; ++step) {
             // children of u in index order
             if (tid == 0) {
                 int n = 0;
-                for (int v = u + 1; v < nT; ++v)
+                for (int v = u + 1; v < nb; ++v)
                     if (s_par[v] == u) s_kids[n++] = v;
                 s_nkids = n;
                 s_next = -1;

@@ -226,3 +226,44 @@ def test_tree_bad_node_counts_reported():
     torch.cuda.synchronize()
     assert host(st).tolist() == [0, sv.SV_ERR_BAD_INPUT, sv.SV_ERR_BAD_INPUT]
     assert (host(acc)[1:] == -1).all()
+
+
+# ------------------------------------------------------------------ stochastic tree
+
+@pytest.mark.parametrize("B,T,V,dtype,counts,seed", [
+    (5, 20, 3000, "bf16", [20, 1, 9, 2, 14], 41),
+    (3, 26, 32000, "bf16", [26, 5, 13], 42),
+    (4, 12, 1001, "f32", [12, 7, 1, 3], 43),
+])
+def test_stochastic_tree_node_counts(orc, B, T, V, dtype, counts, seed):
+    rng = np.random.default_rng(seed)
+    par = np.stack([W.random_tree(T, 6, rng) for _ in range(B)])
+    inp = W.stree_inputs(B, T, V, par, dtype, target_sigma=2.0, draft_sigma=1.0, boost=4.0,
+                         seed=seed)
+    clean = {k: np.copy(v) for k, v in inp.items()}
+    for b, tb in enumerate(counts):
+        inp["target"][b, tb:] = _nan_of(inp["target"])
+        inp["draft"][b, tb:] = _nan_of(inp["draft"])
+        inp["node_tokens"][b, tb:] = -5
+        inp["parents"][b, tb:] = T + 3
+    st = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    acc, path, out = sv.sv_verify_tree_stochastic(
+        dev(inp["target"]), dev(inp["draft"]), dev(inp["node_tokens"]), dev(inp["parents"]),
+        dev(inp["u_accept"]), dev(inp["u_sample"]), seq_status=st,
+        node_counts=dev(np.asarray(counts, np.int32)))
+    torch.cuda.synchronize()
+    acc, path, out = host(acc), host(path), host(out)
+    assert (host(st) == 0).all()
+    for b, tb in enumerate(counts):
+        ref = orc.verify_tree_stochastic(clean["target"][b:b + 1, :tb], clean["draft"][b:b + 1, :tb],
+                                         clean["node_tokens"][b:b + 1, :tb],
+                                         clean["parents"][b:b + 1, :tb],
+                                         clean["u_accept"][b:b + 1, :tb], clean["u_sample"][b:b + 1])
+        assert (path[b, tb:] == -1).all() and (out[b, tb:] == -1).all()
+        f = ref["flags"][0]
+        if f & 1:
+            continue
+        assert acc[b] == ref["accepted_len"][0], b
+        np.testing.assert_array_equal(path[b, :tb], ref["path_nodes"][0])
+        n_cmp = int(acc[b]) if f & 2 else tb
+        np.testing.assert_array_equal(out[b, :n_cmp], ref["out_tokens"][0, :n_cmp])
