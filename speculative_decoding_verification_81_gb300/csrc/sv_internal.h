@@ -58,6 +58,7 @@ struct VocabPlan {
     int chunk_elems;
     int res_chunks;       // residual-draw chunks per sequence (chain only)
     int res_chunk_elems;
+    int walk_cluster;     // CTAs per sequence of the stochastic tree walk (set at launch)
     bool vec;             // rows are 16-byte aligned: vector loads
     int recs_per_unit;    // chain: (max, sum) records per (row, chunk)
     size_t off_counters;  // 2*B + 4 ints: arrivals per sequence, then [2*B] a timeout flag

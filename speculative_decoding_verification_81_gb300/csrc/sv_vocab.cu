@@ -22,6 +22,7 @@
 // No CTA ever waits for another: the "last CTA" is whoever brings a
 // per-sequence arrival counter to its final value; it resets the counter.
 #include <climits>
+#include <mutex>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -1275,14 +1276,38 @@ __global__ void __launch_bounds__(kVT) tree_decide_kernel(TreeArgs a, VocabPlan 
 // max(0, p_u - c q_u) (p_u when that sums to zero).
 //
 // Kernel 1: the (max, sum) records of every target row and of the draft row of
-// every node with children, one CTA per (row, chunk).  Kernel 2: one CTA of
-// 1024 threads per sequence walks the tree; each N(c) and the final draw are
-// block-wide passes over the row pair in coalesced 8192-element chunks.
+// every node with children, one CTA per (row, chunk).  Kernel 2: one
+// thread-block cluster per sequence walks the tree.  Every CTA of the cluster
+// takes the same decisions from the same inputs; each N(c) and the final draw
+// are passes over the row pair in which every thread sums its own contiguous
+// segment of the vocabulary (CTA rank, then thread, then element: index
+// order), the CTAs' partial sums meeting in distributed shared memory.
 
-constexpr int kWT = 1024;                 // threads of the walking CTA
+constexpr int kWT = 256;                  // threads of a walking CTA
 constexpr int kWWarps = kWT / 32;
-constexpr int kWChunk = kWT * 8;          // elements of a pass chunk: 8 consecutive a thread
-constexpr int kMaxWChunks = 512;          // V <= 2^22
+constexpr int kWClusterMax = 16;          // CTAs of a walking cluster (16: non-portable)
+constexpr int kMaxWSeg = 4096;            // elements a thread owns in a pass
+
+// Thread-block clusters: this CTA's rank, a barrier over every thread of the
+// cluster (release/acquire: shared-memory writes before it are visible to the
+// other CTAs after it), and a load from another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_shared_cluster_f32(const float *local, uint32_t rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT) stree_stats_kernel(STreeArgs a, VocabPlan p, float2 *rec) {
@@ -1345,39 +1370,58 @@ struct STreeRow {
     }
 };
 
-// The weight of element e in the residual max(0, p - c q) (p itself for c = 0).
-template <typename T>
-__device__ __forceinline__ float stree_weight(const T *trow, const T *drow, const STreeRow &rs,
-                                              float c, int e) {
-    const float pe = rs.p(Elem<T>::at(trow, e));
-    if (c == 0.f) return pe;
-    return fmaxf(__fsub_rn(pe, __fmul_rn(c, rs.q(Elem<T>::at(drow, e)))), 0.f);
-}
-
-// This thread's sum over its 8 consecutive elements of chunk k (index order).
-template <typename T>
-__device__ __forceinline__ float stree_thread_sum(const T *trow, const T *drow, const STreeRow &rs,
-                                                  float c, int V, int k) {
-    const int e0 = k * kWChunk + (int)threadIdx.x * 8;
-    float s = 0.f;
+// Elements [e0, e1) of the thread's segment in index order: their weights
+// summed one by one (words of 8 or 4 elements when the rows are 16-byte
+// aligned), or, with `want` in range, the first element where `acc` plus the
+// running sum passes `theta` (and the last element with weight) -- the same
+// additions in the same order either way.
+template <typename T, bool VEC>
+__device__ __forceinline__ float stree_seg(const T *trow, const T *drow, const STreeRow &rs, float c,
+                                           int e0, int e1, float acc, float theta, int *hit,
+                                           int *last) {
+    constexpr int PV = Elem<T>::kPerVec;
+    float s = acc;
+    for (int e = e0; e < e1; e += PV) {
+        float xt[PV], xd[PV];
+        if (VEC && e + PV <= e1) {
+            Elem<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(trow + e)), xt);
+            if (c != 0.f) Elem<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(drow + e)), xd);
+        } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        if (e0 + j < V) s = __fadd_rn(s, stree_weight<T>(trow, drow, rs, c, e0 + j));
+            for (int j = 0; j < PV; ++j) {
+                xt[j] = e + j < e1 ? Elem<T>::at(trow, e + j) : kNegInf;
+                xd[j] = (c != 0.f && e + j < e1) ? Elem<T>::at(drow, e + j) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < PV; ++j) {
+            if (e + j >= e1) break;
+            const float pe = rs.p(xt[j]);
+            const float w = c == 0.f ? pe : fmaxf(__fsub_rn(pe, __fmul_rn(c, rs.q(xd[j]))), 0.f);
+            s = __fadd_rn(s, w);
+            if (hit) {
+                if (w > 0.f) *last = e + j;
+                if (*hit < 0 && s > theta) *hit = e + j;
+            }
+        }
+    }
     return s;
 }
 
-template <typename T>
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan p, const float2 *rec) {
     __shared__ int s_par[kMaxTreeT], s_tok[kMaxTreeT], s_kids[kMaxTreeT];
     __shared__ unsigned char s_child[kMaxTreeT];
     __shared__ float2 s_ms[2][kMaxTreeT];  // merged (max, sum) of the target / draft row of each node
     __shared__ float s_red[kWWarps];
-    __shared__ float s_chunk[kMaxWChunks];
+    __shared__ float s_part[2];            // this CTA's partial sum of a pass (two in turn)
     __shared__ int s_bad, s_nkids, s_next, s_pick;
     __shared__ float s_prefix[kWT];
     griddep_wait();
     griddep_launch_dependents();
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = p.walk_cluster;
+    const int rank = (int)cluster_ctarank();
+    const int b = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nT = a.T, V = a.V;
     // this sequence's nodes; those past T_b are padding
     const int tb_raw = a.node_counts ? a.node_counts[b] : nT;
@@ -1415,7 +1459,27 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
         }
     }
     __syncthreads();
+    // every CTA reaches the same verdict from the same inputs, so all of them
+    // take the same path through the cluster barriers below
     const bool bad = s_bad != 0;
+    // this thread's segment of the vocabulary (a multiple of 8 elements long):
+    // CTA rank, then thread, in index order
+    const int seg = ((V + C * kWT - 1) / (C * kWT) + 7) & ~7;
+    const int gt = rank * kWT + tid;
+    const int e0 = min(V, gt * seg), e1 = min(V, e0 + seg);
+    int pass = 0;
+    // the cluster's sum of one value per thread: CTA sums in a fixed order,
+    // then the CTAs in rank order (every CTA gets the same total)
+    auto cluster_total = [&](float v, float *cta_total) -> float {
+        const float t = walk_block_sum(v, s_red);
+        if (cta_total) *cta_total = t;
+        if (tid == 0) s_part[pass & 1] = t;
+        cluster_sync();
+        float tot = 0.f;
+        for (int k = 0; k < C; ++k) tot = __fadd_rn(tot, ld_shared_cluster_f32(&s_part[pass & 1], (uint32_t)k));
+        ++pass;  // the other buffer next: a CTA may run ahead into the next pass
+        return tot;
+    };
     int depth = 0, u = 0;
     if (!bad) {
         for (int step = 0; step < nb; ++step) {
@@ -1436,16 +1500,13 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
             rs.it = __frcp_rn(s_ms[0][u].y);
             rs.md = nk > 0 ? s_ms[1][u].x : 0.f;
             rs.id = nk > 0 ? __frcp_rn(s_ms[1][u].y) : 0.f;
-            const int nchunks = (V + kWChunk - 1) / kWChunk;
             float c = 0.f;
             for (int i = 0; i < nk; ++i) {
                 // N(c): 1 for c = 0, else a pass over the row pair
-                float n = 1.f;
-                if (c != 0.f) {
-                    n = 0.f;
-                    for (int k = 0; k < nchunks; ++k)
-                        n = __fadd_rn(n, walk_block_sum(stree_thread_sum<T>(trow, drow, rs, c, V, k), s_red));
-                }
+                const float n = c == 0.f ? 1.f
+                                         : cluster_total(stree_seg<T, VEC>(trow, drow, rs, c, e0, e1, 0.f,
+                                                                           0.f, nullptr, nullptr),
+                                                         nullptr);
                 const int v = s_kids[i];
                 if (tid == 0) {
                     const int x = s_tok[v];
@@ -1463,98 +1524,89 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
             if (next >= 0) {
                 u = next;
                 ++depth;
-                if (tid == 0) {
+                if (tid == 0 && rank == 0) {
                     a.path_nodes[(size_t)b * nT + depth] = u;
                     a.out_tokens[(size_t)b * nT + depth - 1] = s_tok[u];
                 }
                 __syncthreads();  // s_next and s_kids are rewritten for the next node
                 continue;
             }
-            // ---- the final draw: chunk totals, then the chunk, the thread, the element
-            float S = 0.f;
-            for (int k = 0; k < nchunks; ++k) {
-                const float t = walk_block_sum(stree_thread_sum<T>(trow, drow, rs, c, V, k), s_red);
-                if (tid == 0) s_chunk[k] = t;
-                S = __fadd_rn(S, t);
-            }
+            // ---- the final draw: the CTA totals, the CTA, the thread, the element
+            float ts = stree_seg<T, VEC>(trow, drow, rs, c, e0, e1, 0.f, 0.f, nullptr, nullptr);
+            float cta = 0.f;
+            float S = cluster_total(ts, &cta);
             if (!(S > 0.f)) {  // the residual vanished: draw from p_u
                 c = 0.f;
-                S = 0.f;
-                for (int k = 0; k < nchunks; ++k) {
-                    const float t = walk_block_sum(stree_thread_sum<T>(trow, drow, rs, c, V, k), s_red);
-                    if (tid == 0) s_chunk[k] = t;
-                    S = __fadd_rn(S, t);
-                }
+                ts = stree_seg<T, VEC>(trow, drow, rs, c, e0, e1, 0.f, 0.f, nullptr, nullptr);
+                S = cluster_total(ts, &cta);
             }
-            __syncthreads();
             const float theta = __fmul_rn(a.u_sample[b], S);
-            int ks = nchunks - 1;
-            float base = 0.f;
-            {
-                float run = 0.f;
-                int found = -1;
-                for (int k = 0; k < nchunks; ++k) {  // every thread, the same order
-                    const float nb = __fadd_rn(run, s_chunk[k]);
-                    if (found < 0 && nb > theta) {
-                        found = k;
-                        base = run;
-                    }
-                    run = nb;
+            // the CTA where the cluster prefix passes theta (rank order; the
+            // same search in every CTA)
+            const int pb = (pass - 1) & 1;  // the buffer of the last pass
+            int kstar = -1, klast = 0;
+            float base = 0.f, run = 0.f;
+            for (int k = 0; k < C; ++k) {
+                const float t = ld_shared_cluster_f32(&s_part[pb], (uint32_t)k);
+                if (t > 0.f) klast = k;
+                const float nb2 = __fadd_rn(run, t);
+                if (kstar < 0 && nb2 > theta) {
+                    kstar = k;
+                    base = run;
                 }
-                if (found < 0) {  // rounding left no crossing: the last chunk with weight
-                    for (int k = nchunks - 1; k >= 0; --k)
-                        if (s_chunk[k] > 0.f) {
-                            found = k;
+                run = nb2;
+            }
+            bool fallback = false;
+            if (kstar < 0) {  // rounding left no crossing: the last CTA with weight
+                fallback = true;
+                kstar = klast;
+                base = 0.f;
+                for (int k = 0; k < kstar; ++k)
+                    base = __fadd_rn(base, ld_shared_cluster_f32(&s_part[pb], (uint32_t)k));
+            }
+            if (rank == kstar) {
+                // inclusive prefix of this CTA's thread sums (warp scan, then the warps in order)
+                float incl = ts;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float t = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl = __fadd_rn(incl, t);
+                }
+                __syncthreads();  // the last block sum's readers are done with s_red
+                if (lane == 31) s_red[warp] = incl;
+                if (tid == 0) s_pick = kWT;
+                __syncthreads();
+                float wbase = 0.f;
+                for (int w = 0; w < warp; ++w) wbase = __fadd_rn(wbase, s_red[w]);
+                incl = __fadd_rn(wbase, incl);
+                s_prefix[tid] = incl;
+                if (!fallback && __fadd_rn(base, incl) > theta) atomicMin(&s_pick, tid);
+                __syncthreads();
+                int pick = s_pick;
+                if (pick >= kWT) {  // no crossing: the last thread holding weight
+                    pick = 0;
+                    for (int t2 = kWT - 1; t2 > 0; --t2)
+                        if (s_prefix[t2] > s_prefix[t2 - 1]) {
+                            pick = t2;
                             break;
                         }
-                    base = 0.f;
-                    for (int k = 0; k < found; ++k) base = __fadd_rn(base, s_chunk[k]);
                 }
-                ks = found < 0 ? 0 : found;
-            }
-            // inclusive prefix of the thread sums of chunk ks (warp scan, then warps in order)
-            const float ts = stree_thread_sum<T>(trow, drow, rs, c, V, ks);
-            float incl = ts;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float t = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl = __fadd_rn(incl, t);
-            }
-            if (lane == 31) s_red[warp] = incl;
-            if (tid == 0) s_pick = kWT;
-            __syncthreads();
-            float wbase = 0.f;
-            for (int w = 0; w < warp; ++w) wbase = __fadd_rn(wbase, s_red[w]);
-            incl = __fadd_rn(wbase, incl);
-            s_prefix[tid] = incl;
-            if (__fadd_rn(base, incl) > theta) atomicMin(&s_pick, tid);
-            __syncthreads();
-            int pick = s_pick;
-            if (pick >= kWT) {  // no crossing: the last thread holding weight
-                pick = 0;
-                for (int t2 = kWT - 1; t2 > 0; --t2)
-                    if (s_prefix[t2] > s_prefix[t2 - 1]) {
-                        pick = t2;
-                        break;
-                    }
-            }
-            if (tid == pick) {
-                const int e0 = ks * kWChunk + pick * 8;
-                float acc = __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f);
-                int y = -1, last = -1;
-                for (int j = 0; j < 8; ++j) {
-                    if (e0 + j >= V) break;
-                    const float wj = stree_weight<T>(trow, drow, rs, c, e0 + j);
-                    acc = __fadd_rn(acc, wj);
-                    if (wj > 0.f) last = e0 + j;
-                    if (y < 0 && acc > theta) y = e0 + j;
+                if (tid == pick) {
+                    const int gp = rank * kWT + pick;
+                    const int p0 = min(V, gp * seg), p1 = min(V, p0 + seg);
+                    int y = -1, last = -1;
+                    stree_seg<T, VEC>(trow, drow, rs, c, p0, p1,
+                                      __fadd_rn(base, pick > 0 ? s_prefix[pick - 1] : 0.f),
+                                      fallback ? __int_as_float(0x7f800000) : theta, &y, &last);
+                    if (y < 0) y = last >= 0 ? last : max(p0, 0);
+                    a.out_tokens[(size_t)b * nT + depth] = y;
                 }
-                if (y < 0) y = last >= 0 ? last : max(e0, 0);
-                a.out_tokens[(size_t)b * nT + depth] = y;
             }
             break;
         }
     }
+    cluster_sync();  // no CTA leaves while another may still read its partial sums
+    if (rank != 0) return;
     __syncthreads();
     // outputs: the path and tokens past the end, the length and the status
     for (int i = tid; i < nT; i += kWT) {
@@ -1703,6 +1755,44 @@ VocabPlan plan_vocab_stree(int B, int T, int V, int dtype) {
     return p;
 }
 
+// Largest cluster the device schedules for the walk: 16 CTAs (a non-portable
+// size) where it can run one, else the portable 8.  Queried once per device
+// and kernel.
+static int walk_cluster_max(const void *fn) {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int n;
+    };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int ncache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ncache; ++i)
+        if (cache[i].dev == dev && cache[i].fn == fn) return cache[i].n;
+    int n = 8;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kWClusterMax;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kWClusterMax);
+        cfg.blockDim = dim3(kWT);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
+            n = kWClusterMax;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind
+    if (ncache < 16) cache[ncache++] = Entry{dev, fn, n};
+    return n;
+}
+
 template <typename T, bool VEC>
 static cudaError_t launch_stree_t(STreeArgs a, VocabPlan p, float2 *rec, cudaStream_t st) {
     void *args[] = {&a, &p, &rec};
@@ -1710,13 +1800,30 @@ static cudaError_t launch_stree_t(STreeArgs a, VocabPlan p, float2 *rec, cudaStr
     cudaError_t e = launch_pdl((const void *)stree_stats_kernel<T, VEC>, dim3(items), dim3(kVT), 0,
                                st, args);
     if (e != cudaSuccess) return e;
-    return launch_pdl((const void *)stree_walk_kernel<T>, dim3((unsigned)a.B), dim3(kWT), 0, st,
-                      args);
+    // the walk: one cluster per sequence, launched after the statistics pass has
+    // finished (a cluster placed early, beside that pass, can wait long for SMs)
+    const void *wfn = (const void *)stree_walk_kernel<T, VEC>;
+    const int C = walk_cluster_max(wfn);
+    if (C < 1) return cudaErrorUnknown;
+    p.walk_cluster = C;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * C));
+    cfg.blockDim = dim3(kWT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, wfn, args);
 }
 
 sv_status launch_verify_tree_stochastic(const STreeArgs &a, int dtype, const VocabPlan &p, void *ws,
                                         cudaStream_t st) {
-    if (a.T > kMaxTreeT || (a.V + kWChunk - 1) / kWChunk > kMaxWChunks) return SV_ERR_UNSUPPORTED;
+    if (a.T > kMaxTreeT || (a.V + 8 * kWT - 1) / (8 * kWT) > kMaxWSeg) return SV_ERR_UNSUPPORTED;
     float2 *rec = static_cast<float2 *>(ws);
     cudaError_t e;
     if (dtype == SV_BF16)
