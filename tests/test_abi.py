@@ -93,6 +93,29 @@ def test_verify_tree_host_validation(L):
     assert call(ws=FAKE, wsb=need - 16) == sv.SV_ERR_WORKSPACE
 
 
+def test_verify_tree_stochastic_host_validation(L):
+    def call(**kw):
+        a = dict(t=FAKE, d=FAKE, dt=sv.SV_BF16, tok=FAKE, par=FAKE, cnt=None, ua=FAKE, us=FAKE, B=2,
+                 T=26, V=32000, acc=FAKE, path=FAKE, out=FAKE, ws=None, wsb=0)
+        a.update(kw)
+        return L.sv_verify_tree_stochastic(a["t"], a["d"], a["dt"], a["tok"], a["par"], a["cnt"],
+                                           a["ua"], a["us"], a["B"], a["T"], a["V"], a["acc"],
+                                           a["path"], a["out"], None, a["ws"], a["wsb"], None)
+    assert call(d=None) == sv.SV_ERR_INVALID_ARG
+    assert call(ua=None) == sv.SV_ERR_INVALID_ARG
+    assert call(dt=9) == sv.SV_ERR_INVALID_ARG
+    assert call(T=0) == sv.SV_ERR_INVALID_ARG
+    assert call(d=MISALIGNED) == sv.SV_ERR_INVALID_ARG
+    assert call(T=1025) == sv.SV_ERR_UNSUPPORTED
+    assert call(V=(1 << 22) + 1) == sv.SV_ERR_UNSUPPORTED
+    assert call(par=None) == sv.SV_ERR_WORKSPACE  # NULL parents: a chain, valid
+    assert call(cnt=FAKE) == sv.SV_ERR_WORKSPACE  # node counts are checked on the device
+    need = L.sv_workspace_size(sv.SV_OP_VERIFY_TREE_STOCHASTIC, 2, 26, 32000, sv.SV_BF16, 0, 0)
+    assert need > 0
+    assert call(ws=FAKE, wsb=need - 16) == sv.SV_ERR_WORKSPACE
+    assert call(ws=MISALIGNED, wsb=need) == sv.SV_ERR_WORKSPACE
+
+
 def test_attention_host_validation(L):
     def call(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, pl=FAKE, par=None, cnt=None, B=2, T=9, Hq=32, Hkv=8,
