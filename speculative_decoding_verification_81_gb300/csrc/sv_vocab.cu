@@ -1417,6 +1417,9 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     __shared__ float s_part[2];            // this CTA's partial sum of a pass (two in turn)
     __shared__ int s_bad, s_nkids, s_next, s_pick;
     __shared__ float s_prefix[kWT];
+    // for each node v: its acceptance uniform, and the target and draft logits
+    // of its token at its parent (gathered once, so a child's test reads no memory)
+    __shared__ float s_ua[kMaxTreeT], s_lt[kMaxTreeT], s_ld[kMaxTreeT];
     griddep_wait();
     griddep_launch_dependents();
     const int C = p.walk_cluster;
@@ -1427,37 +1430,65 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     const int tb_raw = a.node_counts ? a.node_counts[b] : nT;
     const bool tb_ok = tb_raw >= 1 && tb_raw <= nT;
     const int nb = tb_ok ? tb_raw : 1;
-    for (int i = tid; i < nT; i += kWT) {
+    for (int i = tid; i < nb; i += kWT) {
         s_par[i] = a.parents ? a.parents[(size_t)b * nT + i] : i - 1;  // NULL: a chain
         s_tok[i] = a.tokens[(size_t)b * nT + i];
+        s_ua[i] = i > 0 ? a.u_accept[(size_t)b * nT + i] : 0.f;
         s_child[i] = 0;
     }
     if (tid == 0) s_bad = tb_ok ? 0 : 1;
+    // merge the records of the target and draft rows of the first T_b nodes
+    // (a row that is not read has the empty record), kRB rows a warp at once
+    // so that their loads are in flight together; each row's merge order is
+    // fixed: its lane's chunks in order, then the lanes by xor shuffles
+    constexpr int kRB = 8;
+    for (int rb = warp * kRB; rb < 2 * nT; rb += kWWarps * kRB) {
+        float m[kRB], s[kRB];
+#pragma unroll
+        for (int j = 0; j < kRB; ++j) {
+            m[j] = kNegInf;
+            s[j] = 0.f;
+        }
+        for (int c = lane; c < p.nchunks; c += 32) {
+            float2 r2[kRB];
+#pragma unroll
+            for (int j = 0; j < kRB; ++j) {
+                const int rr = rb + j;
+                const bool live = rr < 2 * nT && (rr < nT ? rr : rr - nT) < nb;
+                r2[j] = live ? __ldcg(rec + ((size_t)b * 2 * nT + rr) * p.nchunks + c)
+                             : make_float2(kNegInf, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kRB; ++j) merge_ms(m[j], s[j], r2[j].x, r2[j].y);
+        }
+#pragma unroll
+        for (int j = 0; j < kRB; ++j) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                merge_ms(m[j], s[j], __shfl_xor_sync(0xffffffffu, m[j], off),
+                         __shfl_xor_sync(0xffffffffu, s[j], off));
+            const int rr = rb + j, u = rr < nT ? rr : rr - nT;
+            if (lane == 0 && rr < 2 * nT && u < nb) s_ms[rr < nT ? 0 : 1][u] = make_float2(m[j], s[j]);
+        }
+    }
     __syncthreads();
     for (int i = 1 + tid; i < nb; i += kWT) {
-        const int pa = s_par[i];
-        if (pa < 0 || pa >= i || s_tok[i] < 0 || s_tok[i] >= V) s_bad = 1;
-        else s_child[pa] = 1;
+        const int pa = s_par[i], x = s_tok[i];
+        if (pa < 0 || pa >= i || x < 0 || x >= V) {
+            s_bad = 1;
+        } else {
+            s_child[pa] = 1;
+            s_lt[i] = Elem<T>::at(static_cast<const T *>(a.target) + ((size_t)b * nT + pa) * V, x);
+            s_ld[i] = Elem<T>::at(static_cast<const T *>(a.draft) + ((size_t)b * nT + pa) * V, x);
+        }
     }
     if (tid == 0 && s_par[0] != -1) s_bad = 1;
     __syncthreads();
-    // merge the records of each used row; a row without a finite distribution is bad input
-    for (int rr = warp; rr < 2 * nT; rr += kWWarps) {
-        const int u = rr < nT ? rr : rr - nT;
-        if (u >= nb || (rr >= nT && !s_child[u])) continue;
-        float m = kNegInf, s = 0.f;
-        for (int c = lane; c < p.nchunks; c += 32) {
-            const float2 r2 = __ldcg(rec + ((size_t)b * 2 * nT + rr) * p.nchunks + c);
-            merge_ms(m, s, r2.x, r2.y);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            merge_ms(m, s, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, s, off));
-        if (lane == 0) {
-            s_ms[rr < nT ? 0 : 1][u] = make_float2(m, s);
-            if (!(isfinite(m) && isfinite(s) && s > 0.f)) s_bad = 1;
-        }
-    }
+    // a used row (every target row, the draft rows of nodes with children)
+    // without a finite distribution is bad input
+    auto finite_ms = [](float2 v) { return isfinite(v.x) && isfinite(v.y) && v.y > 0.f; };
+    for (int u = tid; u < nb; u += kWT)
+        if (!finite_ms(s_ms[0][u]) || (s_child[u] && !finite_ms(s_ms[1][u]))) s_bad = 1;
     __syncthreads();
     // every CTA reaches the same verdict from the same inputs, so all of them
     // take the same path through the cluster barriers below
@@ -1470,26 +1501,36 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     int pass = 0;
     // the cluster's sum of one value per thread: CTA sums in a fixed order,
     // then the CTAs in rank order (every CTA gets the same total)
+    // (lane k of every warp reads CTA k's sum, all C loads in flight together;
+    // `part` keeps it for the final draw's search)
+    float part = 0.f;
     auto cluster_total = [&](float v, float *cta_total) -> float {
         const float t = walk_block_sum(v, s_red);
         if (cta_total) *cta_total = t;
         if (tid == 0) s_part[pass & 1] = t;
         cluster_sync();
+        part = lane < C ? ld_shared_cluster_f32(&s_part[pass & 1], (uint32_t)lane) : 0.f;
         float tot = 0.f;
-        for (int k = 0; k < C; ++k) tot = __fadd_rn(tot, ld_shared_cluster_f32(&s_part[pass & 1], (uint32_t)k));
+        for (int k = 0; k < C; ++k) tot = __fadd_rn(tot, __shfl_sync(0xffffffffu, part, k));
         ++pass;  // the other buffer next: a CTA may run ahead into the next pass
         return tot;
     };
     int depth = 0, u = 0;
     if (!bad) {
         for (int step = 0; step < nb; ++step) {
-            // children of u in index order
-            if (tid == 0) {
+            // children of u in index order (warp 0, 32 nodes a ballot)
+            if (warp == 0) {
                 int n = 0;
-                for (int v = u + 1; v < nb; ++v)
-                    if (s_par[v] == u) s_kids[n++] = v;
-                s_nkids = n;
-                s_next = -1;
+                for (int v0 = u + 1; v0 < nb; v0 += 32) {
+                    const bool kid = v0 + lane < nb && s_par[v0 + lane] == u;
+                    const unsigned mk = __ballot_sync(0xffffffffu, kid);
+                    if (kid) s_kids[n + __popc(mk & ((1u << lane) - 1u))] = v0 + lane;
+                    n += __popc(mk);
+                }
+                if (lane == 0) {
+                    s_nkids = n;
+                    s_next = -1;
+                }
             }
             __syncthreads();
             const int nk = s_nkids;
@@ -1509,11 +1550,10 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
                                                          nullptr);
                 const int v = s_kids[i];
                 if (tid == 0) {
-                    const int x = s_tok[v];
-                    const float px = __fdiv_rn(exp2_diff_accurate(Elem<T>::at(trow, x), rs.mt), s_ms[0][u].y);
-                    const float qx = __fdiv_rn(exp2_diff_accurate(Elem<T>::at(drow, x), rs.md), s_ms[1][u].y);
+                    const float px = __fdiv_rn(exp2_diff_accurate(s_lt[v], rs.mt), s_ms[0][u].y);
+                    const float qx = __fdiv_rn(exp2_diff_accurate(s_ld[v], rs.md), s_ms[1][u].y);
                     const float r = fmaxf(__fsub_rn(px, __fmul_rn(c, qx)), 0.f);
-                    const float lhs = __fmul_rn(__fmul_rn(a.u_accept[(size_t)b * nT + v], qx), n);
+                    const float lhs = __fmul_rn(__fmul_rn(s_ua[v], qx), n);
                     if (lhs < r) s_next = v;
                 }
                 __syncthreads();
@@ -1543,11 +1583,10 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
             const float theta = __fmul_rn(a.u_sample[b], S);
             // the CTA where the cluster prefix passes theta (rank order; the
             // same search in every CTA)
-            const int pb = (pass - 1) & 1;  // the buffer of the last pass
             int kstar = -1, klast = 0;
             float base = 0.f, run = 0.f;
             for (int k = 0; k < C; ++k) {
-                const float t = ld_shared_cluster_f32(&s_part[pb], (uint32_t)k);
+                const float t = __shfl_sync(0xffffffffu, part, k);  // CTA k's sum in the last pass
                 if (t > 0.f) klast = k;
                 const float nb2 = __fadd_rn(run, t);
                 if (kstar < 0 && nb2 > theta) {
@@ -1561,8 +1600,7 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
                 fallback = true;
                 kstar = klast;
                 base = 0.f;
-                for (int k = 0; k < kstar; ++k)
-                    base = __fadd_rn(base, ld_shared_cluster_f32(&s_part[pb], (uint32_t)k));
+                for (int k = 0; k < kstar; ++k) base = __fadd_rn(base, __shfl_sync(0xffffffffu, part, k));
             }
             if (rank == kstar) {
                 // inclusive prefix of this CTA's thread sums (warp scan, then the warps in order)
