@@ -1438,38 +1438,23 @@ __global__ void __launch_bounds__(kWT) stree_walk_kernel(STreeArgs a, VocabPlan 
     }
     if (tid == 0) s_bad = tb_ok ? 0 : 1;
     // merge the records of the target and draft rows of the first T_b nodes
-    // (a row that is not read has the empty record), kRB rows a warp at once
-    // so that their loads are in flight together; each row's merge order is
-    // fixed: its lane's chunks in order, then the lanes by xor shuffles
-    constexpr int kRB = 8;
-    for (int rb = warp * kRB; rb < 2 * nT; rb += kWWarps * kRB) {
-        float m[kRB], s[kRB];
+    // (a row that is not read has the empty record): a thread a row, its
+    // chunks in order, eight records in flight (short code: it runs once per
+    // launch, fetched cold)
+    for (int rr = tid; rr < 2 * nT; rr += kWT) {
+        const int u = rr < nT ? rr : rr - nT;
+        if (u >= nb) continue;
+        const float2 *r0 = rec + ((size_t)b * 2 * nT + rr) * p.nchunks;
+        float m = kNegInf, s = 0.f;
+        for (int c0 = 0; c0 < p.nchunks; c0 += 8) {
+            float2 r2[8];
 #pragma unroll
-        for (int j = 0; j < kRB; ++j) {
-            m[j] = kNegInf;
-            s[j] = 0.f;
+            for (int j = 0; j < 8; ++j)
+                r2[j] = c0 + j < p.nchunks ? __ldcg(r0 + c0 + j) : make_float2(kNegInf, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) merge_ms(m, s, r2[j].x, r2[j].y);
         }
-        for (int c = lane; c < p.nchunks; c += 32) {
-            float2 r2[kRB];
-#pragma unroll
-            for (int j = 0; j < kRB; ++j) {
-                const int rr = rb + j;
-                const bool live = rr < 2 * nT && (rr < nT ? rr : rr - nT) < nb;
-                r2[j] = live ? __ldcg(rec + ((size_t)b * 2 * nT + rr) * p.nchunks + c)
-                             : make_float2(kNegInf, 0.f);
-            }
-#pragma unroll
-            for (int j = 0; j < kRB; ++j) merge_ms(m[j], s[j], r2[j].x, r2[j].y);
-        }
-#pragma unroll
-        for (int j = 0; j < kRB; ++j) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                merge_ms(m[j], s[j], __shfl_xor_sync(0xffffffffu, m[j], off),
-                         __shfl_xor_sync(0xffffffffu, s[j], off));
-            const int rr = rb + j, u = rr < nT ? rr : rr - nT;
-            if (lane == 0 && rr < 2 * nT && u < nb) s_ms[rr < nT ? 0 : 1][u] = make_float2(m[j], s[j]);
-        }
+        s_ms[rr < nT ? 0 : 1][u] = make_float2(m, s);
     }
     __syncthreads();
     for (int i = 1 + tid; i < nb; i += kWT) {
