@@ -52,6 +52,8 @@ MUTANTS = [
      "const double lhs = (double)u_accept[(size_t)b * T + v] * qu[x] * n;",
      "const double lhs = (double)u_accept[(size_t)b * T + v] * qu[x];",
      [lambda o: TS.test_first_token_follows_target_at_root(3, 3.0)]),
+    ("residual constant carried from the parent node", "            c = 0.0;\n            int next = -1;",
+     "            int next = -1;", [lambda o: TS.test_later_tokens_follow_target_below_the_root()]),
     ("tree's final draw from p after rejections",
      "w[k] = c == 0.0 ? pu[k] : (d > 0.0 ? d : 0.0);", "w[k] = pu[k];",
      [lambda o: TS.test_chain_tree_equals_chain_rule(64, 4, 300, "f32", 1),

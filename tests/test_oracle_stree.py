@@ -7,6 +7,9 @@ target choose among drafted paths without a rule):
 - the first emitted token is distributed as the target's p at the root when
   the root's children are drawn i.i.d. from q (chi-square over 2e5 trials):
   a residual that is not updated between siblings fails it;
+- below the root, given the accepted path so far, the next emitted token is
+  distributed as the target's p at the accepted node (a two-level tree): a
+  residual carried over from the parent node fails it;
 - a draft equal to the target accepts the first child at every node;
 - structural invariants of the outputs."""
 import numpy as np
@@ -123,3 +126,39 @@ def test_bad_inputs_reported():
                                       rng.random(B, dtype=np.float32))
     assert r["status"].tolist() == [0, 6, 6]
     assert (r["accepted_len"][1:] == -1).all()
+
+
+def test_later_tokens_follow_target_below_the_root():
+    """A two-level tree, two children a node, each node's children drawn
+    i.i.d. from the drafter at that node, every node of a level with the same
+    rows.  Given that a first-level child was accepted, the second emitted
+    token follows the target at the first level, and given a second-level
+    child, the third follows the target at the leaves: the residual restarts
+    at every accepted node (chi-square over 2e5 trials)."""
+    rng = np.random.default_rng(31)
+    V, n = 6, 200_000
+    par = np.array([-1, 0, 0, 1, 1, 2, 2], np.int32)
+    T = len(par)
+    z = [(rng.standard_normal(V) * 1.5).astype(np.float32) for _ in range(3)]
+    d = [(z[k] + rng.standard_normal(V)).astype(np.float32) for k in range(2)]
+    level = [0, 1, 1, 2, 2, 2, 2]
+    rows_t = np.stack([z[lv] for lv in level])
+    rows_d = np.stack([d[min(lv, 1)] for lv in level])  # the leaves' draft rows are not used
+    p = [special.softmax(zk.astype(np.float64)) for zk in z]
+    q = [special.softmax(dk.astype(np.float64)) for dk in d]
+    tok = np.zeros((n, T), np.int32)
+    tok[:, 1:3] = rng.choice(V, size=(n, 2), p=q[0])
+    tok[:, 3:7] = rng.choice(V, size=(n, 4), p=q[1])
+    r = oracle.verify_tree_stochastic(np.broadcast_to(rows_t, (n, T, V)).copy(),
+                                      np.broadcast_to(rows_d, (n, T, V)).copy(), tok,
+                                      np.broadcast_to(par, (n, T)).copy(),
+                                      rng.random((n, T), dtype=np.float32),
+                                      rng.random(n, dtype=np.float32))
+    acc = r["accepted_len"]
+    assert (r["status"] == 0).all() and acc.max() == 2
+    for depth in (1, 2):
+        sel = acc >= depth
+        assert sel.mean() > 0.1, (depth, sel.mean())
+        obs = np.bincount(r["out_tokens"][sel, depth], minlength=V)
+        chi = stats.chisquare(obs, p[depth] * sel.sum())
+        assert chi.pvalue > 1e-3, (depth, chi, obs / sel.sum(), p[depth])
