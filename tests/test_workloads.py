@@ -137,3 +137,21 @@ def test_workloads_are_deterministic_and_seeded():
     # sigma of the recipe: target ~ N(0, 3^2) away from the boosted token
     t = W.bf16_bits_to_f32(a["target"]).astype(np.float64)
     assert abs(np.median(np.abs(t)) / 0.6745 - 3.0) < 0.05
+
+
+@pytest.mark.parametrize("page_size", [8, 16, 128])
+def test_paged_cache_round_trip(page_size):
+    """Scattering a cache into pages and gathering it back is the identity;
+    the page table is a permutation of distinct pages; spare pages and page
+    slots past S_max stay NaN."""
+    a = W.attention_inputs(3, 4, 8, 2, 128, [30, 5, 50], S_max=70, seed=9, unused_fill="zero")
+    kp, vp, table = W.paged_cache(a["k"], a["v"], page_size, seed=10, spare_pages=3)
+    np.testing.assert_array_equal(W.gather_paged(kp, table, 70), a["k"])
+    np.testing.assert_array_equal(W.gather_paged(vp, table, 70), a["v"])
+    assert len(np.unique(table)) == table.size and table.min() >= 0 and table.max() < len(kp)
+    spare = np.setdiff1d(np.arange(len(kp)), table.ravel())
+    assert len(spare) == 3 and np.isnan(W.bf16_bits_to_f32(kp[spare])).all()
+    tail = 70 % page_size
+    if tail:  # the last page of each sequence holds S_max's remainder, then NaN
+        last = table[:, -1]
+        assert np.isnan(W.bf16_bits_to_f32(kp[last][:, :, tail:])).all()
