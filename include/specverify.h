@@ -81,7 +81,8 @@ typedef enum sv_op {
  *   SV_OP_VERIFY_CHAIN:       B, N (as T_or_N), V, dtype as Hq (0 f32 / 1 bf16)
  *   SV_OP_VERIFY_TREE_GREEDY: B, T, V, dtype as Hq
  *   SV_OP_VERIFY_TREE_STOCHASTIC: B, T, V, dtype as Hq
- * Returns 0 for invalid arguments.
+ * Returns 0 for invalid arguments and for shapes the call refuses as
+ * SV_ERR_UNSUPPORTED.
  */
 size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, int D);
 

@@ -43,11 +43,18 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
         case SV_OP_VERIFY_CHAIN:
         case SV_OP_VERIFY_TREE_GREEDY: {
             if (V <= 0 || (Hq != SV_F32 && Hq != SV_BF16)) return 0;
-            return sv::plan_vocab(op == SV_OP_VERIFY_CHAIN, B, T_or_N, V, Hq).bytes;
+            // the shapes the calls refuse as unsupported have no size
+            if (T_or_N > (op == SV_OP_VERIFY_CHAIN ? 63 : 1024) || V >= (1 << 30)) return 0;
+            const sv::VocabPlan pl = sv::plan_vocab(op == SV_OP_VERIFY_CHAIN, B, T_or_N, V, Hq);
+            if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return 0;
+            return pl.bytes;
         }
         case SV_OP_VERIFY_TREE_STOCHASTIC: {
             if (V <= 0 || (Hq != SV_F32 && Hq != SV_BF16)) return 0;
-            return sv::plan_vocab_stree(B, T_or_N, V, Hq).bytes;
+            if (T_or_N > 1024 || V > (1 << 22)) return 0;
+            const sv::VocabPlan pl = sv::plan_vocab_stree(B, T_or_N, V, Hq);
+            if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return 0;
+            return pl.bytes;
         }
     }
     return 0;

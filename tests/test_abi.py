@@ -155,3 +155,20 @@ def test_workspace_sizes_scale_with_shape(L):
     assert 0 < a < b
     assert L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 0, 8, 1000, sv.SV_BF16, 0, 0) == 0
     assert L.sv_workspace_size(sv.SV_OP_VERIFY_CHAIN, 1, 8, 1000, 5, 0, 0) == 0
+
+
+@pytest.mark.parametrize("op,T,V", [
+    (sv.SV_OP_VERIFY_CHAIN, 64, 1000),                   # N > 63
+    (sv.SV_OP_VERIFY_CHAIN, 8, 1 << 30),
+    (sv.SV_OP_VERIFY_TREE_GREEDY, 1025, 1000),
+    (sv.SV_OP_VERIFY_TREE_GREEDY, (1 << 31) - 1, 1000),  # 2T would overflow an int
+    (sv.SV_OP_VERIFY_TREE_STOCHASTIC, 1025, 1000),
+    (sv.SV_OP_VERIFY_TREE_STOCHASTIC, (1 << 31) - 1, 1000),
+    (sv.SV_OP_VERIFY_TREE_STOCHASTIC, 8, (1 << 22) + 1),
+])
+def test_workspace_size_is_zero_for_unsupported_shapes(L, op, T, V):
+    assert L.sv_workspace_size(op, 2, T, V, sv.SV_BF16, 0, 0) == 0
+    # the largest supported sizes still get a workspace
+    top = {sv.SV_OP_VERIFY_CHAIN: (63, (1 << 30) - 1), sv.SV_OP_VERIFY_TREE_GREEDY: (1024, 1 << 22),
+           sv.SV_OP_VERIFY_TREE_STOCHASTIC: (1024, 1 << 22)}[op]
+    assert L.sv_workspace_size(op, 1, top[0], top[1], sv.SV_BF16, 0, 0) > 0
