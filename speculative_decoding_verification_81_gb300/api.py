@@ -110,13 +110,32 @@ def _dtype_code(t):
     raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
 
 
+def _on_device(t):
+    return t.is_cuda
+
+
 def _req(t, name, dtype=None, ndim=None):
-    if not t.is_cuda or not t.is_contiguous():
+    if not _on_device(t) or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def _shape(t, name, shape):
+    """The kernels index every array by the call's sizes: a tensor of another
+    shape would be read or written out of bounds, so it is refused here."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _opt(t, name, dtype, shape):
+    """An optional array (an input or a caller-provided output): checked when given."""
+    if t is not None:
+        _shape(_req(t, name, dtype, len(shape)), name, shape)
     return t
 
 
@@ -155,16 +174,19 @@ def sv_tree_attention(q, k_cache, v_cache, prefix_lens, parents=None, scale=None
     _req(prefix_lens, "prefix_lens", torch.int32, 1)
     B, T, Hq, D = q.shape
     _, Hkv, S_max, _ = k_cache.shape
-    if parents is not None:
-        _req(parents, "parents", torch.int32, 2)
+    _shape(k_cache, "k_cache", (B, Hkv, S_max, D))
+    _shape(v_cache, "v_cache", k_cache.shape)
+    _shape(prefix_lens, "prefix_lens", (B,))
+    _opt(parents, "parents", torch.int32, (B, T))
+    _opt(node_counts, "node_counts", torch.int32, (B,))
+    _opt(out, "out", torch.bfloat16, q.shape)
+    _opt(seq_status, "seq_status", torch.int32, (B,))
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
     if ws is None:
         ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
-    if node_counts is not None:
-        _req(node_counts, "node_counts", torch.int32, 1)
     rc = lib().sv_tree_attention(_p(q), _p(k_cache), _p(v_cache), _p(prefix_lens), _p(parents),
                                  _p(node_counts), B, T, Hq, Hkv, D, S_max, float(scale), _p(out),
                                  _p(seq_status), _p(ws), ws.numel(), _stream(stream))
@@ -186,22 +208,38 @@ def sv_tree_attention_paged(q, k_pages, v_pages, block_table, prefix_lens, paren
     B, T, Hq, D = q.shape
     num_pages, Hkv, page_size, _ = k_pages.shape
     max_pages = block_table.shape[1]
-    if parents is not None:
-        _req(parents, "parents", torch.int32, 2)
+    _shape(k_pages, "k_pages", (num_pages, Hkv, page_size, D))
+    _shape(v_pages, "v_pages", k_pages.shape)
+    _shape(block_table, "block_table", (B, max_pages))
+    _shape(prefix_lens, "prefix_lens", (B,))
+    _opt(parents, "parents", torch.int32, (B, T))
+    _opt(node_counts, "node_counts", torch.int32, (B,))
+    _opt(out, "out", torch.bfloat16, q.shape)
+    _opt(seq_status, "seq_status", torch.int32, (B,))
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
     if ws is None:
         ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
-    if node_counts is not None:
-        _req(node_counts, "node_counts", torch.int32, 1)
     rc = lib().sv_tree_attention_paged(_p(q), _p(k_pages), _p(v_pages), _p(block_table), max_pages,
                                        num_pages, page_size, _p(prefix_lens), _p(parents),
                                        _p(node_counts), B, T, Hq, Hkv, D, float(scale), _p(out),
                                        _p(seq_status), _p(ws), ws.numel(), _stream(stream))
     _check("sv_tree_attention_paged", rc)
     return out
+
+
+def _chain_shapes(B, N, V, draft_logits, draft_tokens, u_accept, u_sample, accepted_len,
+                  out_tokens, probs_out, seq_status):
+    _shape(draft_logits, "draft_logits", (B, N, V))
+    _shape(draft_tokens, "draft_tokens", (B, N))
+    _shape(u_accept, "u_accept", (B, N))
+    _shape(u_sample, "u_sample", (B,))
+    _opt(accepted_len, "accepted_len", torch.int32, (B,))
+    _opt(out_tokens, "out_tokens", torch.int32, (B, N + 1))
+    _opt(probs_out, "probs_out", torch.float32, (B, N, 2))
+    _opt(seq_status, "seq_status", torch.int32, (B,))
 
 
 def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sample,
@@ -215,11 +253,12 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
     _req(draft_tokens, "draft_tokens", torch.int32, 2)
     _req(u_accept, "u_accept", torch.float32, 2)
     _req(u_sample, "u_sample", torch.float32, 1)
-    if draft_lens is not None:
-        _req(draft_lens, "draft_lens", torch.int32, 1)
     dt = _dtype_code(target_logits)
     B, N1, V = target_logits.shape
     N = N1 - 1
+    _chain_shapes(B, N, V, draft_logits, draft_tokens, u_accept, u_sample, accepted_len,
+                  out_tokens, probs_out, seq_status)
+    _opt(draft_lens, "draft_lens", torch.int32, (B,))
     dev = target_logits.device
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
@@ -235,6 +274,17 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
     return accepted_len, out_tokens
 
 
+def _tree_shapes(B, T, node_tokens, parents, node_counts, accepted_len, path_nodes, out_tokens,
+                 seq_status):
+    _shape(node_tokens, "node_tokens", (B, T))
+    _opt(parents, "parents", torch.int32, (B, T))
+    _opt(node_counts, "node_counts", torch.int32, (B,))
+    _opt(accepted_len, "accepted_len", torch.int32, (B,))
+    _opt(path_nodes, "path_nodes", torch.int32, (B, T))
+    _opt(out_tokens, "out_tokens", torch.int32, (B, T))
+    _opt(seq_status, "seq_status", torch.int32, (B,))
+
+
 def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None, path_nodes=None,
                           out_tokens=None, seq_status=None, ws=None, stream=None,
                           node_counts=None):
@@ -244,12 +294,10 @@ def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None
     Returns (accepted_len [B], path_nodes [B,T], out_tokens [B,T])."""
     _req(target_logits, "target_logits", None, 3)
     _req(node_tokens, "node_tokens", torch.int32, 2)
-    if parents is not None:
-        _req(parents, "parents", torch.int32, 2)
-    if node_counts is not None:
-        _req(node_counts, "node_counts", torch.int32, 1)
     dt = _dtype_code(target_logits)
     B, T, V = target_logits.shape
+    _tree_shapes(B, T, node_tokens, parents, node_counts, accepted_len, path_nodes, out_tokens,
+                 seq_status)
     dev = target_logits.device
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
@@ -278,14 +326,15 @@ def sv_verify_tree_stochastic(target_logits, draft_logits, node_tokens, parents,
     _req(target_logits, "target_logits", None, 3)
     _req(draft_logits, "draft_logits", target_logits.dtype, 3)
     _req(node_tokens, "node_tokens", torch.int32, 2)
-    if parents is not None:
-        _req(parents, "parents", torch.int32, 2)
     _req(u_accept, "u_accept", torch.float32, 2)
     _req(u_sample, "u_sample", torch.float32, 1)
-    if node_counts is not None:
-        _req(node_counts, "node_counts", torch.int32, 1)
     dt = _dtype_code(target_logits)
     B, T, V = target_logits.shape
+    _shape(draft_logits, "draft_logits", (B, T, V))
+    _shape(u_accept, "u_accept", (B, T))
+    _shape(u_sample, "u_sample", (B,))
+    _tree_shapes(B, T, node_tokens, parents, node_counts, accepted_len, path_nodes, out_tokens,
+                 seq_status)
     dev = target_logits.device
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
@@ -313,9 +362,15 @@ def sv_compact_kv(k_cache, v_cache, prefix_lens, accepted_len, path_nodes=None, 
     _req(prefix_lens, "prefix_lens", torch.int32, 1)
     _req(accepted_len, "accepted_len", torch.int32, 1)
     B, Hkv, S_max, D = k_cache.shape
+    _shape(v_cache, "v_cache", k_cache.shape)
+    _shape(prefix_lens, "prefix_lens", (B,))
+    _shape(accepted_len, "accepted_len", (B,))
+    _opt(new_kv_lens, "new_kv_lens", torch.int32, (B,))
+    _opt(seq_status, "seq_status", torch.int32, (B,))
     stride = 0
     if path_nodes is not None:
         _req(path_nodes, "path_nodes", torch.int32, 2)
+        _shape(path_nodes, "path_nodes", (B, path_nodes.shape[1]))
         stride = path_nodes.shape[1]
     if new_kv_lens is None:
         new_kv_lens = torch.empty_like(prefix_lens)
@@ -338,9 +393,15 @@ def sv_compact_kv_paged(k_pages, v_pages, block_table, prefix_lens, accepted_len
     _req(accepted_len, "accepted_len", torch.int32, 1)
     num_pages, Hkv, page_size, D = k_pages.shape
     B, max_pages = block_table.shape
+    _shape(v_pages, "v_pages", k_pages.shape)
+    _shape(prefix_lens, "prefix_lens", (B,))
+    _shape(accepted_len, "accepted_len", (B,))
+    _opt(new_kv_lens, "new_kv_lens", torch.int32, (B,))
+    _opt(seq_status, "seq_status", torch.int32, (B,))
     stride = 0
     if path_nodes is not None:
         _req(path_nodes, "path_nodes", torch.int32, 2)
+        _shape(path_nodes, "path_nodes", (B, path_nodes.shape[1]))
         stride = path_nodes.shape[1]
     if new_kv_lens is None:
         new_kv_lens = torch.empty_like(prefix_lens)
@@ -366,6 +427,8 @@ def sv_verify_chain_noalloc(target_logits, draft_logits, draft_tokens, u_accept,
     _req(out_tokens, "out_tokens", torch.int32, 2)
     dt = _dtype_code(target_logits)
     B, N1, V = target_logits.shape
+    _chain_shapes(B, N1 - 1, V, draft_logits, draft_tokens, u_accept, u_sample, accepted_len,
+                  out_tokens, probs_out, seq_status)
     rc = lib().sv_verify_chain_noalloc(_p(target_logits), _p(draft_logits), dt, _p(draft_tokens),
                                        _p(u_accept), _p(u_sample), B, N1 - 1, V,
                                        _p(accepted_len), _p(out_tokens), _p(probs_out),
