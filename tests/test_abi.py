@@ -172,3 +172,42 @@ def test_workspace_size_is_zero_for_unsupported_shapes(L, op, T, V):
     top = {sv.SV_OP_VERIFY_CHAIN: (63, (1 << 30) - 1), sv.SV_OP_VERIFY_TREE_GREEDY: (1024, 1 << 22),
            sv.SV_OP_VERIFY_TREE_STOCHASTIC: (1024, 1 << 22)}[op]
     assert L.sv_workspace_size(op, 1, top[0], top[1], sv.SV_BF16, 0, 0) > 0
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "specverify.h"
+
+int main(void) {
+    int32_t acc[2], out[10];
+    size_t ws;
+    if (sv_version() < 100) return 1;
+    if (strncmp(sv_status_string(SV_ERR_BAD_INPUT), "SV_ERR_BAD_INPUT", 16) != 0) return 2;
+    ws = sv_workspace_size(SV_OP_VERIFY_TREE_STOCHASTIC, 2, 26, 32000, SV_BF16, 0, 0);
+    if (ws == 0 || sv_workspace_size(SV_OP_VERIFY_CHAIN, 0, 4, 1000, SV_BF16, 0, 0) != 0) return 3;
+    /* host-side validation answers before any launch: no GPU is needed */
+    if (sv_verify_chain(NULL, NULL, SV_BF16, NULL, NULL, NULL, NULL, 2, 4, 1000, acc, out, NULL,
+                        NULL, NULL, 0, (sv_stream_t)0) != SV_ERR_INVALID_ARG) return 4;
+    if (sv_compact_kv(NULL, NULL, NULL, NULL, NULL, 0, NULL, 1, 1, 128, 16, NULL,
+                      (sv_stream_t)0) != SV_ERR_INVALID_ARG) return 5;
+    printf("ok %zu\n", ws);
+    return 0;
+}
+"""
+
+
+def test_plain_c_program_uses_the_header_and_library(L, tmp_path):
+    """The header is plain C99 (no C++ and no CUDA headers needed), and a C
+    program links against the library and gets the documented answers."""
+    import subprocess
+    src = tmp_path / "use_api.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_api"
+    libdir = os.path.dirname(svbuild.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                           f"-I{os.path.dirname(HEADER)}", str(src), f"-L{libdir}", "-lspecverify",
+                           f"-Wl,-rpath,{libdir}", "-o", str(exe)])
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.startswith("ok ")
