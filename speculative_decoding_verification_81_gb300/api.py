@@ -57,31 +57,44 @@ def lib() -> ctypes.CDLL:
             raise ImportError(f"libspecverify.so is not built ({_build.LIB_PATH}); "
                               "run __graft_entry__.build() or python -m "
                               "speculative_decoding_verification_81_gb300.build")
-        L = ctypes.CDLL(_build.LIB_PATH)
-        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-        L.sv_workspace_size.argtypes = [I, I, I, I, I, I, I]
-        L.sv_workspace_size.restype = Z
-        L.sv_tree_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P,
-                                        Z, P]
-        L.sv_verify_chain.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, P, P, P, Z, P]
-        L.sv_verify_tree_greedy.argtypes = [P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
-        L.sv_verify_chain_noalloc.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
-        L.sv_compact_kv.argtypes = [P, P, P, P, P, I, P, I, I, I, I, P, P]
-        L.sv_tree_attention_paged.argtypes = [P, P, P, P, I, I, I, P, P, P, I, I, I, I, I,
-                                              ctypes.c_float, P, P, P, Z, P]
-        L.sv_compact_kv_paged.argtypes = [P, P, P, I, I, I, P, P, P, I, P, I, I, I, P, P]
-        L.sv_verify_tree_stochastic.argtypes = [P, P, I, P, P, P, P, P, I, I, I, P, P, P, P, P, Z,
-                                                P]
-        for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
-                   "sv_verify_chain_noalloc", "sv_tree_attention_paged", "sv_compact_kv_paged",
-                   "sv_verify_tree_stochastic"):
-            getattr(L, fn).restype = I
-        L.sv_status_string.argtypes = [I]
-        L.sv_status_string.restype = ctypes.c_char_p
-        L.sv_version.argtypes = []
-        L.sv_version.restype = I
-        _lib = L
+        _lib = load(_build.LIB_PATH)
     return _lib
+
+
+def use_library(path: str) -> ctypes.CDLL:
+    """Route every call of this module to the library at `path` (a build of
+    the same sources, e.g. the phase-stamped one of the ``phases`` tool)."""
+    global _lib
+    _lib = load(path)
+    return _lib
+
+
+def load(path: str) -> ctypes.CDLL:
+    """Load a build of libspecverify and declare its entry points' C types."""
+    L = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.sv_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    L.sv_workspace_size.restype = Z
+    L.sv_tree_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P,
+                                    Z, P]
+    L.sv_verify_chain.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+    L.sv_verify_tree_greedy.argtypes = [P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+    L.sv_verify_chain_noalloc.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
+    L.sv_compact_kv.argtypes = [P, P, P, P, P, I, P, I, I, I, I, P, P]
+    L.sv_tree_attention_paged.argtypes = [P, P, P, P, I, I, I, P, P, P, I, I, I, I, I,
+                                          ctypes.c_float, P, P, P, Z, P]
+    L.sv_compact_kv_paged.argtypes = [P, P, P, I, I, I, P, P, P, I, P, I, I, I, P, P]
+    L.sv_verify_tree_stochastic.argtypes = [P, P, I, P, P, P, P, P, I, I, I, P, P, P, P, P, Z,
+                                            P]
+    for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
+               "sv_verify_chain_noalloc", "sv_tree_attention_paged", "sv_compact_kv_paged",
+               "sv_verify_tree_stochastic"):
+        getattr(L, fn).restype = I
+    L.sv_status_string.argtypes = [I]
+    L.sv_status_string.restype = ctypes.c_char_p
+    L.sv_version.argtypes = []
+    L.sv_version.restype = I
+    return L
 
 
 def status_string(status: int) -> str:

@@ -37,7 +37,8 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
         case SV_OP_TREE_ATTENTION: {
             if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
             sv::AttnPlan pl;
-            if (sv::plan_attention(B, T_or_N, Hq, Hkv, D, &pl) != SV_OK) return 0;
+            // (the workspace does not depend on the cache length)
+            if (sv::plan_attention(B, T_or_N, Hq, Hkv, D, 1 << 30, &pl) != SV_OK) return 0;
             return pl.bytes;
         }
         case SV_OP_VERIFY_CHAIN:
@@ -72,7 +73,7 @@ sv_status sv_tree_attention(const void *q, const void *k_cache, const void *v_ca
         return SV_ERR_INVALID_ARG;
     if ((long long)B * Hkv * S_max >= (1LL << 31)) return SV_ERR_UNSUPPORTED;
     sv::AttnPlan pl;
-    const sv_status st = sv::plan_attention(B, T, Hq, Hkv, D, &pl);
+    const sv_status st = sv::plan_attention(B, T, Hq, Hkv, D, S_max, &pl);
     if (st != SV_OK) return st;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
     sv::AttnArgs a{q,   k_cache, v_cache, prefix_lens, parents,    B,       T, Hq, Hkv, D,
@@ -104,7 +105,7 @@ sv_status sv_tree_attention_paged(const void *q, const void *k_pages, const void
     if ((long long)num_pages * Hkv * page_size >= (1LL << 31) || S_max >= (1LL << 30))
         return SV_ERR_UNSUPPORTED;
     sv::AttnPlan pl;
-    const sv_status st = sv::plan_attention(B, T, Hq, Hkv, D, &pl);
+    const sv_status st = sv::plan_attention(B, T, Hq, Hkv, D, (int)S_max, &pl);
     if (st != SV_OK) return st;
     if (!workspace || workspace_bytes < pl.bytes || !aligned16(workspace)) return SV_ERR_WORKSPACE;
     sv::AttnArgs a{q,  k_pages, v_pages, prefix_lens, parents,     B,         T,        Hq,

@@ -99,6 +99,41 @@ static int cached_occupancy(const void *fn, int threads, int max_smem, int smem,
     return occ;
 }
 
+// Largest number of clusters of `cs` CTAs of the attention kernel that the
+// current device keeps resident at once (0 if none), cached like the occupancy.
+static int cached_max_clusters(const void *fn, int smem, int cs) {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int smem, cs, n;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int ncache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ncache; ++i)
+        if (cache[i].dev == dev && cache[i].fn == fn && cache[i].smem == smem && cache[i].cs == cs)
+            return cache[i].n;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    cudaGetLastError();  // a refused query leaves no error behind
+    if (ncache < 64) cache[ncache++] = Entry{dev, fn, smem, cs, n};
+    return n;
+}
+
 static void plan_workspace(AttnPlan &pl, int B, int Hkv) {
     size_t off = 0;
     pl.off_pair_ctr = off;  // [pair][arrived, ready][softmax warp]
@@ -110,7 +145,7 @@ static void plan_workspace(AttnPlan &pl, int B, int Hkv) {
     pl.bytes = off;
 }
 
-sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
+sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPlan *plan) {
     if (D != kD || T > kMaxT || B > kMaxB) return SV_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
     const int M = G * T;
@@ -134,7 +169,26 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan) {
                                      pl.smem, &sms);
     if (occ < 1) return SV_ERR_CUDA;
     pl.grid = sms * occ;
-    plan_workspace(pl, B, Hkv);
+    pl.cluster = 1;
+    plan_workspace(pl, B, Hkv);  // sized for the flat split whichever mode runs
+    // Few row groups (fewer than half the CTAs the device holds): one cluster
+    // per group, its tiles shared by the cluster's CTAs and merged in
+    // distributed shared memory, instead of a flat split whose groups straddle
+    // CTAs and merge through global memory.  The largest cluster size whose
+    // clusters the device keeps resident all at once, up to the tiles a group
+    // can have.
+    const long long groups = (long long)B * Hkv * pl.rg;
+    const int max_tiles = (S_max + kBK - 1) / kBK;
+    if (groups * 2 <= pl.grid) {
+        for (int cs = kMaxCluster; cs >= 2; cs >>= 1) {
+            if (cs > max_tiles || groups * cs > pl.grid) continue;
+            if (cached_max_clusters(tc_kernel_fn(pl.stages, pl.mrows), pl.smem, cs) >= groups) {
+                pl.cluster = cs;
+                pl.grid = (int)(groups * cs);
+                break;
+            }
+        }
+    }
     *plan = pl;
     return SV_OK;
 }
@@ -175,11 +229,28 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.num_pages = a.num_pages;
     p.page_size = a.page_size;
     p.node_counts = a.node_counts;
+    p.cluster = pl.cluster;
     void *args[] = {&tmk, &tmv, &tmq, &p};
-    return launch_pdl(tc_kernel_fn(pl.stages, pl.mrows), dim3(pl.grid), dim3(kTcThreads),
-                      pl.smem, st, args) == cudaSuccess
-               ? SV_OK
-               : SV_ERR_CUDA;
+    const void *fn = tc_kernel_fn(pl.stages, pl.mrows);
+    if (pl.cluster <= 1)
+        return launch_pdl(fn, dim3(pl.grid), dim3(kTcThreads), pl.smem, st, args) == cudaSuccess
+                   ? SV_OK
+                   : SV_ERR_CUDA;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)pl.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = (size_t)pl.smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace sv

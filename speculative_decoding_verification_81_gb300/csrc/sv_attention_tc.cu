@@ -14,7 +14,12 @@
 // persistent grid (one CTA per SM) takes equal contiguous ranges of it, so the
 // load is balanced whatever the prefix lengths.  A (sequence, KV head) whose
 // tiles fall to several CTAs is merged by the CTA that finishes its part
-// last: it combines the others' partials (O, max, sum) with its own O.  Inside a CTA (12 warps):
+// last: it combines the others' partials (O, max, sum) with its own O.
+// Small problems (few row groups: the Medusa tree, short batches) run in
+// cluster mode instead: one thread-block cluster per row group, its CTAs
+// taking contiguous shares of the group's tiles, the shares exchanged
+// through L2 after one cluster barrier, each CTA finishing a slice of the
+// rows.  Inside a CTA (12 warps):
 //
 //   warps 0, 11 TMA producers: K and V tiles (2-D tensor maps, 128-byte
 //               swizzle) into a ring of STAGES shared-memory stages, K and
@@ -60,6 +65,35 @@ namespace sv {
 // operand of S, sits in shared memory (double-buffered, loaded by TMA ahead
 // of its segment).
 constexpr uint32_t kTcCols = 512;
+
+// Phase stamps (a diagnostic build only, -DSV_PHASE_STAMPS): the SM clock at
+// fixed points of every CTA's run (slot 0: the globaltimer at entry, slot 1
+// the clock there, to place the CTAs on one time line), read back by
+// sv_debug_attention_stamps.  The library proper compiles them out.
+#ifdef SV_PHASE_STAMPS
+constexpr int kStampSlots = 32;
+constexpr int kStampCtas = 1024;
+static __device__ long long g_stamps[kStampCtas * kStampSlots];
+__device__ __forceinline__ void phase_stamp(int slot, long long value) {
+    if (blockIdx.x < kStampCtas) g_stamps[blockIdx.x * kStampSlots + slot] = value;
+}
+__device__ __forceinline__ long long global_ns() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+#define SV_STAMP(slot) phase_stamp((slot), clock64())
+#define SV_STAMP_ENTRY()                \
+    do {                                \
+        phase_stamp(1, clock64());      \
+        phase_stamp(0, global_ns());    \
+    } while (0)
+#define SV_STAMP_VALUE(slot, v) phase_stamp((slot), (long long)(v))
+#else
+#define SV_STAMP(slot) ((void)0)
+#define SV_STAMP_ENTRY() ((void)0)
+#define SV_STAMP_VALUE(slot, v) ((void)0)
+#endif
 constexpr uint32_t kColS = 0, kColO = 256;
 
 // Byte offset of 16-byte chunk c (0..7) of row `row` in a 128-byte-swizzled
@@ -83,6 +117,114 @@ struct TcSmem {
     int abort_flag;
 };
 
+// ---------------------------------------------------------------- cluster mode
+//
+// The CTAs of a cluster each hold an unnormalised share (O, max, sum) of every
+// row of the group; CTA k finishes rows k*MROWS/cs .. (its "own" rows).  Each
+// CTA writes its share to its slot of the workspace (the flat mode's partial
+// slots: f32 O rows of 512 bytes, and a (max, sum) pair per row), the
+// cluster meets at a barrier (release/acquire: the writes are visible after
+// it), and each CTA reads the shares of its own rows back from L2.  (Shares
+// sent through distributed shared memory -- per-thread loads, or one bulk
+// copy per owner -- took longer: about 1.5 us against 0.7 here, on the
+// Medusa-tree shape.)
+
+// A softmax thread's half row of O (64 columns at TMEM address o_half) and,
+// from the first half's thread, the row's (max, sum), into this CTA's share.
+// Warp-collective (TMEM loads): every lane calls it; has_row: the lane owns
+// row r (with 64-row groups, lanes 16-31 own none).
+__device__ __forceinline__ void cluster_stage(float *o_row, float2 *ml_row, uint32_t o_half,
+                                              int half, bool has_row, bool row_valid, float m,
+                                              float lrow) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t ov[32];
+        __syncwarp();
+        tc::tmem_ld32(o_half + 32 * h, ov);
+        tc::wait_ld();
+        if (!row_valid) continue;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            __stcg(reinterpret_cast<float4 *>(o_row + 64 * half + 32 * h) + c,
+                   make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
+                               __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3])));
+    }
+    if (half == 0 && has_row) __stcg(ml_row, row_valid ? make_float2(m, lrow) : make_float2(kNegInf, 0.f));
+}
+
+// Rows crank*MROWS/CS .. of the cluster's group from the CS shares (CTA i of
+// the cluster: O rows at o_base + i * o_stride, (max, sum) at ml_base +
+// i * ml_stride, floats): weights 2^(m_i - max m), the weighted O rows summed
+// in rank order and divided by the weighted row sums; bf16 out.  t256: the
+// thread's index among the 256 softmax threads.
+template <int MROWS, int CS>
+__device__ __forceinline__ void cluster_merge_cs(const AttnKParams &p, const float *o_base,
+                                                 size_t o_stride, const float *ml_base,
+                                                 size_t ml_stride, int crank, int b, int kvh,
+                                                 int rg, int ntiles, int t256) {
+    constexpr int kRpc = MROWS / CS;                  // rows this CTA finishes
+    constexpr int kTpr = kSoftmaxWarps * 32 / kRpc;   // threads per row
+    constexpr int kChunks = 32 / kTpr;                // 16-byte chunks (4 columns) per thread
+    static_assert(kTpr <= 32 && kChunks >= 1, "cluster too large for the row group");
+    const int lr = t256 / kTpr, part = t256 - lr * kTpr;
+    const int r = crank * kRpc + lr;
+    const int rglob = rg * p.rows_per_rg + r;
+    if (b >= p.B || ntiles <= 0 || r >= p.rows_per_rg || rglob >= p.M) return;
+    const int t = rglob / p.G, g = rglob - t * p.G;
+    if (t >= nodes_of(p, b)) return;
+    // every share's (max, sum) and O chunks in flight at once; chunks
+    // interleaved over the row's threads (consecutive lanes, consecutive 16 bytes)
+    float2 ml[CS];
+    float4 o[kChunks][CS];
+#pragma unroll
+    for (int i = 0; i < CS; ++i) {
+        ml[i] = __ldcg(reinterpret_cast<const float2 *>(ml_base + i * ml_stride) + r);
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j)
+            o[j][i] = __ldcg(reinterpret_cast<const float4 *>(o_base + i * o_stride + (size_t)r * kD) +
+                             j * kTpr + part);
+    }
+    float ms = kNegInf;
+#pragma unroll
+    for (int i = 0; i < CS; ++i) ms = fmaxf(ms, ml[i].x);
+    float w[CS], lsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < CS; ++i) {
+        w[i] = ml[i].x == kNegInf ? 0.f : ex2_approx(ml[i].x - ms);  // an empty share weighs 0
+        lsum = __fmaf_rn(ml[i].y, w[i], lsum);
+    }
+    const float inv = 1.f / lsum;
+    uint16_t *orow = p.out + (((size_t)b * p.T + t) * p.Hq + kvh * p.G + g) * kD;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < CS; ++i) {
+            // an empty share's slot holds no O: select, never multiply, it
+            const bool use = w[i] != 0.f;
+            acc.x = use ? __fmaf_rn(o[j][i].x, w[i], acc.x) : acc.x;
+            acc.y = use ? __fmaf_rn(o[j][i].y, w[i], acc.y) : acc.y;
+            acc.z = use ? __fmaf_rn(o[j][i].z, w[i], acc.z) : acc.z;
+            acc.w = use ? __fmaf_rn(o[j][i].w, w[i], acc.w) : acc.w;
+        }
+        *reinterpret_cast<uint2 *>(orow + 4 * (j * kTpr + part)) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
+}
+
+template <int MROWS>
+__device__ __forceinline__ void cluster_merge(const AttnKParams &p, const float *o_base,
+                                              size_t o_stride, const float *ml_base,
+                                              size_t ml_stride, int cs, int crank, int b, int kvh,
+                                              int rg, int ntiles, int t256) {
+    if (cs == 2)
+        cluster_merge_cs<MROWS, 2>(p, o_base, o_stride, ml_base, ml_stride, crank, b, kvh, rg, ntiles, t256);
+    else if (cs == 4)
+        cluster_merge_cs<MROWS, 4>(p, o_base, o_stride, ml_base, ml_stride, crank, b, kvh, rg, ntiles, t256);
+    else
+        cluster_merge_cs<MROWS, 8>(p, o_base, o_stride, ml_base, ml_stride, crank, b, kvh, rg, ntiles, t256);
+}
+
 // MROWS query rows per group: 128 (M=128 products, row r in TMEM lane r) or
 // 64 (M=64 products, row r in lane 32*(r/16) + r%16: lanes 0-15 of each
 // 32-lane quarter) for groups of at most 64 rows.
@@ -104,12 +246,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = tid >> 5, lane = tid & 31;
     const int HR = p.Hkv * p.RG;
 
-    griddep_wait();
-    griddep_launch_dependents();
-    // the prologue's first loads go out before the barrier set-up
-    const int pre_L = tid < p.B ? p.prefix_lens[tid] : 0;
-    const int pre_T = tid < p.B ? nodes_of(p, tid) : 0;
-
+    if (tid == 0) SV_STAMP_ENTRY();
+    // The set-up that reads no global memory (barriers, tensor-map prefetch,
+    // the Q padding rows, the tensor memory) comes before the wait for the
+    // previous kernel: with programmatic launch it overlaps that kernel's tail.
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sh->full_k[s], 1);
@@ -147,14 +287,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             make_uint4(0u, 0u, 0u, 0u);
     }
     tc::fence_proxy_async_smem();
+    if (warp == 1) tc::tmem_alloc(&sh->tmem, kTcCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tbase = sh->tmem;
+
+    griddep_wait();
+    griddep_launch_dependents();
+    if (tid == 0) SV_STAMP(2);
+    const int pre_L = tid < p.B ? p.prefix_lens[tid] : 0;
+    const int pre_T = tid < p.B ? nodes_of(p, tid) : 0;
     attn_prologue(p, tile_base, kTcThreads, pre_L, pre_T);
 
     // With several row groups per KV head, the CTAs go in lanes, one per row
     // group: CTA c works in lane c % RG, and the lanes split the (sequence,
     // KV head, tile) units identically, so the RG CTAs of a slot stream the
     // same K/V tiles side by side and all but the first read them from L2.
-    const int nlane = p.RG;
-    const PairLane pl{nlane > 1 ? p.Hkv : HR, nlane, (int)blockIdx.x % nlane};
+    //
+    // In cluster mode the units of one (sequence, KV head, row group) go to
+    // one cluster, CTA k taking the k-th contiguous share of its tiles; no CTA
+    // leaves early (all of them meet at the cluster barriers at the end).
+    const bool cl = p.cluster > 1;
+    const int cs = cl ? p.cluster : 1;
+    const int crank = cl ? (int)cluster_ctarank() : 0;
+    const int cpair = (int)blockIdx.x / cs;              // cluster mode: the cluster's group
+    const int cb = cl ? cpair / HR : 0;                  // its sequence
+    const int cpr = cl ? cpair - cb * HR : 0;            // its (KV head, row group)
+    const int cn = cl && cb < p.B ? tile_base[cb + 1] - tile_base[cb] : 0;  // its tiles
+    const int nlane = cl ? 1 : p.RG;
+    const PairLane pl{cl ? HR : nlane > 1 ? p.Hkv : HR, nlane, cl ? 0 : (int)blockIdx.x % nlane};
     const long long U = (long long)tile_base[p.B] * pl.npr;  // units of one lane
     // At least kMinTilesPerCta tiles a slot: below that a CTA's fixed costs
     // (pipeline fill, epilogue) and many-way merges outweigh the parallelism.
@@ -162,16 +324,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const long long want = U / kMinTilesPerCta > 0 ? U / kMinTilesPerCta : 1;
     const int nctas = (int)(want < (long long)slots_max ? want : (long long)slots_max);  // slots in use
     const int myslot = (int)blockIdx.x / nlane;
-    if (myslot >= nctas) return;
-    const long long u_begin = cta_begin(U, nctas, myslot);
-    const long long u_end = cta_begin(U, nctas, myslot + 1);
+    if (!cl && myslot >= nctas) {  // no work: give the tensor memory back
+        if (warp == 1) tc::tmem_dealloc(tbase, kTcCols);
+        return;
+    }
+    long long u_begin, u_end;
+    if (cl) {
+        const long long u0 = (long long)tile_base[cb < p.B ? cb : p.B] * HR + (long long)cpr * cn;
+        u_begin = u0 + (long long)cn * crank / cs;
+        u_end = u0 + (long long)cn * (crank + 1) / cs;
+    } else {
+        u_begin = cta_begin(U, nctas, myslot);
+        u_end = cta_begin(U, nctas, myslot + 1);
+    }
     volatile int *abort_flag = &sh->abort_flag;
-
-    if (warp == 1) tc::tmem_alloc(&sh->tmem, kTcCols);
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tbase = sh->tmem;
+    if (tid == 0) SV_STAMP(3);
 
     auto fail = [&](int b) {
         *abort_flag = 1;
@@ -200,6 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
             long long k = 0;
             uint32_t qseg = 0;  // segments whose Q was issued
+            if (is_k) SV_STAMP(4);
             for (long long u = u_begin; u < u_end; ++u, ++k) {
                 const int s = (int)(k % STAGES);
                 const uint32_t ph = (uint32_t)((k / STAGES) & 1);
@@ -226,6 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
                     tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
                     tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
+                    if (qseg == 0) SV_STAMP(5);
                     ++qseg;
                 }
                 const int kvh = cur.pr / p.RG;
@@ -286,7 +455,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             load(st + kBox + i * ps * 128, 64, y[i], &full[s]);
                         }
                 }
-                if (is_k && k == 0) mbar_arrive(&sh->k_first);
+                if (is_k && k == 0) {
+                    mbar_arrive(&sh->k_first);
+                    SV_STAMP(6);
+                }
+                if (!is_k && k == 0) SV_STAMP(18);
+                if (is_k) SV_STAMP(10);
                 cursor_next(cur, tile_base, p.B, pl);
             }
             if (is_k && k == 0) mbar_arrive(&sh->k_first);  // none issued: release the V side
@@ -297,10 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (uint32_t g2 = qseg > 2 ? qseg - 2 : 0; g2 < qseg; ++g2)
                 mbar_wait_bounded(&sh->q_full[g2 & 1], (g2 >> 1) & 1);
         }
-        return;
-    }
-
-    if (warp == 1 || warp == kPvWarp) {
+    } else if (warp == 1 || warp == kPvWarp) {
         // ================= MMA issue: lane 0 of warp 1 the S = Q K^T
         // products, lane 0 of the last warp the O += P V products, each in
         // tile order behind (bounded) blocking waits, so neither polls nor
@@ -321,6 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ++seg;
                     }
                     if (ok) ok = mbar_wait_bounded(&sh->full_k[s], (uint32_t)((j / STAGES) & 1));
+                    if (j == 0) SV_STAMP(7);
                     if (ok && j >= 2)
                         ok = mbar_wait_bounded(&sh->pv_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
                     if (!ok || *abort_flag) {
@@ -353,6 +525,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const bool first = (j == 0) || cur.tile == 0;  // O starts over
                     ok = mbar_wait_bounded(&sh->p_full[j & 1], (uint32_t)((j >> 1) & 1));
                     if (ok) ok = mbar_wait_bounded(&sh->full_v[s], (uint32_t)((j / STAGES) & 1));
+                    if (j == 0) SV_STAMP(19);
                     if (!ok || *abort_flag) {
                         ok = false;
                         break;
@@ -386,9 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_after();
             tc::tmem_dealloc(tbase, kTcCols);
         }
-        return;
-    }
-
+    } else {
     // ===================== softmax warps 2..9: two threads per query row
     const int quarter = warp & 3;          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;      // 0: keys / output columns 0-63, 1: 64-127
@@ -403,6 +574,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t anc = 0;
     uint32_t pair_uses = 0;
     int *ready_ctr = nullptr;  // a partial of this warp waiting to be flagged ready
+    bool staged = false;       // cluster mode: this warp's rows are in the merge buffer
     // The warp's partial writes are visible before the ready count moves.
     auto flag_ready = [&](int *c) {
         __syncwarp();
@@ -462,7 +634,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // trip overlaps this tile; the last CTA to arrive merges.
         int *ctr = nullptr;
         int arrived = 0;
-        if (seg_end && !whole && warp_active) {
+        if (!cl && seg_end && !whole && warp_active) {
             ctr = p.pair_ctr + ((size_t)((cur.b * p.Hkv + kvh) * p.RG + rg) * 2) * kSoftmaxWarps + (warp - 2);
             if (lane == 0) arrived = atomicAdd(ctr, 1);
         }
@@ -474,6 +646,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
         }
         tc::fence_after();
+        if (warp == 2 && lane == 0) {
+            if (jt == 0) SV_STAMP(8);
+            SV_STAMP(9);
+            SV_STAMP_VALUE(17, jt + 1);
+        }
         if (warp_active) {
             float sv[64];
             {
@@ -587,6 +764,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             tc::fence_after();
+            if (warp == 2 && lane == 0) SV_STAMP(11);
             // row sum = first half's part + second half's part (same order in both)
             sh->xl[quarter][half][lane] = l;
             if (!group_sync(&sh->pair[quarter], pair_uses)) {
@@ -594,6 +772,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             const float lrow = sh->xl[quarter][0][lane] + sh->xl[quarter][1][lane];
+            if (cl) {
+                // cluster mode: this CTA's share of the group, unnormalised,
+                // into the merge buffer (the K/V ring is idle now: every copy
+                // has landed and every product has read it)
+                cluster_stage(p.part_o + ((size_t)blockIdx.x * 2 * MROWS + r) * kD,
+                              reinterpret_cast<float2 *>(p.part_ml) + (size_t)blockIdx.x * 2 * MROWS * 2 + r,
+                              tl + kColO + hc, half, lane_has_row, row_valid, m, lrow);
+                staged = true;
+                if (warp == 2 && lane == 0) SV_STAMP(12);
+                tc::fence_before();
+                cursor_next(cur, tile_base, p.B, pl);
+                continue;
+            }
             const int t = row_valid ? rglob / p.G : 0;
             const int g = row_valid ? rglob - t * p.G : 0;
             uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD + hc;
@@ -767,13 +958,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (ctr) ready_ctr = ctr + kSoftmaxWarps;  // flagged after the next tile (or at the end)
                 }
             }
+            if (warp == 2 && lane == 0) SV_STAMP(12);
             tc::fence_before();
         }
         cursor_next(cur, tile_base, p.B, pl);
     }
     if (ready_ctr) flag_ready(ready_ctr);
+    if (cl && !staged && lane_has_row && half == 0) {
+        // no tile of the group fell to this CTA (or a wait gave up): an empty share
+        __stcg(reinterpret_cast<float2 *>(p.part_ml) + (size_t)blockIdx.x * 2 * MROWS * 2 + r,
+               make_float2(kNegInf, 0.f));
+    }
     tc::fence_before();
     named_bar_sync(1, (2 + kSoftmaxWarps) * 32);
+    }  // softmax warps
+
+    if (p.cluster > 1) {
+        // (the cluster's group again, rather than kept live through the loop)
+        const int cs = p.cluster;
+        const int crank = (int)cluster_ctarank();
+        const int cb = (int)blockIdx.x / cs / HR, cpr = (int)blockIdx.x / cs - cb * HR;
+        const int cn = cb < p.B ? tile_base[cb + 1] - tile_base[cb] : 0;
+        // Every CTA's share is in the workspace once all have passed the
+        // barrier; then each finishes its own rows.
+        cluster_sync_any();
+        if (tid == 64) SV_STAMP(13);
+        if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
+            const int kvh = cpr / p.RG, rg = cpr - kvh * p.RG;
+            const size_t c0 = (size_t)(blockIdx.x - crank);  // the cluster's first CTA
+            cluster_merge<MROWS>(p, p.part_o + c0 * 2 * MROWS * kD, (size_t)2 * MROWS * kD,
+                                 p.part_ml + c0 * 2 * MROWS * 4, (size_t)2 * MROWS * 4, cs, crank,
+                                 cb, kvh, rg, cn, tid - 64);
+#ifdef SV_PHASE_STAMPS
+            if (tid == 64) SV_STAMP(20);
+            cluster_merge<MROWS>(p, p.part_o + c0 * 2 * MROWS * kD, (size_t)2 * MROWS * kD,
+                                 p.part_ml + c0 * 2 * MROWS * 4, (size_t)2 * MROWS * 4, cs, crank,
+                                 cb, kvh, rg, cn, tid - 64);
+            if (tid == 64) SV_STAMP(21);
+#endif
+        }
+        if (tid == 64) SV_STAMP(15);
+    }
+    if (tid == 0) SV_STAMP(16);
 }
 
 // ---------------------------------------------------------------- host side
@@ -781,6 +1007,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 int tc_smem_bytes(int stages, int mrows, int B) {
     return 1024 + stages * kStageBytes + 2 * 2 * mrows * 128 + (int)sizeof(TcSmem) + (B + 1) * 4;
 }
+
+#ifdef SV_PHASE_STAMPS
+}  // namespace sv
+// Copies the phase stamps of the last attention launch (kStampSlots per CTA,
+// CTA-major) to host memory; diagnostic builds only.
+extern "C" int sv_debug_attention_stamps(long long *dst, int ctas) {
+    if (ctas > sv::kStampCtas) ctas = sv::kStampCtas;
+    return cudaMemcpyFromSymbol(dst, sv::g_stamps, sizeof(long long) * ctas * sv::kStampSlots) ==
+                   cudaSuccess
+               ? 0
+               : -1;
+}
+extern "C" int sv_debug_attention_clear(void) {
+    static long long zeros[sv::kStampCtas * sv::kStampSlots];
+    return cudaMemcpyToSymbol(sv::g_stamps, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+namespace sv {
+#endif
 
 const void *tc_kernel_fn(int stages, int mrows) {
     if (stages == 3 && mrows == 128) return reinterpret_cast<const void *>(&tree_attention_tc_kernel<3, 128>);

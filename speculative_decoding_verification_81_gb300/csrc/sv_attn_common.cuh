@@ -16,6 +16,7 @@ constexpr int kMinPage = 8;                      // smallest page (a swizzle ato
 constexpr int kMaxSubBlocks = kBK / kMinPage;    // pages per key tile at most
 constexpr int kMaxT = 64;
 constexpr int kMinTilesPerCta = 8;  // key tiles a CTA takes at least (small problems)
+constexpr int kMaxCluster = 8;      // CTAs of a cluster in cluster mode (a portable size)
 constexpr int kSoftmaxWarps = 8;                      // warps 2-9: two per TMEM lane quarter
 constexpr int kPvWarp = 2 + kSoftmaxWarps;              // issues the PV products
 constexpr int kVLoadWarp = 3 + kSoftmaxWarps;           // loads the V tiles
@@ -38,6 +39,11 @@ struct AttnKParams {
     int max_pages, num_pages, page_size;
     // per-sequence node counts T_b (1 <= T_b <= T; nodes past T_b are padding), or null: all T
     const int32_t *node_counts;
+    // cluster mode (cluster > 1): one thread-block cluster of `cluster` CTAs per
+    // (sequence, KV head, row group), CTA k of it taking the k-th contiguous
+    // share of that group's key tiles; the shares are merged in distributed
+    // shared memory.  0 or 1: the flat split over persistent CTAs.
+    int cluster;
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.

@@ -128,7 +128,8 @@ struct AttnPlan {
     int mrows;        // the MMA's M: 64 or 128
     int rows_per_rg;  // query rows per row group: the largest multiple of G <= mrows
     int rg;           // row groups per (sequence, KV head)
-    int grid;         // persistent CTAs
+    int grid;         // CTAs launched
+    int cluster;      // CTAs per cluster in cluster mode (one cluster per row group), else 1
     int smem;         // dynamic shared memory bytes
     size_t off_pair_ctr;
     size_t off_part_o;
@@ -136,7 +137,7 @@ struct AttnPlan {
     size_t bytes;
 };
 
-sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, AttnPlan *plan);
+sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPlan *plan);
 
 // tcgen05 attention kernel (sv_attention_tc.cu)
 struct AttnKParams;

@@ -1288,27 +1288,6 @@ constexpr int kWWarps = kWT / 32;
 constexpr int kWClusterMax = 16;          // CTAs of a walking cluster (16: non-portable)
 constexpr int kMaxWSeg = 4096;            // elements a thread owns in a pass
 
-// Thread-block clusters: this CTA's rank, a barrier over every thread of the
-// cluster (release/acquire: shared-memory writes before it are visible to the
-// other CTAs after it), and a load from another CTA's shared memory.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_shared_cluster_f32(const float *local, uint32_t rank) {
-    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-    uint32_t ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-    return v;
-}
-
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kVT) stree_stats_kernel(STreeArgs a, VocabPlan p, float2 *rec) {
     __shared__ float red[2 * kVWarps];

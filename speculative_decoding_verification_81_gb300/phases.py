@@ -1,0 +1,176 @@
+"""Phase timeline of the verification attention kernel (a diagnostic tool).
+
+Builds the library a second time with -DSV_PHASE_STAMPS (into _build/phases/,
+beside the product library, which stays stamp-free), runs one attention
+shape through it and prints, for each stamped point of a CTA's run, the
+spread over the CTAs of its globaltimer reading, in microseconds from the
+moment the kernel was allowed to start (the earliest return from the wait
+for the previous kernel).
+
+    python -m speculative_decoding_verification_81_gb300.phases [--shape medusa|chain|small]
+        [--reps N] [--behind N]
+
+--behind N: the stamped launch is the last of N + 1 calls in one CUDA graph,
+as in a stream of steps; its CTAs may be placed while the call before it
+still runs.  --copies C: the calls cycle through C input sets, so that with
+enough of them (C * the inputs' bytes > 3 x L2) each call reads its K/V from
+HBM rather than from L2.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+PHASES_DIR = os.path.join(_build.BUILD_DIR, "phases")
+PHASES_LIB = os.path.join(PHASES_DIR, "libspecverify_phases.so")
+SLOTS = 32
+# slot 0: globaltimer at CTA entry; slot 1: the SM clock there; the others:
+# the SM clock at the point (slot 17: tiles the CTA processed)
+POINTS = [
+    (1, "CTA entry (placed on its SM)"),
+    (2, "wait for the previous kernel returned"),
+    (3, "prologue + unit range done"),
+    (4, "K producer: cursor ready"),
+    (5, "first Q rows requested"),
+    (6, "first K tile requested"),
+    (18, "first V tile requested"),
+    (7, "first K tile landed (S lane)"),
+    (8, "first S product ready (softmax warp)"),
+    (19, "first V tile landed (PV lane)"),
+    (9, "last S product ready (softmax warp)"),
+    (10, "last K tile requested"),
+    (11, "last PV product done (segment end)"),
+    (12, "O staged / written out"),
+    (13, "cluster barrier 1 passed"),
+    (20, "cluster merge done (stamped build: once more)"),
+    (21, "cluster merge done a second time (warm code)"),
+    (15, "cluster merge done"),
+    (16, "CTA end"),
+]
+
+SHAPES = {
+    # name: (B, L, T, tree)
+    "medusa": (4, 2048, 26, "medusa"),
+    "chain": (32, 4096, 9, None),
+    "small": (2, 300, 9, None),
+}
+
+
+def build_phases_lib(force: bool = False) -> str:
+    return _build.build(force=force, defines=("SV_PHASE_STAMPS",), lib_path=PHASES_LIB,
+                        build_dir=PHASES_DIR)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--shape", choices=sorted(SHAPES), default="medusa")
+    ap.add_argument("--reps", type=int, default=5, help="stamped runs (the table is their median)")
+    ap.add_argument("--behind", type=int, default=3)
+    ap.add_argument("--sm-ghz", type=float, default=2.07,
+                    help="SM clock under load, to turn clock ticks into time")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="input sets cycled (default: enough for 3 x 126 MB)")
+    args = ap.parse_args()
+
+    import torch
+
+    from . import api
+    from . import workloads as W
+
+    path = build_phases_lib()
+    L_ = api.use_library(path)
+    L_.sv_debug_attention_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    ghz = args.sm_ghz
+    L_.sv_debug_attention_stamps.restype = ctypes.c_int
+    L_.sv_debug_attention_clear.restype = ctypes.c_int
+
+    B, L, T, tree = SHAPES[args.shape]
+    Hq, Hkv, D = 32, 8, 128
+    S = L + 64
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(3)
+    one = B * Hkv * S * D * 4 + 2 * B * T * Hq * D * 2
+    copies = args.copies or max(1, -(-3 * 126 * 2**20 // one))
+    sets = []
+    for _ in range(copies):
+        q = torch.randn(B, T, Hq, D, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16)
+        sets.append((q, k, v, torch.empty_like(q)))
+    pl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    par = (torch.from_numpy(np.broadcast_to(W.medusa_tree(T), (B, T)).copy()).to(dev)
+           if tree == "medusa" else None)
+    ws = api.workspace(api.SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, dev)
+
+    # every set is read once per replay, the stamped (last) call's set least recently
+    ncalls = max(args.behind + 1, copies)
+
+    def call(i=0):
+        q, k, v, out = sets[i % copies]
+        api.sv_tree_attention(q, k, v, pl, par, out=out, ws=ws)
+
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(ncalls):
+            call(i)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    ctas = 1024
+    runs = []
+    for _ in range(args.reps):
+        assert L_.sv_debug_attention_clear() == 0
+        graph.replay()
+        torch.cuda.synchronize()
+        buf = np.zeros(ctas * SLOTS, np.int64)
+        assert L_.sv_debug_attention_stamps(buf.ctypes.data, ctas) == 0
+        raw = buf.reshape(ctas, SLOTS)
+        raw = raw[raw[:, 0] > 0]
+        # every point on the globaltimer line (ns): entry time + clock ticks since entry
+        st = np.zeros(raw.shape, np.float64)
+        for slot in range(SLOTS):
+            if slot in (0, 17):
+                continue
+            ok = raw[:, slot] != 0
+            st[ok, slot] = raw[ok, 0] + (raw[ok, slot] - raw[ok, 1]) / ghz
+        st[:, 17] = raw[:, 17]
+        t0 = st[:, 2][st[:, 2] > 0].min()
+        runs.append((st, t0))
+    n = runs[0][0].shape[0]
+    print(f"shape {args.shape}: B={B} L={L} T={T} tree={tree or 'chain'}; {n} CTAs; "
+          f"SM clock taken as {ghz} GHz; "
+          f"{copies} input sets, the last of {ncalls} calls stamped; median of {args.reps} runs; "
+          f"us from the earliest return of the wait for the previous kernel")
+    print(f"{'point':44s} {'min':>8s} {'median':>8s} {'max':>8s}")
+    for slot, name in POINTS:
+        rows = []
+        for st, t0 in runs:
+            col = st[:, slot]
+            col = col[col > 0]
+            if col.size == 0:
+                continue
+            rel = (col - t0) / 1e3
+            rows.append((rel.min(), np.median(rel), rel.max()))
+        if not rows:
+            continue
+        a = np.median(np.array(rows), axis=0)
+        print(f"{name:44s} {a[0]:8.2f} {a[1]:8.2f} {a[2]:8.2f}")
+    tiles = runs[0][0][:, 17]
+    print(f"tiles per CTA: min {tiles.min():.0f} max {tiles.max():.0f}")
+
+
+if __name__ == "__main__":
+    main()
