@@ -277,9 +277,9 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     newl = torch.empty(B, dtype=torch.int32, device=dev)
     ua = torch.rand(B, T, device=dev, generator=g)
     us = torch.rand(B, device=dev, generator=g)
-    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, dev)
-    ws_t = sv.workspace(sv.SV_OP_VERIFY_TREE_GREEDY, B, T, V, sv.SV_BF16, 0, 0, dev)
-    ws_s = sv.workspace(sv.SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, sv.SV_BF16, 0, 0, dev)
+    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, T, Hq=Hq, Hkv=Hkv, D=D, device=dev)
+    ws_t = sv.workspace(sv.SV_OP_VERIFY_TREE_GREEDY, B, T, V, sv.SV_BF16, device=dev)
+    ws_s = sv.workspace(sv.SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, sv.SV_BF16, device=dev)
 
     def attention(x):
         sv.sv_tree_attention(x["q"], x["k"], x["v"], pl, par, out=x["out"], ws=ws_a)
@@ -367,8 +367,9 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     toks = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
     newl = torch.empty(B, dtype=torch.int32, device=dev)
-    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, N + 1, 0, cfg["Hq"], cfg["Hkv"], cfg["D"], dev)
-    ws_c = sv.workspace(sv.SV_OP_VERIFY_CHAIN, B, N, V, sv.SV_BF16, 0, 0, dev)
+    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, N + 1, Hq=cfg["Hq"], Hkv=cfg["Hkv"], D=cfg["D"],
+                        device=dev)
+    ws_c = sv.workspace(sv.SV_OP_VERIFY_CHAIN, B, N, V, sv.SV_BF16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(dd):
@@ -466,7 +467,8 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     for Tq in (1, 5):
         qx = torch.randn(B, Tq, cfg["Hq"], cfg["D"], device=dev).to(torch.bfloat16)
         ox = torch.empty_like(qx)
-        wsx = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, Tq, 0, cfg["Hq"], cfg["Hkv"], cfg["D"], dev)
+        wsx = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, Tq, Hq=cfg["Hq"], Hkv=cfg["Hkv"],
+                           D=cfg["D"], device=dev)
 
         def call_t(qx=qx, ox=ox, wsx=wsx):
             sv.sv_tree_attention(qx, d["k"], d["v"], d["prefix_lens"], None, out=ox, ws=wsx)

@@ -71,20 +71,26 @@ typedef enum sv_op {
     SV_OP_TREE_ATTENTION = 0,
     SV_OP_VERIFY_CHAIN = 1,
     SV_OP_VERIFY_TREE_GREEDY = 2,
-    SV_OP_VERIFY_TREE_STOCHASTIC = 3
+    SV_OP_VERIFY_TREE_STOCHASTIC = 3,
+    SV_OP_VERIFY_STEP_CHAIN = 4,
+    SV_OP_VERIFY_STEP_TREE_GREEDY = 5
 } sv_op;
 
 /*
  * Bytes of workspace a call needs, for the CURRENT device (the kernels size
- * their persistent grids by its SM count).  Arguments are those of the call:
- *   SV_OP_TREE_ATTENTION:     B, T, Hq, Hkv, D       (V ignored)
- *   SV_OP_VERIFY_CHAIN:       B, N (as T_or_N), V, dtype as Hq (0 f32 / 1 bf16)
- *   SV_OP_VERIFY_TREE_GREEDY: B, T, V, dtype as Hq
- *   SV_OP_VERIFY_TREE_STOCHASTIC: B, T, V, dtype as Hq
+ * their persistent grids by its SM count).  Arguments are those of the call;
+ * the ones an operation does not use are ignored:
+ *   SV_OP_TREE_ATTENTION:          B, T, Hq, Hkv, D
+ *   SV_OP_VERIFY_CHAIN:            B, N (as T_or_N), V, dtype
+ *   SV_OP_VERIFY_TREE_GREEDY:      B, T, V, dtype
+ *   SV_OP_VERIFY_TREE_STOCHASTIC:  B, T, V, dtype
+ *   SV_OP_VERIFY_STEP_CHAIN:       B, N (as T_or_N), V, dtype, Hq, Hkv, D
+ *   SV_OP_VERIFY_STEP_TREE_GREEDY: B, T, V, dtype, Hq, Hkv, D
  * Returns 0 for invalid arguments and for shapes the call refuses as
  * SV_ERR_UNSUPPORTED.
  */
-size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, int D);
+size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, sv_dtype dtype, int Hq, int Hkv,
+                         int D);
 
 /*
  * Verification attention over a prefix KV cache plus each node's ancestors.
@@ -298,6 +304,76 @@ sv_status sv_compact_kv_paged(void *k_pages, void *v_pages, const int32_t *block
                               const int32_t *path_nodes, int path_stride,
                               const int32_t *accepted_len, int B, int Hkv, int D,
                               int32_t *seq_status, sv_stream_t stream);
+
+/*
+ * The fused verification step on a chain: sv_tree_attention with the causal
+ * mask, sv_verify_chain and the compaction of the accepted rows, in one call.
+ * Source: "Chapitre 9 -- Décodage spéculatif" §9.1 (one pass over the prefix
+ * and the N candidates yields the N+1 distributions the acceptance reads;
+ * the accepted prefix is kept) and §9.3 (the verification pass bounds the
+ * speed-up).  The logits are inputs, so the attention and the acceptance are
+ * independent: the attention runs on the caller's stream over most of the
+ * SMs while the acceptance runs on the rest, on a side stream of the library
+ * forked from `stream` and joined back to it (two events); the SMs are split
+ * in proportion to the bytes each side streams.  A chain's accepted rows are
+ * already in place (node d at slot L_b + d), so compaction writes only the
+ * new cache lengths.
+ *
+ * Arguments as sv_tree_attention (parents = NULL; node counts N_b + 1 from
+ * draft_lens) and sv_verify_chain, plus
+ *   attn_status    int32 [B] or NULL: sv_tree_attention's seq_status
+ *   verify_status  int32 [B] or NULL: sv_verify_chain's seq_status
+ *   new_kv_lens    int32 [B]: L_b + a_b + 1, or L_b when a_b < 0 or
+ *                  L_b + N_b + 1 > S_max; must not alias prefix_lens (the
+ *                  attention reads those while the acceptance writes these)
+ *   workspace      >= sv_workspace_size(SV_OP_VERIFY_STEP_CHAIN, B, N, V,
+ *                  dtype, Hq, Hkv, D) bytes, zero-filled before its first use
+ * Supported: as the two calls.  The first step call on a device creates the
+ * side stream and events (make it before any stream capture); calls from
+ * several host threads are serialised around the fork and the join.
+ */
+sv_status sv_verify_step_chain(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *prefix_lens, int Hq, int Hkv, int D, int S_max,
+                               float scale, void *attn_out, int32_t *attn_status,
+                               const void *target_logits, const void *draft_logits,
+                               sv_dtype dtype, const int32_t *draft_tokens,
+                               const int32_t *draft_lens, const float *u_accept,
+                               const float *u_sample, int B, int N, int V, int32_t *accepted_len,
+                               int32_t *out_tokens, float *probs_out, int32_t *verify_status,
+                               int32_t *new_kv_lens, void *workspace, size_t workspace_bytes,
+                               sv_stream_t stream);
+
+/*
+ * The fused verification step on a draft tree: sv_tree_attention,
+ * sv_verify_tree_greedy and sv_compact_kv in one call.  Sources as those
+ * three calls and sv_verify_step_chain.  The attention and the greedy
+ * acceptance run side by side as in sv_verify_step_chain.  When the
+ * attention runs in cluster mode (few row groups: B * Hkv * ceil(Hq/Hkv * T
+ * / 128) clusters fit on the device at once) and the logits rows are 16-byte
+ * aligned, compaction happens inside the two kernels: for each (sequence, KV
+ * head), whichever of the attention (done reading that head's rows) and the
+ * tree walk (path known) arrives last moves the rows.  Otherwise a compaction
+ * kernel runs after both.
+ *
+ * Arguments as the three calls (path_nodes has T columns), plus attn_status,
+ * verify_status (nullable, as above) and
+ *   k_cache, v_cache  read by the attention, then compacted in place
+ *   new_kv_lens       int32 [B]: L_b + a_b + 1, or L_b when a_b < 0 or the
+ *                     cache cannot hold the nodes; must not alias prefix_lens
+ *   workspace         >= sv_workspace_size(SV_OP_VERIFY_STEP_TREE_GREEDY, B,
+ *                     T, V, dtype, Hq, Hkv, D) bytes, zero-filled before first use
+ * Supported: as the three calls, with Hkv <= 256.
+ */
+sv_status sv_verify_step_tree_greedy(const void *q, void *k_cache, void *v_cache,
+                                     const int32_t *prefix_lens, const int32_t *parents,
+                                     const int32_t *node_counts, int B, int T, int Hq, int Hkv,
+                                     int D, int S_max, float scale, void *attn_out,
+                                     int32_t *attn_status, const void *target_logits,
+                                     sv_dtype dtype, const int32_t *node_tokens, int V,
+                                     int32_t *accepted_len, int32_t *path_nodes,
+                                     int32_t *out_tokens, int32_t *verify_status,
+                                     int32_t *new_kv_lens, void *workspace,
+                                     size_t workspace_bytes, sv_stream_t stream);
 
 /*
  * Chain acceptance with no caller workspace.  There is no counterpart of this

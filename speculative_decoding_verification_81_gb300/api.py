@@ -31,10 +31,13 @@ SV_OP_TREE_ATTENTION = 0
 SV_OP_VERIFY_CHAIN = 1
 SV_OP_VERIFY_TREE_GREEDY = 2
 SV_OP_VERIFY_TREE_STOCHASTIC = 3
+SV_OP_VERIFY_STEP_CHAIN = 4
+SV_OP_VERIFY_STEP_TREE_GREEDY = 5
 
 EXPORTS = ("sv_workspace_size", "sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy",
            "sv_compact_kv", "sv_status_string", "sv_version", "sv_verify_chain_noalloc",
-           "sv_tree_attention_paged", "sv_compact_kv_paged", "sv_verify_tree_stochastic")
+           "sv_tree_attention_paged", "sv_compact_kv_paged", "sv_verify_tree_stochastic",
+           "sv_verify_step_chain", "sv_verify_step_tree_greedy")
 
 # Length of the fixed scratch array behind sv_verify_chain_noalloc.
 SV_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -73,7 +76,7 @@ def load(path: str) -> ctypes.CDLL:
     """Load a build of libspecverify and declare its entry points' C types."""
     L = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-    L.sv_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    L.sv_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     L.sv_workspace_size.restype = Z
     L.sv_tree_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, P, P, P,
                                     Z, P]
@@ -86,9 +89,14 @@ def load(path: str) -> ctypes.CDLL:
     L.sv_compact_kv_paged.argtypes = [P, P, P, I, I, I, P, P, P, I, P, I, I, I, P, P]
     L.sv_verify_tree_stochastic.argtypes = [P, P, I, P, P, P, P, P, I, I, I, P, P, P, P, P, Z,
                                             P]
+    F = ctypes.c_float
+    L.sv_verify_step_chain.argtypes = [P, P, P, P, I, I, I, I, F, P, P, P, P, I, P, P, P, P, I, I,
+                                       I, P, P, P, P, P, P, Z, P]
+    L.sv_verify_step_tree_greedy.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, I, P,
+                                             I, P, P, P, P, P, P, Z, P]
     for fn in ("sv_tree_attention", "sv_verify_chain", "sv_verify_tree_greedy", "sv_compact_kv",
                "sv_verify_chain_noalloc", "sv_tree_attention_paged", "sv_compact_kv_paged",
-               "sv_verify_tree_stochastic"):
+               "sv_verify_tree_stochastic", "sv_verify_step_chain", "sv_verify_step_tree_greedy"):
         getattr(L, fn).restype = I
     L.sv_status_string.argtypes = [I]
     L.sv_status_string.restype = ctypes.c_char_p
@@ -152,23 +160,23 @@ def _opt(t, name, dtype, shape):
     return t
 
 
-def sv_workspace_size(op: int, B: int, T_or_N: int, V: int = 0, Hq: int = 0, Hkv: int = 0,
-                      D: int = 0) -> int:
-    return int(lib().sv_workspace_size(op, B, T_or_N, V, Hq, Hkv, D))
+def sv_workspace_size(op: int, B: int, T_or_N: int, V: int = 0, dtype: int = SV_BF16, Hq: int = 0,
+                      Hkv: int = 0, D: int = 0) -> int:
+    return int(lib().sv_workspace_size(op, B, T_or_N, V, dtype, Hq, Hkv, D))
 
 
 _ws_cache: dict = {}
 
 
-def workspace(op: int, B: int, T_or_N: int, V: int = 0, Hq: int = 0, Hkv: int = 0, D: int = 0,
-              device=None) -> torch.Tensor:
+def workspace(op: int, B: int, T_or_N: int, V: int = 0, dtype: int = SV_BF16, Hq: int = 0,
+              Hkv: int = 0, D: int = 0, device=None) -> torch.Tensor:
     """A zero-filled workspace for one call shape, cached per (shape, device).
     Calls sharing it must not overlap on the GPU."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    key = (op, B, T_or_N, V, Hq, Hkv, D, str(device))
+    key = (op, B, T_or_N, V, dtype, Hq, Hkv, D, str(device))
     ws = _ws_cache.get(key)
     if ws is None:
-        n = sv_workspace_size(op, B, T_or_N, V, Hq, Hkv, D)
+        n = sv_workspace_size(op, B, T_or_N, V, dtype, Hq, Hkv, D)
         if n == 0:
             raise SpecVerifyError("sv_workspace_size", SV_ERR_UNSUPPORTED)
         ws = torch.zeros(n, dtype=torch.uint8, device=device)
@@ -199,7 +207,7 @@ def sv_tree_attention(q, k_cache, v_cache, prefix_lens, parents=None, scale=None
     if out is None:
         out = torch.empty_like(q)
     if ws is None:
-        ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
+        ws = workspace(SV_OP_TREE_ATTENTION, B, T, Hq=Hq, Hkv=Hkv, D=D, device=q.device)
     rc = lib().sv_tree_attention(_p(q), _p(k_cache), _p(v_cache), _p(prefix_lens), _p(parents),
                                  _p(node_counts), B, T, Hq, Hkv, D, S_max, float(scale), _p(out),
                                  _p(seq_status), _p(ws), ws.numel(), _stream(stream))
@@ -234,7 +242,7 @@ def sv_tree_attention_paged(q, k_pages, v_pages, block_table, prefix_lens, paren
     if out is None:
         out = torch.empty_like(q)
     if ws is None:
-        ws = workspace(SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, q.device)
+        ws = workspace(SV_OP_TREE_ATTENTION, B, T, Hq=Hq, Hkv=Hkv, D=D, device=q.device)
     rc = lib().sv_tree_attention_paged(_p(q), _p(k_pages), _p(v_pages), _p(block_table), max_pages,
                                        num_pages, page_size, _p(prefix_lens), _p(parents),
                                        _p(node_counts), B, T, Hq, Hkv, D, float(scale), _p(out),
@@ -278,7 +286,7 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
     if out_tokens is None:
         out_tokens = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
     if ws is None:
-        ws = workspace(SV_OP_VERIFY_CHAIN, B, N, V, dt, 0, 0, dev)
+        ws = workspace(SV_OP_VERIFY_CHAIN, B, N, V, dt, device=dev)
     rc = lib().sv_verify_chain(_p(target_logits), _p(draft_logits), dt, _p(draft_tokens),
                                _p(draft_lens), _p(u_accept), _p(u_sample), B, N, V, _p(accepted_len),
                                _p(out_tokens), _p(probs_out), _p(seq_status), _p(ws), ws.numel(),
@@ -319,7 +327,7 @@ def sv_verify_tree_greedy(target_logits, node_tokens, parents, accepted_len=None
     if out_tokens is None:
         out_tokens = torch.empty(B, T, dtype=torch.int32, device=dev)
     if ws is None:
-        ws = workspace(SV_OP_VERIFY_TREE_GREEDY, B, T, V, dt, 0, 0, dev)
+        ws = workspace(SV_OP_VERIFY_TREE_GREEDY, B, T, V, dt, device=dev)
     rc = lib().sv_verify_tree_greedy(_p(target_logits), dt, _p(node_tokens), _p(parents),
                                      _p(node_counts), B, T, V,
                                      _p(accepted_len), _p(path_nodes), _p(out_tokens),
@@ -356,7 +364,7 @@ def sv_verify_tree_stochastic(target_logits, draft_logits, node_tokens, parents,
     if out_tokens is None:
         out_tokens = torch.empty(B, T, dtype=torch.int32, device=dev)
     if ws is None:
-        ws = workspace(SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, dt, 0, 0, dev)
+        ws = workspace(SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, dt, device=dev)
     rc = lib().sv_verify_tree_stochastic(_p(target_logits), _p(draft_logits), dt, _p(node_tokens),
                                          _p(parents), _p(node_counts), _p(u_accept),
                                          _p(u_sample), B, T, V,
@@ -364,6 +372,108 @@ def sv_verify_tree_stochastic(target_logits, draft_logits, node_tokens, parents,
                                          _p(seq_status), _p(ws), ws.numel(), _stream(stream))
     _check("sv_verify_tree_stochastic", rc)
     return accepted_len, path_nodes, out_tokens
+
+
+def _attn_shapes(q, k_cache, v_cache, prefix_lens, out, seq_status):
+    _req(q, "q", torch.bfloat16, 4)
+    _req(k_cache, "k_cache", torch.bfloat16, 4)
+    _req(v_cache, "v_cache", torch.bfloat16, 4)
+    _req(prefix_lens, "prefix_lens", torch.int32, 1)
+    B, T, Hq, D = q.shape
+    _, Hkv, S_max, _ = k_cache.shape
+    _shape(k_cache, "k_cache", (B, Hkv, S_max, D))
+    _shape(v_cache, "v_cache", k_cache.shape)
+    _shape(prefix_lens, "prefix_lens", (B,))
+    _opt(out, "attn_out", torch.bfloat16, q.shape)
+    _opt(seq_status, "attn_status", torch.int32, (B,))
+    return B, T, Hq, D, Hkv, S_max
+
+
+def sv_verify_step_chain(q, k_cache, v_cache, prefix_lens, target_logits, draft_logits,
+                         draft_tokens, u_accept, u_sample, attn_out=None, accepted_len=None,
+                         out_tokens=None, new_kv_lens=None, probs_out=None, attn_status=None,
+                         verify_status=None, draft_lens=None, scale=None, ws=None, stream=None):
+    """The fused chain step.  q [B,N+1,Hq,D] bf16; caches [B,Hkv,S_max,D] bf16;
+    prefix_lens [B] int32; logits and draws as sv_verify_chain.
+    Returns (attn_out, accepted_len, out_tokens, new_kv_lens)."""
+    B, T, Hq, D, Hkv, S_max = _attn_shapes(q, k_cache, v_cache, prefix_lens, attn_out,
+                                            attn_status)
+    _req(target_logits, "target_logits", None, 3)
+    _req(draft_logits, "draft_logits", target_logits.dtype, 3)
+    _req(draft_tokens, "draft_tokens", torch.int32, 2)
+    _req(u_accept, "u_accept", torch.float32, 2)
+    _req(u_sample, "u_sample", torch.float32, 1)
+    dt = _dtype_code(target_logits)
+    N = T - 1
+    V = target_logits.shape[2]
+    _shape(target_logits, "target_logits", (B, T, V))
+    _chain_shapes(B, N, V, draft_logits, draft_tokens, u_accept, u_sample, accepted_len,
+                  out_tokens, probs_out, verify_status)
+    _opt(draft_lens, "draft_lens", torch.int32, (B,))
+    _opt(new_kv_lens, "new_kv_lens", torch.int32, (B,))
+    dev = q.device
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if attn_out is None:
+        attn_out = torch.empty_like(q)
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    if new_kv_lens is None:
+        new_kv_lens = torch.empty_like(prefix_lens)
+    if ws is None:
+        ws = workspace(SV_OP_VERIFY_STEP_CHAIN, B, N, V, dt, Hq, Hkv, D, device=dev)
+    rc = lib().sv_verify_step_chain(
+        _p(q), _p(k_cache), _p(v_cache), _p(prefix_lens), Hq, Hkv, D, S_max, float(scale),
+        _p(attn_out), _p(attn_status), _p(target_logits), _p(draft_logits), dt, _p(draft_tokens),
+        _p(draft_lens), _p(u_accept), _p(u_sample), B, N, V, _p(accepted_len), _p(out_tokens),
+        _p(probs_out), _p(verify_status), _p(new_kv_lens), _p(ws), ws.numel(), _stream(stream))
+    _check("sv_verify_step_chain", rc)
+    return attn_out, accepted_len, out_tokens, new_kv_lens
+
+
+def sv_verify_step_tree_greedy(q, k_cache, v_cache, prefix_lens, parents, target_logits,
+                               node_tokens, attn_out=None, accepted_len=None, path_nodes=None,
+                               out_tokens=None, new_kv_lens=None, attn_status=None,
+                               verify_status=None, node_counts=None, scale=None, ws=None,
+                               stream=None):
+    """The fused tree step (greedy acceptance; the caches are compacted in
+    place).  q [B,T,Hq,D] bf16; caches [B,Hkv,S_max,D] bf16; parents [B,T]
+    int32 or None (a chain); logits [B,T,V]; node_tokens [B,T] int32.
+    Returns (attn_out, accepted_len, path_nodes, out_tokens, new_kv_lens)."""
+    B, T, Hq, D, Hkv, S_max = _attn_shapes(q, k_cache, v_cache, prefix_lens, attn_out,
+                                            attn_status)
+    _req(target_logits, "target_logits", None, 3)
+    _req(node_tokens, "node_tokens", torch.int32, 2)
+    dt = _dtype_code(target_logits)
+    V = target_logits.shape[2]
+    _shape(target_logits, "target_logits", (B, T, V))
+    _tree_shapes(B, T, node_tokens, parents, node_counts, accepted_len, path_nodes, out_tokens,
+                 verify_status)
+    _opt(new_kv_lens, "new_kv_lens", torch.int32, (B,))
+    dev = q.device
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if attn_out is None:
+        attn_out = torch.empty_like(q)
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if path_nodes is None:
+        path_nodes = torch.empty(B, T, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, T, dtype=torch.int32, device=dev)
+    if new_kv_lens is None:
+        new_kv_lens = torch.empty_like(prefix_lens)
+    if ws is None:
+        ws = workspace(SV_OP_VERIFY_STEP_TREE_GREEDY, B, T, V, dt, Hq, Hkv, D, device=dev)
+    rc = lib().sv_verify_step_tree_greedy(
+        _p(q), _p(k_cache), _p(v_cache), _p(prefix_lens), _p(parents), _p(node_counts), B, T, Hq,
+        Hkv, D, S_max, float(scale), _p(attn_out), _p(attn_status), _p(target_logits), dt,
+        _p(node_tokens), V, _p(accepted_len), _p(path_nodes), _p(out_tokens), _p(verify_status),
+        _p(new_kv_lens), _p(ws), ws.numel(), _stream(stream))
+    _check("sv_verify_step_tree_greedy", rc)
+    return attn_out, accepted_len, path_nodes, out_tokens, new_kv_lens
 
 
 def sv_compact_kv(k_cache, v_cache, prefix_lens, accepted_len, path_nodes=None, new_kv_lens=None,

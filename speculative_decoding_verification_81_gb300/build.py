@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libspecverify.so")
 
 SOURCES = ["sv_api.cu", "sv_attention.cu", "sv_attention_tc.cu", "sv_vocab.cu", "sv_compact.cu",
-           "sv_noalloc.cu"]
+           "sv_noalloc.cu", "sv_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

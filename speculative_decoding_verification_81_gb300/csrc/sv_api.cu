@@ -31,7 +31,8 @@ const char *sv_status_string(sv_status s) {
     return "unknown sv_status";
 }
 
-size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, int D) {
+size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, sv_dtype dtype, int Hq, int Hkv,
+                         int D) {
     if (B <= 0 || T_or_N <= 0) return 0;
     switch (op) {
         case SV_OP_TREE_ATTENTION: {
@@ -43,19 +44,29 @@ size_t sv_workspace_size(sv_op op, int B, int T_or_N, int V, int Hq, int Hkv, in
         }
         case SV_OP_VERIFY_CHAIN:
         case SV_OP_VERIFY_TREE_GREEDY: {
-            if (V <= 0 || (Hq != SV_F32 && Hq != SV_BF16)) return 0;
+            if (V <= 0 || (dtype != SV_F32 && dtype != SV_BF16)) return 0;
             // the shapes the calls refuse as unsupported have no size
             if (T_or_N > (op == SV_OP_VERIFY_CHAIN ? 63 : 1024) || V >= (1 << 30)) return 0;
-            const sv::VocabPlan pl = sv::plan_vocab(op == SV_OP_VERIFY_CHAIN, B, T_or_N, V, Hq);
+            const sv::VocabPlan pl = sv::plan_vocab(op == SV_OP_VERIFY_CHAIN, B, T_or_N, V, dtype);
             if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return 0;
             return pl.bytes;
         }
         case SV_OP_VERIFY_TREE_STOCHASTIC: {
-            if (V <= 0 || (Hq != SV_F32 && Hq != SV_BF16)) return 0;
+            if (V <= 0 || (dtype != SV_F32 && dtype != SV_BF16)) return 0;
             if (T_or_N > 1024 || V > (1 << 22)) return 0;
-            const sv::VocabPlan pl = sv::plan_vocab_stree(B, T_or_N, V, Hq);
+            const sv::VocabPlan pl = sv::plan_vocab_stree(B, T_or_N, V, dtype);
             if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return 0;
             return pl.bytes;
+        }
+        case SV_OP_VERIFY_STEP_CHAIN:
+        case SV_OP_VERIFY_STEP_TREE_GREEDY: {
+            const bool chain = op == SV_OP_VERIFY_STEP_CHAIN;
+            if (V <= 0 || (dtype != SV_F32 && dtype != SV_BF16)) return 0;
+            if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
+            if (T_or_N > (chain ? 63 : 1024) || V >= (1 << 30) || (!chain && Hkv > 256)) return 0;
+            const sv::VocabPlan pl = sv::plan_vocab(chain, B, T_or_N, V, dtype);
+            if ((size_t)B * pl.rows_per_seq * pl.nchunks >= (1u << 31)) return 0;
+            return sv::step_workspace_size(chain, B, T_or_N, V, dtype, Hq, Hkv, D);
         }
     }
     return 0;

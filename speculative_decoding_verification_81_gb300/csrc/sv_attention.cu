@@ -145,7 +145,8 @@ static void plan_workspace(AttnPlan &pl, int B, int Hkv) {
     pl.bytes = off;
 }
 
-sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPlan *plan) {
+sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPlan *plan,
+                         int max_ctas) {
     if (D != kD || T > kMaxT || B > kMaxB) return SV_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
     const int M = G * T;
@@ -170,7 +171,8 @@ sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPl
     if (occ < 1) return SV_ERR_CUDA;
     pl.grid = sms * occ;
     pl.cluster = 1;
-    plan_workspace(pl, B, Hkv);  // sized for the flat split whichever mode runs
+    plan_workspace(pl, B, Hkv);  // sized for the whole device's flat split, whichever mode runs
+    if (max_ctas > 0 && max_ctas < pl.grid) pl.grid = max_ctas;
     // Few row groups (fewer than half the CTAs the device holds): one cluster
     // per group, its tiles shared by the cluster's CTAs and merged in
     // distributed shared memory, instead of a flat split whose groups straddle
@@ -229,7 +231,12 @@ sv_status launch_tree_attention(const AttnArgs &a, const AttnPlan &pl, void *ws,
     p.num_pages = a.num_pages;
     p.page_size = a.page_size;
     p.node_counts = a.node_counts;
+    p.node_count_add = a.node_count_add;
     p.cluster = pl.cluster;
+    p.hook = a.hook;
+    p.hook_acc = a.hook_acc;
+    p.hook_path = a.hook_path;
+    p.hook_path_stride = a.hook_path_stride;
     void *args[] = {&tmk, &tmv, &tmq, &p};
     const void *fn = tc_kernel_fn(pl.stages, pl.mrows);
     if (pl.cluster <= 1)

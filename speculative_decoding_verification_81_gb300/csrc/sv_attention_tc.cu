@@ -115,6 +115,7 @@ struct TcSmem {
     float xl[4][2][32];          // [quarter][half][lane]: half-row sums at a segment end
     uint32_t tmem;
     int abort_flag;
+    int hook_last;  // fused step: this cluster brought its counter to the end
 };
 
 // ---------------------------------------------------------------- cluster mode
@@ -209,6 +210,41 @@ __device__ __forceinline__ void cluster_merge_cs(const AttnKParams &p, const flo
         }
         *reinterpret_cast<uint2 *>(orow + 4 * (j * kTpr + part)) =
             make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
+}
+
+// Compaction of one (sequence, KV head) in a fused tree step, by the 128
+// threads of the producer and MMA warps (t128), idle once the cluster barrier
+// is passed: rows L + path[d] -> L + d for d = 1..a, K and V.  Every source
+// row goes to shared memory (the idle K/V ring) before any row is written,
+// so an in-place move never reads a row another move has overwritten.
+// bar_id: a named barrier over exactly these 128 threads.
+__device__ __forceinline__ void hook_move_rows(const AttnKParams &p, int b, int kvh, uint4 *bounce,
+                                               int t128, int bar_id) {
+    const int a = __ldcg(p.hook_acc + b);
+    const int L = __ldcg(p.hook.prefix_lens + b);
+    const int Tb = nodes_of(p, b);
+    // a < 0: the sequence's tree or tokens were invalid; a cache that cannot
+    // hold the nodes: nothing was read for it either way
+    if (a <= 0 || L < 0 || Tb <= 0 || (long long)L + Tb > p.S_max || a >= Tb) return;
+    const int32_t *path = p.hook_path + (size_t)b * p.hook_path_stride;
+    constexpr int kWords = kD * 2 / 16;  // 16-byte words of a row
+    const size_t head = ((size_t)b * p.Hkv + kvh) * p.S_max;
+    const int n = a * 2 * kWords;
+    for (int w = t128; w < n; w += 128) {
+        const int d = 1 + w / (2 * kWords), kv = (w / kWords) & 1, word = w % kWords;
+        int src = __ldcg(path + d);
+        if (src < d || src >= Tb) src = d;  // (a walk's path never does this; stay in the sequence's rows)
+        const uint4 *from = kv ? p.hook.v : p.hook.k;
+        bounce[w] = from[(head + L + src) * kWords + word];
+    }
+    __syncwarp();
+    named_bar_sync(bar_id, 128);
+    for (int w = t128; w < n; w += 128) {
+        const int d = 1 + w / (2 * kWords), kv = (w / kWords) & 1, word = w % kWords;
+        if (__ldcg(path + d) == d) continue;  // already in place
+        uint4 *to = kv ? p.hook.v : p.hook.k;
+        to[(head + L + d) * kWords + word] = bounce[w];
     }
 }
 
@@ -983,6 +1019,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // barrier; then each finishes its own rows.
         cluster_sync_any();
         if (tid == 64) SV_STAMP(13);
+        if (p.hook.step_ctr && crank == 0 && !(warp >= 2 && warp < 2 + kSoftmaxWarps)) {
+            // fused tree step: every CTA of the cluster has read its tiles, so
+            // this row group is done with (sequence cb, KV head kvh); the last
+            // of its row groups and the walk to arrive moves the path's rows
+            const int kvh = cpr / p.RG;
+            // warps 0-1 -> 0..63, warps 2 + kSoftmaxWarps .. (10, 11) -> 64..127
+            const int t128 = warp < 2 ? tid : tid - 32 * kSoftmaxWarps;
+            int *ctr = p.hook.step_ctr + (size_t)cb * p.Hkv + kvh;
+            if (t128 == 0) {
+                const int old = atomicAdd(ctr, 1);
+                sh->hook_last = old == p.hook.rg_count;
+            }
+            __syncwarp();
+            named_bar_sync(2, 128);
+            if (sh->hook_last) {
+                __threadfence();  // the walk's path, written before its arrival
+                hook_move_rows(p, cb, kvh, reinterpret_cast<uint4 *>(smem), t128, 2);
+                if (t128 == 0) *ctr = 0;  // ready for the next call
+            }
+        }
         if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
             const int kvh = cpr / p.RG, rg = cpr - kvh * p.RG;
             const size_t c0 = (size_t)(blockIdx.x - crank);  // the cluster's first CTA

@@ -4,6 +4,7 @@
 #pragma once
 
 #include "sv_device.cuh"
+#include "sv_internal.h"
 
 namespace sv {
 
@@ -44,6 +45,15 @@ struct AttnKParams {
     // share of that group's key tiles; the shares are merged in distributed
     // shared memory.  0 or 1: the flat split over persistent CTAs.
     int cluster;
+    int node_count_add;  // T_b = node_counts[b] + node_count_add
+    // fused tree step in cluster mode (hook.step_ctr null otherwise): after a
+    // cluster's group is read, it arrives on its (sequence, KV head) counter;
+    // the last arrival moves the accepted path's rows (hook_acc, hook_path:
+    // the walk's outputs, path rows hook_path_stride apart)
+    StepHook hook;
+    const int32_t *hook_acc;
+    const int32_t *hook_path;
+    int hook_path_stride;
 };
 
 // Position in the unit list: sequence, (kv head * RG + row group), tile.
@@ -127,7 +137,7 @@ constexpr float kRescaleThreshold = 8.0f;
 // Nodes of sequence b: T_b, or 0 when out of range (the sequence is then invalid).
 __device__ __forceinline__ int nodes_of(const AttnKParams &p, int b) {
     if (!p.node_counts) return p.T;
-    const int n = p.node_counts[b];
+    const int n = p.node_counts[b] + p.node_count_add;
     return (n >= 1 && n <= p.T) ? n : 0;
 }
 

@@ -59,6 +59,7 @@ struct VocabPlan {
     int res_chunks;       // residual-draw chunks per sequence (chain only)
     int res_chunk_elems;
     int walk_cluster;     // CTAs per sequence of the stochastic tree walk (set at launch)
+    int max_ctas;         // cap on the streaming pass's persistent grid (0: one CTA per SM)
     bool vec;             // rows are 16-byte aligned: vector loads
     int recs_per_unit;    // chain: (max, sum) records per (row, chunk)
     size_t off_counters;  // 2*B + 4 ints: arrivals per sequence, then [2*B] a timeout flag
@@ -68,6 +69,8 @@ struct VocabPlan {
 };
 
 VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype);
+
+constexpr int kMaxResChunks = 256;  // chunks of a row in the chain's residual draw, at most
 
 struct ChainArgs {
     const void *target;
@@ -81,6 +84,24 @@ struct ChainArgs {
     int32_t *out_tokens;
     float *probs;
     int32_t *seq_status;
+    // fused step only (null otherwise): new_kv_lens[b] = prefix_lens[b] + a + 1
+    // when the sequence's cache holds its nodes (prefix_lens[b] + N_b + 1 <= S_max), else prefix_lens[b]
+    const int32_t *prefix_lens;
+    int32_t *new_kv_lens;
+    int S_max;
+};
+
+// Compaction folded into a fused tree step: the K/V rows of (sequence b, KV
+// head h) move once both the attention has finished reading them and the
+// path is known.  step_ctr[b * Hkv + h] counts those arrivals (rg_count row
+// groups of the attention, then the walk); whoever brings it to
+// rg_count + 1 moves the rows and resets it.
+struct StepHook {
+    int *step_ctr;             // [B * Hkv], zero between calls
+    uint4 *k, *v;              // contiguous caches [B, Hkv, S_max, D] as 16-byte words
+    const int32_t *prefix_lens;
+    int32_t *new_kv_lens;      // written by the walk
+    int Hkv, rg_count, S_max, D;
 };
 
 struct TreeArgs {
@@ -93,6 +114,10 @@ struct TreeArgs {
     int32_t *path_nodes;
     int32_t *out_tokens;
     int32_t *seq_status;
+    // fused step only: the compaction hook (step_ctr null otherwise), and
+    // new_kv_lens / prefix_lens written without it when the step compacts in
+    // a kernel of its own (then step_ctr null and new_kv_lens null)
+    StepHook hook;
 };
 
 // Stochastic (multi-draft) acceptance on a tree.
@@ -137,7 +162,10 @@ struct AttnPlan {
     size_t bytes;
 };
 
-sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPlan *plan);
+// max_ctas > 0 caps the CTAs the call may use (a fused step leaves the
+// rest of the SMs to the vocabulary pass); 0: the whole device.
+sv_status plan_attention(int B, int T, int Hq, int Hkv, int D, int S_max, AttnPlan *plan,
+                         int max_ctas = 0);
 
 // tcgen05 attention kernel (sv_attention_tc.cu)
 struct AttnKParams;
@@ -157,6 +185,11 @@ struct AttnArgs {
     const int32_t *block_table;  // null: contiguous caches [B, Hkv, S_max, D]
     int max_pages, num_pages, page_size;
     const int32_t *node_counts;  // per-sequence T_b, or null
+    int node_count_add;          // T_b = node_counts[b] + this (1 for a chain's draft lengths)
+    StepHook hook;               // fused tree step in cluster mode (step_ctr null otherwise)
+    const int32_t *hook_acc;     // the walk's accepted lengths and paths [B, path_stride]
+    const int32_t *hook_path;
+    int hook_path_stride;
 };
 
 sv_status launch_tree_attention(const AttnArgs &args, const AttnPlan &plan, void *ws,
@@ -182,5 +215,10 @@ struct CompactArgs {
 sv_status launch_compact_kv(const CompactArgs &args, cudaStream_t stream);
 
 int device_sm_count();
+
+// Workspace of a fused step: attention, vocabulary pass, then (trees) the
+// compaction counters, each 256-byte aligned; 0 if the attention shape is unsupported.
+size_t step_workspace_size(bool chain, int B, int T_or_N, int V, int dtype, int Hq, int Hkv,
+                           int D);
 
 }  // namespace sv

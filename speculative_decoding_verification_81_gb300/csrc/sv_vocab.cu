@@ -35,7 +35,6 @@ constexpr int kLoadsPerThread = 8;         // 16-byte loads per thread per strea
 constexpr int kResLoadsPerThread = 4;      // 16-byte loads per thread per row in the residual draw
 constexpr int kMaxChainN = 63;
 constexpr int kMaxTreeT = 1024;
-constexpr int kMaxResChunks = 256;
 
 template <typename T>
 struct Elem;
@@ -801,6 +800,13 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
         if (tid == 0) {
             a.accepted_len[b] = acc;
             if (a.seq_status) a.seq_status[b] = late ? SV_ERR_TIMEOUT : bad ? SV_ERR_BAD_INPUT : SV_OK;
+            if (a.new_kv_lens) {
+                // fused step: a chain's accepted rows are already in place
+                // (node d at slot L + d), so compaction is the new length
+                const int L = a.prefix_lens[b];
+                const bool fits = L >= 0 && (long long)L + Nb + 1 <= a.S_max;
+                a.new_kv_lens[b] = (fits && acc >= 0) ? L + acc + 1 : L;
+            }
         }
         for (int j = tid; j <= a.N; j += kVT) {
             int v = -1;
@@ -1231,6 +1237,67 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
 }
 
+// Fused tree step: the walk's half of the compaction.  It writes the new
+// cache length, then arrives on the counter of every KV head of sequence b;
+// for each head where it arrives last (the attention has read that head's
+// rows) it moves the path's rows itself: rows L + path[d] -> L + d, d = 1..a,
+// K and V, every source read into registers before any row is written.
+constexpr int kMaxStepHkv = 256;
+constexpr int kStepRowWords = 16;  // 16-byte words of a 128-dim bf16 row
+constexpr int kStepMoveRegs = 8;   // words a thread holds: 256 * 8 >= 63 rows * 2 * 16
+
+__device__ __forceinline__ void step_hook_arrive(const TreeArgs &a, int b, const TreeWalkSmem &ts) {
+    __shared__ unsigned char s_last[kMaxStepHkv];
+    __shared__ int s_any;
+    const StepHook &h = a.hook;
+    const int acc = ts.bad ? -1 : ts.depth[ts.best];
+    const int L = h.prefix_lens[b];
+    const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+    const bool fits = L >= 0 && tb_raw >= 1 && tb_raw <= a.T && (long long)L + tb_raw <= h.S_max;
+    if (threadIdx.x == 0) {
+        h.new_kv_lens[b] = (fits && acc >= 0) ? L + acc + 1 : L;
+        s_any = 0;
+    }
+    __threadfence();  // this thread's path and token writes, before the arrivals
+    __syncthreads();
+    for (int hh = threadIdx.x; hh < h.Hkv; hh += kVT) {
+        const int old = atomicAdd(h.step_ctr + (size_t)b * h.Hkv + hh, 1);
+        s_last[hh] = old == h.rg_count;
+        if (old == h.rg_count) s_any = 1;
+    }
+    __syncthreads();
+    if (!s_any) return;
+    __threadfence();  // the attention has finished with these rows
+    const bool move = fits && acc > 0;
+    for (int hh = 0; hh < h.Hkv; ++hh) {
+        if (!s_last[hh]) continue;
+        if (move) {
+            const size_t head = ((size_t)b * h.Hkv + hh) * h.S_max;
+            const int n = acc * 2 * kStepRowWords;
+            uint4 reg[kStepMoveRegs];
+#pragma unroll
+            for (int k = 0; k < kStepMoveRegs; ++k) {
+                const int wi = threadIdx.x + k * kVT;
+                if (wi < n) {
+                    const int d = 1 + wi / (2 * kStepRowWords), kv = (wi / kStepRowWords) & 1;
+                    reg[k] = (kv ? h.v : h.k)[(head + L + ts.path[d]) * kStepRowWords + wi % kStepRowWords];
+                }
+            }
+            __syncthreads();  // every source of this head is read
+#pragma unroll
+            for (int k = 0; k < kStepMoveRegs; ++k) {
+                const int wi = threadIdx.x + k * kVT;
+                if (wi < n) {
+                    const int d = 1 + wi / (2 * kStepRowWords), kv = (wi / kStepRowWords) & 1;
+                    if (ts.path[d] != d)
+                        (kv ? h.v : h.k)[(head + L + d) * kStepRowWords + wi % kStepRowWords] = reg[k];
+                }
+            }
+        }
+        if (threadIdx.x == 0) h.step_ctr[(size_t)b * h.Hkv + hh] = 0;  // ready for the next call
+    }
+}
+
 // The greedy walk after the streaming argmax pass: one CTA per sequence
 // merges each node row's records into the row's argmax, then walks.
 template <typename T>
@@ -1259,6 +1326,7 @@ __global__ void __launch_bounds__(kVT) tree_decide_kernel(TreeArgs a, VocabPlan 
     }
     const bool late = __ldcg(w.counters + 2 * a.B) != 0;
     tree_walk(a, b, late, ts);
+    if (a.hook.step_ctr) step_hook_arrive(a, b, ts);
 }
 
 // ---------------------------------------------------------------- stochastic tree
@@ -1666,8 +1734,9 @@ static cudaError_t launch_chain_t(ChainArgs a, VocabPlan p, WsView w, cudaStream
                 return e;
             attr_set[dev] = 1;
         }
-        const int sms = device_sm_count();
+        int sms = device_sm_count();
         if (sms <= 0) return cudaErrorUnknown;
+        if (p.max_ctas > 0 && p.max_ctas < sms) sms = p.max_ctas;
         const unsigned grid = (unsigned)(items < (unsigned)sms ? items : (unsigned)sms);
         e = launch_pdl(fn, dim3(grid), dim3(kSThreads), smem, st, args);
     } else {
@@ -1698,8 +1767,9 @@ static cudaError_t launch_tree_t(TreeArgs a, VocabPlan p, WsView w, cudaStream_t
                 return e;
             attr_set[dev] = 1;
         }
-        const int sms = device_sm_count();
+        int sms = device_sm_count();
         if (sms <= 0) return cudaErrorUnknown;
+        if (p.max_ctas > 0 && p.max_ctas < sms) sms = p.max_ctas;
         const unsigned grid = (unsigned)(items < (unsigned)sms ? items : (unsigned)sms);
         if ((e = launch_pdl(fn, dim3(grid), dim3(kSThreads), smem, st, args)) != cudaSuccess) return e;
         return launch_pdl((const void *)tree_decide_kernel<T>, dim3((unsigned)a.B), dim3(kVT), 0, st,

@@ -105,7 +105,7 @@ def main():
     pl = torch.full((B,), L, dtype=torch.int32, device=dev)
     par = (torch.from_numpy(np.broadcast_to(W.medusa_tree(T), (B, T)).copy()).to(dev)
            if tree == "medusa" else None)
-    ws = api.workspace(api.SV_OP_TREE_ATTENTION, B, T, 0, Hq, Hkv, D, dev)
+    ws = api.workspace(api.SV_OP_TREE_ATTENTION, B, T, Hq=Hq, Hkv=Hkv, D=D, device=dev)
 
     # every set is read once per replay, the stamped (last) call's set least recently
     ncalls = max(args.behind + 1, copies)
