@@ -4,9 +4,12 @@ Workload (default): the fused chain verify step -- B=32 sequences, N=8 draft
 tokens (T=9 query positions), prefix KV length 4096, 32 query / 8 KV heads,
 head_dim 128, bf16 K/V ~ N(0,1); bf16 target and draft logits over
 V=128256 (target ~ N(0,3) plus one boosted token per row, draft = target +
-N(0,1)); seeded uniforms.  One step = tree attention with the causal chain
-mask + stochastic acceptance with residual resample / bonus token + KV
-compaction, all through the library's C ABI.
+N(0,1)); seeded uniforms.  One step = one call of the library's C ABI,
+sv_verify_step_chain: attention with the causal chain mask beside the
+stochastic acceptance (residual resample / bonus token), and KV compaction.
+Also reported: each call alone, the three calls one after another, the
+Medusa and EAGLE tree steps, the latency-bound chain workloads 1-2, a ragged
+batch, decode-shaped and paged attention.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,7 +45,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-sample-seqs", type=int, default=32)
+    ap.add_argument("--cpu-sample-seqs", type=int, default=12)
     ap.add_argument("--profile", action="store_true",
                     help="device-resident steps only (for ncu): no graph, e2e, clocks or CPU leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -198,41 +201,110 @@ def whole_job_rate(world, steps_per_rank, ms):
     return world * steps_per_rank / (ms / 1e3)
 
 
+def host_description():
+    """The host the CPU numbers were taken on: logical CPUs and CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
 def run_reference(args, cfg, inp, rank, budget_s=60.0):
-    """The oracle as it stands, one core.  A step of the reference is one
-    sequence of the workload (its attention rows, its chain acceptance, its
-    compaction) scaled by B to a full step; as many steps as fit in about a
-    minute are timed (at most --steps), so that any --steps/--warmup finishes
-    in a few minutes."""
+    """The oracle as it stands, one core.  A step of the reference is a
+    bounded sample of the workload: one of its B sequences (that sequence's
+    attention rows, chain acceptance and compaction), timed as it runs
+    (`ms_per_step` is that sample's time) and reported in full steps/s (the
+    sample is 1/B of a step).  As many steps as fit in about a minute are
+    timed (at most --steps), after --warmup untimed ones."""
     if rank != 0:
         return None
     nseq = 1
-    t_first = oracle_sample(cfg, inp, nseq) if args.warmup > 0 else None
-    if t_first is None:
+    t_first = None
+    for _ in range(max(1, args.warmup)):
         t_first = oracle_sample(cfg, inp, nseq)
     n = max(1, min(args.steps, int(budget_s / max(t_first, 1e-3))))
     times = [oracle_sample(cfg, inp, nseq) for _ in range(n)]
-    per_step = sum(times) / len(times) * cfg["B"] / nseq      # seconds per full step
-    value = 1.0 / per_step
+    per_sample = sum(times) / len(times)
+    value = (nseq / cfg["B"]) / per_sample  # full steps per second
     sample = (f"{nseq} of {cfg['B']} sequences per timed step (attention for all its heads and "
-              f"positions, chain acceptance, compaction), {n} steps timed, scaled to full steps")
+              f"positions, chain acceptance, compaction), {n} steps timed; value in full steps/s")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-        "n_gpus": args.gpus, "steps": n, "requested_steps": args.steps, "warmup": 1,
-        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "n_gpus": args.gpus, "steps": n, "requested_steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_sample * 1e3, "sample_fraction_of_step": nseq / cfg["B"],
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_desc(cfg),
         "positions_per_s": value * cfg["B"] * (cfg["N"] + 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_description()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
 # ------------------------------------------------------------------ GPU path
 
+def make_capture(dev, stream):
+    """fn captured as a CUDA graph (run once eagerly first: the library makes
+    its side stream and tables on a call's first run, never inside a capture)."""
+    import torch
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize(dev)
+        return g
+    return capture
+
+
+def graph_ms(capture, fn, reps, dev, stream, per_replay=1):
+    """Milliseconds per unit of fn: fn captured once, the graph replayed reps
+    times back to back (CUDA events on the launching stream), divided by the
+    per_replay units one replay runs."""
+    import torch
+    g = capture(fn)
+    for _ in range(3):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / (reps * per_replay)
+
+
+def l2_bytes(dev):
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        return 126 * 2**20
+
+
 def tree_step_bench(cfg, dev, capture, stream, reps):
-    """Steps/s and HBM fraction of one tree verification step (attention over
-    the tree, greedy acceptance, compaction) on synthetic inputs of `cfg`."""
+    """Steps/s and HBM fraction of one tree verification step -- the fused
+    call sv_verify_step_tree_greedy (attention beside the greedy acceptance,
+    compaction folded in) -- on synthetic inputs of `cfg`; the step's three
+    calls one after another, each call alone, and the stochastic acceptance
+    of the same trees as context.  The graphs cycle through enough input sets
+    that their total exceeds 3x L2, so each step reads its inputs from HBM."""
     import torch
     import speculative_decoding_verification_81_gb300 as sv
     from speculative_decoding_verification_81_gb300 import workloads as W
@@ -244,8 +316,11 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     else:
         par_np = np.stack([W.random_tree(T, cfg["max_depth"], rng) for _ in range(B)])
     g = torch.Generator(device=dev).manual_seed(5)
-    one = (B * Hkv * S_max * D * 2 * 2 + 2 * B * T * Hq * D * 2 + 2 * B * T * V * 2)
-    copies = max(1, -(-160 * 2**20 // one))  # enough copies to exceed L2
+    kv = B * Hkv * (L + T) * D * 2 * 2
+    qo = 2 * B * T * Hq * D * 2
+    attn_bytes = kv + qo
+    step_bytes = attn_bytes + B * T * V * 2
+    copies = max(1, -(-int(3.05 * l2_bytes(dev)) // step_bytes))
     sets = []
     for _ in range(copies):
         x = dict(q=torch.randn(B, T, Hq, D, device=dev, generator=g).to(torch.bfloat16),
@@ -280,6 +355,13 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
     ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, T, Hq=Hq, Hkv=Hkv, D=D, device=dev)
     ws_t = sv.workspace(sv.SV_OP_VERIFY_TREE_GREEDY, B, T, V, sv.SV_BF16, device=dev)
     ws_s = sv.workspace(sv.SV_OP_VERIFY_TREE_STOCHASTIC, B, T, V, sv.SV_BF16, device=dev)
+    ws_f = sv.workspace(sv.SV_OP_VERIFY_STEP_TREE_GREEDY, B, T, V, sv.SV_BF16, Hq, Hkv, D,
+                        device=dev)
+
+    def fused(x):
+        sv.sv_verify_step_tree_greedy(x["q"], x["k"], x["v"], pl, par, x["logits"], x["tok"],
+                                      attn_out=x["out"], accepted_len=acc, path_nodes=path,
+                                      out_tokens=otok, new_kv_lens=newl, ws=ws_f)
 
     def attention(x):
         sv.sv_tree_attention(x["q"], x["k"], x["v"], pl, par, out=x["out"], ws=ws_a)
@@ -295,49 +377,114 @@ def tree_step_bench(cfg, dev, capture, stream, reps):
         sv.sv_verify_tree_stochastic(x["logits"], x["draft"], x["stok"], par, ua, us,
                                      accepted_len=acc, path_nodes=path, out_tokens=otok, ws=ws_s)
 
-    def cycle(fns):
+    def per_step(fns):
         def f():
             for x in sets:
                 for fn in fns:
                     fn(x)
-        return f
-
-    def per_step(fns):
-        gr = capture(cycle(fns))
-        for _ in range(3):
-            gr.replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        n = max(20, reps // copies)
-        e0.record(stream)
-        for _ in range(n):
-            gr.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / (n * copies)
+        return graph_ms(capture, f, max(20, reps // copies), dev, stream, per_replay=copies)
 
     peak, _ = load_peaks()
-    step_ms = per_step([attention, greedy, compact])
+    step_ms = per_step([fused])
+    fused_acc = float(acc.float().mean().item())
+    serial_ms = per_step([attention, greedy, compact])
     attn_ms = per_step([attention])
     greedy_ms = per_step([greedy])
-    greedy_acc = float(acc.float().mean().item())
     stochastic_ms = per_step([stochastic])
     stoch_acc = float(acc.float().mean().item())
-    kv = B * Hkv * (L + T) * D * 2 * 2
-    qo = 2 * B * T * Hq * D * 2
-    attn_bytes = kv + qo
-    step_bytes = attn_bytes + B * T * V * 2
-    res = {"workload": cfg["name"], "steps_per_s": 1e3 / step_ms,
+    res = {"workload": cfg["name"], "call": "sv_verify_step_tree_greedy",
+           "steps_per_s": 1e3 / step_ms,
            "verified_positions_per_s": B * T * 1e3 / step_ms, "step_ms": step_ms,
-           "attention_ms": attn_ms, "greedy_ms": greedy_ms,
+           "serial_step_ms": serial_ms, "attention_ms": attn_ms, "greedy_ms": greedy_ms,
            "stochastic_ms": stochastic_ms, "stochastic_accepted_mean": stoch_acc,
            "step_hbm_frac": step_bytes / (step_ms / 1e3) / 1e9 / peak,
            "attention_hbm_frac": attn_bytes / (attn_ms / 1e3) / 1e9 / peak,
            "algorithmic_bytes": {"step": step_bytes, "attention": attn_bytes},
-           "l2": f"{copies} input copies cycled" if copies > 1 else "inputs larger than L2",
-           "accepted_mean": greedy_acc}
+           "l2": f"{copies} input sets cycled ({copies * step_bytes / 2**20:.0f} MB, "
+                 f"{copies * step_bytes / l2_bytes(dev):.1f}x L2)",
+           "accepted_mean": fused_acc,
+           "serial": "sv_tree_attention, sv_verify_tree_greedy, sv_compact_kv one after another"}
     del sets
     return res
+
+
+def latency_bench(k, dev, capture, stream):
+    """Chain acceptance alone on workload k (1: B=1 N=4 V=1024 f32; 2: B=8
+    N=5 V=32000 bf16), latency-bound: the time of one call as the only node
+    of a graph (what a lone step waits, graph launch gap included) and the
+    throughput of 64 calls per graph (steps that follow each other)."""
+    import torch
+    import speculative_decoding_verification_81_gb300 as sv
+    from speculative_decoding_verification_81_gb300 import workloads as W
+    inp = W.workload(k)
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+    t, d = up(inp["target"]), up(inp["draft"])
+    tok, ua, us = up(inp["draft_tokens"]), up(inp["u_accept"]), up(inp["u_sample"])
+    B, N = inp["draft_tokens"].shape
+    V = inp["target"].shape[2]
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.SV_OP_VERIFY_CHAIN, B, N, V,
+                      sv.SV_F32 if t.dtype == torch.float32 else sv.SV_BF16, device=dev)
+
+    def call():
+        sv.sv_verify_chain(t, d, tok, ua, us, accepted_len=acc, out_tokens=out, ws=ws)
+
+    lone_ms = graph_ms(capture, call, 2000, dev, stream)
+
+    def many():
+        for _ in range(64):
+            call()
+    many_ms = graph_ms(capture, many, 200, dev, stream, per_replay=64)
+    esz = 4 if t.dtype == torch.float32 else 2
+    return {"workload": W.WORKLOADS[k]["name"], "call": "sv_verify_chain",
+            "latency_us": lone_ms * 1e3, "steps_per_s": 1e3 / many_ms,
+            "verified_positions_per_s": B * (N + 1) * 1e3 / many_ms,
+            "algorithmic_bytes": B * (2 * N + 1) * V * esz,
+            "how": "latency: one call per graph replay; steps/s: 64 calls per graph replay "
+                   "(inputs stay in L2: these shapes are latency-bound, not HBM-bound)"}
+
+
+def ragged_bench(cfg, d, dev, capture, stream, reps):
+    """The fused chain step on a variable-length batch (f2): the bench's
+    caches and logits, with per-sequence prefix lengths uniform in
+    [L/2, L] and draft lengths uniform in [1, N] (seeded)."""
+    import torch
+    import speculative_decoding_verification_81_gb300 as sv
+    B, N, L, Hq, Hkv, D, V = (cfg[k] for k in ("B", "N", "L", "Hq", "Hkv", "D", "V"))
+    rng = np.random.default_rng(2024)
+    Ls = rng.integers(L // 2, L + 1, B).astype(np.int32)
+    Ns = rng.integers(1, N + 1, B).astype(np.int32)
+    pl = torch.from_numpy(Ls).to(dev)
+    dl = torch.from_numpy(Ns).to(dev)
+    out = torch.empty_like(d["q"])
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    newl = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.SV_OP_VERIFY_STEP_CHAIN, B, N, V, sv.SV_BF16, Hq, Hkv, D, device=dev)
+
+    def step():
+        sv.sv_verify_step_chain(d["q"], d["k"], d["v"], pl, d["target"], d["draft"], d["tokens"],
+                                d["ua"], d["us"], attn_out=out, accepted_len=acc,
+                                out_tokens=toks, new_kv_lens=newl, draft_lens=dl, ws=ws)
+    ms = graph_ms(capture, step, reps, dev, stream)
+    kv = int(sum(Hkv * (int(Ls[b]) + int(Ns[b]) + 1) * D * 4 for b in range(B)))
+    qo = int(sum(2 * (int(Ns[b]) + 1) * Hq * D * 2 for b in range(B)))
+    logits = int(sum((2 * int(Ns[b]) + 1) * V * 2 for b in range(B)))
+    peak, _ = load_peaks()
+    step_bytes = kv + qo + logits
+    return {"workload": f"ragged fused chain step: B={B}, prefix lengths in [{L // 2}, {L}], "
+                        f"draft lengths in [1, {N}], 32q/8kv D=128 V={V}",
+            "call": "sv_verify_step_chain (draft_lens)", "step_ms": ms,
+            "steps_per_s": 1e3 / ms, "verified_positions_per_s": int((Ns + 1).sum()) * 1e3 / ms,
+            "step_hbm_frac": step_bytes / (ms / 1e3) / 1e9 / peak,
+            "algorithmic_bytes": step_bytes, "prefix_lens_mean": float(Ls.mean()),
+            "draft_lens_mean": float(Ns.mean())}
 
 
 def run_ours(args, cfg, inp, rank, world, local_rank):
@@ -348,6 +495,7 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     torch.cuda.set_device(dev)
     a, c = inp["attn"], inp["chain"]
     B, N, V = cfg["B"], cfg["N"], cfg["V"]
+    Hq, Hkv, D = cfg["Hq"], cfg["Hkv"], cfg["D"]
 
     def to_host(x):
         x = np.ascontiguousarray(x)
@@ -367,20 +515,19 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     toks = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
     newl = torch.empty(B, dtype=torch.int32, device=dev)
-    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, N + 1, Hq=cfg["Hq"], Hkv=cfg["Hkv"], D=cfg["D"],
-                        device=dev)
+    ws_f = sv.workspace(sv.SV_OP_VERIFY_STEP_CHAIN, B, N, V, sv.SV_BF16, Hq, Hkv, D, device=dev)
+    ws_a = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, N + 1, Hq=Hq, Hkv=Hkv, D=D, device=dev)
     ws_c = sv.workspace(sv.SV_OP_VERIFY_CHAIN, B, N, V, sv.SV_BF16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(dd):
-        sv.sv_tree_attention(dd["q"], dd["k"], dd["v"], dd["prefix_lens"], None, out=out, ws=ws_a)
-        sv.sv_verify_chain(dd["target"], dd["draft"], dd["tokens"], dd["ua"], dd["us"],
-                           accepted_len=acc, out_tokens=toks, ws=ws_c)
-        sv.sv_compact_kv(dd["k"], dd["v"], dd["prefix_lens"], acc, None, new_kv_lens=newl)
+        """One verification step through the public C ABI: the fused call."""
+        sv.sv_verify_step_chain(dd["q"], dd["k"], dd["v"], dd["prefix_lens"], dd["target"],
+                                dd["draft"], dd["tokens"], dd["ua"], dd["us"], attn_out=out,
+                                accepted_len=acc, out_tokens=toks, new_kv_lens=newl, ws=ws_f)
 
-    # attention (split pairs merged in-kernel), chain statistics, decisions and
-    # residual draw, compaction: four kernels a step
-    launches_per_step = 4
+    # the attention, the chain statistics, the decisions and residual draw: three kernels
+    launches_per_step = 3
 
     def barrier():
         if world > 1:
@@ -400,33 +547,9 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
         return {"profile": True, "steps": args.steps, "warmup": args.warmup,
                 "launches": launches_per_step * (args.steps + args.warmup)}
     K = args.steps
-
-    # The step, and each call alone, captured as CUDA graphs: replaying them
-    # keeps the GPU queue full, so the timings are the GPU's own and not the
-    # host's launch rate.
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            fn()
-        stream.wait_stream(side)
-        torch.cuda.synchronize(dev)
-        with torch.cuda.graph(g):
-            fn()
-        torch.cuda.synchronize(dev)
-        return g
-
-    def call_attention():
-        sv.sv_tree_attention(d["q"], d["k"], d["v"], d["prefix_lens"], None, out=out, ws=ws_a)
-
-    def call_chain():
-        sv.sv_verify_chain(d["target"], d["draft"], d["tokens"], d["ua"], d["us"],
-                           accepted_len=acc, out_tokens=toks, ws=ws_c)
-
-    def call_compact():
-        sv.sv_compact_kv(d["k"], d["v"], d["prefix_lens"], acc, None, new_kv_lens=newl)
-
+    capture = make_capture(dev, stream)
+    # The step captured as a CUDA graph: replaying it keeps the GPU queue
+    # full, so the timing is the GPU's own and not the host's launch rate.
     g_step = capture(lambda: step(d))
     for _ in range(args.warmup):
         g_step.replay()
@@ -442,37 +565,40 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     total_ms = slowest(t0.elapsed_time(t1))
     clk = clocks.summary()
 
-    def time_graph(fn, reps):
-        g = capture(fn)
-        for _ in range(3):
-            g.replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / reps
-
     reps = max(50, min(K, 2000))
-    attn_ms = time_graph(call_attention, reps)
-    chain_ms = time_graph(call_chain, reps)
-    compact_ms = time_graph(call_compact, reps)
+
+    def call_attention():
+        sv.sv_tree_attention(d["q"], d["k"], d["v"], d["prefix_lens"], None, out=out, ws=ws_a)
+
+    def call_chain():
+        sv.sv_verify_chain(d["target"], d["draft"], d["tokens"], d["ua"], d["us"],
+                           accepted_len=acc, out_tokens=toks, ws=ws_c)
+
+    def call_compact():
+        sv.sv_compact_kv(d["k"], d["v"], d["prefix_lens"], acc, None, new_kv_lens=newl)
+
+    def serial_step():
+        call_attention()
+        call_chain()
+        call_compact()
+
+    attn_ms = graph_ms(capture, call_attention, reps, dev, stream)
+    chain_ms = graph_ms(capture, call_chain, reps, dev, stream)
+    compact_ms = graph_ms(capture, call_compact, reps, dev, stream)
+    serial_ms = graph_ms(capture, serial_step, reps, dev, stream)
 
     # ---- the verification pass against plain decoding: the same attention
     # call with T = 1 (one new token per sequence) and T = 5 (N = 4), over the
     # same caches; the ratio to T = 1 is the verification overhead per pass
     decode = {}
     for Tq in (1, 5):
-        qx = torch.randn(B, Tq, cfg["Hq"], cfg["D"], device=dev).to(torch.bfloat16)
+        qx = torch.randn(B, Tq, Hq, D, device=dev).to(torch.bfloat16)
         ox = torch.empty_like(qx)
-        wsx = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, Tq, Hq=cfg["Hq"], Hkv=cfg["Hkv"],
-                           D=cfg["D"], device=dev)
+        wsx = sv.workspace(sv.SV_OP_TREE_ATTENTION, B, Tq, Hq=Hq, Hkv=Hkv, D=D, device=dev)
 
         def call_t(qx=qx, ox=ox, wsx=wsx):
             sv.sv_tree_attention(qx, d["k"], d["v"], d["prefix_lens"], None, out=ox, ws=wsx)
-        decode[Tq] = time_graph(call_t, reps)
+        decode[Tq] = graph_ms(capture, call_t, reps, dev, stream)
     # ---- the same attention over a paged cache (page table in random order):
     # page_size 128 (a page per key tile) and 16 (eight pages per tile)
     paged = {}
@@ -480,46 +606,47 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     for ps in (128, 16):
         max_pages = -(-S_max // ps)
         num_pages = B * max_pages
-        g = torch.Generator(device="cpu").manual_seed(ps)
-        table = torch.randperm(num_pages, generator=g).to(torch.int32).view(B, max_pages).to(dev)
-        kp = torch.empty(num_pages, cfg["Hkv"], ps, cfg["D"], dtype=torch.bfloat16, device=dev)
+        gen = torch.Generator(device="cpu").manual_seed(ps)
+        table = torch.randperm(num_pages, generator=gen).to(torch.int32).view(B, max_pages).to(dev)
+        kp = torch.empty(num_pages, Hkv, ps, D, dtype=torch.bfloat16, device=dev)
         vp = torch.empty_like(kp)
         pad = max_pages * ps - S_max
         kl = torch.nn.functional.pad(d["k"], (0, 0, 0, pad))
         vl = torch.nn.functional.pad(d["v"], (0, 0, 0, pad))
         # logical page j of sequence b -> physical page table[b, j]
-        kp[table.flatten().long()] = kl.view(B, cfg["Hkv"], max_pages, ps, cfg["D"]).permute(
-            0, 2, 1, 3, 4).reshape(num_pages, cfg["Hkv"], ps, cfg["D"])
-        vp[table.flatten().long()] = vl.view(B, cfg["Hkv"], max_pages, ps, cfg["D"]).permute(
-            0, 2, 1, 3, 4).reshape(num_pages, cfg["Hkv"], ps, cfg["D"])
+        kp[table.flatten().long()] = kl.view(B, Hkv, max_pages, ps, D).permute(
+            0, 2, 1, 3, 4).reshape(num_pages, Hkv, ps, D)
+        vp[table.flatten().long()] = vl.view(B, Hkv, max_pages, ps, D).permute(
+            0, 2, 1, 3, 4).reshape(num_pages, Hkv, ps, D)
         outp = torch.empty_like(out)
         del kl, vl
 
         def call_p(kp=kp, vp=vp, table=table, outp=outp):
             sv.sv_tree_attention_paged(d["q"], kp, vp, table, d["prefix_lens"], None, out=outp,
                                        ws=ws_a)
-        paged[f"page_size={ps}"] = time_graph(call_p, reps)
+        paged[f"page_size={ps}"] = graph_ms(capture, call_p, reps, dev, stream)
         del kp, vp
     paged_attention = {"attention_ms": paged, "contiguous_ms": attn_ms,
                        "how": "sv_tree_attention_paged alone, one call per CUDA graph"}
 
     # ---- the tree verification steps (Medusa tree, B=4 L=2048 T=26 V=32000;
-    # EAGLE-style random tree, B=16 L=8192 T=64 V=128256): attention, greedy
-    # acceptance and compaction, device-resident, one step per graph replay.
-    # The Medusa step's inputs (41 MB) fit in L2, so its graph cycles through
-    # four copies (164 MB) and each step reads inputs last touched four steps
-    # before.
+    # EAGLE-style random tree, B=16 L=8192 T=64 V=128256): the fused step,
+    # device-resident, cycling through input sets totalling more than 3x L2
     from speculative_decoding_verification_81_gb300 import workloads as W
     tree_steps = {wl: tree_step_bench(W.WORKLOADS[wl], dev, capture, stream, reps)
                   for wl in (3, 5)}
+    latency_steps = {wl: latency_bench(wl, dev, capture, stream) for wl in (1, 2)}
+    ragged = ragged_bench(cfg, d, dev, capture, stream, reps)
 
     decode_baseline = {
-        "attention_ms": {"T=1 (decode)": decode[1], "T=5 (N=4)": decode[5], f"T={N + 1} (N={N})": attn_ms},
+        "attention_ms": {"T=1 (decode)": decode[1], "T=5 (N=4)": decode[5],
+                         f"T={N + 1} (N={N})": attn_ms},
         "verify_over_decode": {"N=4": decode[5] / decode[1], f"N={N}": attn_ms / decode[1]},
         "how": "sv_tree_attention alone, one call per CUDA graph, same K/V caches and prefix",
     }
 
-    # ---- end to end: inputs from pinned host memory, result read back, every step
+    # ---- end to end: inputs from pinned host memory, the fused step, the
+    # result read back, every step
     e2e = None
     if not args.no_e2e:
         pinned = {k: v.pin_memory() for k, v in host.items()}
@@ -552,13 +679,13 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
         barrier()
         e2e_ms = slowest(e0.elapsed_time(e1))
         e2e = {"value": whole_job_rate(world, KE, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": KE}
+               "d2h_bytes_per_step": d2h, "steps": KE,
+               "call": "sv_verify_step_chain with host copies in and out"}
         del pinned, dd
 
     ab = algorithmic_bytes(cfg)
     peak, peak_kind = load_peaks()
-    attn_s = attn_ms / 1e3
-    achieved = ab["attention"] / attn_s / 1e9
+    achieved = ab["attention"] / (attn_ms / 1e3) / 1e9
     step_s = total_ms / 1e3 / K
     value = whole_job_rate(world, K, total_ms)
     res = {
@@ -569,20 +696,25 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
         "config": workload_desc(cfg),
         "positions_per_s": value * B * (N + 1),
         "drafted_positions_per_s": value * B * N,
+        "step_call": "sv_verify_step_chain (attention beside the acceptance; compaction folded in)",
         "step_hbm": {"algorithmic_bytes": ab["step"], "achieved_gbs": ab["step"] / step_s / 1e9,
                      "peak_gbs": peak, "frac": ab["step"] / step_s / 1e9 / peak,
                      "peak_kind": peak_kind},
-        "roofline": {"kernel": "tree_attention_kernel", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "tree_attention_tc_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": committed_traffic(), "algorithmic_bytes": ab["attention"],
                      "avg_launch_ms": attn_ms,
-                     "peak_kind": f"{peak_kind} (copy bandwidth)"},
+                     "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "how": "sv_tree_attention alone (its one kernel), CUDA-graph replays"},
         "call_ms": {"sv_tree_attention": attn_ms, "sv_verify_chain": chain_ms,
-                    "sv_compact_kv": compact_ms,
-                    "how": "each call captured alone in a CUDA graph, replayed back to back"},
+                    "sv_compact_kv": compact_ms, "serial_step": serial_ms,
+                    "how": "each captured alone in a CUDA graph, replayed back to back; "
+                           "serial_step: the three calls one after another"},
         "decode_baseline": decode_baseline,
         "paged_attention": paged_attention,
         "tree_steps": tree_steps,
+        "latency_steps": latency_steps,
+        "ragged_step": ragged,
         "clocks": clk,
         "gpu_launches": launches_per_step * K,
         "timing": "CUDA-graph replays of the whole step, CUDA events on the launching stream",
@@ -627,13 +759,15 @@ def main():
     res = run_ours(args, cfg, inp, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline and not args.profile:
         nseq = args.cpu_sample_seqs
-        secs = oracle_sample(cfg, inp, nseq)
+        runs = sorted(oracle_sample(cfg, inp, nseq) for _ in range(3))
+        secs = runs[1]  # the median of three runs
         v = (nseq / cfg["B"]) / secs
         res["cpu_baseline"] = {
             "value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{nseq} of {cfg['B']} sequences of one step (attention over all heads "
-                      f"and positions, chain acceptance, compaction) in {secs:.1f} s, "
-                      f"scaled to full steps"}
+                      f"and positions, chain acceptance, compaction): median of 3 runs "
+                      f"({', '.join(f'{r:.2f}' for r in runs)} s), scaled to full steps",
+            "host": host_description()}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

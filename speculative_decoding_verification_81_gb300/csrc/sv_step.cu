@@ -20,6 +20,7 @@
 //          (an arrival counter in the workspace); otherwise a compaction
 //          kernel runs after the join.
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "sv_internal.h"
@@ -61,13 +62,22 @@ sv_status side_stream(SideStream **out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// CTAs left to the vocabulary pass: its share of the step's bytes (K/V taken
-// at the cache capacity S_max, the prefix lengths being device data), at
-// least 8 and at most half the device.
-int side_ctas(int sms, double attn_bytes, double vocab_bytes) {
-    int n = (int)std::lround(sms * vocab_bytes / (attn_bytes + vocab_bytes));
+// CTAs left to the vocabulary side: its share of the step's cost, scaled by
+// `boost`, at least 8 and at most half the device.  The costs are bytes (K/V
+// taken at the cache capacity S_max, the prefix lengths being device data),
+// the attention's multiplied by its row groups (each group streams every
+// tile through the tensor cores).  A chain's side ends with the latency-bound
+// residual draw, so it needs its statistics done well before the attention:
+// boost 1.5 (measured on B=32, N=8, L=4096: the two sides then end
+// together); a tree's walk is shorter: 1.3.
+int side_ctas(int sms, double attn_cost, double vocab_cost, double boost) {
+    int n = (int)std::lround(boost * sms * vocab_cost / (attn_cost + vocab_cost));
     if (n < 8) n = 8;
     if (n > sms / 2) n = sms / 2;
+#ifdef SV_PHASE_STAMPS
+    // the diagnostic build lets the phase tool try other splits
+    if (const char *e = getenv("SV_STEP_SIDE_CTAS")) n = atoi(e);
+#endif
     return n;
 }
 
@@ -118,7 +128,7 @@ sv_status sv_verify_step_chain(const void *q, const void *k_cache, const void *v
     if (sms <= 0) return SV_ERR_CUDA;
     const int esz = dtype == SV_F32 ? 4 : 2;
     const int side = side_ctas(sms, 4.0 * B * Hkv * (double)S_max * D,
-                               (double)B * (2 * N + 1) * V * esz);
+                               (double)B * (2 * N + 1) * V * esz, 1.5);
     AttnPlan ap;
     sv_status st = plan_attention(B, T, Hq, Hkv, D, S_max, &ap, sms - side);
     if (st != SV_OK) return st;
@@ -217,7 +227,8 @@ sv_status sv_verify_step_tree_greedy(const void *q, void *k_cache, void *v_cache
     sv_status st = plan_attention(B, T, Hq, Hkv, D, S_max, &ap, sms - 8);
     if (st != SV_OK) return st;
     if (ap.cluster <= 1) {
-        const int side = side_ctas(sms, 4.0 * B * Hkv * (double)S_max * D, (double)B * T * V * esz);
+        const int side = side_ctas(sms, 4.0 * B * Hkv * (double)S_max * D * ap.rg,
+                                   (double)B * T * V * esz, 1.3);
         if ((st = plan_attention(B, T, Hq, Hkv, D, S_max, &ap, sms - side)) != SV_OK) return st;
     }
     VocabPlan vp = plan_vocab(false, B, T, V, dtype);

@@ -29,6 +29,32 @@
 
 namespace sv {
 
+// Kernel spans (a diagnostic build only, -DSV_PHASE_STAMPS): the first start
+// and the last end (globaltimer) of each streaming / decision kernel over the
+// launches since sv_debug_vocab_clear, read by sv_debug_vocab_spans.  The
+// library proper compiles them out.
+#ifdef SV_PHASE_STAMPS
+enum { kSpanChainStats, kSpanChainResidual, kSpanTreeStats, kSpanTreeDecide, kSpanCount };
+static __device__ unsigned long long g_vspan[kSpanCount][2];
+__device__ __forceinline__ unsigned long long span_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+struct SpanGuard {  // the end is taken at every exit of the warp
+    int id;
+    __device__ explicit SpanGuard(int i) : id(i) {
+        if (threadIdx.x == 0) atomicMin(&g_vspan[id][0], span_now());
+    }
+    __device__ ~SpanGuard() {
+        if ((threadIdx.x & 31) == 0) atomicMax(&g_vspan[id][1], span_now());
+    }
+};
+#define SV_SPAN(id) SpanGuard sv_span_guard_(id)
+#else
+#define SV_SPAN(id) ((void)0)
+#endif
+
 constexpr int kVT = 256;                   // threads per vocabulary CTA
 constexpr int kVWarps = kVT / 32;
 constexpr int kLoadsPerThread = 8;         // 16-byte loads per thread per streaming item
@@ -379,6 +405,7 @@ constexpr int kSWordsPerLane = kSUnitBytes / 16 / kSGroupWarps / 32;  // 16-byte
 template <typename T>
 __global__ void __launch_bounds__(kSThreads, 1)
     chain_stats_stream_kernel(ChainArgs a, VocabPlan p, WsView w) {
+    SV_SPAN(kSpanChainStats);
     extern __shared__ __align__(128) uint8_t ring[];  // kSStages * kSUnitBytes
     __shared__ uint64_t full[kSStages], empty[kSStages];
     constexpr int PV = Elem<T>::kPerVec;
@@ -821,6 +848,7 @@ template <typename T, bool VEC>
 // (Aligned rows: at most 64 registers, so that four CTAs per SM keep a
 // B = 32, V = 128256 grid in one wave.)
 __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
+    SV_SPAN(kSpanChainResidual);
     constexpr int EPT = kResLoadsPerThread * Elem<T>::kPerVec;
     __shared__ float2 wsum[kVWarps];
     __shared__ float2 s_tot[kMaxResChunks];
@@ -1008,22 +1036,30 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
 struct TreeWalkSmem {
     int am[kMaxTreeT], par[kMaxTreeT], tok[kMaxTreeT], depth[kMaxTreeT], path[kMaxTreeT];
     unsigned char ok[kMaxTreeT];
-    int best, bad;
+    int best, bad, tb_raw;
+    int prefix_len;  // fused step: L_b, read with the other inputs
 };
 
-// Greedy longest agreeing path of sequence b from the target's argmax per
-// node (ts.am, -1 for none), by a whole CTA of kVT threads: validation, the
-// walk in node order, then the outputs.  `late`: the statistics pass gave
-// up, so no decision is taken.
-__device__ __forceinline__ void tree_walk(const TreeArgs &a, int b, bool late, TreeWalkSmem &ts) {
+// The walk's inputs of sequence b -- parents, node tokens, node count -- into
+// shared memory, by the whole CTA (a barrier must follow before they are read).
+__device__ __forceinline__ void tree_walk_load(const TreeArgs &a, int b, TreeWalkSmem &ts) {
     for (int i = threadIdx.x; i < a.T; i += kVT) {
         ts.par[i] = a.parents ? a.parents[(size_t)b * a.T + i] : i - 1;  // NULL: a chain
         ts.tok[i] = a.tokens[(size_t)b * a.T + i];
     }
+    if (threadIdx.x == 0) ts.tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+    if (threadIdx.x == 32 && a.hook.step_ctr) ts.prefix_len = a.hook.prefix_lens[b];
+}
+
+// Greedy longest agreeing path of sequence b from the target's argmax per
+// node (ts.am, -1 for none) and the inputs tree_walk_load brought in, by a
+// whole CTA of kVT threads: validation, the walk in node order, then the
+// outputs.  `late`: the statistics pass gave up, so no decision is taken.
+__device__ __forceinline__ void tree_walk(const TreeArgs &a, int b, bool late, TreeWalkSmem &ts) {
     __syncthreads();
     if (threadIdx.x == 0) {
         // this sequence's nodes; those past T_b are padding
-        const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+        const int tb_raw = ts.tb_raw;
         int bad = late || ts.par[0] != -1 || tb_raw < 1 || tb_raw > a.T;
         const int Tb = bad ? 1 : tb_raw;
         for (int i = 1; i < Tb && !bad; ++i)
@@ -1109,6 +1145,7 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
             w.partials + (size_t)b * per_seq + (size_t)rr * p.nchunks, p.nchunks);
         if (lane == 0) ts.am[rr] = rp.idx == INT_MAX ? -1 : rp.idx;
     }
+    tree_walk_load(a, b, ts);
     tree_walk(a, b, false, ts);
     if (threadIdx.x == 0) w.counters[b] = 0;  // ready for the next call
 }
@@ -1125,6 +1162,7 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
 template <typename T>
 __global__ void __launch_bounds__(kSThreads, 1)
     tree_stats_stream_kernel(TreeArgs a, VocabPlan p, WsView w) {
+    SV_SPAN(kSpanTreeStats);
     extern __shared__ __align__(128) uint8_t ring[];  // kSStages * kSUnitBytes
     __shared__ uint64_t full[kSStages], empty[kSStages];
     constexpr int PV = Elem<T>::kPerVec;
@@ -1251,8 +1289,8 @@ __device__ __forceinline__ void step_hook_arrive(const TreeArgs &a, int b, const
     __shared__ int s_any;
     const StepHook &h = a.hook;
     const int acc = ts.bad ? -1 : ts.depth[ts.best];
-    const int L = h.prefix_lens[b];
-    const int tb_raw = a.node_counts ? a.node_counts[b] : a.T;
+    const int L = ts.prefix_len;
+    const int tb_raw = ts.tb_raw;
     const bool fits = L >= 0 && tb_raw >= 1 && tb_raw <= a.T && (long long)L + tb_raw <= h.S_max;
     if (threadIdx.x == 0) {
         h.new_kv_lens[b] = (fits && acc >= 0) ? L + acc + 1 : L;
@@ -1302,27 +1340,50 @@ __device__ __forceinline__ void step_hook_arrive(const TreeArgs &a, int b, const
 // merges each node row's records into the row's argmax, then walks.
 template <typename T>
 __global__ void __launch_bounds__(kVT) tree_decide_kernel(TreeArgs a, VocabPlan p, WsView w) {
+    SV_SPAN(kSpanTreeDecide);
     __shared__ TreeWalkSmem ts;
+    const int b = blockIdx.x;
+    // The tree and its tokens are inputs of the call, not outputs of the
+    // argmax pass: they are read while that pass still runs (this grid starts
+    // only after the pass has passed its own wait for the work before the
+    // call, so they are complete); only the records wait for the pass.
+    tree_walk_load(a, b, ts);
     griddep_wait();
     griddep_launch_dependents();
-    const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per_row = p.nchunks * kSGroupWarps;
     const float2 *rec = reinterpret_cast<const float2 *>(w.partials) + (size_t)b * a.T * per_row;
-    for (int rr = warp; rr < a.T; rr += kVWarps) {
-        float best = kNegInf;
-        int idx = INT_MAX;
-        for (int i = lane; i < per_row; i += 32) {
-            const float2 r2 = __ldcg(rec + (size_t)rr * per_row + i);
-            merge_argmax(best, idx, r2.x, __float_as_int(r2.y));
+    // a warp per row, four rows of a warp with their loads in flight together
+    for (int r0 = warp; r0 < a.T; r0 += 4 * kVWarps) {
+        float best[4];
+        int idx[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            best[q] = kNegInf;
+            idx[q] = INT_MAX;
+        }
+        for (int i0 = 0; i0 < per_row; i0 += 32) {
+            float2 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rr = r0 + q * kVWarps, i = i0 + lane;
+                v[q] = (rr < a.T && i < per_row) ? __ldcg(rec + (size_t)rr * per_row + i)
+                                                 : make_float2(kNegInf, __int_as_float(INT_MAX));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) merge_argmax(best[q], idx[q], v[q].x, __float_as_int(v[q].y));
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float b2 = __shfl_xor_sync(0xffffffffu, best, off);
-            const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
-            merge_argmax(best, idx, b2, i2);
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float b2 = __shfl_xor_sync(0xffffffffu, best[q], off);
+                const int i2 = __shfl_xor_sync(0xffffffffu, idx[q], off);
+                merge_argmax(best[q], idx[q], b2, i2);
+            }
+            const int rr = r0 + q * kVWarps;
+            if (lane == 0 && rr < a.T) ts.am[rr] = idx[q] == INT_MAX ? -1 : idx[q];
         }
-        if (lane == 0) ts.am[rr] = idx == INT_MAX ? -1 : idx;
     }
     const bool late = __ldcg(w.counters + 2 * a.B) != 0;
     tree_walk(a, b, late, ts);
@@ -1908,3 +1969,19 @@ sv_status launch_verify_tree_stochastic(const STreeArgs &a, int dtype, const Voc
 }
 
 }  // namespace sv
+
+#ifdef SV_PHASE_STAMPS
+// Spans of the kernels above (first start, last end; globaltimer ns), in the
+// order chain statistics, chain residual draw, tree argmax pass, tree walk.
+extern "C" int sv_debug_vocab_spans(unsigned long long *dst) {
+    return cudaMemcpyFromSymbol(dst, sv::g_vspan, sizeof(sv::g_vspan)) == cudaSuccess ? 0 : -1;
+}
+extern "C" int sv_debug_vocab_clear(void) {
+    unsigned long long init[sv::kSpanCount][2];
+    for (int i = 0; i < sv::kSpanCount; ++i) {
+        init[i][0] = ~0ull;
+        init[i][1] = 0ull;
+    }
+    return cudaMemcpyToSymbol(sv::g_vspan, init, sizeof(init)) == cudaSuccess ? 0 : -1;
+}
+#endif

@@ -9,6 +9,8 @@ for the previous kernel).
 
     python -m speculative_decoding_verification_81_gb300.phases [--shape medusa|chain|small]
         [--reps N] [--behind N]
+    python -m speculative_decoding_verification_81_gb300.phases --step chain|medusa|eagle
+        [--side-ctas N]
 
 --behind N: the stamped launch is the last of N + 1 calls in one CUDA graph,
 as in a stream of steps; its CTAs may be placed while the call before it
@@ -53,6 +55,119 @@ POINTS = [
     (16, "CTA end"),
 ]
 
+def step_timeline(args):
+    """The kernels of one fused step on a time line: for the attention, its
+    CTAs' first entry, first return from the wait for the previous kernel and
+    last end; for the acceptance's kernels, their first start and last end.
+    The step is the only node of its graph, replayed once after a warm one;
+    the inputs are cycled (3 x L2) as in the bench."""
+    import torch
+
+    from . import api
+    from . import workloads as W
+
+    if args.side_ctas:
+        os.environ["SV_STEP_SIDE_CTAS"] = str(args.side_ctas)
+    L_ = api.use_library(build_phases_lib())
+    for fn in ("sv_debug_attention_stamps", "sv_debug_vocab_spans"):
+        getattr(L_, fn).restype = ctypes.c_int
+    L_.sv_debug_attention_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    L_.sv_debug_vocab_spans.argtypes = [ctypes.c_void_p]
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(9)
+    Hq, Hkv, D = 32, 8, 128
+    if args.step == "chain":
+        cfg = W.WORKLOADS[4]
+        B, L, T, V = cfg["B"], cfg["L"], cfg["N"] + 1, cfg["V"]
+    else:
+        cfg = W.WORKLOADS[3 if args.step == "medusa" else 5]
+        B, L, T, V = cfg["B"], cfg["L"], cfg["T"], cfg["V"]
+    S = L + 64
+    rows = (2 * T - 1) if args.step == "chain" else T
+    one = B * Hkv * S * D * 4 + B * rows * V * 2
+    copies = max(1, -(-3 * 126 * 2**20 // one))
+    sets = []
+    for _ in range(copies):
+        x = dict(q=torch.randn(B, T, Hq, D, device=dev, generator=g).to(torch.bfloat16),
+                 k=torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16),
+                 v=torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16),
+                 t=(torch.randn(B, T, V, device=dev, generator=g) * 3).to(torch.bfloat16))
+        if args.step == "chain":
+            x["d"] = (x["t"][:, :T - 1].float() + torch.randn(B, T - 1, V, device=dev,
+                                                               generator=g)).to(torch.bfloat16)
+            x["tok"] = torch.randint(0, V, (B, T - 1), device=dev, generator=g, dtype=torch.int32)
+        else:
+            x["tok"] = torch.randint(0, V, (B, T), device=dev, generator=g, dtype=torch.int32)
+        sets.append(x)
+    pl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    newl = torch.empty_like(pl)
+    ua = torch.rand(B, T, device=dev, generator=g)
+    us = torch.rand(B, device=dev, generator=g)
+    if args.step == "medusa":
+        par = torch.from_numpy(np.broadcast_to(W.medusa_tree(T), (B, T)).copy()).to(dev)
+    elif args.step == "eagle":
+        r = np.random.default_rng(5)
+        par = torch.from_numpy(np.stack([W.random_tree(T, 8, r) for _ in range(B)])).to(dev)
+
+    def step(i):
+        x = sets[i % copies]
+        if args.step == "chain":
+            api.sv_verify_step_chain(x["q"], x["k"], x["v"], pl, x["t"], x["d"], x["tok"],
+                                     ua_c, us,
+                                     new_kv_lens=newl)
+        else:
+            api.sv_verify_step_tree_greedy(x["q"], x["k"], x["v"], pl, par, x["t"], x["tok"],
+                                           new_kv_lens=newl)
+    ua_c = ua[:, :T - 1].contiguous()
+    stream = torch.cuda.current_stream()
+    for i in range(copies):
+        step(i)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(copies):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            step(i)
+        graphs.append(gr)
+    rows_out = []
+    for rep_i in range(args.reps):
+        for gr in graphs[:-1]:
+            gr.replay()
+        torch.cuda.synchronize()
+        L_.sv_debug_attention_clear()
+        L_.sv_debug_vocab_clear()
+        graphs[-1].replay()
+        torch.cuda.synchronize()
+        buf = np.zeros(1024 * SLOTS, np.int64)
+        assert L_.sv_debug_attention_stamps(buf.ctypes.data, 1024) == 0
+        raw = buf.reshape(1024, SLOTS)
+        raw = raw[raw[:, 0] > 0]
+        ghz = args.sm_ghz
+        entry = raw[:, 0].astype(np.float64)
+        waited = entry + (raw[:, 2] - raw[:, 1]) / ghz
+        end = entry + (raw[:, 16] - raw[:, 1]) / ghz
+        spans = np.zeros(8, np.uint64)
+        assert L_.sv_debug_vocab_spans(spans.ctypes.data) == 0
+        spans = spans.reshape(4, 2).astype(np.float64)
+        t0 = min(entry.min(), spans[spans[:, 1] > 0, 0].min())
+        row = {"attention: first CTA entry": entry.min() - t0,
+               "attention: first wait return": waited.min() - t0,
+               "attention: last CTA end": end.max() - t0}
+        names = ["chain statistics", "chain decisions + residual draw", "tree argmax pass",
+                 "tree walk (+ compaction)"]
+        for i, nm in enumerate(names):
+            if spans[i, 1] > 0:
+                row[f"{nm}: start"] = spans[i, 0] - t0
+                row[f"{nm}: end"] = spans[i, 1] - t0
+        rows_out.append(row)
+    print(f"step {args.step}: B={B} L={L} T={T} V={V}; {copies} input sets; "
+          f"side CTAs override {args.side_ctas or 'none'}; median of {args.reps} steps; "
+          f"us from the first kernel start")
+    for k in rows_out[0]:
+        vals = [r[k] for r in rows_out if k in r]
+        print(f"{k:44s} {np.median(vals) / 1e3:8.2f}")
+
+
 SHAPES = {
     # name: (B, L, T, tree)
     "medusa": (4, 2048, 26, "medusa"),
@@ -69,6 +184,10 @@ def build_phases_lib(force: bool = False) -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--shape", choices=sorted(SHAPES), default="medusa")
+    ap.add_argument("--step", choices=["chain", "medusa", "eagle"], default=None,
+                    help="time line of one fused step instead of the attention's phases")
+    ap.add_argument("--side-ctas", type=int, default=0,
+                    help="chain step: SMs left to the acceptance (default: the library's split)")
     ap.add_argument("--reps", type=int, default=5, help="stamped runs (the table is their median)")
     ap.add_argument("--behind", type=int, default=3)
     ap.add_argument("--sm-ghz", type=float, default=2.07,
@@ -76,6 +195,9 @@ def main():
     ap.add_argument("--copies", type=int, default=0,
                     help="input sets cycled (default: enough for 3 x 126 MB)")
     args = ap.parse_args()
+    if args.step:
+        step_timeline(args)
+        return
 
     import torch
 

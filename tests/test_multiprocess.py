@@ -75,7 +75,11 @@ def test_reference_arm_under_torchrun_prints_once():
                 "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
-    assert d["ms_per_step"] * d["value"] == pytest.approx(1e3, rel=1e-6)  # one rate, two units
+    # ms_per_step is the time of one timed (sampled) step, value is in full
+    # steps/s: the sample is sample_fraction_of_step of a step
+    frac = d["sample_fraction_of_step"]
+    assert 0 < frac <= 1
+    assert d["ms_per_step"] * d["value"] == pytest.approx(1e3 * frac, rel=1e-6)
     cb, e2e = d["cpu_baseline"], d["e2e"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
