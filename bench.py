@@ -48,6 +48,11 @@ def parse():
     ap.add_argument("--cpu-sample-seqs", type=int, default=12)
     ap.add_argument("--profile", action="store_true",
                     help="device-resident steps only (for ncu): no graph, e2e, clocks or CPU leg")
+    ap.add_argument("--profile-workload", default="chain",
+                    choices=["chain", "chain-b8", "medusa", "eagle", "eagle-b4"],
+                    help="with --profile: the fused chain step (B=32, or B=8), or the tree "
+                         "workloads' kernels one call at a time (Medusa B=4 T=26 L=2048; "
+                         "EAGLE-style B=16, or B=4, T=64 L=8192)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -487,6 +492,77 @@ def ragged_bench(cfg, d, dev, capture, stream, reps):
             "draft_lens_mean": float(Ns.mean())}
 
 
+def profile_run(args, dev):
+    """--profile: --warmup then --steps eager rounds of one workload's calls
+    (no graphs, no timing), so that a profiler sees every kernel launch.
+    chain / chain-b8: the fused chain step.  medusa / eagle / eagle-b4: the
+    fused tree step, then sv_tree_attention, sv_verify_tree_greedy,
+    sv_verify_tree_stochastic and sv_compact_kv, one call each a round."""
+    import torch
+    import speculative_decoding_verification_81_gb300 as sv
+    from speculative_decoding_verification_81_gb300 import workloads as W
+    name = args.profile_workload
+    g = torch.Generator(device=dev).manual_seed(11)
+    Hq, Hkv, D = 32, 8, 128
+    if name.startswith("chain"):
+        cfg = W.WORKLOADS[4]
+        B, N, L, V = (8 if name == "chain-b8" else cfg["B"]), cfg["N"], cfg["L"], cfg["V"]
+        T = N + 1
+    else:
+        cfg = W.WORKLOADS[3 if name == "medusa" else 5]
+        B, T, L, V = cfg["B"], cfg["T"], cfg["L"], cfg["V"]
+        if name == "eagle-b4":
+            B = 4
+    S = L + 64
+    q = torch.randn(B, T, Hq, D, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16)
+    pl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    newl = torch.empty_like(pl)
+    out = torch.empty_like(q)
+    us = torch.rand(B, device=dev, generator=g)
+    calls = []
+    if name.startswith("chain"):
+        t = (torch.randn(B, T, V, device=dev, generator=g) * 3).to(torch.bfloat16)
+        d = (t[:, :N].float() + torch.randn(B, N, V, device=dev, generator=g)).to(torch.bfloat16)
+        tok = torch.randint(0, V, (B, N), device=dev, generator=g, dtype=torch.int32)
+        ua = torch.rand(B, N, device=dev, generator=g)
+        calls.append(lambda: sv.sv_verify_step_chain(q, k, v, pl, t, d, tok, ua, us, attn_out=out,
+                                                     new_kv_lens=newl))
+        launches = 3
+    else:
+        if name == "medusa":
+            par = torch.from_numpy(np.broadcast_to(W.medusa_tree(T), (B, T)).copy()).to(dev)
+        else:
+            r = np.random.default_rng(5)
+            par = torch.from_numpy(np.stack([W.random_tree(T, 8, r) for _ in range(B)])).to(dev)
+        t = (torch.randn(B, T, V, device=dev, generator=g) * 3).to(torch.bfloat16)
+        d = (t.float() + torch.randn(B, T, V, device=dev, generator=g)).to(torch.bfloat16)
+        am = t.float().argmax(-1).to(torch.int32)
+        tok = torch.where(torch.rand(B, T, device=dev, generator=g) < cfg["p_match"],
+                          am.gather(1, par.clamp(min=0).long()),
+                          torch.randint(0, V, (B, T), device=dev, generator=g, dtype=torch.int32))
+        ua = torch.rand(B, T, device=dev, generator=g)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        path = torch.empty(B, T, dtype=torch.int32, device=dev)
+        calls.append(lambda: sv.sv_verify_step_tree_greedy(q, k, v, pl, par, t, tok, attn_out=out,
+                                                           new_kv_lens=newl))
+        calls.append(lambda: sv.sv_tree_attention(q, k, v, pl, par, out=out))
+        calls.append(lambda: sv.sv_verify_tree_greedy(t, tok, par, accepted_len=acc,
+                                                      path_nodes=path))
+        calls.append(lambda: sv.sv_verify_tree_stochastic(t, d, tok, par, ua, us))
+        calls.append(lambda: sv.sv_compact_kv(k, v, pl, acc, path, new_kv_lens=newl))
+        # the fused step (attention, argmax pass, walk; + a compaction kernel in
+        # the flat split), then attention, greedy (2), stochastic (2), compaction
+        launches = 3 + 1 + 2 + 2 + 1
+    for _ in range(args.warmup + args.steps):
+        for c in calls:
+            c()
+    torch.cuda.synchronize(dev)
+    return {"profile": name, "steps": args.steps, "warmup": args.warmup,
+            "launches": launches * (args.steps + args.warmup)}
+
+
 def run_ours(args, cfg, inp, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_81_gb300 as sv
@@ -540,12 +616,6 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     # ---- device-resident timed region
     for _ in range(args.warmup):
         step(d)
-    if args.profile:
-        for _ in range(args.steps):
-            step(d)
-        torch.cuda.synchronize(dev)
-        return {"profile": True, "steps": args.steps, "warmup": args.warmup,
-                "launches": launches_per_step * (args.steps + args.warmup)}
     K = args.steps
     capture = make_capture(dev, stream)
     # The step captured as a CUDA graph: replaying it keeps the GPU queue
@@ -754,6 +824,9 @@ def main():
     if world > 1:
         torch.distributed.barrier()
         __graft_entry__.build()
+    if args.profile:
+        print(json.dumps(profile_run(args, torch.device("cuda", local_rank))), flush=True)
+        return
     # every rank verifies its own independent batch (different seed)
     inp = W.workload(4, seed=1004 + 7919 * rank)
     res = run_ours(args, cfg, inp, rank, world, local_rank)

@@ -381,18 +381,20 @@ sv_status sv_verify_step_tree_greedy(const void *q, void *k_cache, void *v_cache
  *
  * Some callers cannot hand the library a workspace because they cannot
  * allocate device memory where they call it: a plugin whose host has given
- * all device memory to its own pool and exposes no allocator, a real-time
+ * all device memory to its own pool and exposes no allocator, or a real-time
  * loop that must not take the device-wide synchronisation cudaMalloc and
- * cudaFree imply, or code that runs while a stream capture is open.  This
- * call computes exactly what sv_verify_chain computes (same arguments, same
- * outputs, same kernels) but keeps its scratch in a fixed array inside the
- * library, SV_NOALLOC_SCRATCH_BYTES long.  Every GPU that loads the library
- * holds that array until the process exits.
+ * cudaFree imply.  This call computes what sv_verify_chain computes with
+ * draft_lens = NULL (every sequence drafted all N tokens; a ragged batch
+ * goes through sv_verify_chain), with the same kernels and outputs, but keeps
+ * its scratch in a fixed array inside the library, SV_NOALLOC_SCRATCH_BYTES
+ * long.  Every GPU that loads the library holds that array until the process
+ * exits.
  *
  * - It calls no cudaMalloc, cudaFree or other allocating routine.
  * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture on the device.
+ *   (cudaGetSymbolAddress) with that device current and keeps it for the
+ *   life of the process: call it in the device's primary context, and not
+ *   after a cudaDeviceReset of that device.
  * - All calls share the one array, which keeps the last call's contents; each
  *   call clears the part that must start at zero (cudaMemsetAsync on
  *   `stream`).  Calls that overlap on the GPU (other streams, other host

@@ -20,7 +20,8 @@ std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached for the process: valid in
+// the device's primary context until a cudaDeviceReset of the device.
 sv_status scratch_on_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;

@@ -1,14 +1,16 @@
 """sv_verify_chain_noalloc, the chain-acceptance entry point for callers that
 cannot allocate device memory where they call the library (a plugin whose
-host owns all device memory, a real-time loop that must avoid cudaMalloc's
-device-wide synchronisation, code inside an open stream capture).  It takes
-no workspace and keeps its scratch in a fixed array of the library.
+host owns all device memory and exposes no allocator, a real-time loop that
+must not take the device-wide synchronisation of cudaMalloc and cudaFree).
+It takes no workspace and keeps its scratch in a fixed array of the library.
 
 Checked through the C ABI: two calls in a row give exactly the outputs of
-sv_verify_chain on the same inputs (the same kernels run), and a shape whose
-scratch exceeds the fixed array is refused before anything is launched.
-This file is collected last so that a failure here leaves every other test
-already run; it also passes on its own in a fresh process.
+sv_verify_chain on the same inputs (the same kernels run) and agree with the
+oracle (tokens and lengths bit-exact except the oracle's flagged near-ties,
+p and q within 1e-5 relative), and a shape whose scratch exceeds the fixed
+array is refused before anything is launched.  This file is collected last
+so that a failure here leaves every other test already run; it also passes
+on its own in a fresh process.
 """
 import ctypes
 
@@ -42,7 +44,7 @@ def _noalloc_call(t, d, tok, ua, us, acc, out, probs, status):
 
 
 @pytest.mark.parametrize("case", ["llama_vocab", "fused_step_logits", "fp32_small"])
-def test_noalloc_matches_workspace_entry_point(case):
+def test_noalloc_matches_workspace_entry_point(orc, case):
     if case == "llama_vocab":
         inp = W.workload(2)
     elif case == "fused_step_logits":
@@ -74,6 +76,17 @@ def test_noalloc_matches_workspace_entry_point(case):
         assert torch.equal(status, ref_status), call
         rel = ((probs - ref_probs).abs() / ref_probs.abs().clamp_min(1e-30)).max().item()
         assert rel <= 1e-5, (call, rel)
+        # and against the oracle itself
+        o = orc.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp["u_accept"],
+                             inp["u_sample"])
+        ok = o["flags"] == 0
+        np.testing.assert_array_equal(acc.cpu().numpy()[ok], o["accepted_len"][ok])
+        np.testing.assert_array_equal(out.cpu().numpy()[ok], o["out_tokens"][ok])
+        np.testing.assert_array_equal(status.cpu().numpy(), o["status"])
+        good = o["status"] == 0
+        rp, gp = o["probs"][good], probs.cpu().numpy()[good].astype(np.float64)
+        big = rp > 1e-30
+        assert (np.abs(gp[big] - rp[big]) / rp[big]).max(initial=0.0) <= 1e-5, call
 
 
 def test_noalloc_binding_and_oversize_refusal():
