@@ -347,13 +347,16 @@ sv_status sv_verify_step_chain(const void *q, const void *k_cache, const void *v
  * The fused verification step on a draft tree: sv_tree_attention,
  * sv_verify_tree_greedy and sv_compact_kv in one call.  Sources as those
  * three calls and sv_verify_step_chain.  The attention and the greedy
- * acceptance run side by side as in sv_verify_step_chain.  When the
- * attention runs in cluster mode (few row groups: B * Hkv * ceil(Hq/Hkv * T
- * / 128) clusters fit on the device at once) and the logits rows are 16-byte
- * aligned, compaction happens inside the two kernels: for each (sequence, KV
- * head), whichever of the attention (done reading that head's rows) and the
- * tree walk (path known) arrives last moves the rows.  Otherwise a compaction
- * kernel runs after both.
+ * acceptance run side by side as in sv_verify_step_chain, except when the
+ * attention has several row groups per KV head (Hq/Hkv * T > 128) and too many
+ * of them for cluster mode: then it is paced by its own tensor and softmax
+ * work, and the kernels run one after another, each with the whole device.
+ * When the attention runs in cluster mode (few row groups: B * Hkv *
+ * ceil(Hq/Hkv * T / 128) clusters fit on the device at once) and the logits
+ * rows are 16-byte aligned, compaction happens inside the two kernels: for
+ * each (sequence, KV head), whichever of the attention (done reading that
+ * head's rows) and the tree walk (path known) arrives last moves the rows.
+ * Otherwise a compaction kernel runs after both.
  *
  * Arguments as the three calls (path_nodes has T columns), plus attn_status,
  * verify_status (nullable, as above) and

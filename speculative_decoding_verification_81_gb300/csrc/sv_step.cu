@@ -222,18 +222,27 @@ sv_status sv_verify_step_tree_greedy(const void *q, void *k_cache, void *v_cache
     if (sms <= 0) return SV_ERR_CUDA;
     const int esz = dtype == SV_F32 ? 4 : 2;
     // Attention first: in cluster mode it takes the CTAs its clusters need
-    // (leaving at least 8 SMs), in the flat split its share of the bytes.
+    // (leaving at least 8 SMs), in the flat split its share of the cost.
+    // With several row groups per KV head in the flat split (the EAGLE-size
+    // trees: 256 query rows per KV head) the attention is paced by its tensor
+    // and softmax work, not by HBM, so SMs taken from it cost more than the
+    // overlap gives back (B=16, T=64, L=8192: 192 us side by side, 187 us one
+    // kernel after another): there the kernels run in sequence on the
+    // caller's stream, each with the whole device.
     AttnPlan ap;
     sv_status st = plan_attention(B, T, Hq, Hkv, D, S_max, &ap, sms - 8);
     if (st != SV_OK) return st;
-    if (ap.cluster <= 1) {
+    const bool serial = ap.cluster <= 1 && ap.rg >= 2;
+    if (serial) {
+        if ((st = plan_attention(B, T, Hq, Hkv, D, S_max, &ap)) != SV_OK) return st;
+    } else if (ap.cluster <= 1) {
         const int side = side_ctas(sms, 4.0 * B * Hkv * (double)S_max * D * ap.rg,
                                    (double)B * T * V * esz, 1.3);
         if ((st = plan_attention(B, T, Hq, Hkv, D, S_max, &ap, sms - side)) != SV_OK) return st;
     }
     VocabPlan vp = plan_vocab(false, B, T, V, dtype);
     if ((size_t)B * vp.rows_per_seq * vp.nchunks >= (1u << 31)) return SV_ERR_UNSUPPORTED;
-    vp.max_ctas = sms - ap.grid;
+    vp.max_ctas = serial ? 0 : sms - ap.grid;
     const size_t off_v = align_up(ap.bytes, 256);
     const size_t off_c = off_v + align_up(vp.bytes, 256);
     if (!workspace || !aligned16(workspace) ||
@@ -290,20 +299,28 @@ sv_status sv_verify_step_tree_greedy(const void *q, void *k_cache, void *v_cache
     ta.hook = hk;
 
     cudaStream_t main = reinterpret_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_side_mu);
-    SideStream *sd = nullptr;
-    if ((st = side_stream(&sd)) != SV_OK) return st;
-    if (cudaEventRecord(sd->fork, main) != cudaSuccess ||
-        cudaStreamWaitEvent(sd->stream, sd->fork, 0) != cudaSuccess)
-        return SV_ERR_CUDA;
-    const sv_status st2 = launch_tree_attention(aa, ap, workspace, main);
-    st = launch_verify_tree_greedy(ta, dtype, vp, static_cast<char *>(workspace) + off_v,
-                                   sd->stream);
-    if (cudaEventRecord(sd->join, sd->stream) != cudaSuccess ||
-        cudaStreamWaitEvent(main, sd->join, 0) != cudaSuccess)
-        return SV_ERR_CUDA;
-    if (st != SV_OK) return st;
-    if (st2 != SV_OK) return st2;
+    if (serial) {
+        // one kernel after another (programmatic launch chains them)
+        if ((st = launch_tree_attention(aa, ap, workspace, main)) != SV_OK) return st;
+        if ((st = launch_verify_tree_greedy(ta, dtype, vp, static_cast<char *>(workspace) + off_v,
+                                            main)) != SV_OK)
+            return st;
+    } else {
+        std::lock_guard<std::mutex> lock(g_side_mu);
+        SideStream *sd = nullptr;
+        if ((st = side_stream(&sd)) != SV_OK) return st;
+        if (cudaEventRecord(sd->fork, main) != cudaSuccess ||
+            cudaStreamWaitEvent(sd->stream, sd->fork, 0) != cudaSuccess)
+            return SV_ERR_CUDA;
+        const sv_status st2 = launch_tree_attention(aa, ap, workspace, main);
+        st = launch_verify_tree_greedy(ta, dtype, vp, static_cast<char *>(workspace) + off_v,
+                                       sd->stream);
+        if (cudaEventRecord(sd->join, sd->stream) != cudaSuccess ||
+            cudaStreamWaitEvent(main, sd->join, 0) != cudaSuccess)
+            return SV_ERR_CUDA;
+        if (st != SV_OK) return st;
+        if (st2 != SV_OK) return st2;
+    }
     if (hook) return SV_OK;
     CompactArgs c{};
     c.k = k_cache;

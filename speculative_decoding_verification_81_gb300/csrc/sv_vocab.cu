@@ -1038,6 +1038,7 @@ struct TreeWalkSmem {
     unsigned char ok[kMaxTreeT];
     int best, bad, tb_raw;
     int prefix_len;  // fused step: L_b, read with the other inputs
+    int red[kVWarps];
 };
 
 // The walk's inputs of sequence b -- parents, node tokens, node count -- into
@@ -1057,25 +1058,47 @@ __device__ __forceinline__ void tree_walk_load(const TreeArgs &a, int b, TreeWal
 // outputs.  `late`: the statistics pass gave up, so no decision is taken.
 __device__ __forceinline__ void tree_walk(const TreeArgs &a, int b, bool late, TreeWalkSmem &ts) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // this sequence's nodes; those past T_b are padding
-        const int tb_raw = ts.tb_raw;
-        int bad = late || ts.par[0] != -1 || tb_raw < 1 || tb_raw > a.T;
-        const int Tb = bad ? 1 : tb_raw;
-        for (int i = 1; i < Tb && !bad; ++i)
-            if (ts.par[i] < 0 || ts.par[i] >= i || ts.tok[i] < 0 || ts.tok[i] >= a.V) bad = 1;
+    const int tid = threadIdx.x;
+    // this sequence's nodes; those past T_b are padding
+    const int tb_raw = ts.tb_raw;
+    const bool tb_bad = late || ts.par[0] != -1 || tb_raw < 1 || tb_raw > a.T;
+    const int Tb = tb_bad ? 1 : tb_raw;
+    int bad = tb_bad;
+    for (int i = tid; i < Tb; i += kVT)
+        if (i > 0 && (ts.par[i] < 0 || ts.par[i] >= i || ts.tok[i] < 0 || ts.tok[i] >= a.V)) bad = 1;
+    bad = __syncthreads_or(bad);
+    // Every node at once: a thread follows its nodes' parent chains (parents
+    // precede their children, so a chain ends at the root after depth steps):
+    // ok = every node on the chain holds the target's argmax at its parent.
+    // The deepest ok node wins, the smallest index among equal depths: the
+    // largest key depth * 1024 + (1023 - node).
+    int key = -1;
+    if (!bad) {
+        for (int i = tid; i < Tb; i += kVT) {
+            int node = i, d = 0;
+            bool okc = true;
+            while (node > 0) {
+                const int pa = ts.par[node];
+                okc = okc && ts.tok[node] == ts.am[pa];
+                node = pa;
+                ++d;
+            }
+            ts.depth[i] = d;
+            ts.ok[i] = okc;
+            if (okc) key = max(key, d * 1024 + (1023 - i));
+        }
+    }
+    key = __reduce_max_sync(0xffffffffu, key);
+    if ((tid & 31) == 0) ts.red[tid >> 5] = key;
+    __syncthreads();
+    if (tid == 0) {
+        int k = ts.red[0];
+        for (int w = 1; w < kVWarps; ++w) k = max(k, ts.red[w]);
         int bst = 0;
         if (!bad) {
-            ts.ok[0] = 1;
-            ts.depth[0] = 0;
-            for (int i = 1; i < Tb; ++i) {
-                const int pa = ts.par[i];
-                ts.ok[i] = ts.ok[pa] && ts.tok[i] == ts.am[pa];
-                ts.depth[i] = ts.depth[pa] + 1;
-                if (ts.ok[i] && ts.depth[i] > ts.depth[bst]) bst = i;
-            }
+            bst = 1023 - (k & 1023);  // the root is always ok: k >= 1023
             int node = bst;
-            for (int dd = ts.depth[bst]; dd >= 0; --dd) {
+            for (int dd = k >> 10; dd >= 0; --dd) {
                 ts.path[dd] = node;
                 node = ts.par[node];
             }

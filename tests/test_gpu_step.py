@@ -171,9 +171,26 @@ def test_tree_step_medusa_full_size(orc):
     assert ref["accepted_len"].max() > 0  # rows moved
 
 
+def test_tree_step_flat_split_side_by_side(orc):
+    """Many single row groups (B=24, T=16, 8 KV heads: 192 groups of 64 rows):
+    the attention's flat split beside the greedy pass, and a compaction
+    kernel after the join."""
+    rng = np.random.default_rng(6)
+    B, T = 24, 16
+    par = np.stack([W.random_tree(T, 6, rng) for _ in range(B)])
+    tr = W.tree_logit_inputs(B, T, 8000, par, 0.7, seed=6)
+    a = W.attention_inputs(B, T, 32, 8, 128, rng.integers(0, 700, B), parents=par, seed=6,
+                           unused_fill="zero")
+    res = _tree_step(a, tr)
+    sel = _sample_rows(rng, B, T, 32, 256)
+    ref = _check_tree(orc, a, tr, res, sel)
+    assert ref["accepted_len"].max() > 0
+
+
 def test_tree_step_flat_split(orc):
-    """Many row groups (B=16, T=64, 8 KV heads: 256 groups): the attention's
-    flat split and a compaction kernel after the join."""
+    """Many row groups (B=16, T=64, 8 KV heads: 256 groups, two per KV head):
+    the attention's flat split, the kernels one after another, and a
+    compaction kernel at the end."""
     rng = np.random.default_rng(5)
     B, T = 16, 64
     par = np.stack([W.random_tree(T, 8, rng) for _ in range(B)])
