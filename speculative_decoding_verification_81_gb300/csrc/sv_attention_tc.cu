@@ -123,20 +123,29 @@ struct TcSmem {
 // The CTAs of a cluster each hold an unnormalised share (O, max, sum) of every
 // row of the group; CTA k finishes rows k*MROWS/cs .. (its "own" rows).  Each
 // CTA writes its share to its slot of the workspace (the flat mode's partial
-// slots: f32 O rows of 512 bytes, and a (max, sum) pair per row), the
-// cluster meets at a barrier (release/acquire: the writes are visible after
-// it), and each CTA reads the shares of its own rows back from L2.  (Shares
-// sent through distributed shared memory -- per-thread loads, or one bulk
-// copy per owner -- took longer: about 1.5 us against 0.7 here, on the
-// Medusa-tree shape.)
+// slots), the cluster meets at a barrier (release/acquire: the writes are
+// visible after it), and each CTA reads the shares of its own rows back from
+// L2.  In a slot, O is stored chunk-major -- 16-byte chunk c (columns 4c..4c+3)
+// of row r at (c * MROWS + r) * 16 bytes -- so that the lanes of a warp, one
+// row each, write and read consecutive 16 bytes; the (max, sum) pairs follow
+// at float offset MROWS * kD, one per row.  (Shares sent through distributed
+// shared memory -- per-thread loads, or one bulk copy per owner -- took
+// longer on the Medusa-tree shape: about 1.5 us against 0.7.)
+
+// Floats of a CTA's share: O (MROWS x kD) then the (max, sum) pairs; it fits
+// in the CTA's flat-mode partial region of 2 * MROWS * kD floats.
+template <int MROWS>
+constexpr size_t kClusterSlot = (size_t)MROWS * kD + 2 * MROWS;
+static_assert(kClusterSlot<128> <= 2 * 128 * kD && kClusterSlot<64> <= 2 * 64 * kD,
+              "cluster share larger than the partial slot");
 
 // A softmax thread's half row of O (64 columns at TMEM address o_half) and,
-// from the first half's thread, the row's (max, sum), into this CTA's share.
-// Warp-collective (TMEM loads): every lane calls it; has_row: the lane owns
-// row r (with 64-row groups, lanes 16-31 own none).
-__device__ __forceinline__ void cluster_stage(float *o_row, float2 *ml_row, uint32_t o_half,
-                                              int half, bool has_row, bool row_valid, float m,
-                                              float lrow) {
+// from the first half's thread, the row's (max, sum), into this CTA's share
+// `slot`.  Warp-collective (TMEM loads): every lane calls it; has_row: the
+// lane owns row r (with 64-row groups, lanes 16-31 own none).
+template <int MROWS>
+__device__ __forceinline__ void cluster_stage(float *slot, uint32_t o_half, int r, int half,
+                                              bool has_row, bool row_valid, float m, float lrow) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t ov[32];
@@ -146,44 +155,45 @@ __device__ __forceinline__ void cluster_stage(float *o_row, float2 *ml_row, uint
         if (!row_valid) continue;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-            __stcg(reinterpret_cast<float4 *>(o_row + 64 * half + 32 * h) + c,
+            __stcg(reinterpret_cast<float4 *>(slot) + (size_t)(half * 16 + h * 8 + c) * MROWS + r,
                    make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
                                __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3])));
     }
-    if (half == 0 && has_row) __stcg(ml_row, row_valid ? make_float2(m, lrow) : make_float2(kNegInf, 0.f));
+    if (half == 0 && has_row)
+        __stcg(reinterpret_cast<float2 *>(slot + MROWS * kD) + r,
+               row_valid ? make_float2(m, lrow) : make_float2(kNegInf, 0.f));
 }
 
 // Rows crank*MROWS/CS .. of the cluster's group from the CS shares (CTA i of
-// the cluster: O rows at o_base + i * o_stride, (max, sum) at ml_base +
-// i * ml_stride, floats): weights 2^(m_i - max m), the weighted O rows summed
-// in rank order and divided by the weighted row sums; bf16 out.  t256: the
-// thread's index among the 256 softmax threads.
+// the cluster: its slot at slot0 + i * slot_stride floats): weights
+// 2^(m_i - max m), the weighted O rows summed in rank order and divided by the
+// weighted row sums; bf16 out.  Thread t256 of the 256 softmax threads takes
+// row t256 % rows and the chunks t256 / rows + j * (256 / rows): a warp reads
+// one chunk of consecutive rows.
 template <int MROWS, int CS>
-__device__ __forceinline__ void cluster_merge_cs(const AttnKParams &p, const float *o_base,
-                                                 size_t o_stride, const float *ml_base,
-                                                 size_t ml_stride, int crank, int b, int kvh,
+__device__ __forceinline__ void cluster_merge_cs(const AttnKParams &p, const float *slot0,
+                                                 size_t slot_stride, int crank, int b, int kvh,
                                                  int rg, int ntiles, int t256) {
-    constexpr int kRpc = MROWS / CS;                  // rows this CTA finishes
-    constexpr int kTpr = kSoftmaxWarps * 32 / kRpc;   // threads per row
-    constexpr int kChunks = 32 / kTpr;                // 16-byte chunks (4 columns) per thread
-    static_assert(kTpr <= 32 && kChunks >= 1, "cluster too large for the row group");
-    const int lr = t256 / kTpr, part = t256 - lr * kTpr;
+    constexpr int kRpc = MROWS / CS;                 // rows this CTA finishes
+    constexpr int kGroups = kSoftmaxWarps * 32 / kRpc;  // chunk groups: threads per row
+    constexpr int kChunks = 32 / kGroups;            // 16-byte chunks (4 columns) per thread
+    static_assert(kGroups <= 32 && kChunks >= 1, "cluster too large for the row group");
+    const int lr = t256 % kRpc, cg = t256 / kRpc;
     const int r = crank * kRpc + lr;
     const int rglob = rg * p.rows_per_rg + r;
     if (b >= p.B || ntiles <= 0 || r >= p.rows_per_rg || rglob >= p.M) return;
     const int t = rglob / p.G, g = rglob - t * p.G;
     if (t >= nodes_of(p, b)) return;
-    // every share's (max, sum) and O chunks in flight at once; chunks
-    // interleaved over the row's threads (consecutive lanes, consecutive 16 bytes)
+    // every share's (max, sum) and O chunks in flight at once
     float2 ml[CS];
     float4 o[kChunks][CS];
 #pragma unroll
     for (int i = 0; i < CS; ++i) {
-        ml[i] = __ldcg(reinterpret_cast<const float2 *>(ml_base + i * ml_stride) + r);
+        const float *sl = slot0 + i * slot_stride;
+        ml[i] = __ldcg(reinterpret_cast<const float2 *>(sl + MROWS * kD) + r);
 #pragma unroll
         for (int j = 0; j < kChunks; ++j)
-            o[j][i] = __ldcg(reinterpret_cast<const float4 *>(o_base + i * o_stride + (size_t)r * kD) +
-                             j * kTpr + part);
+            o[j][i] = __ldcg(reinterpret_cast<const float4 *>(sl) + (size_t)(cg + j * kGroups) * MROWS + r);
     }
     float ms = kNegInf;
 #pragma unroll
@@ -208,9 +218,18 @@ __device__ __forceinline__ void cluster_merge_cs(const AttnKParams &p, const flo
             acc.z = use ? __fmaf_rn(o[j][i].z, w[i], acc.z) : acc.z;
             acc.w = use ? __fmaf_rn(o[j][i].w, w[i], acc.w) : acc.w;
         }
-        *reinterpret_cast<uint2 *>(orow + 4 * (j * kTpr + part)) =
+        *reinterpret_cast<uint2 *>(orow + 4 * (cg + j * kGroups)) =
             make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     }
+}
+
+template <int MROWS>
+__device__ __forceinline__ void cluster_merge(const AttnKParams &p, const float *slot0,
+                                              size_t slot_stride, int cs, int crank, int b,
+                                              int kvh, int rg, int ntiles, int t256) {
+    if (cs == 2) cluster_merge_cs<MROWS, 2>(p, slot0, slot_stride, crank, b, kvh, rg, ntiles, t256);
+    else if (cs == 4) cluster_merge_cs<MROWS, 4>(p, slot0, slot_stride, crank, b, kvh, rg, ntiles, t256);
+    else cluster_merge_cs<MROWS, 8>(p, slot0, slot_stride, crank, b, kvh, rg, ntiles, t256);
 }
 
 // Compaction of one (sequence, KV head) in a fused tree step, by the 128
@@ -812,9 +831,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // cluster mode: this CTA's share of the group, unnormalised,
                 // into the merge buffer (the K/V ring is idle now: every copy
                 // has landed and every product has read it)
-                cluster_stage(p.part_o + ((size_t)blockIdx.x * 2 * MROWS + r) * kD,
-                              reinterpret_cast<float2 *>(p.part_ml) + (size_t)blockIdx.x * 2 * MROWS * 2 + r,
-                              tl + kColO + hc, half, lane_has_row, row_valid, m, lrow);
+                cluster_stage<MROWS>(p.part_o + (size_t)blockIdx.x * kClusterSlot<MROWS>,
+                                     tl + kColO + hc, r, half, lane_has_row, row_valid, m, lrow);
                 staged = true;
                 if (warp == 2 && lane == 0) SV_STAMP(12);
                 tc::fence_before();
@@ -1002,7 +1020,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (ready_ctr) flag_ready(ready_ctr);
     if (cl && !staged && lane_has_row && half == 0) {
         // no tile of the group fell to this CTA (or a wait gave up): an empty share
-        __stcg(reinterpret_cast<float2 *>(p.part_ml) + (size_t)blockIdx.x * 2 * MROWS * 2 + r,
+        __stcg(reinterpret_cast<float2 *>(p.part_o + (size_t)blockIdx.x * kClusterSlot<MROWS> +
+                                          MROWS * kD) + r,
                make_float2(kNegInf, 0.f));
     }
     tc::fence_before();
@@ -1042,14 +1061,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
             const int kvh = cpr / p.RG, rg = cpr - kvh * p.RG;
             const size_t c0 = (size_t)(blockIdx.x - crank);  // the cluster's first CTA
-            cluster_merge<MROWS>(p, p.part_o + c0 * 2 * MROWS * kD, (size_t)2 * MROWS * kD,
-                                 p.part_ml + c0 * 2 * MROWS * 4, (size_t)2 * MROWS * 4, cs, crank,
-                                 cb, kvh, rg, cn, tid - 64);
+            const float *slot0 = p.part_o + c0 * kClusterSlot<MROWS>;
+            cluster_merge<MROWS>(p, slot0, kClusterSlot<MROWS>, cs, crank, cb, kvh, rg, cn, tid - 64);
 #ifdef SV_PHASE_STAMPS
             if (tid == 64) SV_STAMP(20);
-            cluster_merge<MROWS>(p, p.part_o + c0 * 2 * MROWS * kD, (size_t)2 * MROWS * kD,
-                                 p.part_ml + c0 * 2 * MROWS * 4, (size_t)2 * MROWS * 4, cs, crank,
-                                 cb, kvh, rg, cn, tid - 64);
+            cluster_merge<MROWS>(p, slot0, kClusterSlot<MROWS>, cs, crank, cb, kvh, rg, cn, tid - 64);
             if (tid == 64) SV_STAMP(21);
 #endif
         }
