@@ -405,7 +405,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the last warp the V halves.  A K half is refilled as soon as the S
         // product that read it is done, a V half once its PV product is, so
         // the next K tiles stream in while a tile's softmax and PV run.
-        if (lane == 0) {
+        if (p.block_table && p.page_size < kBK) {
+            // Paged, pages of 8-64 slots: a tile is 128 / page_size blocks of
+            // page_size rows, one per page.  Lane i reads page i's id and
+            // issues that block's two boxes, so a tile's blocks go out
+            // together instead of one after another from one thread.  The
+            // waits are the warp's (one verdict for all lanes); lane 0 does
+            // the barrier accounting and the Q loads.  (Pages past the
+            // sequence's end may hold any id: one out of range reads zeros,
+            // and those keys are masked anyway.)
+            const bool is_k = warp == 0;
+            uint64_t *full = is_k ? sh->full_k : sh->full_v;
+            uint64_t *empty = is_k ? sh->empty_k : sh->empty_v;
+            const CUtensorMap *map = is_k ? &tmk : &tmv;
+            const int half_off = is_k ? 0 : 2 * kBox;
+            const uint64_t pol = l2_policy_evict_first();
+            const int ps = p.page_size;
+            Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
+            long long k = 0;
+            uint32_t qseg = 0;
+            for (long long u = u_begin; u < u_end; ++u, ++k) {
+                const int s = (int)(k % STAGES);
+                const uint32_t ph = (uint32_t)((k / STAGES) & 1);
+                if (!is_k && k == 0 && !warp_wait_bounded(&sh->k_first, 0)) {
+                    fail(cur.b);
+                    break;
+                }
+                if (is_k && (u == u_begin || cur.tile == 0)) {
+                    const int qb = (int)(qseg & 1);
+                    if (!warp_wait_bounded(&sh->q_empty[qb], ((qseg >> 1) & 1) ^ 1u)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    if (lane == 0) {
+                        const int kvh = cur.pr / p.RG, rg = cur.pr - kvh * p.RG;
+                        const int z = cur.b * p.T + rg * (p.rows_per_rg / p.G);
+                        uint8_t *qd = qbuf + qb * 2 * kQBox;
+                        mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
+                        tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
+                        tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
+                    }
+                    ++qseg;
+                }
+                const int kvh = cur.pr / p.RG;
+                const int kb = cur.tile * kBK;
+                const int nsub = min(kBK / ps, p.max_pages - kb / ps);
+                int y = -kBK;
+                if (lane < nsub) {
+                    const int pg = p.block_table[(size_t)cur.b * p.max_pages + kb / ps + lane];
+                    y = (pg >= 0 && pg < p.num_pages) ? (pg * p.Hkv + kvh) * ps : -kBK;
+                }
+                if (!warp_wait_bounded(&empty[s], ph ^ 1u)) {
+                    fail(cur.b);
+                    break;
+                }
+                if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+                uint8_t *st = smem + s * kStageBytes + half_off;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], 2u * 128u * (uint32_t)(nsub * ps));
+                __syncwarp();  // the expected bytes are set before any block lands
+                if (lane < nsub) {
+                    tma_load_2d_hint(st + lane * ps * 128, map, 0, y, &full[s], pol);
+                    tma_load_2d_hint(st + kBox + lane * ps * 128, map, 64, y, &full[s], pol);
+                }
+                if (is_k && k == 0 && lane == 0) mbar_arrive(&sh->k_first);
+                cursor_next(cur, tile_base, p.B, pl);
+            }
+            if (is_k && k == 0 && lane == 0) mbar_arrive(&sh->k_first);  // none issued
+            if (lane == 0) {  // every copy issued must land before the CTA may exit
+                const long long first = k > STAGES ? k - STAGES : 0;
+                for (long long j = first; j < k; ++j)
+                    mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
+                for (uint32_t g2 = qseg > 2 ? qseg - 2 : 0; g2 < qseg; ++g2)
+                    mbar_wait_bounded(&sh->q_full[g2 & 1], (g2 >> 1) & 1);
+            }
+        } else if (lane == 0) {
             const bool is_k = warp == 0;
             uint64_t *full = is_k ? sh->full_k : sh->full_v;
             uint64_t *empty = is_k ? sh->empty_k : sh->empty_v;
@@ -466,7 +539,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_expect_tx(&full[s], 2 * kBox);
                     load(st, 0, y, &full[s]);
                     load(st + kBox, 64, y, &full[s]);
-                } else if (p.page_size >= kBK) {
+                } else {
                     // paged, pages of 128 slots or more: the tile sits in one page
                     // (its id read before the wait, so the load overlaps it); an
                     // id out of range (reported by the prologue) reads zeros
@@ -483,32 +556,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_expect_tx(&full[s], 2 * kBox);
                     load(st, 0, y, &full[s]);
                     load(st + kBox, 64, y, &full[s]);
-                } else {
-                    // paged, smaller pages: one block of page_size rows per page
-                    // (pages past the sequence's end may hold any id: an id out
-                    // of range reads zeros; those keys are masked anyway)
-                    const int ps = p.page_size;
-                    const int nsub = min(kBK / ps, p.max_pages - kb / ps);
-                    int y[kMaxSubBlocks];
-#pragma unroll
-                    for (int i = 0; i < kMaxSubBlocks; ++i)
-                        if (i < nsub) {
-                            const int pg = p.block_table[(size_t)cur.b * p.max_pages + kb / ps + i];
-                            y[i] = (pg >= 0 && pg < p.num_pages) ? (pg * p.Hkv + kvh) * ps : -kBK;
-                        }
-                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
-                        fail(cur.b);
-                        break;
-                    }
-                    if (*abort_flag) break;
-                    uint8_t *st = smem + s * kStageBytes + half_off;
-                    mbar_arrive_expect_tx(&full[s], 2u * 128u * (uint32_t)(nsub * ps));
-#pragma unroll
-                    for (int i = 0; i < kMaxSubBlocks; ++i)
-                        if (i < nsub) {
-                            load(st + i * ps * 128, 0, y[i], &full[s]);
-                            load(st + kBox + i * ps * 128, 64, y[i], &full[s]);
-                        }
                 }
                 if (is_k && k == 0) {
                     mbar_arrive(&sh->k_first);
