@@ -1,23 +1,25 @@
 // sv_vocab.cu -- full-vocabulary passes of the verification step.
 //
 // Chain (stochastic) acceptance, "Chapitre 9 -- Décodage spéculatif" §9.1:
-//   kernel 1  streams every target/draft logits row once, chunk by chunk
-//             (one CTA per (row, chunk), 16-byte non-temporal loads), and
-//             keeps per chunk the max and the sum of exp2 in the log2 domain
-//             (the chunk's max first, by packed bf16 maxima, then one pass of
-//             exp2 against it with paired f32 arithmetic).
-//             The last CTA to finish a sequence merges its chunks, evaluates
-//             p_i(x_i), q_i(x_i), the decisions u*q < p and the first
-//             rejection a.
-//   kernel 2  draws the final token: per chunk of the row pair at a it sums
-//             the weights r = max(0, p_a - q_a) (or p_N for the bonus) and
-//             keeps the per-thread prefix sums; the last CTA per sequence
-//             locates u*S in the chunk prefix, then in the stored thread
-//             prefix of that chunk, then the one thread it falls in walks its
-//             elements.
+//   statistics  rows 16-byte aligned: chain_stats_stream_kernel, a persistent
+//               grid (one CTA per SM, or the SMs a fused step leaves it)
+//               streaming the units (sequence, row, 32 KB chunk) through a
+//               ring of bulk copies; every consumer warp leaves a (max, sum
+//               of exp2) record of its eighth of a unit.  Unaligned rows:
+//               chain_stats_kernel, one CTA per (row, chunk), the same records.
+//   decisions + draw  chain_residual_kernel: every CTA of a sequence first
+//               merges the sequence's records and takes the decisions
+//               u * q(x) < p(x) (p, q from an accurate exp2); then per chunk
+//               of the row pair at the first rejection a it sums the weights
+//               max(0, p_a - q_a) (or p_N for the bonus); the last CTA of the
+//               sequence locates u * S in the chunk totals, then the thread,
+//               then the element.
 // Greedy tree acceptance ("Parallel Decoding" glossary, "L'attention en
-// arbre"; §9.1): the same streaming pass in argmax mode, and the last CTA per
-// sequence walks the tree.
+// arbre"; §9.1): tree_stats_stream_kernel, the same streaming pass in argmax
+// mode, then tree_decide_kernel, one CTA per sequence: the rows' argmax from
+// the records and the walk (every node's ancestor chain in parallel).
+// Unaligned rows: tree_stats_kernel, whose last CTA per sequence walks.
+// Stochastic tree acceptance (multi-draft, the SpecInfer rule): below.
 //
 // No CTA ever waits for another: the "last CTA" is whoever brings a
 // per-sequence arrival counter to its final value; it resets the counter.
