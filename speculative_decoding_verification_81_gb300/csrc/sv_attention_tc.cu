@@ -77,6 +77,11 @@ static __device__ long long g_stamps[kStampCtas * kStampSlots];
 __device__ __forceinline__ void phase_stamp(int slot, long long value) {
     if (blockIdx.x < kStampCtas) g_stamps[blockIdx.x * kStampSlots + slot] = value;
 }
+__device__ __forceinline__ long long sm_id() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
 __device__ __forceinline__ long long global_ns() {
     long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -87,9 +92,20 @@ __device__ __forceinline__ long long global_ns() {
     do {                                \
         phase_stamp(1, clock64());      \
         phase_stamp(0, global_ns());    \
+        phase_stamp(23, sm_id());       \
     } while (0)
 #define SV_STAMP_VALUE(slot, v) phase_stamp((slot), (long long)(v))
+// slot 22: the clock at the exit of the CTA's last warp (every warp, at every exit)
+struct StampExit {
+    __device__ ~StampExit() {
+        if ((threadIdx.x & 31) == 0 && blockIdx.x < kStampCtas)
+            atomicMax(reinterpret_cast<unsigned long long *>(&g_stamps[blockIdx.x * kStampSlots + 22]),
+                      (unsigned long long)clock64());
+    }
+};
+#define SV_STAMP_EXIT() StampExit sv_stamp_exit_
 #else
+#define SV_STAMP_EXIT() ((void)0)
 #define SV_STAMP(slot) ((void)0)
 #define SV_STAMP_ENTRY() ((void)0)
 #define SV_STAMP_VALUE(slot, v) ((void)0)
@@ -302,6 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int HR = p.Hkv * p.RG;
 
     if (tid == 0) SV_STAMP_ENTRY();
+    SV_STAMP_EXIT();
     // The set-up that reads no global memory (barriers, tensor-map prefetch,
     // the Q padding rows, the tensor memory) comes before the wait for the
     // previous kernel: with programmatic launch it overlaps that kernel's tail.

@@ -52,7 +52,8 @@ POINTS = [
     (20, "cluster merge done (stamped build: once more)"),
     (21, "cluster merge done a second time (warm code)"),
     (15, "cluster merge done"),
-    (16, "CTA end"),
+    (16, "CTA end (thread 0)"),
+    (22, "CTA end (its last warp)"),
 ]
 
 def step_timeline(args):
@@ -145,16 +146,15 @@ def step_timeline(args):
         ghz = args.sm_ghz
         entry = raw[:, 0].astype(np.float64)
         waited = entry + (raw[:, 2] - raw[:, 1]) / ghz
-        end = entry + (raw[:, 16] - raw[:, 1]) / ghz
-        spans = np.zeros(8, np.uint64)
+        end = entry + (np.maximum(raw[:, 16], raw[:, 22]) - raw[:, 1]) / ghz
+        spans = np.zeros(2 * len(SPAN_NAMES), np.uint64)
         assert L_.sv_debug_vocab_spans(spans.ctypes.data) == 0
-        spans = spans.reshape(4, 2).astype(np.float64)
+        spans = spans.reshape(len(SPAN_NAMES), 2).astype(np.float64)
         t0 = min(entry.min(), spans[spans[:, 1] > 0, 0].min())
         row = {"attention: first CTA entry": entry.min() - t0,
                "attention: first wait return": waited.min() - t0,
                "attention: last CTA end": end.max() - t0}
-        names = ["chain statistics", "chain decisions + residual draw", "tree argmax pass",
-                 "tree walk (+ compaction)"]
+        names = SPAN_NAMES
         for i, nm in enumerate(names):
             if spans[i, 1] > 0:
                 row[f"{nm}: start"] = spans[i, 0] - t0
@@ -167,6 +167,10 @@ def step_timeline(args):
         vals = [r[k] for r in rows_out if k in r]
         print(f"{k:44s} {np.median(vals) / 1e3:8.2f}")
 
+
+# the vocabulary kernels' spans, in the library's order
+SPAN_NAMES = ["chain statistics", "chain decisions + residual draw", "tree argmax pass",
+              "tree walk (+ compaction)"]
 
 SHAPES = {
     # name: (B, L, T, tree)
