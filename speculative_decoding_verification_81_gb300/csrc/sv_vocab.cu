@@ -150,6 +150,18 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
                           : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
 }
 
+// Largest element of one 16-byte word (bf16: packed maxima, exact; NaN
+// never wins over a number).
+template <typename T>
+__device__ __forceinline__ float word_max(const uint4 &v) {
+    if (sizeof(T) == 2) {
+        const uint32_t a = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+        return fmaxf(bf16_lo(a), bf16_hi(a));
+    }
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+
 // Largest element of the thread's loaded words (bf16: packed maxima, exact).
 template <typename T, int NW = kLoadsPerThread>
 __device__ __forceinline__ float words_max(const uint4 (&buf)[NW]) {
@@ -695,6 +707,40 @@ __device__ __forceinline__ float exp2_diff_accurate(float l, float m) {
     return ldexpf(e, (int)n);
 }
 
+// The inputs of sequence b's decisions that this thread needs (p_i's token
+// and logit on threads 0..N-1, q_i's on threads 64..64+N-1, u_i on thread
+// i), read before the statistics pass has finished: they are inputs of the
+// call, complete once that pass let this kernel launch.
+struct ChainPosIn {
+    int nb_raw;   // the draft length as given
+    bool tok_ok;  // the thread's token is in [0, V)
+    float l;      // the logit at the token
+    float u;      // u_accept of position threadIdx.x
+};
+
+template <typename T>
+__device__ __forceinline__ ChainPosIn chain_pos_inputs(const ChainArgs &a, int b) {
+    const int tid = threadIdx.x;
+    ChainPosIn in;
+    in.nb_raw = a.draft_lens ? a.draft_lens[b] : a.N;
+    const int Nb = (in.nb_raw >= 0 && in.nb_raw <= a.N) ? in.nb_raw : 0;
+    const int i = tid & 63;
+    const int is_q = (tid >> 6) & 1;
+    in.tok_ok = false;
+    in.l = 0.f;
+    in.u = tid < a.N ? a.u_accept[(size_t)b * a.N + tid] : 0.f;
+    if (tid < 128 && i < Nb) {
+        const int x = a.tokens[(size_t)b * a.N + i];
+        in.tok_ok = x >= 0 && x < a.V;
+        if (in.tok_ok) {
+            const T *row = is_q ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V
+                                : static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
+            in.l = Elem<T>::at(row, x);
+        }
+    }
+    return in;
+}
+
 // Decisions of sequence b from its rows' (max, sum) records, by a whole CTA:
 // a warp per row merges the row's records (their maximum first, then the sums
 // rescaled to it, 64 records at a time); p_i(x_i) and q_i(x_i) from the row
@@ -703,10 +749,9 @@ __device__ __forceinline__ float exp2_diff_accurate(float l, float m) {
 // rejection (N if none, -1 if the sequence is invalid).  With `outputs` it
 // also writes accepted_len, seq_status, probs and the emitted tokens except
 // the one drawn at position a.
-template <typename T>
 __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, const VocabPlan &p,
                                                          const float2 *rec, const int *timed_out,
-                                                         int b, bool outputs) {
+                                                         int b, bool outputs, const ChainPosIn &in) {
     __shared__ float s_ms[2 * kMaxChainN + 1][2];
     __shared__ float s_pq[kMaxChainN][2];
     __shared__ int s_bad, s_first;
@@ -714,7 +759,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     const int R = 2 * a.N + 1;
     const int per_row = p.nchunks * p.recs_per_unit;
     // this sequence's draft length; rows and positions past it are padding
-    const int nb_raw = a.draft_lens ? a.draft_lens[b] : a.N;
+    const int nb_raw = in.nb_raw;
     const bool nb_ok = nb_raw >= 0 && nb_raw <= a.N;
     const int Nb = nb_ok ? nb_raw : 0;
     if (tid == 0) {
@@ -723,22 +768,13 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
         s_bad = (nb_ok ? 0 : 1) | (__ldcg(timed_out) != 0 ? 2 : 0);
         s_first = Nb;
     }
-    // p_i on threads 0..N-1, q_i on threads 64..64+N-1: the drafted token and
-    // its logit are fetched first, overlapping the record merges below
+    // p_i on threads 0..N-1, q_i on threads 64..64+N-1 (token and logit
+    // fetched by the caller)
     const int i = tid & 63;
     const int is_q = (tid >> 6) & 1;
     const bool pos_thread = tid < 128 && i < Nb;
-    float l = 0.f;
-    bool tok_ok = false;
-    if (pos_thread) {
-        const int x = a.tokens[(size_t)b * a.N + i];
-        tok_ok = x >= 0 && x < a.V;
-        if (tok_ok) {
-            const T *row = is_q ? static_cast<const T *>(a.draft) + ((size_t)b * a.N + i) * a.V
-                                : static_cast<const T *>(a.target) + ((size_t)b * (a.N + 1) + i) * a.V;
-            l = Elem<T>::at(row, x);
-        }
-    }
+    const float l = in.l;
+    const bool tok_ok = in.tok_ok;
     // rows: a warp per row, four rows of a warp in flight at a time; each row
     // merges its records once (their maximum, then the rescaled sums)
     for (int r0 = warp; r0 < R; r0 += 4 * kVWarps) {
@@ -807,7 +843,7 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     if (tid < a.N) {
         const bool used = tid < Nb;
         const float pp = used ? s_pq[tid][0] : 0.f, qq = used ? s_pq[tid][1] : 0.f;
-        if (used && !(a.u_accept[(size_t)b * a.N + tid] * qq < pp)) atomicMin(&s_first, tid);
+        if (used && !(in.u * qq < pp)) atomicMin(&s_first, tid);
         if (outputs && a.probs) {
             a.probs[((size_t)b * a.N + tid) * 2 + 0] = pp;
             a.probs[((size_t)b * a.N + tid) * 2 + 1] = qq;
@@ -859,15 +895,17 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     __shared__ uint4 s_words[2][kResLoadsPerThread];  // the picked thread's run
     __shared__ float s_base, s_theta;
 
-    griddep_wait();
-    griddep_launch_dependents();
     const int b = blockIdx.x / p.res_chunks;
     const int c = blockIdx.x - b * p.res_chunks;
-    const float u_s = threadIdx.x == 0 ? __ldg(a.u_sample + b) : 0.f;  // for the last CTA's search
+    // the call's inputs first, while the statistics pass may still run
+    const float u_s = threadIdx.x == 0 ? a.u_sample[b] : 0.f;  // for the last CTA's search
+    const ChainPosIn pin = chain_pos_inputs<T>(a, b);
+    griddep_wait();
+    griddep_launch_dependents();
     // every CTA of the sequence takes the decisions; the first one writes them
     const ChainDecision d =
-        decide_sequence<T>(a, p, reinterpret_cast<const float2 *>(w.partials),
-                           w.counters + 2 * a.B, b, c == 0);
+        decide_sequence(a, p, reinterpret_cast<const float2 *>(w.partials),
+                        w.counters + 2 * a.B, b, c == 0, pin);
     if (d.a < 0) return;  // invalid sequence: -1s written above
 
     ResidualRow<T> rw;
@@ -1277,22 +1315,35 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the words are in registers
-        // the warp's maximum (NaN never wins), then the smallest index holding it
-        float vmax = words_max<T, kSWordsPerLane>(buf);
+        // the lane's largest value and the first of its words holding it
+        // (words in index order; NaN never wins), then the warp's maximum and
+        // the smallest index holding it: only the winning word is unpacked
+        float best = kNegInf;
+        int bq = 0;
+#pragma unroll
+        for (int q = 0; q < kSWordsPerLane; ++q) {
+            const float mq = word_max<T>(buf[q]);
+            if (mq > best) {
+                best = mq;
+                bq = q;
+            }
+        }
+        float vmax = best;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
         int idx = INT_MAX;
-        if (vmax != kNegInf && vmax == vmax) {  // some element is larger than -inf
+        if (vmax != kNegInf && best == vmax) {  // this lane holds the maximum
+            uint4 wq = buf[0];
 #pragma unroll
-            for (int q = kSWordsPerLane - 1; q >= 0; --q) {
-                float x[PV];
-                Elem<T>::unpack(buf[q], x);
-                const int e0 = c * kUnitElems + ((gw * kSWordsPerLane + q) * 32 + lane) * PV;
+            for (int q = 1; q < kSWordsPerLane; ++q)
+                if (q == bq) wq = buf[q];
+            float x[PV];
+            Elem<T>::unpack(wq, x);
+            const int e0 = c * kUnitElems + ((gw * kSWordsPerLane + bq) * 32 + lane) * PV;
 #pragma unroll
-                for (int j = PV - 1; j >= 0; --j)
-                    if (x[j] == vmax) idx = e0 + j;
-            }
+            for (int j = PV - 1; j >= 0; --j)
+                if (x[j] == vmax) idx = e0 + j;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, off));
