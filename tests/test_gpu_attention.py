@@ -91,6 +91,19 @@ def test_attention_workload4_sampled(orc):
     _check(orc, inp, None, sel)
 
 
+def test_attention_flat_split_128_row_groups_sampled(orc):
+    """26 chain nodes x 4 heads = 104 query rows per KV head: one 128-row group
+    per (sequence, KV head) with padding rows, and enough groups (256) for the
+    flat split over persistent CTAs, whose groups straddle CTAs and merge."""
+    rng = np.random.default_rng(11)
+    B, T = 32, 26
+    L = [int(x) for x in rng.integers(900, 1100, B)]
+    inp = W.attention_inputs(B, T, 32, 8, 128, L, seed=11)
+    sel = np.concatenate([_sample(rng, B, T, 32, 64),
+                          np.array([[B - 1, T - 1, 31], [0, 0, 0], [5, 25, 3]])])
+    _check(orc, inp, None, sel)
+
+
 def test_attention_workload5_sampled(orc):
     inp = W.workload(5)["attn"]
     rng = np.random.default_rng(5)
