@@ -296,6 +296,280 @@ __device__ __forceinline__ void cluster_merge(const AttnKParams &p, const float 
         cluster_merge_cs<MROWS, 8>(p, o_base, o_stride, ml_base, ml_stride, crank, b, kvh, rg, ntiles, t256);
 }
 
+// Out-of-line pieces of the softmax warps' per-tile loop (each runs at most
+// once a segment or when the running max moves), so that the loop's own code
+// stays short: inline, the code it jumps over cost instruction fetch stalls
+// every tile (the softmax of 128-row groups paced ~6% slower).
+
+// Once the PV product behind `bar` is done: this warp's 64 O columns from
+// TMEM address o_cols times a.  False when the wait gave up (the columns are
+// scaled anyway; the caller reports the failure).
+__device__ __noinline__ bool rescale_o_half(uint64_t *bar, uint32_t parity, uint32_t o_cols, float a) {
+    const bool ok = warp_wait_bounded(bar, parity);
+    tc::fence_after();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t ov[32];
+        tc::tmem_ld32(o_cols + 32 * h, ov);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * a);
+        tc::tmem_st32(o_cols + 32 * h, ov);
+    }
+    return ok;
+}
+
+// Once the V half behind `bar` has landed: its rows z0 .. kBK - 1 (past the
+// sequence's last slot) zeroed in shared memory at vst, by the softmax
+// threads (t: 0 .. 32 * kSoftmaxWarps - 1), visible to the tensor core.
+// False when the wait gave up.
+__device__ __noinline__ bool zero_v_tail(uint64_t *bar, uint32_t parity, uint8_t *vst, int z0, int t) {
+    if (!warp_wait_bounded(bar, parity)) return false;
+    for (int i = t; i < (kBK - z0) * 16; i += 32 * kSoftmaxWarps) {
+        const int row = z0 + (i >> 4), c = i & 15;
+        *reinterpret_cast<uint4 *>(vst + (c >> 3) * kBox + sw128(row, c & 7)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async_smem();
+    return true;
+}
+
+// The end of a segment for one softmax warp: its rows' sum from the column
+// halves, then this half of the O rows out of TMEM -- written out (whole
+// segment, or the merging CTA of a split pair), left as a partial, or staged
+// for the cluster merge.  Kept out of line: it runs once a segment, and the
+// per-tile loop stays short.  Returns the warp's updated pair-barrier count,
+// the partial counter to flag ready after the next tile (or null) and whether
+// the rows were staged; ok is false when a bounded wait gave up.
+struct SegOutputs {  // the kernel parameters it uses, passed by value
+    uint16_t *out;
+    float *part_o, *part_ml;
+    int T, Hq, G;
+};
+
+struct SegEndRet {
+    uint32_t pair_uses;
+    int *ready_ctr;
+    bool staged;
+    bool ok;
+};
+
+template <int MROWS>
+__device__ __noinline__ SegEndRet softmax_segment_end(
+    const SegOutputs p, TcSmem *sh, const int *tile_base, const PairLane pl, const Cursor cur,
+    const long long jt, const long long U, const int nctas, const int nlane, const int myslot,
+    const uint32_t tl, const int quarter, const int half, const int hc, const int lane,
+    const int warp, const int r, const int rglob, const int kvh, const bool lane_has_row,
+    const bool row_valid, const bool warp_active, const bool whole, const bool seg_is_first,
+    const bool cl, const float m, const float l, const int arrived, int *ctr, uint32_t pair_uses,
+    bool staged) {
+    int *ready_ctr = nullptr;
+    auto done = [&](bool ok) {
+        SegEndRet ret;
+        ret.pair_uses = pair_uses;
+        ret.ready_ctr = ready_ctr;
+        ret.staged = staged;
+        ret.ok = ok;
+        return ret;
+    };
+    if (!warp_wait_bounded(&sh->pv_done[jt & 1], (uint32_t)((jt >> 1) & 1))) {
+        return done(false);
+    }
+    tc::fence_after();
+    if (warp == 2 && lane == 0) SV_STAMP(11);
+    // row sum = first half's part + second half's part (same order in both)
+    sh->xl[quarter][half][lane] = l;
+    if (!group_sync(&sh->pair[quarter], pair_uses)) {
+        return done(false);
+    }
+    const float lrow = sh->xl[quarter][0][lane] + sh->xl[quarter][1][lane];
+    if (cl) {
+        // cluster mode: this CTA's share of the group, unnormalised,
+        // into the merge buffer (the K/V ring is idle now: every copy
+        // has landed and every product has read it)
+        cluster_stage<MROWS>(p.part_o + (size_t)blockIdx.x * kClusterSlot<MROWS>,
+                             tl + kColO + hc, r, half, lane_has_row, row_valid, m, lrow);
+        staged = true;
+        if (warp == 2 && lane == 0) SV_STAMP(12);
+        tc::fence_before();
+        return done(true);
+    }
+    const int t = row_valid ? rglob / p.G : 0;
+    const int g = row_valid ? rglob - t * p.G : 0;
+    uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD + hc;
+    // A split pair: the last CTA to arrive merges the others'
+    // partials into its own O; the others leave a partial and flag it
+    // ready once it is visible.  Nobody waits for a CTA that has not
+    // already arrived.
+    int nc = 1, c0 = 0, slot0 = 0;
+    bool merger = whole;
+    if (!whole && warp_active) {
+        const long long ub = (long long)tile_base[cur.b] * pl.npr + (long long)cur.pi * cur.n;
+        c0 = cta_of(U, nctas, ub);  // slots; contributor i is CTA (c0 + i) * nlane + lane
+        nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;
+        slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;
+        const int pos = __shfl_sync(0xffffffffu, arrived, 0);
+        merger = pos == nc - 1;
+        if (merger) {
+            bool ready = true;
+            if (lane == 0) {
+                const long long t0 = clock64();
+                while (ld_acquire_gpu(ctr + kSoftmaxWarps) < nc - 1)
+                    if (clock64() - t0 > kWaitCycles) {
+                        ready = false;
+                        break;
+                    }
+                if (ready) {
+                    ctr[0] = 0;  // ready for the next call
+                    ctr[kSoftmaxWarps] = 0;
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                return done(false);
+            }
+            __syncwarp();  // the others' partials are read after lane 0's acquire
+        }
+    }
+    if (warp_active) {
+        // the other contributors' (max, sum) of this row half
+        auto part_row = [&](int i) -> size_t {
+            return ((size_t)((c0 + i) * nlane + pl.poff) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
+        };
+        // The merge takes the contributors in index order with the same
+        // arithmetic whoever merges, so the result does not depend on
+        // which CTA finished last.
+        const int self = myslot - c0;
+        auto ml_of = [&](int i) -> float2 {
+            return i == self ? make_float2(m, lrow)
+                             : __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
+        };
+        float mstar = m, lsum = lrow;
+        if (!whole && merger && row_valid && nc != 2) {
+            for (int i = 0; i < nc; ++i) mstar = fmaxf(mstar, ml_of(i).x);
+            lsum = 0.f;
+            for (int i = 0; i < nc; ++i) {
+                const float2 ml = ml_of(i);
+                const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
+                lsum = __fmaf_rn(ml.y, w, lsum);
+            }
+        }
+        const int slot = seg_is_first ? 0 : 1;
+        float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
+        if (!whole && merger && nc == 2) {  // (the same in every lane)
+            // two contributors (the usual split): the other's partial
+            // fetched in one go, then the same arithmetic as below
+            const int oth = 1 - self;
+            const size_t pro = part_row(oth);
+            float2 mlo = make_float2(kNegInf, 0.f);
+            float4 oo[16];
+            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + pro * kD + hc);
+            if (row_valid) {
+                mlo = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pro * 4 + half * 2));
+    #pragma unroll
+                for (int c = 0; c < 16; ++c) oo[c] = __ldcg(src + c);
+            } else {
+    #pragma unroll
+                for (int c = 0; c < 16; ++c) oo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float ms2 = fmaxf(m, mlo.x);
+            const float ws = m == kNegInf ? 0.f : ex2_approx(m - ms2);
+            const float wo = mlo.x == kNegInf ? 0.f : ex2_approx(mlo.x - ms2);
+            const float w0 = self == 0 ? ws : wo, w1 = self == 0 ? wo : ws;
+            const float l0 = self == 0 ? lrow : mlo.y, l1 = self == 0 ? mlo.y : lrow;
+            const float inv2 = 1.f / __fmaf_rn(l1, w1, __fmaf_rn(l0, w0, 0.f));
+    #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t ov[32];
+                __syncwarp();  // converged for the warp-collective load
+                tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
+                tc::wait_ld();
+                if (!row_valid) continue;
+                float acc[32];
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 o = oo[8 * h + c];
+                    const float xo[4] = {o.x, o.y, o.z, o.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float xs = __uint_as_float(ov[4 * c + e]);
+                        const float x0 = self == 0 ? xs : xo[e], x1 = self == 0 ? xo[e] : xs;
+                        acc[4 * c + e] = __fmaf_rn(x1, w1, __fmaf_rn(x0, w0, 0.f));
+                    }
+                }
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 wv;
+                    wv.x = pack_bf16x2(acc[8 * c + 0] * inv2, acc[8 * c + 1] * inv2);
+                    wv.y = pack_bf16x2(acc[8 * c + 2] * inv2, acc[8 * c + 3] * inv2);
+                    wv.z = pack_bf16x2(acc[8 * c + 4] * inv2, acc[8 * c + 5] * inv2);
+                    wv.w = pack_bf16x2(acc[8 * c + 6] * inv2, acc[8 * c + 7] * inv2);
+                    *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = wv;
+                }
+            }
+        } else {
+        const float inv = 1.f / lsum;
+    #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t ov[32];
+            __syncwarp();  // converged for the warp-collective load
+            tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
+            tc::wait_ld();
+            if (!row_valid) continue;
+            if (merger) {
+                float acc[32];
+    #pragma unroll
+                for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(ov[j]);
+                if (!whole) {
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+                    for (int i = 0; i < nc; ++i) {
+                        const float2 ml = ml_of(i);
+                        const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
+                        if (i == self) {
+    #pragma unroll
+                            for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(__uint_as_float(ov[j]), w, acc[j]);
+                        } else {
+                            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + part_row(i) * kD + hc + 32 * h);
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const float4 o = __ldcg(src + c);
+                                acc[4 * c] = __fmaf_rn(o.x, w, acc[4 * c]);
+                                acc[4 * c + 1] = __fmaf_rn(o.y, w, acc[4 * c + 1]);
+                                acc[4 * c + 2] = __fmaf_rn(o.z, w, acc[4 * c + 2]);
+                                acc[4 * c + 3] = __fmaf_rn(o.w, w, acc[4 * c + 3]);
+                            }
+                        }
+                    }
+                }
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 wv;
+                    wv.x = pack_bf16x2(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
+                    wv.y = pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+                    wv.z = pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+                    wv.w = pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+                    *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = wv;
+                }
+            } else {
+    #pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4 *>(po + 32 * h + 4 * c) =
+                        make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
+                                    __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
+            }
+        }
+        }
+        if (!merger) {
+            if (row_valid)
+                *reinterpret_cast<float2 *>(p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 4 +
+                                            half * 2) = make_float2(m, lrow);
+            if (ctr) ready_ctr = ctr + kSoftmaxWarps;  // flagged after the next tile (or at the end)
+        }
+    }
+    if (warp == 2 && lane == 0) SV_STAMP(12);
+    tc::fence_before();
+    return done(true);
+}
+
 // MROWS query rows per group: 128 (M=128 products, row r in TMEM lane r) or
 // 64 (M=64 products, row r in lane 32*(r/16) + r%16: lanes 0-15 of each
 // 32-lane quarter) for groups of at most 64 rows.
@@ -708,6 +982,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int next_L = 0, next_T = 0;  // the next segment's prefix length and nodes, read ahead
     int2 next_par = make_int2(-1, -1);  // and its parents (two nodes a lane)
     bool have_next_L = false;
+    const SegOutputs seg_out{p.out, p.part_o, p.part_ml, p.T, p.Hq, p.G};
     Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
     long long jt = 0;
     for (long long u = u_begin; u < u_end; ++u, ++jt) {
@@ -833,17 +1108,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // O holds earlier tiles of this segment at the old max: once
                 // the last PV is done, rescale this half of the row in TMEM
                 // (before P is released, so this tile's PV sees it)
-                ok = warp_wait_bounded(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1));
-                tc::fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t ov[32];
-                    tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * a);
-                    tc::tmem_st32(tl + kColO + hc + 32 * h, ov);
-                }
+                ok = rescale_o_half(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1),
+                                    tl + kColO + hc, a);
             }
             tc::wait_st();
             if (!ok) {
@@ -855,18 +1121,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // V rows past the sequence's last slot may hold anything (even NaN,
             // and 0 * NaN is NaN in the product): zero them in this stage,
             // once its V half has landed
-            if (!warp_wait_bounded(&sh->full_v[jt % STAGES], (uint32_t)((jt / STAGES) & 1))) {
+            if (!zero_v_tail(&sh->full_v[jt % STAGES], (uint32_t)((jt / STAGES) & 1),
+                             smem + (int)(jt % STAGES) * kStageBytes + 2 * kBox, kv_end - kbase,
+                             (warp - 2) * 32 + lane)) {
                 fail(cur.b);
                 break;
             }
-            const int z0 = kv_end - kbase;
-            uint8_t *vst = smem + (int)(jt % STAGES) * kStageBytes + 2 * kBox;
-            for (int i = (warp - 2) * 32 + lane; i < (kBK - z0) * 16; i += 32 * kSoftmaxWarps) {
-                const int row = z0 + (i >> 4), c = i & 15;
-                *reinterpret_cast<uint4 *>(vst + (c >> 3) * kBox + sw128(row, c & 7)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            tc::fence_proxy_async_smem();
         }
         tc::fence_before();
         __syncwarp();
@@ -878,206 +1138,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // ---- end of a segment: this half of the O row out of TMEM
         if (last_of_pair || u == u_end - 1) {
-            if (!warp_wait_bounded(&sh->pv_done[jt & 1], (uint32_t)((jt >> 1) & 1))) {
+            const SegEndRet se = softmax_segment_end<MROWS>(
+                seg_out, sh, tile_base, pl, cur, jt, U, nctas, nlane, myslot, tl, quarter, half, hc, lane,
+                warp, r, rglob, kvh, lane_has_row, row_valid, warp_active, whole, seg_is_first, cl, m,
+                l, arrived, ctr, pair_uses, staged);
+            pair_uses = se.pair_uses;
+            ready_ctr = se.ready_ctr;
+            staged = se.staged;
+            if (!se.ok) {
                 fail(cur.b);
                 break;
             }
-            tc::fence_after();
-            if (warp == 2 && lane == 0) SV_STAMP(11);
-            // row sum = first half's part + second half's part (same order in both)
-            sh->xl[quarter][half][lane] = l;
-            if (!group_sync(&sh->pair[quarter], pair_uses)) {
-                fail(cur.b);
-                break;
-            }
-            const float lrow = sh->xl[quarter][0][lane] + sh->xl[quarter][1][lane];
-            if (cl) {
-                // cluster mode: this CTA's share of the group, unnormalised,
-                // into the merge buffer (the K/V ring is idle now: every copy
-                // has landed and every product has read it)
-                cluster_stage<MROWS>(p.part_o + (size_t)blockIdx.x * kClusterSlot<MROWS>,
-                                     tl + kColO + hc, r, half, lane_has_row, row_valid, m, lrow);
-                staged = true;
-                if (warp == 2 && lane == 0) SV_STAMP(12);
-                tc::fence_before();
-                cursor_next(cur, tile_base, p.B, pl);
-                continue;
-            }
-            const int t = row_valid ? rglob / p.G : 0;
-            const int g = row_valid ? rglob - t * p.G : 0;
-            uint16_t *orow = p.out + (((size_t)cur.b * p.T + t) * p.Hq + kvh * p.G + g) * kD + hc;
-            // A split pair: the last CTA to arrive merges the others'
-            // partials into its own O; the others leave a partial and flag it
-            // ready once it is visible.  Nobody waits for a CTA that has not
-            // already arrived.
-            int nc = 1, c0 = 0, slot0 = 0;
-            bool merger = whole;
-            if (!whole && warp_active) {
-                const long long ub = (long long)tile_base[cur.b] * pl.npr + (long long)cur.pi * cur.n;
-                c0 = cta_of(U, nctas, ub);  // slots; contributor i is CTA (c0 + i) * nlane + lane
-                nc = cta_of(U, nctas, ub + cur.n - 1) - c0 + 1;
-                slot0 = cta_begin(U, nctas, c0) >= ub ? 0 : 1;
-                const int pos = __shfl_sync(0xffffffffu, arrived, 0);
-                merger = pos == nc - 1;
-                if (merger) {
-                    bool ready = true;
-                    if (lane == 0) {
-                        const long long t0 = clock64();
-                        while (ld_acquire_gpu(ctr + kSoftmaxWarps) < nc - 1)
-                            if (clock64() - t0 > kWaitCycles) {
-                                ready = false;
-                                break;
-                            }
-                        if (ready) {
-                            ctr[0] = 0;  // ready for the next call
-                            ctr[kSoftmaxWarps] = 0;
-                        }
-                    }
-                    if (!__shfl_sync(0xffffffffu, ready, 0)) {
-                        fail(cur.b);
-                        break;
-                    }
-                    __syncwarp();  // the others' partials are read after lane 0's acquire
-                }
-            }
-            if (warp_active) {
-                // the other contributors' (max, sum) of this row half
-                auto part_row = [&](int i) -> size_t {
-                    return ((size_t)((c0 + i) * nlane + pl.poff) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
-                };
-                // The merge takes the contributors in index order with the same
-                // arithmetic whoever merges, so the result does not depend on
-                // which CTA finished last.
-                const int self = myslot - c0;
-                auto ml_of = [&](int i) -> float2 {
-                    return i == self ? make_float2(m, lrow)
-                                     : __ldcg(reinterpret_cast<const float2 *>(p.part_ml + part_row(i) * 4 + half * 2));
-                };
-                float mstar = m, lsum = lrow;
-                if (!whole && merger && row_valid && nc != 2) {
-                    for (int i = 0; i < nc; ++i) mstar = fmaxf(mstar, ml_of(i).x);
-                    lsum = 0.f;
-                    for (int i = 0; i < nc; ++i) {
-                        const float2 ml = ml_of(i);
-                        const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
-                        lsum = __fmaf_rn(ml.y, w, lsum);
-                    }
-                }
-                const int slot = seg_is_first ? 0 : 1;
-                float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
-                if (!whole && merger && nc == 2) {  // (the same in every lane)
-                    // two contributors (the usual split): the other's partial
-                    // fetched in one go, then the same arithmetic as below
-                    const int oth = 1 - self;
-                    const size_t pro = part_row(oth);
-                    float2 mlo = make_float2(kNegInf, 0.f);
-                    float4 oo[16];
-                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + pro * kD + hc);
-                    if (row_valid) {
-                        mlo = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pro * 4 + half * 2));
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) oo[c] = __ldcg(src + c);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) oo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    const float ms2 = fmaxf(m, mlo.x);
-                    const float ws = m == kNegInf ? 0.f : ex2_approx(m - ms2);
-                    const float wo = mlo.x == kNegInf ? 0.f : ex2_approx(mlo.x - ms2);
-                    const float w0 = self == 0 ? ws : wo, w1 = self == 0 ? wo : ws;
-                    const float l0 = self == 0 ? lrow : mlo.y, l1 = self == 0 ? mlo.y : lrow;
-                    const float inv2 = 1.f / __fmaf_rn(l1, w1, __fmaf_rn(l0, w0, 0.f));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t ov[32];
-                        __syncwarp();  // converged for the warp-collective load
-                        tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
-                        tc::wait_ld();
-                        if (!row_valid) continue;
-                        float acc[32];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float4 o = oo[8 * h + c];
-                            const float xo[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float xs = __uint_as_float(ov[4 * c + e]);
-                                const float x0 = self == 0 ? xs : xo[e], x1 = self == 0 ? xo[e] : xs;
-                                acc[4 * c + e] = __fmaf_rn(x1, w1, __fmaf_rn(x0, w0, 0.f));
-                            }
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint4 wv;
-                            wv.x = pack_bf16x2(acc[8 * c + 0] * inv2, acc[8 * c + 1] * inv2);
-                            wv.y = pack_bf16x2(acc[8 * c + 2] * inv2, acc[8 * c + 3] * inv2);
-                            wv.z = pack_bf16x2(acc[8 * c + 4] * inv2, acc[8 * c + 5] * inv2);
-                            wv.w = pack_bf16x2(acc[8 * c + 6] * inv2, acc[8 * c + 7] * inv2);
-                            *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = wv;
-                        }
-                    }
-                } else {
-                const float inv = 1.f / lsum;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t ov[32];
-                    __syncwarp();  // converged for the warp-collective load
-                    tc::tmem_ld32(tl + kColO + hc + 32 * h, ov);
-                    tc::wait_ld();
-                    if (!row_valid) continue;
-                    if (merger) {
-                        float acc[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(ov[j]);
-                        if (!whole) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-                            for (int i = 0; i < nc; ++i) {
-                                const float2 ml = ml_of(i);
-                                const float w = ml.x == kNegInf ? 0.f : ex2_approx(ml.x - mstar);
-                                if (i == self) {
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(__uint_as_float(ov[j]), w, acc[j]);
-                                } else {
-                                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + part_row(i) * kD + hc + 32 * h);
-#pragma unroll
-                                    for (int c = 0; c < 8; ++c) {
-                                        const float4 o = __ldcg(src + c);
-                                        acc[4 * c] = __fmaf_rn(o.x, w, acc[4 * c]);
-                                        acc[4 * c + 1] = __fmaf_rn(o.y, w, acc[4 * c + 1]);
-                                        acc[4 * c + 2] = __fmaf_rn(o.z, w, acc[4 * c + 2]);
-                                        acc[4 * c + 3] = __fmaf_rn(o.w, w, acc[4 * c + 3]);
-                                    }
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint4 wv;
-                            wv.x = pack_bf16x2(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv);
-                            wv.y = pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
-                            wv.z = pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
-                            wv.w = pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
-                            *reinterpret_cast<uint4 *>(orow + 32 * h + 8 * c) = wv;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<float4 *>(po + 32 * h + 4 * c) =
-                                make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
-                                            __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
-                    }
-                }
-                }
-                if (!merger) {
-                    if (row_valid)
-                        *reinterpret_cast<float2 *>(p.part_ml + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * 4 +
-                                                    half * 2) = make_float2(m, lrow);
-                    if (ctr) ready_ctr = ctr + kSoftmaxWarps;  // flagged after the next tile (or at the end)
-                }
-            }
-            if (warp == 2 && lane == 0) SV_STAMP(12);
-            tc::fence_before();
         }
         cursor_next(cur, tile_base, p.B, pl);
     }
