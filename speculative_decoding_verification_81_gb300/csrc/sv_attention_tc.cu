@@ -696,7 +696,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the last warp the V halves.  A K half is refilled as soon as the S
         // product that read it is done, a V half once its PV product is, so
         // the next K tiles stream in while a tile's softmax and PV run.
-        if (p.block_table && p.page_size < kBK) {
+        if (!(p.block_table && p.page_size < kBK)) {
+            if (lane == 0) {
+                const bool is_k = warp == 0;
+                uint64_t *full = is_k ? sh->full_k : sh->full_v;
+                uint64_t *empty = is_k ? sh->empty_k : sh->empty_v;
+                const CUtensorMap *map = is_k ? &tmk : &tmv;
+                const int half_off = is_k ? 0 : 2 * kBox;
+                // K/V tiles are streamed: evict-first keeps the stream from
+                // pushing code, Q and partials out of L2.  (Among evict-first
+                // lines the oldest go first, so a tile still outlives the few
+                // microseconds between the reads of the lanes of one slot.)
+                const uint64_t pol = l2_policy_evict_first();
+                auto load = [&](void *dst, int x, int y, uint64_t *bar) {
+                    tma_load_2d_hint(dst, map, x, y, bar, pol);
+                };
+                Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
+                long long k = 0;
+                uint32_t qseg = 0;  // segments whose Q was issued
+                if (is_k) SV_STAMP(4);
+                for (long long u = u_begin; u < u_end; ++u, ++k) {
+                    const int s = (int)(k % STAGES);
+                    const uint32_t ph = (uint32_t)((k / STAGES) & 1);
+                    // At the start every SM asks for its ring at once: the first V
+                    // tile waits until the first K tile (which the first S
+                    // product needs) has been requested.
+                    if (!is_k && k == 0 && !mbar_wait_bounded(&sh->k_first, 0)) {
+                        fail(cur.b);
+                        break;
+                    }
+                    if (is_k && (u == u_begin || cur.tile == 0)) {
+                        // this segment's Q rows (rows_per_rg of them: rows_per_rg / G
+                        // nodes x G heads, a 3-D box) into Q buffer qseg & 1, once
+                        // the S products of the segment two back are done
+                        const int qb = (int)(qseg & 1);
+                        if (!mbar_wait_bounded(&sh->q_empty[qb], ((qseg >> 1) & 1) ^ 1u)) {
+                            fail(cur.b);
+                            break;
+                        }
+                        const int kvh = cur.pr / p.RG, rg = cur.pr - kvh * p.RG;
+                        const int tpr = p.rows_per_rg / p.G;  // nodes per row group
+                        const int z = cur.b * p.T + rg * tpr;
+                        uint8_t *qd = qbuf + qb * 2 * kQBox;
+                        mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
+                        tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
+                        tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
+                        if (qseg == 0) SV_STAMP(5);
+                        ++qseg;
+                    }
+                    const int kvh = cur.pr / p.RG;
+                    const int kb = cur.tile * kBK;
+                    if (!p.block_table) {
+                        // contiguous caches: the tile is 128 consecutive rows
+                        if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                            fail(cur.b);
+                            break;
+                        }
+                        if (*abort_flag) break;
+                        const int y = (cur.b * p.Hkv + kvh) * p.S_max + kb;
+                        uint8_t *st = smem + s * kStageBytes + half_off;
+                        mbar_arrive_expect_tx(&full[s], 2 * kBox);
+                        load(st, 0, y, &full[s]);
+                        load(st + kBox, 64, y, &full[s]);
+                    } else {
+                        // paged, pages of 128 slots or more: the tile sits in one page
+                        // (its id read before the wait, so the load overlaps it); an
+                        // id out of range (reported by the prologue) reads zeros
+                        const int pg = p.block_table[(size_t)cur.b * p.max_pages + kb / p.page_size];
+                        const int y = (pg >= 0 && pg < p.num_pages)
+                                          ? (pg * p.Hkv + kvh) * p.page_size + kb % p.page_size
+                                          : -kBK;
+                        if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
+                            fail(cur.b);
+                            break;
+                        }
+                        if (*abort_flag) break;
+                        uint8_t *st = smem + s * kStageBytes + half_off;
+                        mbar_arrive_expect_tx(&full[s], 2 * kBox);
+                        load(st, 0, y, &full[s]);
+                        load(st + kBox, 64, y, &full[s]);
+                    }
+                    if (is_k && k == 0) {
+                        mbar_arrive(&sh->k_first);
+                        SV_STAMP(6);
+                    }
+                    if (!is_k && k == 0) SV_STAMP(18);
+                    if (is_k) SV_STAMP(10);
+                    cursor_next(cur, tile_base, p.B, pl);
+                }
+                if (is_k && k == 0) mbar_arrive(&sh->k_first);  // none issued: release the V side
+                // every copy issued must land before the CTA may exit
+                const long long first = k > STAGES ? k - STAGES : 0;
+                for (long long j = first; j < k; ++j)
+                    mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
+                for (uint32_t g2 = qseg > 2 ? qseg - 2 : 0; g2 < qseg; ++g2)
+                    mbar_wait_bounded(&sh->q_full[g2 & 1], (g2 >> 1) & 1);
+            }
+        } else {
             // Paged, pages of 8-64 slots: a tile is 128 / page_size blocks of
             // page_size rows, one per page.  Lane i reads page i's id and
             // issues that block's two boxes, so a tile's blocks go out
@@ -769,100 +865,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (uint32_t g2 = qseg > 2 ? qseg - 2 : 0; g2 < qseg; ++g2)
                     mbar_wait_bounded(&sh->q_full[g2 & 1], (g2 >> 1) & 1);
             }
-        } else if (lane == 0) {
-            const bool is_k = warp == 0;
-            uint64_t *full = is_k ? sh->full_k : sh->full_v;
-            uint64_t *empty = is_k ? sh->empty_k : sh->empty_v;
-            const CUtensorMap *map = is_k ? &tmk : &tmv;
-            const int half_off = is_k ? 0 : 2 * kBox;
-            // K/V tiles are streamed: evict-first keeps the stream from
-            // pushing code, Q and partials out of L2.  (Among evict-first
-            // lines the oldest go first, so a tile still outlives the few
-            // microseconds between the reads of the lanes of one slot.)
-            const uint64_t pol = l2_policy_evict_first();
-            auto load = [&](void *dst, int x, int y, uint64_t *bar) {
-                tma_load_2d_hint(dst, map, x, y, bar, pol);
-            };
-            Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
-            long long k = 0;
-            uint32_t qseg = 0;  // segments whose Q was issued
-            if (is_k) SV_STAMP(4);
-            for (long long u = u_begin; u < u_end; ++u, ++k) {
-                const int s = (int)(k % STAGES);
-                const uint32_t ph = (uint32_t)((k / STAGES) & 1);
-                // At the start every SM asks for its ring at once: the first V
-                // tile waits until the first K tile (which the first S
-                // product needs) has been requested.
-                if (!is_k && k == 0 && !mbar_wait_bounded(&sh->k_first, 0)) {
-                    fail(cur.b);
-                    break;
-                }
-                if (is_k && (u == u_begin || cur.tile == 0)) {
-                    // this segment's Q rows (rows_per_rg of them: rows_per_rg / G
-                    // nodes x G heads, a 3-D box) into Q buffer qseg & 1, once
-                    // the S products of the segment two back are done
-                    const int qb = (int)(qseg & 1);
-                    if (!mbar_wait_bounded(&sh->q_empty[qb], ((qseg >> 1) & 1) ^ 1u)) {
-                        fail(cur.b);
-                        break;
-                    }
-                    const int kvh = cur.pr / p.RG, rg = cur.pr - kvh * p.RG;
-                    const int tpr = p.rows_per_rg / p.G;  // nodes per row group
-                    const int z = cur.b * p.T + rg * tpr;
-                    uint8_t *qd = qbuf + qb * 2 * kQBox;
-                    mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
-                    tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
-                    tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
-                    if (qseg == 0) SV_STAMP(5);
-                    ++qseg;
-                }
-                const int kvh = cur.pr / p.RG;
-                const int kb = cur.tile * kBK;
-                if (!p.block_table) {
-                    // contiguous caches: the tile is 128 consecutive rows
-                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
-                        fail(cur.b);
-                        break;
-                    }
-                    if (*abort_flag) break;
-                    const int y = (cur.b * p.Hkv + kvh) * p.S_max + kb;
-                    uint8_t *st = smem + s * kStageBytes + half_off;
-                    mbar_arrive_expect_tx(&full[s], 2 * kBox);
-                    load(st, 0, y, &full[s]);
-                    load(st + kBox, 64, y, &full[s]);
-                } else {
-                    // paged, pages of 128 slots or more: the tile sits in one page
-                    // (its id read before the wait, so the load overlaps it); an
-                    // id out of range (reported by the prologue) reads zeros
-                    const int pg = p.block_table[(size_t)cur.b * p.max_pages + kb / p.page_size];
-                    const int y = (pg >= 0 && pg < p.num_pages)
-                                      ? (pg * p.Hkv + kvh) * p.page_size + kb % p.page_size
-                                      : -kBK;
-                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u)) {
-                        fail(cur.b);
-                        break;
-                    }
-                    if (*abort_flag) break;
-                    uint8_t *st = smem + s * kStageBytes + half_off;
-                    mbar_arrive_expect_tx(&full[s], 2 * kBox);
-                    load(st, 0, y, &full[s]);
-                    load(st + kBox, 64, y, &full[s]);
-                }
-                if (is_k && k == 0) {
-                    mbar_arrive(&sh->k_first);
-                    SV_STAMP(6);
-                }
-                if (!is_k && k == 0) SV_STAMP(18);
-                if (is_k) SV_STAMP(10);
-                cursor_next(cur, tile_base, p.B, pl);
-            }
-            if (is_k && k == 0) mbar_arrive(&sh->k_first);  // none issued: release the V side
-            // every copy issued must land before the CTA may exit
-            const long long first = k > STAGES ? k - STAGES : 0;
-            for (long long j = first; j < k; ++j)
-                mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
-            for (uint32_t g2 = qseg > 2 ? qseg - 2 : 0; g2 < qseg; ++g2)
-                mbar_wait_bounded(&sh->q_full[g2 & 1], (g2 >> 1) & 1);
         }
     } else if (warp == 1 || warp == kPvWarp) {
         // ================= MMA issue: lane 0 of warp 1 the S = Q K^T

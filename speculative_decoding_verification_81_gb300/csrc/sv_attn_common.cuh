@@ -141,6 +141,33 @@ __device__ __forceinline__ int nodes_of(const AttnKParams &p, int b) {
     return (n >= 1 && n <= p.T) ? n : 0;
 }
 
+// Every sequence's inputs checked and its status written, by CTA 0 (out of
+// line: the other CTAs jump over one call instead of the whole check).
+static __device__ __noinline__ void check_sequences(const AttnKParams &p, int nt) {
+    const int tid = threadIdx.x;
+    for (int b = tid; b < p.B; b += nt) {
+        const int L = p.prefix_lens[b], Tb = nodes_of(p, b);
+        bool ok = L >= 0 && Tb > 0 && (long long)L + Tb <= p.S_max;
+        if (ok && p.block_table) {  // the pages holding slots [0, L + T_b) exist
+            const int np = (L + Tb + p.page_size - 1) / p.page_size;
+            for (int j = 0; j < np; ++j) {
+                const int pg = p.block_table[(size_t)b * p.max_pages + j];
+                if (pg < 0 || pg >= p.num_pages) ok = false;
+            }
+        }
+        p.seq_status[b] = ok ? SV_OK : SV_ERR_BAD_INPUT;
+    }
+    __syncthreads();
+    if (p.parents) {
+        for (int i = tid; i < p.B * p.T; i += nt) {
+            const int b = i / p.T, t = i - b * p.T;
+            if (t >= nodes_of(p, b)) continue;  // padding node
+            const int pa = p.parents[i];
+            if (t == 0 ? pa != -1 : (pa < 0 || pa >= t)) p.seq_status[b] = SV_ERR_BAD_INPUT;
+        }
+    }
+}
+
 // pre_L, pre_T: prefix length and node count of sequence threadIdx.x, loaded
 // by the caller ahead of its own set-up.
 __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_base, int nt, int pre_L,
@@ -169,29 +196,7 @@ __device__ __forceinline__ void attn_prologue(const AttnKParams &p, int *tile_ba
         }
         if (tid == 0) tile_base[p.B] = carry;
     }
-    if (blockIdx.x == 0 && p.seq_status) {
-        for (int b = tid; b < p.B; b += nt) {
-            const int L = p.prefix_lens[b], Tb = nodes_of(p, b);
-            bool ok = L >= 0 && Tb > 0 && (long long)L + Tb <= p.S_max;
-            if (ok && p.block_table) {  // the pages holding slots [0, L + T_b) exist
-                const int np = (L + Tb + p.page_size - 1) / p.page_size;
-                for (int j = 0; j < np; ++j) {
-                    const int pg = p.block_table[(size_t)b * p.max_pages + j];
-                    if (pg < 0 || pg >= p.num_pages) ok = false;
-                }
-            }
-            p.seq_status[b] = ok ? SV_OK : SV_ERR_BAD_INPUT;
-        }
-        __syncthreads();
-        if (p.parents) {
-            for (int i = tid; i < p.B * p.T; i += nt) {
-                const int b = i / p.T, t = i - b * p.T;
-                if (t >= nodes_of(p, b)) continue;  // padding node
-                const int pa = p.parents[i];
-                if (t == 0 ? pa != -1 : (pa < 0 || pa >= t)) p.seq_status[b] = SV_ERR_BAD_INPUT;
-            }
-        }
-    }
+    if (blockIdx.x == 0 && p.seq_status) check_sequences(p, nt);
     __syncthreads();
 }
 
