@@ -264,3 +264,34 @@ def test_tree_step_ragged_node_counts(orc):
         np.testing.assert_array_equal(k[b:b + 1], rc["k"])
         np.testing.assert_array_equal(v[b:b + 1], rc["v"])
         assert newl[b] == rc["new_kv_lens"][0]
+
+
+def test_tree_step_flat_split_ragged_node_counts(orc):
+    """The flat split's kernels in sequence (B=16, T=64: two row groups per KV
+    head) with node counts T_b < T and NaN logits on the padding nodes' rows:
+    each sequence's paths, tokens and compacted rows equal the oracle on its
+    first T_b nodes alone."""
+    rng = np.random.default_rng(41)
+    B, T, V = 16, 64, 5000
+    par = np.stack([W.random_tree(T, 8, rng) for _ in range(B)])
+    counts = rng.integers(1, T + 1, B).astype(np.int32)
+    counts[0], counts[1] = T, 1
+    tr = W.tree_logit_inputs(B, T, V, par, 0.7, seed=41)
+    for b in range(B):
+        tr["target"][b, counts[b]:] = 0x7FC0  # bf16 NaN: padding rows are never read
+    a = W.attention_inputs(B, T, 32, 8, 128, rng.integers(0, 300, B), parents=par, seed=41,
+                           unused_fill="zero")
+    out, acc, path, toks, newl, k, v, ast, vst = _tree_step(a, tr, node_counts=counts)
+    for b in range(B):
+        n = int(counts[b])
+        ref = orc.verify_tree_greedy(tr["target"][b:b + 1, :n], tr["node_tokens"][b:b + 1, :n],
+                                     par[b:b + 1, :n])
+        assert acc[b] == ref["accepted_len"][0]
+        np.testing.assert_array_equal(path[b, :n], ref["path_nodes"][0])
+        np.testing.assert_array_equal(toks[b, :n], ref["out_tokens"][0])
+        rc = orc.compact_kv(a["k"][b:b + 1], a["v"][b:b + 1], a["prefix_lens"][b:b + 1],
+                            ref["path_nodes"], ref["accepted_len"])
+        np.testing.assert_array_equal(k[b:b + 1], rc["k"])
+        np.testing.assert_array_equal(v[b:b + 1], rc["v"])
+        assert newl[b] == rc["new_kv_lens"][0]
+    assert acc.max() > 0
