@@ -53,6 +53,8 @@
 // of a tile the moment its P is written, and no K/V stage is held longer
 // than its own tile needs.  Every wait is bounded (SV_ERR_TIMEOUT on expiry);
 // the TMEM is always released.
+#include <type_traits>
+
 #include "sv_attn_common.cuh"
 #include "sv_internal.h"
 
@@ -986,61 +988,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool have_next_L = false;
     const SegOutputs seg_out{p.out, p.part_o, p.part_ml, p.T, p.Hq, p.G};
     Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
-    long long jt = 0;
-    for (long long u = u_begin; u < u_end; ++u, ++jt) {
-        const bool new_seg = (u == u_begin) || cur.tile == 0;
-        if (new_seg) {
-            kvh = cur.pr / p.RG;
-            rg = cur.pr - kvh * p.RG;
-            L = have_next_L ? next_L : p.prefix_lens[cur.b];
-            const int Tb = have_next_L ? next_T : nodes_of(p, cur.b);
-            const int2 par = have_next_L ? next_par : load_parents_warp(p.parents, p.T, cur.b, lane);
-            have_next_L = false;
-            kv_end = L + Tb;
-            seg_first_tile = cur.tile;
-            seg_is_first = (u == u_begin);
-            // the group's rows are rows_per_rg (a multiple of G) of the MMA's
-            // MROWS; the others are padding
-            rglob = rg * p.rows_per_rg + r;
-            row_valid = lane_has_row && r < p.rows_per_rg && rglob < p.M && rglob / p.G < Tb;
-            warp_active = quarter * kRowsPerQuarter < p.rows_per_rg &&
-                          rg * p.rows_per_rg + quarter * kRowsPerQuarter < p.M;
-            m = kNegInf;
-            l = 0.f;
-            anc = ancestors_warp(p.parents == nullptr, par.x, par.y, rglob / p.G, row_valid);
-        }
-        // A few tiles before this segment ends: read the next segment's prefix
-        // length (its Q is brought in by the producer).
-        if (cur.tile == max(seg_first_tile, cur.n - 5) && u + (cur.n - cur.tile) < u_end) {
-            Cursor nx = cur;
-            nx.tile = nx.n - 1;
-            cursor_next(nx, tile_base, p.B, pl);
-            next_L = p.prefix_lens[nx.b];
-            next_T = nodes_of(p, nx.b);
-            next_par = load_parents_warp(p.parents, p.T, nx.b, lane);
-            have_next_L = true;
-        }
-        const bool first_tile = new_seg;  // O is overwritten by this tile's PV
+    long long jt = 0, u = u_begin;
+    // One tile: the tile at cur, unit u, tile jt of the run; false when a
+    // bounded wait gave up.  FULL adds the pieces only some tiles need: a
+    // segment's first tile (O starts over; a partial left by the previous
+    // segment is flagged ready), the tiles with keys at or past L (the ancestor
+    // mask), the segment's last tile in the run (the split pair's counter, the
+    // V rows past the sequence's end, the end of the segment).  The tiles in
+    // between run the short form, whose code has almost no branches: a taken
+    // branch in this loop costs instruction fetch on every tile.
+    auto tile = [&](auto full_tag) -> bool {
+        constexpr bool FULL = decltype(full_tag)::value;
+        const bool first_tile = FULL && cur.tile == seg_first_tile;  // O is overwritten by this tile's PV
         const int kbase = cur.tile * kBK;
-        const bool last_of_pair = cur.tile == cur.n - 1;
-        const bool seg_end = last_of_pair || u == u_end - 1;
+        const bool last_of_pair = FULL && cur.tile == cur.n - 1;
+        const bool seg_end = FULL && (last_of_pair || u == u_end - 1);
         const bool whole = seg_first_tile == 0 && last_of_pair;
         // The last tile of a split segment: arrive on the pair's counter now
         // (per warp: its rows, its half of the columns), so the atomic's round
         // trip overlaps this tile; the last CTA to arrive merges.
         int *ctr = nullptr;
         int arrived = 0;
-        if (!cl && seg_end && !whole && warp_active) {
+        if (FULL && !cl && seg_end && !whole && warp_active) {
             ctr = p.pair_ctr + ((size_t)((cur.b * p.Hkv + kvh) * p.RG + rg) * 2) * kSoftmaxWarps + (warp - 2);
             if (lane == 0) arrived = atomicAdd(ctr, 1);
         }
         const uint32_t sbuf = tl + kColS + (uint32_t)(jt & 1) * kBK + hc;  // this half's S columns
 
         // ---- half S row from TMEM; P written back over its first 32 columns
-        if (!warp_wait_bounded(&sh->s_full[jt & 1], (uint32_t)((jt >> 1) & 1))) {
-            fail(cur.b);
-            break;
-        }
+        if (!warp_wait_bounded(&sh->s_full[jt & 1], (uint32_t)((jt >> 1) & 1))) return false;
         tc::fence_after();
         if (warp == 2 && lane == 0) {
             if (jt == 0) SV_STAMP(8);
@@ -1061,7 +1037,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             const int k0 = kbase + hc;  // key of sv[0]
-            if (k0 + 64 > L) {
+            if (FULL && k0 + 64 > L) {
                 // bit j: key k0 + j visible to this row (a prefix key, or a
                 // new node on the row's root path; anc has no bit past T)
                 const int dl = L - k0;  // keys before L in this half tile (may be <= 0)
@@ -1114,32 +1090,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     tl + kColO + hc, a);
             }
             tc::wait_st();
-            if (!ok) {
-                fail(cur.b);
-                break;
-            }
+            if (!ok) return false;
         }
-        if (last_of_pair && kbase + kBK > kv_end) {
+        if (FULL && last_of_pair && kbase + kBK > kv_end) {
             // V rows past the sequence's last slot may hold anything (even NaN,
             // and 0 * NaN is NaN in the product): zero them in this stage,
             // once its V half has landed
             if (!zero_v_tail(&sh->full_v[jt % STAGES], (uint32_t)((jt / STAGES) & 1),
                              smem + (int)(jt % STAGES) * kStageBytes + 2 * kBox, kv_end - kbase,
-                             (warp - 2) * 32 + lane)) {
-                fail(cur.b);
-                break;
-            }
+                             (warp - 2) * 32 + lane))
+                return false;
         }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->p_full[jt & 1]);
-        if (ready_ctr) {  // the partial left at the previous tile has drained by now
+        if (FULL && ready_ctr) {  // the partial left at the previous tile has drained by now
             flag_ready(ready_ctr);
             ready_ctr = nullptr;
         }
 
         // ---- end of a segment: this half of the O row out of TMEM
-        if (last_of_pair || u == u_end - 1) {
+        if (FULL && seg_end) {
             const SegEndRet se = softmax_segment_end<MROWS>(
                 seg_out, sh, tile_base, pl, cur, jt, U, nctas, nlane, myslot, tl, quarter, half, hc, lane,
                 warp, r, rglob, kvh, lane_has_row, row_valid, warp_active, whole, seg_is_first, cl, m,
@@ -1147,12 +1118,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pair_uses = se.pair_uses;
             ready_ctr = se.ready_ctr;
             staged = se.staged;
-            if (!se.ok) {
-                fail(cur.b);
-                break;
-            }
+            if (!se.ok) return false;
         }
         cursor_next(cur, tile_base, p.B, pl);
+        ++u;
+        ++jt;
+        return true;
+    };
+    while (u < u_end) {
+        // ---- a segment: the tiles of one (sequence, KV head, row group) in this run
+        kvh = cur.pr / p.RG;
+        rg = cur.pr - kvh * p.RG;
+        L = have_next_L ? next_L : p.prefix_lens[cur.b];
+        const int Tb = have_next_L ? next_T : nodes_of(p, cur.b);
+        const int2 par = have_next_L ? next_par : load_parents_warp(p.parents, p.T, cur.b, lane);
+        have_next_L = false;
+        kv_end = L + Tb;
+        seg_first_tile = cur.tile;
+        seg_is_first = (u == u_begin);
+        // the group's rows are rows_per_rg (a multiple of G) of the MMA's
+        // MROWS; the others are padding
+        rglob = rg * p.rows_per_rg + r;
+        row_valid = lane_has_row && r < p.rows_per_rg && rglob < p.M && rglob / p.G < Tb;
+        warp_active = quarter * kRowsPerQuarter < p.rows_per_rg &&
+                      rg * p.rows_per_rg + quarter * kRowsPerQuarter < p.M;
+        m = kNegInf;
+        l = 0.f;
+        anc = ancestors_warp(p.parents == nullptr, par.x, par.y, rglob / p.G, row_valid);
+        // tiles of the segment in this run (t0 ..); the first this warp masks
+        // (its keys reach L); the tiles after the first and before those run
+        // the short form
+        int left = (int)min((long long)(cur.n - cur.tile), u_end - u);
+        const int t0 = cur.tile;
+        const int lm = L - hc - 64;
+        const int t_short_end = min(lm < 0 ? 0 : lm / kBK + 1, t0 + left - 1);
+        bool ok = true, shorts_done = false;
+        while (ok && left > 0) {
+            ok = tile(std::true_type{});
+            --left;
+            if (ok && left > 0 && !shorts_done) {
+                shorts_done = true;
+                const int t_early = max(t0 + 1, t_short_end - 4);
+                while (ok && cur.tile < t_early) {
+                    ok = tile(std::false_type{});
+                    --left;
+                }
+                if (ok && u + (cur.n - cur.tile) < u_end) {
+                    // the next segment's prefix length, node count and parents, read
+                    // a few tiles before this one ends (its Q is brought in by the producer)
+                    Cursor nx = cur;
+                    nx.tile = nx.n - 1;
+                    cursor_next(nx, tile_base, p.B, pl);
+                    next_L = p.prefix_lens[nx.b];
+                    next_T = nodes_of(p, nx.b);
+                    next_par = load_parents_warp(p.parents, p.T, nx.b, lane);
+                    have_next_L = true;
+                }
+                while (ok && cur.tile < t_short_end) {
+                    ok = tile(std::false_type{});
+                    --left;
+                }
+            }
+        }
+        if (!ok) {
+            fail(cur.b);
+            break;
+        }
     }
     if (ready_ctr) flag_ready(ready_ctr);
     if (cl && !staged && lane_has_row && half == 0) {
