@@ -10,7 +10,7 @@
 // The G = Hq/Hkv query heads of a KV head and the T nodes form M = G*T query
 // rows that share every K/V tile, so each tile is read from HBM once per
 // (sequence, KV head) and feeds up to 128 rows of tensor-core work.  Work is
-// the flat list of (sequence, KV head, 128-row group, 64-key tile) units; a
+// the flat list of (sequence, KV head, 128-row group, 128-key tile) units; a
 // persistent grid (one CTA per SM) takes equal contiguous ranges of it, so the
 // load is balanced whatever the prefix lengths.  A (sequence, KV head) whose
 // tiles fall to several CTAs is merged by the CTA that finishes its part
@@ -29,8 +29,8 @@
 //               S = Q K^T products (M=128 or 64 rows, N=128 keys, K=128)
 //               into one of two TMEM S buffers.
 //   warp 10     one lane issues O += P V (N=128, K=128 keys) into the TMEM
-//               O accumulator.  Q and P are read from TMEM, K
-//               (K-major) and V (MN-major) from the shared-memory ring.  The
+//               O accumulator.  P is read from TMEM; Q, K (K-major) and V
+//               (MN-major) from shared memory (Q from its own double buffer).  The
 //               tiles are 128 keys wide because a product's issue and
 //               completion take about the same time for small and large
 //               shapes: fewer, larger MMAs keep the tensor pipe fed.
@@ -47,6 +47,9 @@
 //               writes its bf16 P half row over the S columns it came from
 //               (the A operand of the PV MMA), and at the end of a segment
 //               reads its half of the O row and writes it out (or a partial).
+//               The loop runs segment by segment: the tiles between a
+//               segment's first one and those holding new rows take a short
+//               form of the tile code, without those per-tile checks.
 //
 // The two issuing lanes wait (blocking, bounded) on their own barriers, so S
 // of the next tile is issued while the softmax of the current one runs, PV
