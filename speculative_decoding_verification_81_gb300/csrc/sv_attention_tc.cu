@@ -27,7 +27,9 @@
 //               is done, V after its PV).
 //   warp 1      owns the tensor memory (512 columns); one lane issues the
 //               S = Q K^T products (M=128 or 64 rows, N=128 keys, K=128)
-//               into one of two TMEM S buffers.
+//               into one of three TMEM S buffers (columns 0-383; O at
+//               384-511), so that S of tile j + 2 is computed while tile j's
+//               P waits for its PV product.
 //   warp 10     one lane issues O += P V (N=128, K=128 keys) into the TMEM
 //               O accumulator.  P is read from TMEM; Q, K (K-major) and V
 //               (MN-major) from shared memory (Q from its own double buffer).  The
@@ -63,7 +65,7 @@
 
 namespace sv {
 
-// Tensor-memory columns (32-bit each, one row per lane): two S buffers
+// Tensor-memory columns (32-bit each, one row per lane): three S buffers
 // (128 f32 each; the bf16 P of keys 0-63 overwrites S columns 0-31, that of
 // keys 64-127 S columns 64-95) and the O accumulator (128 f32).  P is the A
 // operand of the PV product, read by the tensor core from TMEM; Q, the A
@@ -115,7 +117,11 @@ struct StampExit {
 #define SV_STAMP_ENTRY() ((void)0)
 #define SV_STAMP_VALUE(slot, v) ((void)0)
 #endif
-constexpr uint32_t kColS = 0, kColO = 256;
+// S buffers in tensor memory: with three, S of tile j + 2 is computed while
+// tile j's P waits for its PV product (with two, the softmax waited ~0.1 us a
+// tile for S on 128-row groups)
+constexpr int kSBufs = 3;
+constexpr uint32_t kColS = 0, kColO = kSBufs * 128;
 
 // Byte offset of 16-byte chunk c (0..7) of row `row` in a 128-byte-swizzled
 // block whose rows are 128 bytes (the layout TMA writes with SWIZZLE_128B and
@@ -127,7 +133,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
 struct TcSmem {
     uint64_t full_k[4], empty_k[4];  // TMA ring, K halves of the stages
     uint64_t full_v[4], empty_v[4];  // V halves
-    uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];  // per S buffer
     uint64_t q_full[2], q_empty[2];  // Q tiles in shared memory (double buffer)
     uint64_t fin, fin_pv;
     uint64_t pair[4];            // the two softmax warps of each lane quarter
@@ -376,7 +382,7 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
         ret.ok = ok;
         return ret;
     };
-    if (!warp_wait_bounded(&sh->pv_done[jt & 1], (uint32_t)((jt >> 1) & 1))) {
+    if (!warp_wait_bounded(&sh->pv_done[jt % kSBufs], (uint32_t)((jt / kSBufs) & 1))) {
         return done(false);
     }
     tc::fence_after();
@@ -608,7 +614,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&sh->full_v[s], 1);
             mbar_init(&sh->empty_v[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&sh->s_full[i], 1);
             mbar_init(&sh->p_full[i], kSoftmaxWarps);
             mbar_init(&sh->pv_done[i], 1);
@@ -883,18 +889,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (warp == 1) {
                 constexpr uint32_t idS = tc::idesc_bf16(MROWS, kBK, false);
                 uint32_t seg = 0;  // segments started
+                int sb = 0;        // S buffer of tile j, and the parity of its use
+                uint32_t sph = 0;
                 for (long long j = 0; j < nt; ++j) {
                     const int s = (int)(j % STAGES);
                     // this segment's Q has landed, the K tile has landed, the S
-                    // buffer is free (PV of tile j-2, whose P lived there, is done)
+                    // buffer is free (PV of tile j - kSBufs, whose P lived there, is done)
                     if (j == 0 || cur.tile == 0) {
                         ok = mbar_wait_bounded(&sh->q_full[seg & 1], (seg >> 1) & 1);
                         ++seg;
                     }
                     if (ok) ok = mbar_wait_bounded(&sh->full_k[s], (uint32_t)((j / STAGES) & 1));
                     if (j == 0) SV_STAMP(7);
-                    if (ok && j >= 2)
-                        ok = mbar_wait_bounded(&sh->pv_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
+                    if (ok && j >= kSBufs) ok = mbar_wait_bounded(&sh->pv_done[sb], sph ^ 1u);
                     if (!ok || *abort_flag) {
                         ok = false;
                         break;
@@ -909,10 +916,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint64_t bd = dk + (uint64_t)((kk >> 2) * (kBox >> 4) + (kk & 3) * 2);
                         const uint64_t ad = dq + (uint64_t)((kk >> 2) * (kQBox >> 4) + (kk & 3) * 2);
-                        tc::mma_bf16(tbase + kColS + (uint32_t)(j & 1) * kBK, ad, bd, idS,
+                        tc::mma_bf16(tbase + kColS + (uint32_t)sb * kBK, ad, bd, idS,
                                      kk > 0 ? 1u : 0u);
                     }
-                    tc::commit(&sh->s_full[j & 1]);
+                    tc::commit(&sh->s_full[sb]);
+                    if (++sb == kSBufs) {
+                        sb = 0;
+                        sph ^= 1u;
+                    }
                     if (cur.tile == cur.n - 1 || j == nt - 1)
                         tc::commit(&sh->q_empty[(seg - 1) & 1]);  // Q buffer free once these S are done
                     tc::commit(&sh->empty_k[s]);  // the K half may be refilled once S(j) is done
@@ -920,10 +931,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             } else {
                 constexpr uint32_t idPV = tc::idesc_bf16(MROWS, kD, true);
+                int sb = 0;  // S buffer (holding P) of tile j, and the parity of its use
+                uint32_t sph = 0;
                 for (long long j = 0; j < nt; ++j) {
                     const int s = (int)(j % STAGES);
                     const bool first = (j == 0) || cur.tile == 0;  // O starts over
-                    ok = mbar_wait_bounded(&sh->p_full[j & 1], (uint32_t)((j >> 1) & 1));
+                    ok = mbar_wait_bounded(&sh->p_full[sb], sph);
                     if (ok) ok = mbar_wait_bounded(&sh->full_v[s], (uint32_t)((j / STAGES) & 1));
                     if (j == 0) SV_STAMP(19);
                     if (!ok || *abort_flag) {
@@ -933,7 +946,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::fence_after();
                     // V rows 16kk.. start 2048 bytes apart (descriptor address units of 16 bytes)
                     const uint64_t dv = tc::smem_desc(base_u32 + s * kStageBytes + 2 * kBox, kBox, 1024);
-                    const uint32_t pcol = tbase + kColS + (uint32_t)(j & 1) * kBK;
+                    const uint32_t pcol = tbase + kColS + (uint32_t)sb * kBK;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t bd = dv + (uint64_t)(kk * (2048 >> 4));
@@ -941,7 +954,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc::mma_bf16_ts(tbase + kColO, pcol + kk * 8 + (kk >= 4 ? 32 : 0), bd, idPV,
                                         (kk > 0 || !first) ? 1u : 0u);
                     }
-                    tc::commit(&sh->pv_done[j & 1]);
+                    tc::commit(&sh->pv_done[sb]);
+                    if (++sb == kSBufs) {
+                        sb = 0;
+                        sph ^= 1u;
+                    }
                     tc::commit(&sh->empty_v[s]);  // the V half may be refilled once PV(j) is done
                     cursor_next(cur, tile_base, p.B, pl);
                 }
@@ -992,6 +1009,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const SegOutputs seg_out{p.out, p.part_o, p.part_ml, p.T, p.Hq, p.G};
     Cursor cur = cursor_at(tile_base, p.B, pl, u_begin);
     long long jt = 0, u = u_begin;
+    int sb = 0;         // S buffer of tile jt
+    uint32_t sph = 0;   // and the parity of its use
     // One tile: the tile at cur, unit u, tile jt of the run; false when a
     // bounded wait gave up.  FULL adds the pieces only some tiles need: a
     // segment's first tile (O starts over; a partial left by the previous
@@ -1016,10 +1035,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ctr = p.pair_ctr + ((size_t)((cur.b * p.Hkv + kvh) * p.RG + rg) * 2) * kSoftmaxWarps + (warp - 2);
             if (lane == 0) arrived = atomicAdd(ctr, 1);
         }
-        const uint32_t sbuf = tl + kColS + (uint32_t)(jt & 1) * kBK + hc;  // this half's S columns
+        const uint32_t sbuf = tl + kColS + (uint32_t)sb * kBK + hc;  // this half's S columns
 
         // ---- half S row from TMEM; P written back over its first 32 columns
-        if (!warp_wait_bounded(&sh->s_full[jt & 1], (uint32_t)((jt >> 1) & 1))) return false;
+        if (!warp_wait_bounded(&sh->s_full[sb], sph)) return false;
         tc::fence_after();
         if (warp == 2 && lane == 0) {
             if (jt == 0) SV_STAMP(8);
@@ -1089,7 +1108,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // O holds earlier tiles of this segment at the old max: once
                 // the last PV is done, rescale this half of the row in TMEM
                 // (before P is released, so this tile's PV sees it)
-                ok = rescale_o_half(&sh->pv_done[(jt - 1) & 1], (uint32_t)(((jt - 1) >> 1) & 1),
+                // (tile jt - 1: the buffer before this one)
+                ok = rescale_o_half(&sh->pv_done[sb == 0 ? kSBufs - 1 : sb - 1], sb == 0 ? sph ^ 1u : sph,
                                     tl + kColO + hc, a);
             }
             tc::wait_st();
@@ -1098,7 +1118,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (FULL && last_of_pair && kbase + kBK > kv_end) {
             // V rows past the sequence's last slot may hold anything (even NaN,
             // and 0 * NaN is NaN in the product): zero them in this stage,
-            // once its V half has landed
+            // once its V half has landed.  With more S buffers than stages the
+            // softmax can run ahead of the PV product that last read this
+            // stage (tile jt - STAGES), and the stage's barrier could then
+            // still show that tile's phase: that product is waited for first.
+            if (jt >= STAGES) {
+                const long long jo = jt - STAGES;
+                if (!warp_wait_bounded(&sh->pv_done[jo % kSBufs], (uint32_t)((jo / kSBufs) & 1)))
+                    return false;
+            }
             if (!zero_v_tail(&sh->full_v[jt % STAGES], (uint32_t)((jt / STAGES) & 1),
                              smem + (int)(jt % STAGES) * kStageBytes + 2 * kBox, kv_end - kbase,
                              (warp - 2) * 32 + lane))
@@ -1106,7 +1134,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->p_full[jt & 1]);
+        if (lane == 0) mbar_arrive(&sh->p_full[sb]);
         if (FULL && ready_ctr) {  // the partial left at the previous tile has drained by now
             flag_ready(ready_ctr);
             ready_ctr = nullptr;
@@ -1126,6 +1154,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cursor_next(cur, tile_base, p.B, pl);
         ++u;
         ++jt;
+        if (++sb == kSBufs) {  // (sb, sph) = (jt % kSBufs, (jt / kSBufs) & 1)
+            sb = 0;
+            sph ^= 1u;
+        }
         return true;
     };
     while (u < u_end) {
