@@ -1222,20 +1222,27 @@ __global__ void __launch_bounds__(kVT) tree_stats_kernel(TreeArgs a, VocabPlan p
 // index holding it) -- the packed maximum first, then the first element
 // equal to it -- and leaves one record.  The walk is the next kernel's.
 // Rows of padding nodes (past T_b) are not read.
+// Units a producer claims at a time from the pass's shared counter.
+constexpr int kSClaim = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(kSThreads, 1)
     tree_stats_stream_kernel(TreeArgs a, VocabPlan p, WsView w) {
     SV_SPAN(kSpanTreeStats);
     extern __shared__ __align__(128) uint8_t ring[];  // kSStages * kSUnitBytes
     __shared__ uint64_t full[kSStages], empty[kSStages];
+    __shared__ int unit_of[kSStages];  // the unit in each stage; -1: no more units
     constexpr int PV = Elem<T>::kPerVec;
     constexpr int kUnitElems = kSUnitBytes / (int)sizeof(T);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_seq = a.T * p.nchunks;
-    const long long U = (long long)a.B * per_seq;
-    const long long u_begin = U * blockIdx.x / gridDim.x, u_end = U * (blockIdx.x + 1) / gridDim.x;
+    const int U = a.B * per_seq;  // units (the launch keeps this below 2^31)
     float2 *rec = reinterpret_cast<float2 *>(w.partials);  // [B][T][nchunks][kSGroupWarps]
     int *timed_out = w.counters + 2 * a.B;
+    // The CTAs claim units kSClaim at a time from one counter (the walk
+    // clears it), so that CTAs that start late -- behind an attention kernel
+    // whose CTAs end at different times -- take fewer of them.
+    int *claim = w.counters + 2 * a.B + 1;
     // node r of sequence b is read unless it is padding (node 0 always is read)
     auto row_in_use = [&](int b, int r) {
         return r == 0 || a.node_counts == nullptr || r < a.node_counts[b];
@@ -1257,17 +1264,33 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             long long k = 0;
-            for (long long u = u_begin; u < u_end; ++u, ++k) {
+            int next = 0, lim = 0;  // the claimed units not yet issued
+            int ends = 0;           // "no more units" stages published: one per consumer group
+            while (ends < 2) {
                 const int s = (int)(k % kSStages);
                 if (!mbar_wait_bounded(&empty[s], (uint32_t)(((k / kSStages) & 1) ^ 1))) {
                     atomicExch(timed_out, 1);  // a stage never came free
                     break;
                 }
-                const int b = (int)(u / per_seq);
-                const int rem = (int)(u - (long long)b * per_seq);
+                if (next == lim && ends == 0) {
+                    next = atomicAdd(claim, kSClaim);
+                    lim = min(next + kSClaim, U);
+                }
+                if (next >= lim) {  // the units are all claimed: an end marker, no copy
+                    unit_of[s] = -1;
+                    ++ends;
+                    mbar_arrive(&full[s]);
+                    ++k;
+                    continue;
+                }
+                const int u = next++;
+                unit_of[s] = u;
+                const int b = u / per_seq;
+                const int rem = u - b * per_seq;
                 const int r = rem / p.nchunks, c = rem - r * p.nchunks;
                 if (!row_in_use(b, r)) {  // padding: the stage's phase, no copy
                     mbar_arrive(&full[s]);
+                    ++k;
                     continue;
                 }
                 const T *row = static_cast<const T *>(a.target) + ((size_t)b * a.T + r) * a.V;
@@ -1275,6 +1298,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 const uint32_t bytes = (uint32_t)(min(kUnitElems, a.V - begin) * (int)sizeof(T));
                 mbar_arrive_expect_tx(&full[s], bytes);
                 bulk_load_hint(ring + s * kSUnitBytes, row + begin, bytes, &full[s], pol);
+                ++k;
             }
             // every copy issued must land before the CTA may exit
             const long long first = k > kSStages ? k - kSStages : 0;
@@ -1284,19 +1308,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
         return;
     }
 
-    // ================= consumers: two groups of eight warps, alternate units
+    // ================= consumers: two groups of eight warps, alternate stages
     const int grp = (warp >> 2) & 1, gw = ((warp >> 3) << 2) | (warp & 3);
-    for (long long k = grp; k < u_end - u_begin; k += 2) {
-        const long long u = u_begin + k;
+    for (long long k = grp;; k += 2) {
         const int s = (int)(k % kSStages);
-        const int b = (int)(u / per_seq);
-        const int rem = (int)(u - (long long)b * per_seq);
-        const int r = rem / p.nchunks, c = rem - r * p.nchunks;
-        const int n = min(kUnitElems, a.V - c * kUnitElems);  // elements in this unit (a multiple of PV)
         if (!warp_wait_bounded(&full[s], (uint32_t)((k / kSStages) & 1))) {
             if (lane == 0) atomicExch(timed_out, 1);  // records left unwritten
             break;
         }
+        const int u = unit_of[s];
+        if (u < 0) break;  // no more units
+        const int b = u / per_seq;
+        const int rem = u - b * per_seq;
+        const int r = rem / p.nchunks, c = rem - r * p.nchunks;
+        const int n = min(kUnitElems, a.V - c * kUnitElems);  // elements in this unit (a multiple of PV)
         float2 *dst = rec + (((size_t)b * a.T + r) * p.nchunks + c) * kSGroupWarps + gw;
         if (!row_in_use(b, r)) {  // padding: nothing landed, an empty record
             __syncwarp();
@@ -1426,6 +1451,7 @@ __global__ void __launch_bounds__(kVT) tree_decide_kernel(TreeArgs a, VocabPlan 
     tree_walk_load(a, b, ts);
     griddep_wait();
     griddep_launch_dependents();
+    if (b == 0 && threadIdx.x == 0) w.counters[2 * a.B + 1] = 0;  // the pass's claim counter, for the next call
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per_row = p.nchunks * kSGroupWarps;
     const float2 *rec = reinterpret_cast<const float2 *>(w.partials) + (size_t)b * a.T * per_row;
