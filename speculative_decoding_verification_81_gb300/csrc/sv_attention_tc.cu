@@ -736,25 +736,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         fail(cur.b);
                         break;
                     }
-                    if (is_k && (u == u_begin || cur.tile == 0)) {
-                        // this segment's Q rows (rows_per_rg of them: rows_per_rg / G
-                        // nodes x G heads, a 3-D box) into Q buffer qseg & 1, once
-                        // the S products of the segment two back are done
-                        const int qb = (int)(qseg & 1);
-                        if (!mbar_wait_bounded(&sh->q_empty[qb], ((qseg >> 1) & 1) ^ 1u)) {
-                            fail(cur.b);
-                            break;
-                        }
-                        const int kvh = cur.pr / p.RG, rg = cur.pr - kvh * p.RG;
-                        const int tpr = p.rows_per_rg / p.G;  // nodes per row group
-                        const int z = cur.b * p.T + rg * tpr;
-                        uint8_t *qd = qbuf + qb * 2 * kQBox;
-                        mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
-                        tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
-                        tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
-                        if (qseg == 0) SV_STAMP(5);
-                        ++qseg;
-                    }
                     const int kvh = cur.pr / p.RG;
                     const int kb = cur.tile * kBK;
                     if (!p.block_table) {
@@ -790,6 +771,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (is_k && k == 0) {
                         mbar_arrive(&sh->k_first);
                         SV_STAMP(6);
+                    }
+                    if (is_k && (u == u_begin || cur.tile == 0)) {
+                        // this segment's Q rows (rows_per_rg of them: rows_per_rg / G
+                        // nodes x G heads, a 3-D box) into Q buffer qseg & 1, once
+                        // the S products of the segment two back are done; requested
+                        // after the segment's first K tile, which comes from HBM while Q
+                        // mostly comes from L2
+                        const int qb = (int)(qseg & 1);
+                        if (!mbar_wait_bounded(&sh->q_empty[qb], ((qseg >> 1) & 1) ^ 1u)) {
+                            fail(cur.b);
+                            break;
+                        }
+                        const int kvh = cur.pr / p.RG, rg = cur.pr - kvh * p.RG;
+                        const int tpr = p.rows_per_rg / p.G;  // nodes per row group
+                        const int z = cur.b * p.T + rg * tpr;
+                        uint8_t *qd = qbuf + qb * 2 * kQBox;
+                        mbar_arrive_expect_tx(&sh->q_full[qb], 2u * 128u * (uint32_t)p.rows_per_rg);
+                        tma_load_3d(qd, &tmq, 0, kvh * p.G, z, &sh->q_full[qb]);
+                        tma_load_3d(qd + kQBox, &tmq, 64, kvh * p.G, z, &sh->q_full[qb]);
+                        if (qseg == 0) SV_STAMP(5);
+                        ++qseg;
                     }
                     if (!is_k && k == 0) SV_STAMP(18);
                     if (is_k) SV_STAMP(10);
