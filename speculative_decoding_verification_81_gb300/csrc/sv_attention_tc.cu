@@ -43,7 +43,9 @@
 //               second 64-127.  Each reads its half S row from TMEM, applies
 //               the ancestor mask (a 64-bit set of tree ancestors per row,
 //               only in the tile(s) holding the T new rows), agrees the tile
-//               max with its partner through shared memory, keeps the running
+//               max with its partner through a tagged shared-memory word per
+//               lane (value and tile number in one 64-bit store, polled by
+//               the partner, no barrier), keeps the running
 //               max (moved only when it grows by more than 2^8, its half of
 //               the O row then rescaled in TMEM) and its part of the row sum,
 //               writes its bf16 P half row over the S columns it came from
@@ -136,9 +138,9 @@ struct TcSmem {
     uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];  // per S buffer
     uint64_t q_full[2], q_empty[2];  // Q tiles in shared memory (double buffer)
     uint64_t fin, fin_pv;
-    uint64_t pair[4];            // the two softmax warps of each lane quarter
+    uint64_t pair[4];            // the two softmax warps of each lane quarter, at segment ends
     uint64_t k_first;            // the first K tile has been requested
-    float xmax[2][4][2][32];     // [tile parity][quarter][half][lane]: half-row tile maxima
+    uint64_t xmax[2][4][2][32];  // [tile parity][quarter][half][lane]: half-row tile maxima, tagged
     float xl[4][2][32];          // [quarter][half][lane]: half-row sums at a segment end
     uint32_t tmem;
     int abort_flag;
@@ -643,6 +645,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *reinterpret_cast<uint4 *>(qbuf + box * kQBox + p.rows_per_rg * 128 + w * 16) =
             make_uint4(0u, 0u, 0u, 0u);
     }
+    // no exchange word carries a tag yet (tags start at 1)
+    for (int i = tid; i < 2 * 4 * 2 * 32; i += kTcThreads) (&sh->xmax[0][0][0][0])[i] = 0ull;
     tc::fence_proxy_async_smem();
     if (warp == 1) tc::tmem_alloc(&sh->tmem, kTcCols);
     tc::fence_before();
@@ -1081,9 +1085,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int j = 0; j < 64; ++j) mq[j & 3] = fmaxf(mq[j & 3], sv[j]);
             float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             // the partner holds the other 64 keys of the same rows
-            sh->xmax[jt & 1][quarter][half][lane] = mx;
-            bool ok = group_sync(&sh->pair[quarter], pair_uses);
-            mx = fmaxf(mx, sh->xmax[jt & 1][quarter][half ^ 1][lane]);
+            const uint32_t xtag = (uint32_t)jt + 1u;
+            xchg_put(&sh->xmax[jt & 1][quarter][half][lane], mx, xtag);
+            float mx_other;
+            bool ok = xchg_get(&sh->xmax[jt & 1][quarter][half ^ 1][lane], xtag, mx_other);
+            mx = fmaxf(mx, mx_other);
             const float c = mx * sc;
             const bool up = c > m + kRescaleThreshold;
             const bool any_up = __any_sync(0xffffffffu, up);

@@ -120,6 +120,38 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses) {
     return ok;
 }
 
+// The tile row maxima of the two softmax warps of a lane quarter, exchanged
+// through one 64-bit word per lane: the value's bits with the tile's tag
+// (tile counter + 1) above them, stored and polled with volatile shared
+// accesses.  A naturally aligned 64-bit access is seen whole, so the tag
+// that matches also vouches for the value, and no barrier or fence is needed.
+__device__ __forceinline__ void xchg_put(uint64_t *slot, float v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+    asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(smem_u32(slot)), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ uint64_t xchg_peek(const uint64_t *slot) {
+    uint64_t w;
+    asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(w) : "r"(smem_u32(slot)) : "memory");
+    return w;
+}
+
+// The partner's value for the tile `tag`, by a whole warp (one verdict for
+// all lanes); false after kWaitCycles.
+__device__ __forceinline__ bool xchg_get(const uint64_t *slot, uint32_t tag, float &v) {
+    uint64_t w = xchg_peek(slot);
+    if (!__all_sync(0xffffffffu, (uint32_t)(w >> 32) == tag)) {
+        const long long t0 = clock64();
+        while (true) {
+            w = xchg_peek(slot);
+            if (__all_sync(0xffffffffu, (uint32_t)(w >> 32) == tag)) break;
+            if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) return false;
+        }
+    }
+    v = __uint_as_float((uint32_t)w);
+    return true;
+}
+
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }

@@ -132,9 +132,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity; gives up after
-// kWaitCycles and returns false.
+// kWaitCycles and returns false.  The first probe never suspends (a phase
+// that is already complete costs one test), the later ones may.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
