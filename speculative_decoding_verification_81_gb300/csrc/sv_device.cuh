@@ -245,6 +245,9 @@ __device__ __forceinline__ float ld_shared_cluster_f32(const float *local, uint3
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
     return v;
 }
+__device__ __forceinline__ void st_cluster_f2(uint32_t ra, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(ra), "f"(v.x), "f"(v.y) : "memory");
+}
 __device__ __forceinline__ float2 ld_cluster_f2(uint32_t ra) {
     float2 v;
     asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra) : "memory");

@@ -71,6 +71,7 @@ struct VocabPlan {
 VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype);
 
 constexpr int kMaxResChunks = 256;  // chunks of a row in the chain's residual draw, at most
+constexpr int kMaxResCluster = 16;  // chunks of a row for the residual draw's cluster form, at most
 
 struct ChainArgs {
     const void *target;

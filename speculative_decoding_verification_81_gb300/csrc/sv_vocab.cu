@@ -13,7 +13,10 @@
 //               of the row pair at the first rejection a it sums the weights
 //               max(0, p_a - q_a) (or p_N for the bonus); the last CTA of the
 //               sequence locates u * S in the chunk totals, then the thread,
-//               then the element.
+//               then the element.  Whole-GPU calls with at most 16 chunks a
+//               row and room for the clusters: the sequence's CTAs form a
+//               cluster, the totals go through distributed shared memory,
+//               and the CTA holding the crossing searches its own words.
 // Greedy tree acceptance ("Parallel Decoding" glossary, "L'attention en
 // arbre"; §9.1): tree_stats_stream_kernel, the same streaming pass in argmax
 // mode, then tree_decide_kernel, one CTA per sequence: the rows' argmax from
@@ -882,7 +885,14 @@ __device__ __forceinline__ ChainDecision decide_sequence(const ChainArgs &a, con
     return d;
 }
 
-template <typename T, bool VEC>
+// CLUSTER: the CTAs of a sequence form one thread-block cluster (at most
+// kMaxResCluster chunks a row); each sends its chunk totals into every
+// other's shared memory, and after one cluster barrier all of them run the
+// same search over the totals: the CTA whose chunk holds the crossing goes
+// on with the words still in its registers, the others leave.  Otherwise
+// the totals go through memory and the last CTA of the sequence to count
+// its chunk searches them and loads the crossing chunk again.
+template <typename T, bool VEC, bool CLUSTER>
 // (Aligned rows: at most 64 registers, so that four CTAs per SM keep a
 // B = 32, V = 128256 grid in one wave.)
 __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainArgs a, VocabPlan p, WsView w) {
@@ -928,20 +938,31 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     raw_weight_sums<T>(rw, mode0, rt, rd, sr, sp);
     float2 tot;
     float2 incl = cta_incl_scan2(make_float2(sr, sp), tot, wsum);
-    if (threadIdx.x == 0) {
-        w.chunktot[(size_t)b * p.res_chunks + c] = tot;
+    if constexpr (CLUSTER) {
+        // this chunk's totals into slot c of every CTA of the cluster (rank
+        // r = chunk r); the barrier makes them visible, and no CTA reads
+        // another's shared memory after it, so any may then leave
+        if ((int)threadIdx.x < p.res_chunks)
+            st_cluster_f2(cluster_map(smem_u32(&s_tot[c]), threadIdx.x), tot);
+        __syncwarp();
+        cluster_sync();
+        (void)s_last;
+    } else {
+        if (threadIdx.x == 0) {
+            w.chunktot[(size_t)b * p.res_chunks + c] = tot;
+            __threadfence();
+            const int old = atomicAdd(&w.counters[a.B + b], 1);
+            s_last = (old == p.res_chunks - 1);
+        }
+        __syncthreads();
+        if (!s_last) return;
         __threadfence();
-        const int old = atomicAdd(&w.counters[a.B + b], 1);
-        s_last = (old == p.res_chunks - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
 
-    // ---- last CTA of sequence b: locate u * S in the chunk prefix
-    for (int i = threadIdx.x; i < p.res_chunks; i += kVT)
-        s_tot[i] = __ldcg(w.chunktot + (size_t)b * p.res_chunks + i);
-    __syncthreads();
+        // ---- last CTA of sequence b: locate u * S in the chunk prefix
+        for (int i = threadIdx.x; i < p.res_chunks; i += kVT)
+            s_tot[i] = __ldcg(w.chunktot + (size_t)b * p.res_chunks + i);
+        __syncthreads();
+    }
     if (threadIdx.x == 0) {
         float S = 0.f;
         for (int i = 0; i < p.res_chunks; ++i) S = __fadd_rn(S, s_tot[i].x);
@@ -983,6 +1004,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     }
     __syncthreads();
     const int cstar = s_cstar, mode = s_mode;
+    if (CLUSTER && cstar != c) return;  // the crossing is in another CTA's chunk
     const float base = s_base, theta = s_theta;
     const int f0 = cstar * p.res_chunk_elems + threadIdx.x * EPT;
     const int fn = max(0, min(EPT, a.V - f0));
@@ -1065,7 +1087,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
         }
         if (lane == 0) {
             a.out_tokens[(size_t)b * (a.N + 1) + d.a] = y;
-            w.counters[a.B + b] = 0;  // ready for the next call
+            if (!CLUSTER) w.counters[a.B + b] = 0;  // ready for the next call
         }
     }
 }
@@ -1879,6 +1901,44 @@ VocabPlan plan_vocab(bool chain, int B, int rows_or_n, int V, int dtype) {
     return p;
 }
 
+// How many clusters of `size` CTAs of `threads` threads of `fn` this device
+// holds at once (0: none; sizes above 8 are allowed first), cached per
+// (device, kernel, size).
+static int cluster_capacity(const void *fn, int size, int threads) {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int size;
+        int n;
+    };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int ncache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ncache; ++i)
+        if (cache[i].dev == dev && cache[i].fn == fn && cache[i].size == size) return cache[i].n;
+    int clusters = 0;
+    if (size <= 8 || cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                         cudaSuccess) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)size;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)size);
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) clusters = 0;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind
+    if (ncache < 32) cache[ncache++] = Entry{dev, fn, size, clusters};
+    return clusters;
+}
+
 template <typename T, bool VEC>
 static cudaError_t launch_chain_t(ChainArgs a, VocabPlan p, WsView w, cudaStream_t st) {
     void *args[] = {&a, &p, &w};
@@ -1908,8 +1968,35 @@ static cudaError_t launch_chain_t(ChainArgs a, VocabPlan p, WsView w, cudaStream
     }
     if (e != cudaSuccess) return e;
     const unsigned res = (unsigned)((size_t)a.B * p.res_chunks);
-    return launch_pdl((const void *)chain_residual_kernel<T, VEC>, dim3(res), dim3(kVT), 0, st,
-                      args);
+    if constexpr (VEC) {
+        // The whole GPU: a cluster per sequence, while the sequences take at
+        // most 7/8 of the clusters the device holds at once.  Nearer the
+        // limit (B = 30 and 32 sequences of 16 chunks, against 33 clusters on
+        // 152 SMs) some clusters found no room until others had left, and the
+        // call ran 1.5-2.3 us longer than with the counted form; at 28 it ran
+        // 2.6 us shorter.
+        const void *cfn = (const void *)chain_residual_kernel<T, VEC, true>;
+        if (p.max_ctas == 0 && p.res_chunks <= kMaxResCluster &&
+            (long long)a.B * 8 <= (long long)cluster_capacity(cfn, p.res_chunks, kVT) * 7) {
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)p.res_chunks;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(res);
+            cfg.blockDim = dim3(kVT);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = st;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            return cudaLaunchKernelExC(&cfg, cfn, args);
+        }
+    }
+    return launch_pdl((const void *)chain_residual_kernel<T, VEC, false>, dim3(res), dim3(kVT), 0,
+                      st, args);
 }
 
 template <typename T, bool VEC>
