@@ -227,6 +227,15 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of the cluster barrier, for a wait placed well after the
+// arrival: a relaxed arrival (it orders no earlier writes) and the wait
+// (acquire), each by whole warps.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 // The same barrier for code where the lanes of a warp may have diverged.
 __device__ __forceinline__ void cluster_sync_any() {
     asm volatile("barrier.cluster.arrive.release;\n\t"

@@ -904,6 +904,9 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
     __shared__ int s_last, s_cstar, s_mode, s_fallback, s_pick_min, s_pick_max;
     __shared__ uint4 s_words[2][kResLoadsPerThread];  // the picked thread's run
     __shared__ float s_base, s_theta;
+    // cluster form: every CTA of the cluster has started before any writes
+    // into another's shared memory (the matching wait precedes the sends)
+    if constexpr (CLUSTER) cluster_arrive_relaxed();
 
     const int b = blockIdx.x / p.res_chunks;
     const int c = blockIdx.x - b * p.res_chunks;
@@ -942,6 +945,7 @@ __global__ void __launch_bounds__(kVT, VEC ? 4 : 1) chain_residual_kernel(ChainA
         // this chunk's totals into slot c of every CTA of the cluster (rank
         // r = chunk r); the barrier makes them visible, and no CTA reads
         // another's shared memory after it, so any may then leave
+        cluster_wait();
         if ((int)threadIdx.x < p.res_chunks)
             st_cluster_f2(cluster_map(smem_u32(&s_tot[c]), threadIdx.x), tot);
         __syncwarp();
