@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--profile", action="store_true",
                     help="device-resident steps only (for ncu): no graph, e2e, clocks or CPU leg")
     ap.add_argument("--profile-workload", default="chain",
-                    choices=["chain", "chain-b8", "medusa", "eagle", "eagle-b4"],
+                    choices=["chain", "chain-b8", "chain-call", "medusa", "eagle", "eagle-b4"],
                     help="with --profile: the fused chain step (B=32, or B=8), or the tree "
                          "workloads' kernels one call at a time (Medusa B=4 T=26 L=2048; "
                          "EAGLE-style B=16, or B=4, T=64 L=8192)")
@@ -504,6 +504,22 @@ def profile_run(args, dev):
     name = args.profile_workload
     g = torch.Generator(device=dev).manual_seed(11)
     Hq, Hkv, D = 32, 8, 128
+    if name == "chain-call":
+        # sv_verify_chain alone on the chain-acceptance workload at Llama vocab
+        # (B=8, N=5, V=32000): the statistics pass and the residual draw in its
+        # cluster form
+        cfg = W.WORKLOADS[2]
+        B, N, V = cfg["B"], cfg["N"], cfg["V"]
+        t = (torch.randn(B, N + 1, V, device=dev, generator=g) * 3).to(torch.bfloat16)
+        d = (t[:, :N].float() + torch.randn(B, N, V, device=dev, generator=g)).to(torch.bfloat16)
+        tok = torch.randint(0, V, (B, N), device=dev, generator=g, dtype=torch.int32)
+        ua = torch.rand(B, N, device=dev, generator=g)
+        us = torch.rand(B, device=dev, generator=g)
+        for _ in range(args.warmup + args.steps):
+            sv.sv_verify_chain(t, d, tok, ua, us)
+        torch.cuda.synchronize(dev)
+        return {"profile": name, "steps": args.steps, "warmup": args.warmup,
+                "launches": 2 * (args.steps + args.warmup)}
     if name.startswith("chain"):
         cfg = W.WORKLOADS[4]
         B, N, L, V = (8 if name == "chain-b8" else cfg["B"]), cfg["N"], cfg["L"], cfg["V"]
