@@ -2085,38 +2085,7 @@ VocabPlan plan_vocab_stree(int B, int T, int V, int dtype) {
 // size) where it can run one, else the portable 8.  Queried once per device
 // and kernel.
 static int walk_cluster_max(const void *fn) {
-    struct Entry {
-        int dev;
-        const void *fn;
-        int n;
-    };
-    static std::mutex mu;
-    static Entry cache[16];
-    static int ncache = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < ncache; ++i)
-        if (cache[i].dev == dev && cache[i].fn == fn) return cache[i].n;
-    int n = 8;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kWClusterMax;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kWClusterMax);
-        cfg.blockDim = dim3(kWT);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
-            n = kWClusterMax;
-    }
-    cudaGetLastError();  // a refused query leaves no error behind
-    if (ncache < 16) cache[ncache++] = Entry{dev, fn, n};
-    return n;
+    return cluster_capacity(fn, kWClusterMax, kWT) > 0 ? kWClusterMax : 8;
 }
 
 template <typename T, bool VEC>

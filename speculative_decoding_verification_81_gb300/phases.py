@@ -7,7 +7,7 @@ spread over the CTAs of its globaltimer reading, in microseconds from the
 moment the kernel was allowed to start (the earliest return from the wait
 for the previous kernel).
 
-    python -m speculative_decoding_verification_81_gb300.phases [--shape medusa|chain|small]
+    python -m speculative_decoding_verification_81_gb300.phases [--shape medusa|chain|small|eagle]
         [--reps N] [--behind N]
     python -m speculative_decoding_verification_81_gb300.phases --step chain|medusa|eagle
         [--side-ctas N]
@@ -177,6 +177,7 @@ SHAPES = {
     "medusa": (4, 2048, 26, "medusa"),
     "chain": (32, 4096, 9, None),
     "small": (2, 300, 9, None),
+    "eagle": (16, 8192, 64, "random"),
 }
 
 
@@ -229,8 +230,13 @@ def main():
         v = torch.randn(B, Hkv, S, D, device=dev, generator=g).to(torch.bfloat16)
         sets.append((q, k, v, torch.empty_like(q)))
     pl = torch.full((B,), L, dtype=torch.int32, device=dev)
-    par = (torch.from_numpy(np.broadcast_to(W.medusa_tree(T), (B, T)).copy()).to(dev)
-           if tree == "medusa" else None)
+    if tree == "medusa":
+        par = torch.from_numpy(np.broadcast_to(W.medusa_tree(T), (B, T)).copy()).to(dev)
+    elif tree == "random":  # EAGLE-style trees, as the bench draws them
+        rng = np.random.default_rng(5)
+        par = torch.from_numpy(np.stack([W.random_tree(T, 8, rng) for _ in range(B)])).to(dev)
+    else:
+        par = None
     ws = api.workspace(api.SV_OP_TREE_ATTENTION, B, T, Hq=Hq, Hkv=Hkv, D=D, device=dev)
 
     # every set is read once per replay, the stamped (last) call's set least recently
