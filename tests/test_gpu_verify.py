@@ -80,6 +80,26 @@ def test_chain_random_shapes(orc, B, N, V, dtype, seed):
     _check_chain(orc, inp)
 
 
+def test_chain_residual_forms_agree_bitwise():
+    """The residual draw's two forms -- a thread-block cluster per sequence
+    (whole-GPU calls whose clusters fit with room: B = 8 here) and the arrival
+    counter with the last CTA (B = 32 sequences of 16 chunks, near the
+    device's cluster capacity; and the fused step's acceptance) -- take the
+    same arithmetic, so the same sequences give the same bits whichever runs.
+    Sequences 8..15 of a B = 32 batch against the same 8 sequences alone."""
+    cfg = W.WORKLOADS[4]
+    inp = W.chain_inputs(32, cfg["N"], cfg["V"], "bf16", cfg["target_sigma"], cfg["draft_sigma"],
+                         cfg["boost"], seed=1011)
+    # rejections at every position, and bonus draws where all are accepted
+    inp["u_accept"][8:12] = np.float32(1.0 - 2.0 ** -24)
+    inp["draft"][12:14] = inp["target"][12:14, :cfg["N"]]
+    full = _run_chain(inp)
+    part = _run_chain({k: inp[k][8:16] for k in ("target", "draft", "draft_tokens", "u_accept",
+                                                 "u_sample")})
+    for a, b in zip(full, part):
+        np.testing.assert_array_equal(a[8:16], b)
+
+
 def test_chain_all_accepted_and_all_rejected(orc):
     inp = W.chain_inputs(8, 4, 2000, "bf16", target_sigma=2.0, draft_sigma=1.0, boost=0.0, seed=9)
     same = dict(inp, draft=inp["target"][:, :4].copy())          # p = q: every draft accepted
