@@ -444,8 +444,15 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
     }
     if (warp_active) {
         // the other contributors' (max, sum) of this row half
-        auto part_row = [&](int i) -> size_t {
-            return ((size_t)((c0 + i) * nlane + pl.poff) * 2 + (i == 0 ? slot0 : 0)) * MROWS + r;
+        auto part_slot = [&](int i) -> size_t {
+            return (size_t)((c0 + i) * nlane + pl.poff) * 2 + (i == 0 ? slot0 : 0);
+        };
+        auto part_row = [&](int i) -> size_t { return part_slot(i) * MROWS + r; };
+        // O of a partial slot is chunk-major: 16-byte chunk c (columns 4c..4c+3)
+        // of row r at float4 (slot * 32 + c) * MROWS + r, so that the lanes of a
+        // warp, a row each, store and load consecutive 16 bytes
+        auto part_o4 = [&](size_t slot_i, int c) -> size_t {
+            return (slot_i * (kD / 4) + (size_t)((hc >> 2) + c)) * MROWS + r;
         };
         // The merge takes the contributors in index order with the same
         // arithmetic whoever merges, so the result does not depend on
@@ -466,7 +473,8 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
             }
         }
         const int slot = seg_is_first ? 0 : 1;
-        float *po = p.part_o + (((size_t)blockIdx.x * 2 + slot) * MROWS + r) * kD + hc;
+        float4 *po4 = reinterpret_cast<float4 *>(p.part_o);
+        const size_t my_slot = (size_t)blockIdx.x * 2 + slot;
         if (!whole && merger && nc == 2) {  // (the same in every lane)
             // two contributors (the usual split): the other's partial
             // fetched in one go, then the same arithmetic as below
@@ -474,11 +482,11 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
             const size_t pro = part_row(oth);
             float2 mlo = make_float2(kNegInf, 0.f);
             float4 oo[16];
-            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + pro * kD + hc);
+            const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
             if (row_valid) {
                 mlo = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pro * 4 + half * 2));
     #pragma unroll
-                for (int c = 0; c < 16; ++c) oo[c] = __ldcg(src + c);
+                for (int c = 0; c < 16; ++c) oo[c] = __ldcg(src + part_o4(part_slot(oth), c));
             } else {
     #pragma unroll
                 for (int c = 0; c < 16; ++c) oo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -541,10 +549,11 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
     #pragma unroll
                             for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(__uint_as_float(ov[j]), w, acc[j]);
                         } else {
-                            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + part_row(i) * kD + hc + 32 * h);
+                            const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
+                            const size_t si = part_slot(i);
     #pragma unroll
                             for (int c = 0; c < 8; ++c) {
-                                const float4 o = __ldcg(src + c);
+                                const float4 o = __ldcg(src + part_o4(si, 8 * h + c));
                                 acc[4 * c] = __fmaf_rn(o.x, w, acc[4 * c]);
                                 acc[4 * c + 1] = __fmaf_rn(o.y, w, acc[4 * c + 1]);
                                 acc[4 * c + 2] = __fmaf_rn(o.z, w, acc[4 * c + 2]);
@@ -565,7 +574,7 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
             } else {
     #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(po + 32 * h + 4 * c) =
+                    po4[part_o4(my_slot, 8 * h + c)] =
                         make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
                                     __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
             }

@@ -31,7 +31,7 @@ struct AttnKParams {
     int32_t *seq_status;
     int B, T, Hq, Hkv, G, S_max, M, RG, rows_per_rg;
     float scale_log2;
-    float *part_o;   // [grid][2][rows_per_rg][kD]: unnormalised O of split pairs
+    float *part_o;   // [grid][2][kD / 4][MROWS] float4 (chunk-major): unnormalised O of split pairs
     float *part_ml;  // [grid][2][rows_per_rg][2 halves][2]: (max in log2 units, row sum)
     int *pair_ctr;   // [B][Hkv][RG][2][8]: per softmax warp, CTAs arrived / partials ready (0 after the merge)
     // paged caches (block_table non-null): K/V [num_pages][Hkv][page_size][D];
