@@ -719,8 +719,13 @@ def run_ours(args, cfg, inp, rank, world, local_rank):
     # EAGLE-style random tree, B=16 L=8192 T=64 V=128256): the fused step,
     # device-resident, cycling through input sets totalling more than 3x L2
     from speculative_decoding_verification_81_gb300 import workloads as W
-    tree_steps = {wl: tree_step_bench(W.WORKLOADS[wl], dev, capture, stream, reps)
-                  for wl in (3, 5)}
+    # (clocks sampled here too: these compute-heavy kernels are the first to
+    # show a power cap)
+    tree_steps = {}
+    for wl in (3, 5):
+        with ClockSampler(local_rank) as tclk:
+            tree_steps[wl] = tree_step_bench(W.WORKLOADS[wl], dev, capture, stream, reps)
+        tree_steps[wl]["clocks"] = tclk.summary()
     latency_steps = {wl: latency_bench(wl, dev, capture, stream) for wl in (1, 2)}
     ragged = ragged_bench(cfg, d, dev, capture, stream, reps)
 
