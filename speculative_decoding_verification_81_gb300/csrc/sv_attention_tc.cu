@@ -384,11 +384,16 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
         ret.ok = ok;
         return ret;
     };
-    if (!warp_wait_bounded(&sh->pv_done[jt % kSBufs], (uint32_t)((jt / kSBufs) & 1))) {
-        return done(false);
-    }
-    tc::fence_after();
-    if (warp == 2 && lane == 0) SV_STAMP(11);
+    // The segment's last PV product is waited for only where O is read, so
+    // that the row sums' exchange, the merge bookkeeping and a merger's loads
+    // of the other partial overlap it (warp-collective: call warp-uniformly).
+    auto wait_last_pv = [&]() -> bool {
+        if (!warp_wait_bounded(&sh->pv_done[jt % kSBufs], (uint32_t)((jt / kSBufs) & 1)))
+            return false;
+        tc::fence_after();
+        if (warp == 2 && lane == 0) SV_STAMP(11);
+        return true;
+    };
     // row sum = first half's part + second half's part (same order in both)
     sh->xl[quarter][half][lane] = l;
     if (!group_sync(&sh->pair[quarter], pair_uses)) {
@@ -396,6 +401,7 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
     }
     const float lrow = sh->xl[quarter][0][lane] + sh->xl[quarter][1][lane];
     if (cl) {
+        if (!wait_last_pv()) return done(false);
         // cluster mode: this CTA's share of the group, unnormalised,
         // into the merge buffer (the K/V ring is idle now: every copy
         // has landed and every product has read it)
@@ -491,6 +497,7 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
     #pragma unroll
                 for (int c = 0; c < 16; ++c) oo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            if (!wait_last_pv()) return done(false);
             const float ms2 = fmaxf(m, mlo.x);
             const float ws = m == kNegInf ? 0.f : ex2_approx(m - ms2);
             const float wo = mlo.x == kNegInf ? 0.f : ex2_approx(mlo.x - ms2);
@@ -527,6 +534,7 @@ __device__ __noinline__ SegEndRet softmax_segment_end(
                 }
             }
         } else {
+        if (!wait_last_pv()) return done(false);
         const float inv = 1.f / lsum;
     #pragma unroll
         for (int h = 0; h < 2; ++h) {
