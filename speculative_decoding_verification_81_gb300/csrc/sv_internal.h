@@ -97,6 +97,10 @@ struct ChainArgs {
 // path is known.  step_ctr[b * Hkv + h] counts those arrivals (rg_count row
 // groups of the attention, then the walk); whoever brings it to
 // rg_count + 1 moves the rows and resets it.
+// The walk's side of the hook holds a head's moved rows in registers, room for
+// T - 1 = 63 accepted rows: the attention's node limit (T <= 64).
+constexpr int kStepHookMaxT = 64;
+
 struct StepHook {
     int *step_ctr;             // [B * Hkv], zero between calls
     uint4 *k, *v;              // contiguous caches [B, Hkv, S_max, D] as 16-byte words

@@ -249,8 +249,11 @@ sv_status sv_verify_step_tree_greedy(const void *q, void *k_cache, void *v_cache
         workspace_bytes < off_c + align_up(sizeof(int) * (size_t)B * Hkv, 256))
         return SV_ERR_WORKSPACE;
     // compaction inside the two kernels when the attention runs in clusters and
-    // the walk in a kernel of its own (rows 16-byte aligned); else a kernel after both
-    const bool hook = ap.cluster > 1 && vp.vec && D == 128;
+    // the walk in a kernel of its own (rows 16-byte aligned), for at most
+    // kStepHookMaxT nodes; else a kernel after both (in the serial order too:
+    // the walk moving the rows alone, one sequence a CTA, measured 3 us slower
+    // than the compaction kernel on the EAGLE step)
+    const bool hook = ap.cluster > 1 && vp.vec && D == 128 && T <= kStepHookMaxT;
 
     StepHook hk{};
     if (hook) {

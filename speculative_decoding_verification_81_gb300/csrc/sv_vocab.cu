@@ -1410,6 +1410,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
 constexpr int kMaxStepHkv = 256;
 constexpr int kStepRowWords = 16;  // 16-byte words of a 128-dim bf16 row
 constexpr int kStepMoveRegs = 8;   // words a thread holds: 256 * 8 >= 63 rows * 2 * 16
+static_assert(kVT * kStepMoveRegs >= (kStepHookMaxT - 1) * 2 * kStepRowWords,
+              "the walk cannot hold the accepted rows the hook allows");
 
 __device__ __forceinline__ void step_hook_arrive(const TreeArgs &a, int b, const TreeWalkSmem &ts) {
     __shared__ unsigned char s_last[kMaxStepHkv];
